@@ -1,0 +1,194 @@
+"""FP64 CPU oracle for packed QSA decode.
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` use it; the product package never imports
+it, and it imports nothing from the product package. The arithmetic lives in
+``qsa_oracle.c`` (plain C, FP64, OpenMP over (sequence, head)); this module
+only marshals arrays into it.
+
+Definition followed (sglang PR #36845, "Changes" / "Optimized kernel";
+sglang PR #37798, "Modifications"; 1Cat-vLLM PR #523, "Purpose"): for each
+sequence b and query head h with KV head g = h // (Hq // Hkv),
+``o = softmax(scale * q . Khat[I]^T) @ Vhat[I]`` over the selected slots
+``I = sel[cu[b]:cu[b+1]]`` in order, duplicates kept; an empty selection
+gives zeros. Khat/Vhat are the exactly dequantised pool rows.
+
+Pins: every function here is checked in ``tests/test_oracle_pins.py``
+against closed forms, library routines and brute force (see that file).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "qsa_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+FORMATS = {"bf16": 0, "fp8_e4m3": 1, "int8": 2, "int4": 3}
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile qsa_oracle.c into liboracle.so with gcc (IEEE FP64, no FMA contraction)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+               "-fno-fast-math", "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    build()
+    lib = ctypes.CDLL(_LIB)
+    lib.orc_bf16_to_double.restype = ctypes.c_double
+    lib.orc_bf16_to_double.argtypes = [ctypes.c_uint16]
+    lib.orc_e4m3fn_to_double.restype = ctypes.c_double
+    lib.orc_e4m3fn_to_double.argtypes = [ctypes.c_uint8]
+    lib.orc_int4_value.restype = ctypes.c_int
+    lib.orc_int4_value.argtypes = [ctypes.c_uint8, ctypes.c_int]
+    lib.orc_round_bf16.restype = ctypes.c_uint16
+    lib.orc_round_bf16.argtypes = [ctypes.c_double]
+    lib.orc_round_bf16_array.restype = None
+    lib.orc_round_bf16_array.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64]
+    lib.orc_dequant_row.restype = None
+    lib.orc_dequant_row.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                    ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p]
+    lib.orc_decode.restype = ctypes.c_int
+    lib.orc_decode.argtypes = [
+        ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,          # q, q_sb, q_sh
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,           # k_pool, v_pool, format
+        ctypes.c_int64, ctypes.c_int, ctypes.c_int,               # num_slots, Hkv, D
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_double,        # k_scale, v_scale, scale
+        ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,         # sel, n_sel, cu
+        ctypes.c_int, ctypes.c_int,                               # bs, Hq
+        ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,  # rows, n_rows, out, threads
+    ]
+    lib.orc_max_threads.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+class OracleRefused(ValueError):
+    """The input breaks the decode contract (bad cu_seqlens or slot ids)."""
+
+
+def _np(a, dtype=None):
+    """Contiguous host numpy view of a numpy array or CPU torch tensor."""
+    if hasattr(a, "detach"):
+        import torch
+
+        t = a.detach()
+        if t.device.type != "cpu":
+            raise ValueError("oracle inputs must be host tensors")
+        if t.dtype == torch.bfloat16:
+            t = t.view(torch.int16).view(torch.uint16) if hasattr(torch, "uint16") else t.view(torch.int16)
+        elif t.dtype == torch.float8_e4m3fn:
+            t = t.view(torch.uint8)
+        a = t.contiguous().numpy()
+        if a.dtype == np.int16:
+            a = a.view(np.uint16)
+    a = np.ascontiguousarray(a)
+    if dtype is not None and a.dtype != dtype:
+        a = a.astype(dtype)
+    return a
+
+
+def _ptr(a):
+    return a.ctypes.data_as(ctypes.c_void_p) if a is not None else None
+
+
+def decode(q, k_pool, v_pool, fmt: str, sel, cu, softmax_scale: float,
+           k_scale=None, v_scale=None, rows=None, threads: int = 0) -> np.ndarray:
+    """Oracle decode. Returns float64 [len(rows) or bs, Hq, D].
+
+    q: bf16 [bs, Hq, D] (torch bf16 tensor or uint16 bits); k_pool/v_pool:
+    [num_slots, Hkv, D] (bf16 bits / uint8 e4m3 / int8) or [num_slots, Hkv, D/2]
+    uint8 (int4); sel int32 [n_sel]; cu int32 [bs+1]; scales float32.
+    """
+    lib = _load()
+    f = FORMATS[fmt]
+    qn = _np(q)
+    if qn.dtype != np.uint16:
+        raise ValueError("q must be bf16")
+    bs, Hq, D = qn.shape
+    kn, vn = _np(k_pool), _np(v_pool)
+    num_slots, Hkv = kn.shape[0], kn.shape[1]
+    if f == 3:
+        if kn.shape[2] * 2 != D:
+            raise ValueError("int4 pool rows must hold D/2 bytes")
+    elif kn.shape[2] != D:
+        raise ValueError("pool rows must hold D elements")
+    sn = _np(sel, np.int32)
+    cn = _np(cu, np.int32)
+    if cn.shape[0] != bs + 1:
+        raise ValueError("cu_seqlens must have bs+1 entries")
+    ks = _np(k_scale, np.float32) if k_scale is not None else None
+    vs = _np(v_scale, np.float32) if v_scale is not None else None
+    if f != 0 and (ks is None or vs is None):
+        raise ValueError("quantised pools need k_scale and v_scale")
+    rn = _np(rows, np.int32) if rows is not None else None
+    n_rows = bs if rn is None else rn.shape[0]
+    out = np.zeros((n_rows, Hq, D), dtype=np.float64)
+    rc = lib.orc_decode(_ptr(qn), Hq * D, D, _ptr(kn), _ptr(vn), f, num_slots, Hkv, D,
+                        _ptr(ks), _ptr(vs), float(softmax_scale), _ptr(sn), sn.shape[0],
+                        _ptr(cn), bs, Hq, _ptr(rn), n_rows, _ptr(out), int(threads))
+    if rc != 0:
+        raise OracleRefused({-1: "bad geometry", -2: "bad cu_seqlens",
+                             -3: "slot id out of range"}.get(rc, str(rc)))
+    return out
+
+
+def dequant_rows(pool, fmt: str, slots, g: int, scale=None) -> np.ndarray:
+    """Exact FP64 dequantisation of pool rows (slot, g) for each slot in `slots`."""
+    lib = _load()
+    pn = _np(pool)
+    Hkv = pn.shape[1]
+    D = pn.shape[2] * (2 if fmt == "int4" else 1)
+    sc = _np(scale, np.float32) if scale is not None else None
+    out = np.zeros((len(slots), D), dtype=np.float64)
+    for i, s in enumerate(slots):
+        row = out[i]
+        lib.orc_dequant_row(_ptr(pn), FORMATS[fmt], Hkv, D, _ptr(sc), int(s), int(g),
+                            row.ctypes.data_as(ctypes.c_void_p))
+    return out
+
+
+def e4m3fn_to_double(byte: int) -> float:
+    return _load().orc_e4m3fn_to_double(int(byte))
+
+
+def int4_value(byte: int, hi: int) -> int:
+    return _load().orc_int4_value(int(byte), int(hi))
+
+
+def bf16_to_double(bits: int) -> float:
+    return _load().orc_bf16_to_double(int(bits))
+
+
+def round_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round every element of a float64 array to bf16 (ties to even); returns uint16 bits."""
+    lib = _load()
+    flat = np.ascontiguousarray(x, dtype=np.float64).ravel()
+    bits = np.empty(flat.size, dtype=np.uint16)
+    lib.orc_round_bf16_array(_ptr(flat), _ptr(bits), flat.size)
+    return bits.reshape(np.shape(x))
+
+
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    """float64 values of round_bf16_bits(x)."""
+    bits = round_bf16_bits(x).astype(np.uint32) << 16
+    return bits.view(np.float32).astype(np.float64)
+
+
+def max_threads() -> int:
+    return _load().orc_max_threads()

@@ -1,0 +1,221 @@
+/*
+ * Packed QSA decode oracle: plain FP64 CPU reference.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing in the product path links, loads or
+ * calls this file; only the tests, the package's smoke check and the
+ * benchmark's CPU-baseline leg do. It shares no code, header, table or
+ * constant with the CUDA implementation.
+ *
+ * What it computes (sglang PR #36845 "fix(qsa): restore SM121 correctness",
+ * sections "Changes" and "Optimized kernel"; sglang PR #37798 "quantized KV
+ * pools with dequant-on-gather", section "Modifications"):
+ *
+ *   for every sequence b with L = cu[b+1] - cu[b] selected slots
+ *   I_j = sel[cu[b] + j] (order and duplicates kept, 1Cat-vLLM PR #523,
+ *   "Purpose"), and every query head h with KV head g = h / (Hq / Hkv):
+ *
+ *     s_j = softmax_scale * sum_d q[b,h,d] * Khat[I_j, g, d]
+ *     o_d = sum_j exp(s_j - max s) Vhat[I_j, g, d] / sum_j exp(s_j - max s)
+ *     L == 0  ->  o = 0
+ *
+ * Dequantisation is exact in FP64 and follows the pool formats:
+ *   bf16    : the stored value
+ *   fp8     : e4m3fn(byte) * s_tensor            (one fp32 scale per pool)
+ *   int8    : int8 * s[slot, g]                  (fp32 per (slot, KV head))
+ *   int4    : sext4(nibble) * s[slot, g]; two per byte, element 2i in the
+ *             low nibble (two's-complement nibbles)
+ *
+ * Every step is written as the definition states it: no tiling, no
+ * online softmax, no split, no merge. The scores use one exact max
+ * subtraction, as the textbook softmax does.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum { ORC_BF16 = 0, ORC_FP8_E4M3 = 1, ORC_INT8 = 2, ORC_INT4 = 3 };
+
+/* bf16 -> double: a bf16 is the upper half of an IEEE binary32. */
+double orc_bf16_to_double(uint16_t h) {
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* OCP FP8 E4M3 ("fn": no infinities, S.1111.111 is NaN, max 448): 1 sign,
+ * 4 exponent bits with bias 7, 3 mantissa bits; exponent field 0 encodes
+ * subnormals m/8 * 2^-6. */
+double orc_e4m3fn_to_double(uint8_t b) {
+    int sign = b >> 7;
+    int e = (b >> 3) & 0xF;
+    int m = b & 0x7;
+    double v;
+    if (e == 0xF && m == 0x7) return NAN;
+    if (e == 0)
+        v = ldexp((double)m / 8.0, -6);
+    else
+        v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+/* Two's-complement 4-bit value held in bits [4*hi, 4*hi+3] of `byte`. */
+int orc_int4_value(uint8_t byte, int hi) {
+    int n = hi ? (byte >> 4) & 0xF : byte & 0xF;
+    return n >= 8 ? n - 16 : n;
+}
+
+/* Round a double to the nearest bf16 (ties to even), returning its bits.
+ * bf16 keeps 8 significant bits and the binary32 exponent range. */
+uint16_t orc_round_bf16(double x) {
+    if (isnan(x)) return 0x7FC0;
+    uint16_t sign = signbit(x) ? 0x8000 : 0;
+    double a = fabs(x);
+    if (a == 0.0) return sign;
+    if (isinf(a)) return sign | 0x7F80;
+    int e2;
+    frexp(a, &e2);                 /* a = m * 2^e2, m in [0.5, 1) */
+    int E = e2 - 1;                /* floor(log2 a) */
+    if (E < -126) E = -126;        /* subnormal quantum is 2^-133 */
+    double quantum = ldexp(1.0, E - 7);
+    double r = nearbyint(a / quantum) * quantum; /* default mode: ties to even */
+    if (r > 3.3895313892515355e38) return sign | 0x7F80; /* beyond max bf16 */
+    float f = (float)r;            /* exact: r is a bf16 value */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return sign | (uint16_t)(u >> 16);
+}
+
+/* Element-wise orc_round_bf16 over n doubles. */
+void orc_round_bf16_array(const double* x, uint16_t* bits, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) bits[i] = orc_round_bf16(x[i]);
+}
+
+typedef struct {
+    const void* pool;
+    int format;
+    int Hkv;
+    int D;
+    const float* scale; /* fp8: [1]; int8/int4: [num_slots * Hkv]; bf16: unused */
+} orc_pool;
+
+/* Dequantised element d of pool row (slot, g), exactly in FP64. */
+static double pool_elem(const orc_pool* p, int64_t slot, int g, int d) {
+    int64_t row = slot * p->Hkv + g;
+    switch (p->format) {
+    case ORC_BF16:
+        return orc_bf16_to_double(((const uint16_t*)p->pool)[row * p->D + d]);
+    case ORC_FP8_E4M3:
+        return orc_e4m3fn_to_double(((const uint8_t*)p->pool)[row * p->D + d]) *
+               (double)p->scale[0];
+    case ORC_INT8:
+        return (double)((const int8_t*)p->pool)[row * p->D + d] * (double)p->scale[row];
+    case ORC_INT4: {
+        uint8_t byte = ((const uint8_t*)p->pool)[row * (p->D / 2) + d / 2];
+        return (double)orc_int4_value(byte, d & 1) * (double)p->scale[row];
+    }
+    }
+    return NAN;
+}
+
+/* Dequantise one pool row into `dst` (D doubles). */
+void orc_dequant_row(const void* pool, int format, int Hkv, int D, const float* scale,
+                     int64_t slot, int g, double* dst) {
+    orc_pool p = {pool, format, Hkv, D, scale};
+    for (int d = 0; d < D; ++d) dst[d] = pool_elem(&p, slot, g, d);
+}
+
+/*
+ * Full decode. Returns 0 on success and a negative value when the input
+ * breaks the contract the pages define (the oracle refuses such inputs
+ * instead of guessing an answer):
+ *   -1  bad geometry (Hq not a multiple of Hkv, D odd for int4, unknown format)
+ *   -2  cu_seqlens not monotone, negative, or beyond the index buffer
+ *   -3  a selected slot outside [0, num_slots)
+ *
+ * q       : bf16 bits, element (b, h, d) at q[b*q_sb + h*q_sh + d]
+ * rows    : optional subset of sequences to compute (NULL: all bs rows);
+ *           output row i holds sequence rows[i]
+ * out     : double [n_rows][Hq][D]
+ */
+int orc_decode(const uint16_t* q, int64_t q_sb, int64_t q_sh,
+               const void* k_pool, const void* v_pool, int format,
+               int64_t num_slots, int Hkv, int D,
+               const float* k_scale, const float* v_scale, double softmax_scale,
+               const int32_t* sel, int64_t n_sel, const int32_t* cu, int bs, int Hq,
+               const int32_t* rows, int n_rows, double* out, int nthreads) {
+    if (Hkv <= 0 || Hq <= 0 || Hq % Hkv != 0 || D <= 0) return -1;
+    if (format < ORC_BF16 || format > ORC_INT4) return -1;
+    if (format == ORC_INT4 && (D & 1)) return -1;
+    if (rows == NULL) n_rows = bs;
+    for (int i = 0; i < n_rows; ++i) {
+        int b = rows ? rows[i] : i;
+        if (b < 0 || b >= bs) return -1;
+        int64_t start = cu[b], stop = cu[b + 1];
+        if (start < 0 || stop < start || stop > n_sel) return -2;
+        for (int64_t t = start; t < stop; ++t)
+            if (sel[t] < 0 || (int64_t)sel[t] >= num_slots) return -3;
+    }
+    const int group = Hq / Hkv;
+    orc_pool kp = {k_pool, format, Hkv, D, k_scale};
+    orc_pool vp = {v_pool, format, Hkv, D, v_scale};
+    const int64_t tasks = (int64_t)n_rows * Hq;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t task = 0; task < tasks; ++task) {
+        int i = (int)(task / Hq);
+        int h = (int)(task % Hq);
+        int b = rows ? rows[i] : i;
+        int g = h / group;
+        int64_t L = (int64_t)cu[b + 1] - cu[b];
+        const int32_t* idx = sel + cu[b];
+        double* o = out + ((int64_t)i * Hq + h) * D;
+        for (int d = 0; d < D; ++d) o[d] = 0.0;
+        if (L == 0) continue;
+
+        double* qd = (double*)malloc(sizeof(double) * D);
+        double* s = (double*)malloc(sizeof(double) * L);
+        for (int d = 0; d < D; ++d) qd[d] = orc_bf16_to_double(q[b * q_sb + h * q_sh + d]);
+
+        /* scores */
+        for (int64_t j = 0; j < L; ++j) {
+            double acc = 0.0;
+            for (int d = 0; d < D; ++d) acc += qd[d] * pool_elem(&kp, idx[j], g, d);
+            s[j] = softmax_scale * acc;
+        }
+        /* softmax weights with one max subtraction */
+        double smax = s[0];
+        for (int64_t j = 1; j < L; ++j)
+            if (s[j] > smax) smax = s[j];
+        double z = 0.0;
+        for (int64_t j = 0; j < L; ++j) {
+            s[j] = exp(s[j] - smax);
+            z += s[j];
+        }
+        /* weighted sum of the selected V rows */
+        for (int64_t j = 0; j < L; ++j)
+            for (int d = 0; d < D; ++d) o[d] += s[j] * pool_elem(&vp, idx[j], g, d);
+        for (int d = 0; d < D; ++d) o[d] /= z;
+        free(qd);
+        free(s);
+    }
+    return 0;
+}
+
+/* Threads the OpenMP runtime would use (1 without OpenMP). */
+int orc_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

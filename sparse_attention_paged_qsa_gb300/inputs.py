@@ -1,0 +1,278 @@
+"""Seeded synthetic inputs for packed QSA decode.
+
+This module is shared by the GPU tests, the benchmark and the oracle tests.
+It holds input generation only -- random pools, queries, selected-slot lists
+and cu_seqlens, and the KV-write-side quantisers that turn N(0,1) draws into
+the fp8 / int8 / int4 pool formats. It contains none of the decode
+arithmetic (no dequantisation, no scores, no softmax); neither the CUDA
+path nor the oracle is imported here.
+
+Workload shapes follow the pages: one BF16 query token per sequence with
+24 query / 2 KV heads (TP1) or 12 / 1 (TP2), head dim 256, a paged pool with
+64-token pages and per-sequence selections of up to 2055 slots (sglang PR
+#36845, "Changes"; sglang PR #37798, "Decode routing": page 64, top-k
+2048 + 4 - 1).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+from typing import Optional
+
+import torch
+
+HEAD_DIM = 256
+GQA_GROUP = 12          # query heads per KV head (12:1 GQA)
+PAGE = 64               # slots per page
+MAX_CAPACITY = 2055     # largest selected-KV length of the contract
+SOFTMAX_SCALE = 1.0 / 16.0
+
+FORMATS = ("bf16", "fp8_e4m3", "int8", "int4")
+FP8_E4M3_MAX = 448.0    # largest finite e4m3fn value; the fp8 write saturates here
+
+
+@dataclass
+class Workload:
+    """One decode call's inputs (all tensors on one device)."""
+
+    q: torch.Tensor                  # [bs, Hq, 256] bf16
+    k_pool: torch.Tensor             # [slots, Hkv, 256] bf16/uint8/int8 or [slots, Hkv, 128] uint8
+    v_pool: torch.Tensor
+    sel: torch.Tensor                # int32 [n_sel], packed by cu
+    cu: torch.Tensor                 # int32 [bs+1]
+    fmt: str = "bf16"
+    k_scale: Optional[torch.Tensor] = None   # fp8: [1]; int8/int4: [slots, Hkv] float32
+    v_scale: Optional[torch.Tensor] = None
+    softmax_scale: float = SOFTMAX_SCALE
+    capacity: int = MAX_CAPACITY
+    name: str = ""
+    extra: dict = field(default_factory=dict)
+
+    @property
+    def bs(self) -> int:
+        return self.q.shape[0]
+
+    @property
+    def num_q_heads(self) -> int:
+        return self.q.shape[1]
+
+    @property
+    def num_kv_heads(self) -> int:
+        return self.k_pool.shape[1]
+
+    @property
+    def num_slots(self) -> int:
+        return self.k_pool.shape[0]
+
+    def to(self, device) -> "Workload":
+        mv = lambda t: None if t is None else t.to(device)
+        return Workload(mv(self.q), mv(self.k_pool), mv(self.v_pool), mv(self.sel), mv(self.cu),
+                        self.fmt, mv(self.k_scale), mv(self.v_scale), self.softmax_scale,
+                        self.capacity, self.name, dict(self.extra))
+
+    def lengths(self) -> torch.Tensor:
+        return (self.cu[1:] - self.cu[:-1]).cpu()
+
+
+def _gen(seed: int, device) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    return g
+
+
+# ---------------------------------------------------------------- pool values
+
+def normal_values(shape, seed: int, device="cpu", std: float = 1.0) -> torch.Tensor:
+    """float32 N(0, std^2) draws from torch's seeded generator on `device`."""
+    return torch.randn(shape, generator=_gen(seed, device), device=device,
+                       dtype=torch.float32) * std
+
+
+def quantize_pool(x: torch.Tensor, fmt: str):
+    """KV-write-side quantiser (input generation): float32 [slots, Hkv, D] -> (codes, scale).
+
+    fp8 : one fp32 scale per pool = absmax / 448; codes = e4m3fn(clamp(x / s, +-448))
+          (the clamp mirrors the fp8 write path's saturation before the cast,
+          sglang PR #37798 part 1, "mem_cache/memory_pool.py").
+    int8: fp32 scale per (slot, KV head) = absmax(row) / 127; codes = clamp(rint(x/s), -127, 127).
+    int4: fp32 scale per (slot, KV head) = absmax(row) / 7; codes = clamp(rint(x/s), -8, 7),
+          two's-complement nibbles, two per byte, element 2i in the low nibble.
+    rint is round-half-to-even (torch.round). A zero row gets scale 0 and zero codes.
+    """
+    if fmt == "bf16":
+        return x.to(torch.bfloat16), None
+    if fmt == "fp8_e4m3":
+        amax = x.abs().max().to(torch.float32)
+        s = (amax / FP8_E4M3_MAX).reshape(1)
+        inv = torch.where(s > 0, 1.0 / s, torch.zeros_like(s))
+        y = (x * inv).clamp(-FP8_E4M3_MAX, FP8_E4M3_MAX)
+        return y.to(torch.float8_e4m3fn).view(torch.uint8), s.to(torch.float32)
+    if fmt in ("int8", "int4"):
+        qmax = 127.0 if fmt == "int8" else 7.0
+        qmin = -127.0 if fmt == "int8" else -8.0
+        amax = x.abs().amax(dim=-1)
+        s = (amax / qmax).to(torch.float32)
+        inv = torch.where(s > 0, 1.0 / s, torch.zeros_like(s))
+        qv = torch.round(x * inv.unsqueeze(-1)).clamp(qmin, qmax).to(torch.int8)
+        if fmt == "int8":
+            return qv, s
+        lo = (qv[..., 0::2].to(torch.int16) & 0xF)
+        hi = (qv[..., 1::2].to(torch.int16) & 0xF)
+        return (lo | (hi << 4)).to(torch.uint8), s
+    raise ValueError(f"unknown pool format {fmt!r}")
+
+
+def make_pools(num_slots: int, num_kv_heads: int, fmt: str, seed: int, device="cpu"):
+    """K and V pools [slots, Hkv, 256] from N(0,1) draws, in pool format `fmt`.
+
+    Returns (k_codes, v_codes, k_scale, v_scale)."""
+    shape = (num_slots, num_kv_heads, HEAD_DIM)
+    kx = normal_values(shape, seed * 1000 + 1, device)
+    kc, ks = quantize_pool(kx, fmt)
+    del kx
+    vx = normal_values(shape, seed * 1000 + 2, device)
+    vc, vs = quantize_pool(vx, fmt)
+    del vx
+    return kc, vc, ks, vs
+
+
+def make_query(bs: int, num_q_heads: int, seed: int, device="cpu") -> torch.Tensor:
+    return normal_values((bs, num_q_heads, HEAD_DIM), seed * 1000 + 3, device).to(torch.bfloat16)
+
+
+# ---------------------------------------------------------- selected slots
+
+def cu_from_lengths(lengths) -> torch.Tensor:
+    lens = torch.as_tensor(lengths, dtype=torch.int64)
+    cu = torch.zeros(lens.numel() + 1, dtype=torch.int64)
+    cu[1:] = torch.cumsum(lens, 0)
+    return cu.to(torch.int32)
+
+
+def uniform_indices(n: int, num_slots: int, gen: torch.Generator) -> torch.Tensor:
+    """n slot ids drawn uniformly with replacement (duplicates kept, order as drawn)."""
+    return torch.randint(0, num_slots, (n,), generator=gen, dtype=torch.int64).to(torch.int32)
+
+
+def runs_and_uniform_indices(length: int, num_slots: int, gen: torch.Generator) -> torch.Tensor:
+    """Half page-aligned ascending runs of 64 slots, half uniform slots.
+
+    floor(length/2) rounded down to whole 64-slot runs come first, each run
+    starting at a random page; the remaining ids are uniform."""
+    n_runs = (length // 2) // PAGE
+    pages = torch.randint(0, num_slots // PAGE, (n_runs,), generator=gen, dtype=torch.int64)
+    runs = (pages[:, None] * PAGE + torch.arange(PAGE, dtype=torch.int64)[None, :]).reshape(-1)
+    rest = torch.randint(0, num_slots, (length - runs.numel(),), generator=gen, dtype=torch.int64)
+    return torch.cat([runs, rest]).to(torch.int32)
+
+
+# ------------------------------------------------------------- workloads
+
+def tiny_tp2(seed: int = 0, device="cpu", length: int = 64, fmt: str = "bf16") -> Workload:
+    """bs=1, 12Q/1KV, pool [4096, 1, 256], `length` uniform slots with replacement."""
+    num_slots = 4096
+    kc, vc, ks, vs = make_pools(num_slots, 1, fmt, seed, device)
+    g = _gen(seed, "cpu")
+    sel = uniform_indices(length, num_slots, g)
+    return Workload(make_query(1, 12, seed, device), kc, vc, sel.to(device),
+                    cu_from_lengths([length]).to(device), fmt, ks, vs,
+                    name=f"tiny_tp2_L{length}_{fmt}")
+
+
+def tp1_mixed(seed: int = 1, device="cpu", bs: int = 16, num_slots: int = 262144,
+              fmt: str = "bf16", max_len: int = MAX_CAPACITY, lengths=None) -> Workload:
+    """bs sequences, 24Q/2KV, lengths ~ U[1, max_len], uniform slot ids."""
+    kc, vc, ks, vs = make_pools(num_slots, 2, fmt, seed, device)
+    g = _gen(seed, "cpu")
+    if lengths is None:
+        lengths = torch.randint(1, max_len + 1, (bs,), generator=g, dtype=torch.int64)
+    lengths = torch.as_tensor(lengths, dtype=torch.int64)
+    sel = uniform_indices(int(lengths.sum()), num_slots, g)
+    return Workload(make_query(bs, 24, seed, device), kc, vc, sel.to(device),
+                    cu_from_lengths(lengths).to(device), fmt, ks, vs,
+                    capacity=max(int(lengths.max()), 1) if lengths.numel() else 1,
+                    name=f"tp1_mixed_bs{bs}_{fmt}")
+
+
+def tp1_saturated(seed: int = 2, device="cpu", bs: int = 128, num_slots: int = 1048576,
+                  fmt: str = "bf16", length: int = MAX_CAPACITY, index_seed: Optional[int] = None,
+                  pools=None) -> Workload:
+    """bs sequences of exactly `length` slots: page-aligned 64-slot runs + uniform slots.
+
+    `pools` may pass (k, v, k_scale, v_scale) already resident to build more
+    index sets over the same pool; `index_seed` varies the index draw only."""
+    if pools is None:
+        pools = make_pools(num_slots, 2, fmt, seed, device)
+    kc, vc, ks, vs = pools
+    g = _gen(seed if index_seed is None else index_seed, "cpu")
+    sel = torch.cat([runs_and_uniform_indices(length, kc.shape[0], g) for _ in range(bs)])
+    return Workload(make_query(bs, 24, seed if index_seed is None else index_seed, device),
+                    kc, vc, sel.to(device), cu_from_lengths([length] * bs).to(device), fmt, ks, vs,
+                    capacity=length, name=f"tp1_saturated_bs{bs}_L{length}_{fmt}")
+
+
+# ------------------------------------------- counter-based generator (replays)
+#
+# MurmurHash3's 32-bit finaliser (fmix32, A. Appleby, public domain) used as a
+# counter-based generator: every value is a pure function of (seed, replay,
+# b, j), so the same torch code regenerates a replay's lengths and slot ids
+# on the GPU inside a captured graph and on the host for the oracle.
+
+_M32 = 0xFFFFFFFF
+
+
+def _mul32(h, c: int):
+    """(h * c) mod 2^32 for h in [0, 2^32) (int or int64 tensor), without int64 overflow."""
+    lo = h & 0xFFFF
+    hi = h >> 16
+    return (lo * c + (((hi * (c & 0xFFFF)) & 0xFFFF) << 16)) & _M32
+
+
+def fmix32(h):
+    """MurmurHash3 fmix32 of h in [0, 2^32); works on Python ints and int64 tensors."""
+    h = h ^ (h >> 16)
+    h = _mul32(h, 0x85EBCA6B)
+    h = h ^ (h >> 13)
+    h = _mul32(h, 0xC2B2AE35)
+    h = h ^ (h >> 16)
+    return h
+
+
+def hash_key(seed: int, replay: torch.Tensor, b, j):
+    """fmix32 chain over (seed, replay, b, j) -> int64 values in [0, 2^32).
+
+    `seed` is a Python int; `replay`, `b`, `j` are int64 tensors (or ints)
+    that broadcast; no host<->device traffic happens here."""
+    h = fmix32((replay & _M32) ^ fmix32(int(seed) & _M32))
+    h = fmix32(h ^ (b & _M32))
+    return fmix32(h ^ ((j + 0x9E3779B9) & _M32))
+
+
+BANDS = {"short": (1, 64), "medium": (512, 1024), "saturated": (MAX_CAPACITY, MAX_CAPACITY)}
+
+
+def replay_lengths(seed: int, replay: torch.Tensor, bs: int, band: str, device) -> torch.Tensor:
+    """int64 [bs] lengths of one replay, uniform in the band (inclusive)."""
+    lo, hi = BANDS[band]
+    b = torch.arange(bs, dtype=torch.int64, device=device)
+    h = hash_key(seed, replay, b, -1)
+    return lo + h % (hi - lo + 1)
+
+
+def replay_inputs(seed: int, replay: torch.Tensor, bs: int, band: str, capacity: int,
+                  num_slots: int, sel_out: torch.Tensor, cu_out: torch.Tensor) -> None:
+    """Regenerate one replay's cu_seqlens and packed slot ids in place.
+
+    Everything is torch tensor ops without host readback, so it can run inside
+    a captured CUDA graph; `replay` is a 1-element int64 device tensor.
+    `sel_out` holds bs*capacity ids; entries past cu[bs] are left stale."""
+    dev = sel_out.device
+    lens = replay_lengths(seed, replay, bs, band, dev)
+    cu = torch.zeros(bs + 1, dtype=torch.int64, device=dev)
+    cu[1:] = torch.cumsum(lens, 0)
+    cu_out.copy_(cu.to(torch.int32))
+    pos = torch.arange(bs * capacity, dtype=torch.int64, device=dev)
+    b = torch.searchsorted(cu[1:], pos, right=True).clamp_(max=bs - 1)
+    j = pos - cu[b]
+    ids = hash_key(seed, replay, b, j) % num_slots
+    live = pos < cu[bs]
+    sel_out.copy_(torch.where(live, ids, torch.zeros_like(ids)).to(torch.int32))
