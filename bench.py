@@ -1,0 +1,312 @@
+"""Benchmark: packed QSA decode at bs=128, L=2055, TP1 (24Q/2KV), D=256.
+
+One step = one qsa_decode call over one batch (every selected K/V row
+gathered, QK, softmax, PV, split merge). Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--fmt bf16|fp8_e4m3|int8|int4]
+                  [--impl native|reference]
+
+--impl reference times the FP64 CPU oracle on the host cores on a bounded
+sample of the same workload (the deliberately slow baseline).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from sparse_attention_paged_qsa_gb300 import inputs as I  # noqa: E402
+
+METRIC = "selected-KV HBM GB/s (% of GB300 peak) & qsa_decode calls/s at bs=128, L=2055"
+BS, L, HQ, HKV, SLOTS = 128, I.MAX_CAPACITY, 24, 2, 1048576
+ROW_BYTES = {"bf16": 512, "fp8_e4m3": 256, "int8": 256, "int4": 128}
+SCALE_BYTES = {"bf16": 0, "fp8_e4m3": 0, "int8": 4, "int4": 4}
+
+
+def algorithmic_bytes(fmt: str, bs: int = BS, length: int = L, hq: int = HQ) -> int:
+    """Bytes one call must move: every selected K and V row (with its per-slot
+    scales), the slot ids, q, out and cu_seqlens (per-pool fp8 scales: 8 B)."""
+    hkv = hq // 12
+    kv = bs * hkv * length * 2 * (ROW_BYTES[fmt] + SCALE_BYTES[fmt])
+    idx = bs * length * 4
+    q = out = bs * hq * 256 * 2
+    cu = (bs + 1) * 4
+    extra = 8 if fmt == "fp8_e4m3" else 0
+    return kv + idx + q + out + cu + extra
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.samples = []
+        self._stop = threading.Event()
+        self._t = None
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                out = subprocess.run(
+                    ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                     "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=5)
+                parts = [p.strip() for p in out.stdout.strip().split(",")]
+                if len(parts) == 6:
+                    self.samples.append(parts)
+            except Exception:
+                pass
+            self._stop.wait(0.2)
+
+    def __enter__(self):
+        self._t = threading.Thread(target=self._run, daemon=True)
+        self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        self._stop.set()
+        if self._t:
+            self._t.join(timeout=10)
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = sorted(float(s[0]) for s in self.samples if s[0].replace(".", "").isdigit())
+        mx = max((float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()), default=None)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in self.samples for i in range(4)
+                          if "Active" in s[2 + i] and "Not" not in s[2 + i]})
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": mx, "reasons": reasons,
+                "samples": len(self.samples)}
+
+
+def cpu_baseline(fmt: str, sample_rows: int, work, threads: int = 0):
+    """Time the FP64 oracle on `sample_rows` sequences of the workload; returns a dict."""
+    import oracle
+
+    sub = I.host_subset(work, list(range(sample_rows)))
+    t0 = time.perf_counter()
+    oracle.decode(sub.q, sub.k_pool, sub.v_pool, fmt, sub.sel, sub.cu, sub.softmax_scale,
+                  sub.k_scale, sub.v_scale, threads=threads)
+    dt = time.perf_counter() - t0
+    b = algorithmic_bytes(fmt, bs=sample_rows)
+    return {"value": b / dt / 1e9, "unit": "GB/s", "cores": oracle.max_threads(),
+            "kind": "oracle", "calls_per_s": (sample_rows / BS) / dt,
+            "sample": f"{sample_rows} of {BS} sequences (L={L}, 24Q/2KV), {dt:.2f} s, "
+                      "scaled to bytes of the full call"}
+
+
+def run_reference(args):
+    ws, rank, local = dist_env()
+    if rank != 0:
+        return
+    import oracle
+
+    oracle.build()
+    gen_dev = "cpu"
+    rows = args.ref_rows
+    # host-only generation of exactly the sampled sequences' data
+    w = I.tp1_saturated(seed=2, device=gen_dev, fmt=args.fmt, bs=rows, num_slots=SLOTS // 8)
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle.decode(w.q, w.k_pool, w.v_pool, args.fmt, w.sel, w.cu, w.softmax_scale,
+                      w.k_scale, w.v_scale)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    dt = sum(times) / len(times)
+    gbs = algorithmic_bytes(args.fmt, bs=rows) / dt / 1e9
+    calls = (rows / BS) / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "calls_per_s": calls, "tokens_per_s": calls * BS * L,
+        "config": {"workload": f"packed QSA decode bs={BS} L={L} 24Q/2KV D=256 {args.fmt} pool",
+                   "sample_sequences_per_step": rows, "pool_slots": SLOTS // 8},
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": oracle.max_threads(),
+                         "kind": "oracle",
+                         "sample": f"{rows} of {BS} sequences per step, scaled by bytes"},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_native(args):
+    import sparse_attention_paged_qsa_gb300 as qsa
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    fmt = args.fmt
+    pools = I.make_pools(SLOTS, HKV, fmt, seed=2 + rank, device=dev)
+    works = [I.tp1_saturated(seed=2 + rank, device=dev, fmt=fmt, index_seed=100 + 7 * rank + k,
+                             pools=pools) for k in range(args.index_sets)]
+    w0 = works[0]
+    out = torch.empty_like(w0.q)
+    scratch = qsa.alloc_scratch(BS, HQ, L, dev)
+    meta = qsa.KVQuantMeta(fmt, L, w0.k_scale, w0.v_scale, w0.softmax_scale)
+    stream = torch.cuda.current_stream()
+    grid = qsa.qsa_decode_grid(BS, HQ, L)
+
+    def step(k):
+        w = works[k % len(works)]
+        qsa.qsa_decode(w.q, w.k_pool, w.v_pool, meta, w.sel, w.cu, out, scratch, stream)
+
+    for k in range(args.warmup):
+        step(k)
+    torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        ev[0].record(stream)
+        for k in range(args.steps):
+            step(k)
+            ev[k + 1].record(stream)
+        torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    per = [ev[k].elapsed_time(ev[k + 1]) for k in range(args.steps)]
+    total_ms = ev[0].elapsed_time(ev[-1])
+    err = qsa.qsa_scratch_error(scratch)
+    if err:
+        raise RuntimeError(f"device error flags {err}")
+
+    # e2e: host (pinned) q / slot ids / cu_seqlens -> device, decode, output -> host
+    hq_ = [w.q.cpu().pin_memory() for w in works]
+    hsel = [w.sel.cpu().pin_memory() for w in works]
+    hcu = [w.cu.cpu().pin_memory() for w in works]
+    hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    dq, dsel, dcu = torch.empty_like(w0.q), torch.empty_like(w0.sel), torch.empty_like(w0.cu)
+
+    def e2e_step(k):
+        j = k % len(works)
+        dq.copy_(hq_[j], non_blocking=True)
+        dsel.copy_(hsel[j], non_blocking=True)
+        dcu.copy_(hcu[j], non_blocking=True)
+        qsa.qsa_decode(dq, w0.k_pool, w0.v_pool, meta, dsel, dcu, out, scratch, stream)
+        hout.copy_(out, non_blocking=True)
+
+    for k in range(args.warmup):
+        e2e_step(k)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for k in range(args.steps):
+        e2e_step(k)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    h2d = hq_[0].numel() * 2 + hsel[0].numel() * 4 + hcu[0].numel() * 4
+    d2h = hout.numel() * 2
+
+    step_ms = total_ms / args.steps
+    if ws > 1:
+        t = torch.tensor([step_ms, e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        step_ms, e2e_ms = float(t[0]), float(t[1])
+    abytes = algorithmic_bytes(fmt)
+    value = ws * abytes / (step_ms * 1e-3) / 1e9
+    e2e_val = ws * abytes / (e2e_ms * 1e-3) / 1e9
+    kernel_ms = sum(per) / len(per)
+    achieved = abytes / (kernel_ms * 1e-3) / 1e9
+    peak, peak_kind = measured_peaks()
+    calls = ws / (step_ms * 1e-3)
+
+    cpu = None
+    if rank == 0 and args.cpu_rows > 0:
+        import oracle
+
+        oracle.build()
+        cpu = cpu_baseline(fmt, args.cpu_rows, works[0])
+
+    if rank == 0:
+        traffic = None
+        tpath = os.path.join(ROOT, "profiles", f"traffic_{fmt}.json")
+        if os.path.exists(tpath):
+            with open(tpath) as f:
+                traffic = json.load(f).get("bytes_per_launch")
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": fmt, "data": "synthetic",
+            "calls_per_s": calls, "tokens_per_s": calls * BS * L,
+            "pct_of_hbm_peak": 100.0 * achieved / peak,
+            "config": {"workload": f"packed QSA decode bs={BS} L={L} 24Q/2KV D=256 {fmt} pool",
+                       "pool_slots": SLOTS, "index_sets": args.index_sets, "grid_ctas": grid,
+                       "l2": "inputs larger than L2: 538 MB of K/V rows per call from a 2 GiB "
+                             "pool, rotating index sets",
+                       "parallelism": f"replicas x{ws}"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "peak_source": f"{peak_kind} hbm_gbs",
+                         "bytes_per_launch": abytes, "kernel_ms": kernel_ms},
+            "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": args.steps,
+            "clocks": clk.summary(),
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--fmt", default="bf16", choices=list(I.FORMATS))
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--index-sets", type=int, default=3)
+    ap.add_argument("--cpu-rows", type=int, default=128,
+                    help="sequences of the oracle CPU-baseline sample (0 disables)")
+    ap.add_argument("--ref-rows", type=int, default=8,
+                    help="sequences per step of the --impl reference sample")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_native(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,175 @@
+/*
+ * qsa.h -- C ABI of libqsa: packed Qwen-sparse-attention (QSA) decode over a
+ * paged, optionally quantised K/V pool, on one NVIDIA GB300 (sm_103a).
+ *
+ * The operation (sglang PR #36845 "fix(qsa): restore SM121 correctness",
+ * sections "Changes" and "Optimized kernel"; sglang PR #37798 "quantized KV
+ * pools with dequant-on-gather", section "Modifications"):
+ *
+ *   For every sequence b (one BF16 query token, Hq heads, head dim 256) with
+ *   L_b = cu_seqlens[b+1] - cu_seqlens[b] selected token slots
+ *   I_j = sel_indices[cu_seqlens[b] + j] (order and duplicates kept), and
+ *   every query head h, whose KV head is g = h / 12 (12:1 GQA):
+ *
+ *     out[b,h,:] = sum_j softmax_j(softmax_scale * q[b,h,:] . K[I_j,g,:]) V[I_j,g,:]
+ *
+ *   with K/V dequantised from the pool format on gather. L_b == 0 gives a
+ *   zero row. Supported geometry (the pages' contract): BF16 query/output,
+ *   D = 256, Hq = 24 with Hkv = 2 (TP1) or Hq = 12 with Hkv = 1 (TP2),
+ *   1 <= bs <= 128, 1 <= capacity <= 2055 selected slots per sequence.
+ *   Calls outside it fail with QSA_ERR_UNSUPPORTED and a descriptive message.
+ *
+ * Ownership and ordering. The caller owns every buffer. The library never
+ * allocates, frees or synchronises inside qsa_decode: it validates the
+ * descriptors on the host (reading no device memory) and enqueues exactly one
+ * kernel on `stream`. Live lengths are read from cu_seqlens on the device,
+ * so a captured CUDA graph stays valid when cu_seqlens and sel_indices
+ * change between replays.
+ *
+ * Scratch. A caller-owned device buffer of qsa_decode_scratch_bytes() bytes,
+ * zeroed once with qsa_scratch_init(). It holds a sticky device error word,
+ * one arrival counter per (sequence, KV head) -- zero before and after every
+ * launch, the kernel resets them in the same launch -- and the split-KV
+ * partial results. Launches that share a scratch buffer must be ordered
+ * (same stream or explicit dependencies).
+ */
+#ifndef QSA_H_
+#define QSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element types of qsa_tensor.dtype. */
+enum {
+    QSA_DTYPE_BF16 = 1,
+    QSA_DTYPE_UINT8 = 2, /* fp8 e4m3fn codes and packed int4 nibbles */
+    QSA_DTYPE_INT8 = 3,
+    QSA_DTYPE_INT32 = 4,
+    QSA_DTYPE_FLOAT32 = 5
+};
+
+/* K/V pool formats (qsa_kv_quant_meta.format), sglang PR #37798, "Modifications". */
+enum {
+    QSA_KV_BF16 = 0,     /* [slots, Hkv, 256] bf16 */
+    QSA_KV_FP8_E4M3 = 1, /* [slots, Hkv, 256] uint8 e4m3fn codes, one fp32 scale per pool */
+    QSA_KV_INT8 = 2,     /* [slots, Hkv, 256] int8, fp32 scale per (slot, KV head) */
+    QSA_KV_INT4 = 3      /* [slots, Hkv, 128] uint8: two's-complement nibbles, channel 2i
+                            in the low nibble, fp32 scale per (slot, KV head) */
+};
+
+/* Return codes. Nothing is enqueued when a call returns an error. */
+enum {
+    QSA_OK = 0,
+    QSA_ERR_INVALID_ARGUMENT = -1, /* NULL pointer, dtype/ndim/shape/stride mismatch */
+    QSA_ERR_UNSUPPORTED = -2,      /* well-formed but outside the decode contract */
+    QSA_ERR_SCRATCH_TOO_SMALL = -3,
+    QSA_ERR_MISALIGNED = -4,       /* a base address or stride breaks 16-byte alignment */
+    QSA_ERR_CUDA = -5              /* a CUDA runtime call or the launch failed */
+};
+
+/* Bits of the sticky device error word (see qsa_scratch_error). Bad data
+ * never traps or hangs the GPU: the kernel records it and carries on with a
+ * safe substitute, and the affected sequences' outputs are unspecified. */
+enum {
+    QSA_DEVERR_SLOT_RANGE = 1, /* a selected slot id outside [0, num_slots); slot 0 read instead */
+    QSA_DEVERR_CU_SEQLENS = 2, /* cu_seqlens decreasing, negative, past the index buffer,
+                                  or a length above capacity; the length is clamped */
+    QSA_DEVERR_TIMEOUT = 4     /* an internal pipeline wait exceeded its limit (a library
+                                  fault, not a data fault); the launch gave up early */
+};
+
+/* A strided view of caller memory. `data` is a device pointer for
+ * qsa_decode; strides are in elements. */
+typedef struct {
+    void* data;
+    int32_t dtype;
+    int32_t ndim;
+    int64_t shape[4];
+    int64_t stride[4];
+} qsa_tensor;
+
+/* Pool format and softmax parameters of one call. */
+typedef struct {
+    int32_t format;       /* QSA_KV_* */
+    int32_t capacity;     /* max selected slots per sequence, 1..2055; bounds the split plan */
+    const float* k_scale; /* device; fp8: [1]; int8/int4: [slots * Hkv]; bf16: NULL */
+    const float* v_scale; /* same layout as k_scale */
+    float softmax_scale;  /* finite; 1/16 = 1/sqrt(256) for the pages' model */
+    int32_t max_ctas;     /* 0: library chooses the grid; > 0: cap on CTAs (e.g. 1 forces
+                             one CTA to do all the work, which tests the no-split path) */
+} qsa_kv_quant_meta;
+
+/*
+ * qsa_decode -- enqueue one packed QSA decode.
+ *
+ *  q           bf16 [bs, Hq, 256]; stride[2] == 1; stride[0], stride[1] multiples of 8;
+ *              base 16-byte aligned.
+ *  k_pool,     [num_slots, Hkv, row] contiguous; row = 256 elements (bf16, fp8 as
+ *  v_pool      uint8, int8) or 128 bytes (int4 as uint8); identical shapes; base 16-byte
+ *              aligned. Row (slot, g) is read whole, once per selecting (sequence, g).
+ *  kv_quant_meta  format, scales, softmax scale, capacity, optional CTA cap.
+ *  sel_indices int32 [n_sel], contiguous: the packed selected slot ids.
+ *  cu_seqlens  int32 [bs + 1], device, read on the device only.
+ *  out         bf16 [bs, Hq, 256]; stride[2] == 1; stride[0], stride[1] multiples of 8;
+ *              base 16-byte aligned. Fully written (zeros for empty selections).
+ *  scratch     device buffer of at least qsa_decode_scratch_bytes(bs, Hq, capacity)
+ *              bytes, 256-byte aligned, initialised once by qsa_scratch_init.
+ *  stream      cudaStream_t (NULL: the legacy default stream).
+ *
+ * Returns QSA_OK or a negative QSA_ERR_*; see qsa_last_error_message().
+ */
+int qsa_decode(const qsa_tensor* q, const qsa_tensor* k_pool, const qsa_tensor* v_pool,
+               const qsa_kv_quant_meta* kv_quant_meta, const qsa_tensor* sel_indices,
+               const qsa_tensor* cu_seqlens, const qsa_tensor* out, void* scratch,
+               size_t scratch_bytes, void* stream);
+
+/* Scratch bytes a qsa_decode call with these sizes needs on the current
+ * device (0 when the sizes are outside the contract). Split-KV partials take
+ * two 12 KiB slots per CTA of the grid the library would choose. */
+size_t qsa_decode_scratch_bytes(int32_t bs, int32_t num_q_heads, int32_t capacity);
+
+/* Number of CTAs qsa_decode launches for these sizes on the current device
+ * (after applying max_ctas when > 0); negative QSA_ERR_* on bad sizes. */
+int32_t qsa_decode_grid(int32_t bs, int32_t num_q_heads, int32_t capacity, int32_t max_ctas);
+
+/* Offsets of the scratch regions, for callers that inspect them (tests):
+ * the error word (int32), the counters (int32 [bs * Hkv]) and the partials. */
+typedef struct {
+    size_t error_word_offset;
+    size_t counters_offset;
+    size_t counters_count;
+    size_t partials_offset;
+    size_t partial_slot_bytes;
+    size_t total_bytes;
+} qsa_scratch_layout;
+
+int qsa_decode_scratch_layout(int32_t bs, int32_t num_q_heads, int32_t capacity,
+                              qsa_scratch_layout* layout);
+
+/* Zero a scratch buffer (cudaMemsetAsync on `stream`). Call once after
+ * allocating it; counters then stay zero across launches by themselves. */
+int qsa_scratch_init(void* scratch, size_t scratch_bytes, void* stream);
+
+/* Read the sticky device error word into *flags (QSA_DEVERR_* bits). This
+ * is the library's only device readback: it copies 4 bytes on `stream` and
+ * synchronises that stream. With clear != 0 the word is reset to zero. */
+int qsa_scratch_error(const void* scratch, int32_t* flags, int32_t clear, void* stream);
+
+/* Static description of a return code. */
+const char* qsa_strerror(int code);
+
+/* Descriptive message of the last failing call on this host thread ("" if none). */
+const char* qsa_last_error_message(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int qsa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QSA_H_ */

@@ -1,0 +1,24 @@
+"""Packed Qwen-sparse-attention (QSA) decode for NVIDIA GB300 (sm_103a).
+
+The compute lives in libqsa.so (CUDA kernels behind the C ABI declared in
+include/qsa.h); ``binding`` marshals torch tensors into that ABI, and
+``inputs`` generates seeded synthetic workloads.
+"""
+from .binding import (  # noqa: F401
+    KVQuantMeta,
+    QsaError,
+    alloc_scratch,
+    qsa_decode,
+    qsa_decode_grid,
+    qsa_decode_scratch_bytes,
+    qsa_decode_scratch_layout,
+    qsa_scratch_error,
+    qsa_scratch_init,
+    version,
+)
+
+__all__ = [
+    "KVQuantMeta", "QsaError", "alloc_scratch", "qsa_decode", "qsa_decode_grid",
+    "qsa_decode_scratch_bytes", "qsa_decode_scratch_layout", "qsa_scratch_error",
+    "qsa_scratch_init", "version",
+]

@@ -1,0 +1,211 @@
+"""Thin ctypes binding over libqsa (include/qsa.h).
+
+Argument marshalling only: torch tensors are described by pointer, dtype,
+shape and strides and handed to the C ABI; every step of the decode runs in
+the library's CUDA kernel. There is no fallback path: if libqsa.so is missing
+the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libqsa.so")
+
+# include/qsa.h enums
+DTYPE_BF16, DTYPE_UINT8, DTYPE_INT8, DTYPE_INT32, DTYPE_FLOAT32 = 1, 2, 3, 4, 5
+KV_FORMATS = {"bf16": 0, "fp8_e4m3": 1, "int8": 2, "int4": 3}
+OK, ERR_INVALID_ARGUMENT, ERR_UNSUPPORTED, ERR_SCRATCH_TOO_SMALL, ERR_MISALIGNED, ERR_CUDA = (
+    0, -1, -2, -3, -4, -5)
+DEVERR_SLOT_RANGE, DEVERR_CU_SEQLENS, DEVERR_TIMEOUT = 1, 2, 4
+
+_TORCH_DTYPES = {
+    torch.bfloat16: DTYPE_BF16,
+    torch.uint8: DTYPE_UINT8,
+    torch.int8: DTYPE_INT8,
+    torch.int32: DTYPE_INT32,
+    torch.float32: DTYPE_FLOAT32,
+}
+
+EXPORTED = (
+    "qsa_decode", "qsa_decode_scratch_bytes", "qsa_decode_grid", "qsa_decode_scratch_layout",
+    "qsa_scratch_init", "qsa_scratch_error", "qsa_strerror", "qsa_last_error_message",
+    "qsa_version",
+)
+
+
+class QsaTensor(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * 4), ("stride", ctypes.c_int64 * 4)]
+
+
+class QsaKvQuantMeta(ctypes.Structure):
+    _fields_ = [("format", ctypes.c_int32), ("capacity", ctypes.c_int32),
+                ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
+                ("softmax_scale", ctypes.c_float), ("max_ctas", ctypes.c_int32)]
+
+
+class QsaScratchLayout(ctypes.Structure):
+    _fields_ = [("error_word_offset", ctypes.c_size_t), ("counters_offset", ctypes.c_size_t),
+                ("counters_count", ctypes.c_size_t), ("partials_offset", ctypes.c_size_t),
+                ("partial_slot_bytes", ctypes.c_size_t), ("total_bytes", ctypes.c_size_t)]
+
+
+class QsaError(RuntimeError):
+    def __init__(self, code: int, message: str):
+        super().__init__(f"{message} (code {code})")
+        self.code = code
+
+
+_lib = None
+
+
+def load() -> ctypes.CDLL:
+    """Load libqsa.so from the package directory (raises if it was not built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                           "(nvcc, sm_103a); there is no CPU fallback")
+    lib = ctypes.CDLL(LIB_PATH)
+    P = ctypes.POINTER
+    lib.qsa_decode.restype = ctypes.c_int
+    lib.qsa_decode.argtypes = [P(QsaTensor), P(QsaTensor), P(QsaTensor), P(QsaKvQuantMeta),
+                               P(QsaTensor), P(QsaTensor), P(QsaTensor), ctypes.c_void_p,
+                               ctypes.c_size_t, ctypes.c_void_p]
+    lib.qsa_decode_scratch_bytes.restype = ctypes.c_size_t
+    lib.qsa_decode_scratch_bytes.argtypes = [ctypes.c_int32] * 3
+    lib.qsa_decode_grid.restype = ctypes.c_int32
+    lib.qsa_decode_grid.argtypes = [ctypes.c_int32] * 4
+    lib.qsa_decode_scratch_layout.restype = ctypes.c_int
+    lib.qsa_decode_scratch_layout.argtypes = [ctypes.c_int32] * 3 + [P(QsaScratchLayout)]
+    lib.qsa_scratch_init.restype = ctypes.c_int
+    lib.qsa_scratch_init.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    lib.qsa_scratch_error.restype = ctypes.c_int
+    lib.qsa_scratch_error.argtypes = [ctypes.c_void_p, P(ctypes.c_int32), ctypes.c_int32,
+                                      ctypes.c_void_p]
+    lib.qsa_strerror.restype = ctypes.c_char_p
+    lib.qsa_strerror.argtypes = [ctypes.c_int]
+    lib.qsa_last_error_message.restype = ctypes.c_char_p
+    lib.qsa_last_error_message.argtypes = []
+    lib.qsa_version.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def _check(rc: int) -> None:
+    if rc != OK:
+        lib = load()
+        msg = lib.qsa_last_error_message().decode() or lib.qsa_strerror(rc).decode()
+        raise QsaError(rc, msg)
+
+
+def describe(t: Optional[torch.Tensor]) -> QsaTensor:
+    """qsa_tensor view of a torch tensor (no copy)."""
+    d = QsaTensor()
+    if t is None:
+        return d
+    if t.dim() > 4:
+        raise ValueError("at most 4 dimensions")
+    d.data = t.data_ptr() if t.numel() else None
+    d.dtype = _TORCH_DTYPES.get(t.dtype, 0)
+    d.ndim = t.dim()
+    for i in range(t.dim()):
+        d.shape[i] = t.shape[i]
+        d.stride[i] = t.stride(i)
+    return d
+
+
+@dataclass
+class KVQuantMeta:
+    """Python mirror of qsa_kv_quant_meta."""
+
+    format: str = "bf16"
+    capacity: int = 2055
+    k_scale: Optional[torch.Tensor] = None
+    v_scale: Optional[torch.Tensor] = None
+    softmax_scale: float = 1.0 / 16.0
+    max_ctas: int = 0
+
+    def to_c(self) -> QsaKvQuantMeta:
+        m = QsaKvQuantMeta()
+        m.format = KV_FORMATS[self.format]
+        m.capacity = int(self.capacity)
+        m.k_scale = self.k_scale.data_ptr() if self.k_scale is not None else None
+        m.v_scale = self.v_scale.data_ptr() if self.v_scale is not None else None
+        m.softmax_scale = float(self.softmax_scale)
+        m.max_ctas = int(self.max_ctas)
+        return m
+
+
+def _stream_handle(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else None
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def qsa_decode(q, k_pool, v_pool, kv_quant_meta: KVQuantMeta, sel_indices, cu_seqlens, out,
+               scratch, stream=None) -> None:
+    """Enqueue one packed QSA decode (see include/qsa.h). Raises QsaError on a contract error."""
+    lib = load()
+    meta = kv_quant_meta.to_c()
+    args = [describe(t) for t in (q, k_pool, v_pool)]
+    sel_d, cu_d, out_d = describe(sel_indices), describe(cu_seqlens), describe(out)
+    rc = lib.qsa_decode(ctypes.byref(args[0]), ctypes.byref(args[1]), ctypes.byref(args[2]),
+                        ctypes.byref(meta), ctypes.byref(sel_d), ctypes.byref(cu_d),
+                        ctypes.byref(out_d), scratch.data_ptr() if scratch is not None else None,
+                        scratch.numel() * scratch.element_size() if scratch is not None else 0,
+                        _stream_handle(stream))
+    _check(rc)
+
+
+def qsa_decode_scratch_bytes(bs: int, num_q_heads: int, capacity: int) -> int:
+    n = load().qsa_decode_scratch_bytes(bs, num_q_heads, capacity)
+    if n == 0:
+        _check(ERR_UNSUPPORTED)
+    return n
+
+
+def qsa_decode_grid(bs: int, num_q_heads: int, capacity: int, max_ctas: int = 0) -> int:
+    g = load().qsa_decode_grid(bs, num_q_heads, capacity, max_ctas)
+    if g < 0:
+        _check(g)
+    return g
+
+
+def qsa_decode_scratch_layout(bs: int, num_q_heads: int, capacity: int) -> dict:
+    ly = QsaScratchLayout()
+    _check(load().qsa_decode_scratch_layout(bs, num_q_heads, capacity, ctypes.byref(ly)))
+    return {k: getattr(ly, k) for k, _ in QsaScratchLayout._fields_}
+
+
+def qsa_scratch_init(scratch: torch.Tensor, stream=None) -> None:
+    _check(load().qsa_scratch_init(scratch.data_ptr(), scratch.numel() * scratch.element_size(),
+                                   _stream_handle(stream)))
+
+
+def qsa_scratch_error(scratch: torch.Tensor, clear: bool = False, stream=None) -> int:
+    flags = ctypes.c_int32(0)
+    _check(load().qsa_scratch_error(scratch.data_ptr(), ctypes.byref(flags), int(clear),
+                                    _stream_handle(stream)))
+    return flags.value
+
+
+def alloc_scratch(bs: int, num_q_heads: int, capacity: int, device=None) -> torch.Tensor:
+    """Allocate (torch caching allocator) and zero a scratch buffer for these sizes."""
+    n = qsa_decode_scratch_bytes(bs, num_q_heads, capacity)
+    buf = torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+    qsa_scratch_init(buf)
+    return buf
+
+
+def version() -> int:
+    return load().qsa_version()

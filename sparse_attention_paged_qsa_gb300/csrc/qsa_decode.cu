@@ -1,0 +1,1272 @@
+// Packed QSA decode for NVIDIA GB300 (sm_103a): one launch per call.
+//
+// What it computes (sglang PR #36845 "fix(qsa): restore SM121 correctness",
+// "Changes" and "Optimized kernel"; sglang PR #37798 "quantized KV pools with
+// dequant-on-gather", "Modifications"): for each sequence b and query head h
+// (KV head g = h / 12), out = softmax(scale * q . K[I]^T) V[I] over the
+// selected slots I = sel[cu[b] : cu[b+1]], duplicates and order kept, with the
+// pool rows dequantised on gather. The page's design points kept here: the 12
+// query heads of one KV head share one CTA so every K/V row is read once,
+// tensor-core QK/PV with FP32 online-softmax state, split-KV across CTAs, and
+// a same-launch FP32 log-sum-exp merge whose arrival counter is reset by the
+// merging CTA. Lengths are read from cu_seqlens on the device.
+//
+// GB300 design:
+//  * Persistent, balanced grid: the (sequence, KV head, token) space of the
+//    live lengths is cut into gridDim.x equal token ranges on the device, so
+//    a fixed (graph-captured) grid balances any length mix. A CTA whose range
+//    covers a whole (sequence, KV head) segment writes the output directly;
+//    segments cut between CTAs are merged by the last arriving CTA.
+//  * One producer warp gathers whole K/V rows with per-row bulk async copies
+//    (cp.async.bulk, the TMA engine) into a multi-stage shared-memory ring
+//    completed on mbarriers; slot ids are prefetched several stages ahead.
+//  * Four consumer warps: QK on mma.m16n8k16 (12 heads padded to 16 rows,
+//    8 tokens per warp), a per-stage max exchange with lazy rescaling, and
+//    PV computed transposed (O^T = V^T P^T) with P split into bf16 hi + lo
+//    columns (24 columns: 12 heads x {hi, lo}), each warp owning 64 of the
+//    256 output dims.
+//  * Quantised pools are converted exactly to bf16 in shared memory by the
+//    warp that consumes them; per-slot scales scale the scores (K) and the
+//    probabilities (V) in FP32, per-pool fp8 scales fold into constants.
+//  * Every wait is bounded; bad slot ids / cu_seqlens set a sticky error
+//    word and are clamped, never trapped.
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <initializer_list>
+#include <mutex>
+#include <string>
+
+#include "qsa.h"
+
+namespace qsa {
+
+constexpr int D = 256;
+constexpr int GROUP = 12;               // query heads per KV head
+constexpr int T = 32;                   // tokens per pipeline stage
+constexpr int NW = 4;                   // consumer warps
+constexpr int NTHREADS = (NW + 1) * 32; // + one producer warp
+constexpr int NCT = NW * 32;            // consumer threads
+constexpr int MT = D / NW / 16;         // 16-dim m-tiles per consumer warp in PV
+constexpr int BF_RS = 528;              // smem row stride of bf16 rows (512 + 16 pad)
+constexpr int PRS = T * 2 + 16;         // smem row stride of P^T rows (bytes)
+constexpr int OS_STRIDE = D + 4;        // epilogue rows (floats)
+constexpr float TAU = 8.0f;             // lazy-rescale threshold (log2 units)
+constexpr int MAX_BS = 128;
+constexpr int MAX_CAPACITY = 2055;
+constexpr int MIN_TOKENS_PER_CTA = 64;
+constexpr int PART_O_BYTES = GROUP * D * 4;           // unnormalised O, fp32
+constexpr int PART_BYTES = 12416;                     // O + m[12] + l[12], 128-byte multiple
+constexpr long long WAIT_NS = 2000000000LL;           // bounded-wait limit (2 s)
+constexpr int BAR_CONSUMERS = 1;                      // named barrier id
+
+template <int FMT> struct Traits;
+template <> struct Traits<QSA_KV_BF16> {
+    static constexpr int ROWB = 512, RS = 528, STAGES = 4;
+    static constexpr bool DEQ = false, SCALES = false;
+};
+template <> struct Traits<QSA_KV_FP8_E4M3> {
+    static constexpr int ROWB = 256, RS = 272, STAGES = 8;
+    static constexpr bool DEQ = true, SCALES = false;
+};
+template <> struct Traits<QSA_KV_INT8> {
+    static constexpr int ROWB = 256, RS = 272, STAGES = 8;
+    static constexpr bool DEQ = true, SCALES = true;
+};
+template <> struct Traits<QSA_KV_INT4> {
+    static constexpr int ROWB = 128, RS = 144, STAGES = 12;
+    static constexpr bool DEQ = true, SCALES = true;
+};
+
+template <int FMT> struct Layout {
+    using Tr = Traits<FMT>;
+    static constexpr int STAGE_KV = T * Tr::RS;
+    static constexpr int STAGE_SC = Tr::SCALES ? 2 * T * 4 : 0;
+    static constexpr int STAGE_BYTES = 2 * STAGE_KV + STAGE_SC;
+    static constexpr int PF = Tr::STAGES;       // slot-id prefetch distance (stages)
+    static constexpr int R = PF + 1;            // slot-id ring entries
+    static constexpr int off_stage = 0;
+    static constexpr int off_kbf = off_stage + Tr::STAGES * STAGE_BYTES;
+    static constexpr int kbf_bytes = Tr::DEQ ? 2 * T * BF_RS : 0;
+    static constexpr int off_q = off_kbf + kbf_bytes;
+    static constexpr int off_p = off_q + 2 * 16 * BF_RS;
+    static constexpr int off_os = off_p + 2 * 24 * PRS;
+    static constexpr int off_red = off_os + GROUP * OS_STRIDE * 4;
+    static constexpr int off_mref = off_red + 2 * NW * 16 * 4;
+    static constexpr int off_lred = off_mref + 2 * 16 * 4;
+    static constexpr int off_ring = off_lred + NW * 16 * 4;
+    static constexpr int off_segL = off_ring + R * T * 4;
+    static constexpr int off_segSrc = off_segL + (MAX_BS + 4) * 4;
+    static constexpr int off_segP = off_segSrc + (MAX_BS + 4) * 4;
+    static constexpr int off_misc = off_segP + (MAX_BS + 4) * 4;
+    static constexpr int off_bar = off_misc + 64 * 4;
+    static constexpr int n_bars = 2 * Tr::STAGES + 4;
+    static constexpr int TOTAL = off_bar + n_bars * 8;
+    static_assert(TOTAL <= 227 * 1024, "shared memory budget");
+    static_assert(STAGE_BYTES % 16 == 0 && off_kbf % 16 == 0 && off_q % 16 == 0, "alignment");
+};
+
+struct Params {
+    const __nv_bfloat16* q;
+    long long q_sb, q_sh;
+    const uint8_t* kpool;
+    const uint8_t* vpool;
+    long long num_slots;
+    const float* k_scale;
+    const float* v_scale;
+    const int* sel;
+    long long n_sel;
+    const int* cu;
+    __nv_bfloat16* out;
+    long long o_sb, o_sh;
+    int* err;
+    int* cnt;
+    uint8_t* part;
+    int bs, Hkv, capacity;
+    float scale_log2; // softmax_scale * log2(e)
+};
+
+// ------------------------------------------------------------------ PTX helpers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* ptr) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(ptr));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    [[maybe_unused]] uint64_t state;
+    asm volatile("mbarrier.arrive.shared::cta.b64 %0, [%1];" : "=l"(state) : "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    [[maybe_unused]] uint64_t state;
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 %0, [%1], %2;"
+                 : "=l"(state)
+                 : "r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long globaltimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for the phase with `parity` of an mbarrier, for at most WAIT_NS. On
+// timeout, record QSA_DEVERR_TIMEOUT, raise the CTA abort flag and return false.
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* err,
+                                       volatile int* abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer() - t0 > (unsigned long long)WAIT_NS) {
+                atomicOr(err, QSA_DEVERR_TIMEOUT);
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N> __device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void fence_mbarrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void consumer_sync() {
+    asm volatile("bar.sync %0, %1;" ::"n"(BAR_CONSUMERS), "n"(NCT) : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3,
+                                        uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3,
+                                          uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t& r0, uint32_t& r1, uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];"
+                 : "=r"(r0), "=r"(r1)
+                 : "r"(addr));
+}
+
+// D += A(16x16, row) * B(16x8, col), bf16 inputs, fp32 accumulators.
+__device__ __forceinline__ void mma_bf16(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+// ------------------------------------------------------------ exact dequant
+
+// OCP e4m3fn byte -> float, exactly. The 7 magnitude bits placed at binary32
+// bits [26:20] encode value * 2^-120 for normals and subnormals alike
+// (exponent bias 127 vs 7); multiplying by 2^120 restores the value. The
+// all-ones magnitude is NaN in e4m3fn.
+__device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
+    const uint32_t m = b & 0x7Fu;
+    float v = __uint_as_float(m << 20) * 0x1p120f;
+    v = (m == 0x7Fu) ? __uint_as_float(0x7FC00000u) : v;
+    return (b & 0x80u) ? -v : v;
+}
+
+// 16 raw bytes (8-bit formats) -> 16 bf16, stored as two uint4.
+template <int FMT>
+__device__ __forceinline__ void dequant16_8bit(const uint4 raw, uint4& o0, uint4& o1) {
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+    uint32_t r[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        float f[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const uint32_t byte = (w[k] >> (8 * e)) & 0xFFu;
+            if constexpr (FMT == QSA_KV_FP8_E4M3)
+                f[e] = e4m3_to_f32(byte);
+            else
+                f[e] = static_cast<float>(static_cast<int8_t>(byte));
+        }
+        r[2 * k] = pack_bf16x2(f[0], f[1]);
+        r[2 * k + 1] = pack_bf16x2(f[2], f[3]);
+    }
+    o0 = make_uint4(r[0], r[1], r[2], r[3]);
+    o1 = make_uint4(r[4], r[5], r[6], r[7]);
+}
+
+// 16 raw bytes of int4 (32 nibbles, element 2i in the low nibble) -> 32 bf16.
+__device__ __forceinline__ void dequant32_int4(const uint4 raw, uint4* o) {
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        uint32_t r[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int lo = static_cast<int>(w[k] << (28 - 8 * e)) >> 28;
+            const int hi = static_cast<int>(w[k] << (24 - 8 * e)) >> 28;
+            r[e] = pack_bf16x2(static_cast<float>(lo), static_cast<float>(hi));
+        }
+        o[k] = make_uint4(r[0], r[1], r[2], r[3]);
+    }
+}
+
+// ------------------------------------------------------------ work cursor
+
+// Walks the CTA's token range [t, t_end) of the flattened (b, g, j) space in
+// stages of at most T tokens that never straddle a (b, g) segment.
+struct Cursor {
+    long long t;
+    int b, g, j, j1, kseg;
+    bool segfirst;
+};
+
+__device__ __forceinline__ void cursor_init(Cursor& c, long long t, long long t_end,
+                                            const int* segL, const int* segP, int bs, int Hkv) {
+    int lo = 0, hi = bs - 1; // largest b with Hkv * segP[b] <= t
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if ((long long)Hkv * segP[mid] <= t)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    c.b = lo;
+    const long long off = t - (long long)Hkv * segP[lo];
+    const int L = segL[lo];
+    c.g = static_cast<int>(off / L);
+    c.j = static_cast<int>(off - (long long)c.g * L);
+    c.t = t;
+    c.j1 = static_cast<int>(min((long long)L, c.j + (t_end - t)));
+    c.kseg = 0;
+    c.segfirst = true;
+}
+
+__device__ __forceinline__ int cursor_n(const Cursor& c) { return min(T, c.j1 - c.j); }
+
+__device__ __forceinline__ void cursor_advance(Cursor& c, long long t_end, const int* segL,
+                                               int Hkv) {
+    const int n = cursor_n(c);
+    c.t += n;
+    c.j += n;
+    c.segfirst = false;
+    if (c.j >= c.j1 && c.t < t_end) {
+        if (++c.g == Hkv) {
+            c.g = 0;
+            do {
+                ++c.b;
+            } while (segL[c.b] == 0);
+        }
+        c.j = 0;
+        c.j1 = static_cast<int>(min((long long)segL[c.b], t_end - c.t));
+        ++c.kseg;
+        c.segfirst = true;
+    }
+}
+
+// CTA index whose range holds flattened token t; first token of CTA c.
+__device__ __forceinline__ long long cta_of(long long t, long long N, long long G) {
+    return ((t + 1) * G - 1) / N;
+}
+__device__ __forceinline__ long long cta_begin(long long c, long long N, long long G) {
+    return c * N / G;
+}
+
+// ------------------------------------------------------------------ kernel
+
+template <int FMT>
+__global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p) {
+    using Tr = Traits<FMT>;
+    using Ly = Layout<FMT>;
+    extern __shared__ __align__(128) uint8_t smem[];
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+
+    int* segL = reinterpret_cast<int*>(smem + Ly::off_segL);
+    int* segSrc = reinterpret_cast<int*>(smem + Ly::off_segSrc);
+    int* segP = reinterpret_cast<int*>(smem + Ly::off_segP);
+    int* misc = reinterpret_cast<int*>(smem + Ly::off_misc);
+    volatile int* abort_flag = misc;
+    const uint32_t bar0 = smem_u32(smem + Ly::off_bar);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (Tr::STAGES + s); };
+    auto qfull_bar = [&](int i) { return bar0 + 8u * (2 * Tr::STAGES + i); };
+    auto qempty_bar = [&](int i) { return bar0 + 8u * (2 * Tr::STAGES + 2 + i); };
+
+    // ---------------------------------------------------------------- setup
+    if (tid == 0) {
+        for (int s = 0; s < Tr::STAGES; ++s) {
+            mbar_init(full_bar(s), Tr::SCALES ? 64 : 32);
+            mbar_init(empty_bar(s), NW);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(qfull_bar(i), 1);
+            mbar_init(qempty_bar(i), NW);
+        }
+        misc[0] = 0;
+        fence_mbarrier_init();
+    }
+    // zero the padding rows 12..15 of both Q buffers (rows of the 16-row MMA tile)
+    for (int i = tid; i < 2 * 4 * (BF_RS / 16); i += NTHREADS) {
+        const int buf = i / (4 * (BF_RS / 16));
+        const int rem = i % (4 * (BF_RS / 16));
+        uint4* dst = reinterpret_cast<uint4*>(smem + Ly::off_q + buf * 16 * BF_RS +
+                                              (12 + rem / (BF_RS / 16)) * BF_RS) +
+                     rem % (BF_RS / 16);
+        *dst = make_uint4(0, 0, 0, 0);
+    }
+    // sanitised lengths, index offsets and prefix sums (warp 0; bs <= 128)
+    if (warp == 0) {
+        int bad = 0, Ls[4], run = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int b = lane * 4 + k;
+            int L = 0;
+            if (b < p.bs) {
+                const long long lo = p.cu[b], hi = p.cu[b + 1];
+                if (lo < 0 || hi < lo || hi > p.n_sel || hi - lo > p.capacity) bad = 1;
+                const long long src = lo < 0 ? 0 : lo;
+                long long Ll = hi - lo;
+                Ll = Ll < 0 ? 0 : Ll;
+                Ll = Ll > p.capacity ? p.capacity : Ll;
+                const long long room = p.n_sel - src;
+                Ll = Ll > room ? (room < 0 ? 0 : room) : Ll;
+                L = static_cast<int>(Ll);
+                segL[b] = L;
+                segSrc[b] = static_cast<int>(src < p.n_sel ? src : 0);
+            }
+            Ls[k] = L;
+            run += L;
+        }
+        int incl = run;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int v = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+            if (lane >= off) incl += v;
+        }
+        int excl = incl - run;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int b = lane * 4 + k;
+            if (b < p.bs) segP[b] = excl;
+            excl += Ls[k];
+        }
+        const int total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+        if (lane == 0) {
+            segP[p.bs] = total;
+            segL[p.bs] = 1; // sentinel for the segment walk
+        }
+        bad = __any_sync(0xFFFFFFFFu, bad);
+        if (bad && lane == 0 && blockIdx.x == 0) atomicOr(p.err, QSA_DEVERR_CU_SEQLENS);
+    }
+    __syncthreads();
+
+    const int Hkv = p.Hkv;
+    const long long N = (long long)Hkv * segP[p.bs];
+
+    // empty selections -> zero rows (spread over all CTAs)
+    if (warp < NW) {
+        for (int s = blockIdx.x; s < p.bs * Hkv; s += gridDim.x) {
+            const int b = s / Hkv, g = s % Hkv;
+            if (segL[b] != 0) continue;
+            for (int ch = tid; ch < GROUP * (D / 8); ch += NCT) {
+                const int h = ch / (D / 8), d0 = (ch % (D / 8)) * 8;
+                *reinterpret_cast<uint4*>(p.out + b * p.o_sb + (g * GROUP + h) * p.o_sh + d0) =
+                    make_uint4(0, 0, 0, 0);
+            }
+        }
+    }
+    if (N == 0) return;
+    long long G = (N + MIN_TOKENS_PER_CTA - 1) / MIN_TOKENS_PER_CTA;
+    G = G < (long long)gridDim.x ? G : (long long)gridDim.x;
+    if ((long long)blockIdx.x >= G) return;
+    const long long t_begin = cta_begin(blockIdx.x, N, G);
+    const long long t_end = cta_begin(blockIdx.x + 1, N, G);
+
+    uint8_t* const stage0 = smem + Ly::off_stage;
+    int* const ring = reinterpret_cast<int*>(smem + Ly::off_ring);
+
+    if (warp == NW) {
+        // ============================================================ producer
+        Cursor pc, ic;
+        cursor_init(pc, t_begin, t_end, segL, segP, p.bs, Hkv);
+        ic = pc;
+        auto prefetch = [&](const Cursor& c, int entry) {
+            const int n = cursor_n(c);
+            if (lane < n)
+                cp_async4(smem_u32(ring + entry * T + lane), p.sel + segSrc[c.b] + c.j + lane);
+        };
+#pragma unroll 1
+        for (int i = 0; i < Ly::PF; ++i) {
+            if (pc.t < t_end) {
+                prefetch(pc, i % Ly::R);
+                cursor_advance(pc, t_end, segL, Hkv);
+            }
+            cp_async_commit();
+        }
+#pragma unroll 1
+        for (int i = 0; ic.t < t_end; ++i) {
+            if (pc.t < t_end) {
+                prefetch(pc, (i + Ly::PF) % Ly::R);
+                cursor_advance(pc, t_end, segL, Hkv);
+            }
+            cp_async_commit();
+            cp_async_wait<Ly::PF>();
+            __syncwarp();
+            const int n = cursor_n(ic);
+            const int b = ic.b, g = ic.g;
+            if (ic.segfirst) {
+                const int qb = ic.kseg & 1;
+                if (!mbar_wait(qempty_bar(qb), ((ic.kseg >> 1) & 1) ^ 1, p.err, abort_flag)) break;
+                if (lane == 0) mbar_arrive_expect_tx(qfull_bar(qb), GROUP * D * 2);
+                __syncwarp();
+                if (lane < GROUP)
+                    bulk_g2s(smem_u32(smem + Ly::off_q + qb * 16 * BF_RS + lane * BF_RS),
+                             p.q + b * p.q_sb + (g * GROUP + lane) * p.q_sh, D * 2, qfull_bar(qb));
+            }
+            const int s = i % Tr::STAGES;
+            if (!mbar_wait(empty_bar(s), ((i / Tr::STAGES) & 1) ^ 1, p.err, abort_flag)) break;
+            uint8_t* Ks = stage0 + s * Ly::STAGE_BYTES;
+            uint8_t* Vs = Ks + Ly::STAGE_KV;
+            const bool valid = lane < n;
+            long long row = 0;
+            if (valid) {
+                int slot = ring[(i % Ly::R) * T + lane];
+                if (slot < 0 || (long long)slot >= p.num_slots) {
+                    atomicOr(p.err, QSA_DEVERR_SLOT_RANGE);
+                    slot = 0;
+                }
+                row = (long long)slot * Hkv + g;
+            } else {
+                uint4* z = reinterpret_cast<uint4*>(Vs + lane * Tr::RS);
+#pragma unroll
+                for (int k = 0; k < Tr::ROWB / 16; ++k) z[k] = make_uint4(0, 0, 0, 0);
+                fence_proxy_async();
+            }
+            __syncwarp();
+            if (lane == 0) mbar_expect_tx(full_bar(s), n * 2 * Tr::ROWB);
+            __syncwarp();
+            if (valid) {
+                bulk_g2s(smem_u32(Ks + lane * Tr::RS), p.kpool + row * Tr::ROWB, Tr::ROWB,
+                         full_bar(s));
+                bulk_g2s(smem_u32(Vs + lane * Tr::RS), p.vpool + row * Tr::ROWB, Tr::ROWB,
+                         full_bar(s));
+            }
+            if constexpr (Tr::SCALES) {
+                float* sc = reinterpret_cast<float*>(Vs + Ly::STAGE_KV);
+                if (valid) {
+                    cp_async4(smem_u32(sc + lane), p.k_scale + row);
+                    cp_async4(smem_u32(sc + T + lane), p.v_scale + row);
+                }
+                cp_async_arrive_noinc(full_bar(s));
+            }
+            mbar_arrive(full_bar(s));
+            cursor_advance(ic, t_end, segL, Hkv);
+        }
+        cp_async_wait<0>();
+        return;
+    }
+
+    // ================================================================ consumers
+    const int r = lane >> 2, c = lane & 3;
+    float kscale_g = 1.0f, out_scale = 1.0f;
+    if constexpr (FMT == QSA_KV_FP8_E4M3) {
+        kscale_g = __ldg(p.k_scale);
+        out_scale = __ldg(p.v_scale);
+    }
+    const float cs_base = p.scale_log2 * kscale_g;
+    float* const red = reinterpret_cast<float*>(smem + Ly::off_red);    // [2][NW][16]
+    float* const mref = reinterpret_cast<float*>(smem + Ly::off_mref);  // [2][16]
+    float* const lred = reinterpret_cast<float*>(smem + Ly::off_lred);  // [NW][16]
+    float* const Os = reinterpret_cast<float*>(smem + Ly::off_os);      // [12][OS_STRIDE]
+    float* const mergeM = reinterpret_cast<float*>(misc + 16);
+    float* const mergeDen = reinterpret_cast<float*>(misc + 32);
+
+    uint32_t qa[16][4];
+    float o[MT][3][4];
+    float l0 = 0.f, l1 = 0.f;
+    int v = 0, buf = 0, seg_j0 = 0;
+    const int tok_base = warp * 8;
+    const int tk0 = tok_base + 2 * c;
+
+    Cursor cc;
+    cursor_init(cc, t_begin, t_end, segL, segP, p.bs, Hkv);
+#pragma unroll 1
+    for (int i = 0; cc.t < t_end; ++i) {
+        const int n = cursor_n(cc);
+        const bool first = cc.segfirst;
+        const bool last = cc.j + n >= cc.j1;
+        const int b = cc.b, g = cc.g;
+        if (first) {
+            seg_j0 = cc.j;
+            const int qb = cc.kseg & 1;
+            if (!mbar_wait(qfull_bar(qb), (cc.kseg >> 1) & 1, p.err, abort_flag)) break;
+            const uint32_t qbase = smem_u32(smem + Ly::off_q + qb * 16 * BF_RS);
+#pragma unroll
+            for (int ks = 0; ks < 16; ++ks) {
+                const int mi = lane >> 3;
+                const uint32_t addr =
+                    qbase + ((mi & 1) * 8 + (lane & 7)) * BF_RS + (ks * 16 + (mi >> 1) * 8) * 2;
+                ldsm_x4(qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], addr);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(qempty_bar(qb));
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int j = 0; j < 3; ++j)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) o[mt][j][e] = 0.f;
+            l0 = l1 = 0.f;
+        }
+        const int s = i % Tr::STAGES;
+        if (!mbar_wait(full_bar(s), (i / Tr::STAGES) & 1, p.err, abort_flag)) break;
+        uint8_t* const Ks = stage0 + s * Ly::STAGE_BYTES;
+        uint8_t* const Vs = Ks + Ly::STAGE_KV;
+        const uint8_t* Kb = Ks;   // bf16 rows [T][BF_RS] used by the MMAs
+        const uint8_t* Vb = Vs;
+        float skr[2] = {1.f, 1.f}, svr[2] = {1.f, 1.f};
+
+        if constexpr (Tr::DEQ) {
+            uint8_t* const kbf = smem + Ly::off_kbf;
+            uint8_t* const vbf = kbf + T * BF_RS;
+            const int tt = lane & 7, ch = lane >> 3;
+            if constexpr (FMT == QSA_KV_INT4) {
+                // K: this warp's 8 tokens, 8 chunks of 16 bytes each
+#pragma unroll
+                for (int it = 0; it < 2; ++it) {
+                    const int chunk = ch + 4 * it;
+                    const uint4 raw =
+                        *reinterpret_cast<const uint4*>(Ks + (tok_base + tt) * Tr::RS + chunk * 16);
+                    uint4 ov[4];
+                    dequant32_int4(raw, ov);
+                    uint4* dst = reinterpret_cast<uint4*>(kbf + (tok_base + tt) * BF_RS + chunk * 64);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) dst[k] = ov[k];
+                }
+                // V: this warp's 64 dims (32 bytes) of all T tokens
+                const int t16 = lane & 15, ch2 = lane >> 4;
+#pragma unroll
+                for (int it = 0; it < 2; ++it) {
+                    const int tok = t16 + 16 * it;
+                    const uint4 raw = *reinterpret_cast<const uint4*>(Vs + tok * Tr::RS + warp * 32 +
+                                                                      ch2 * 16);
+                    uint4 ov[4];
+                    dequant32_int4(raw, ov);
+                    uint4* dst = reinterpret_cast<uint4*>(vbf + tok * BF_RS + (warp * 64 + ch2 * 32) * 2);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) dst[k] = ov[k];
+                }
+            } else {
+#pragma unroll
+                for (int it = 0; it < 4; ++it) {
+                    const int chunk = ch + 4 * it;
+                    const uint4 raw =
+                        *reinterpret_cast<const uint4*>(Ks + (tok_base + tt) * Tr::RS + chunk * 16);
+                    uint4 o0, o1;
+                    dequant16_8bit<FMT>(raw, o0, o1);
+                    uint4* dst = reinterpret_cast<uint4*>(kbf + (tok_base + tt) * BF_RS + chunk * 32);
+                    dst[0] = o0;
+                    dst[1] = o1;
+                }
+#pragma unroll
+                for (int it = 0; it < 4; ++it) {
+                    const int tok = tt + 8 * it;
+                    const uint4 raw =
+                        *reinterpret_cast<const uint4*>(Vs + tok * Tr::RS + warp * 64 + ch * 16);
+                    uint4 o0, o1;
+                    dequant16_8bit<FMT>(raw, o0, o1);
+                    uint4* dst = reinterpret_cast<uint4*>(vbf + tok * BF_RS + (warp * 64 + ch * 16) * 2);
+                    dst[0] = o0;
+                    dst[1] = o1;
+                }
+            }
+            if constexpr (Tr::SCALES) {
+                const float* sc = reinterpret_cast<const float*>(Vs + Ly::STAGE_KV);
+                skr[0] = sc[tk0];
+                skr[1] = sc[tk0 + 1];
+                svr[0] = sc[T + tk0];
+                svr[1] = sc[T + tk0 + 1];
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty_bar(s));
+            Kb = kbf;
+            Vb = vbf;
+        }
+
+        // ---------------------------------------------------------------- QK
+        float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        {
+            const uint32_t kbase = smem_u32(Kb) + (tok_base + (lane & 7)) * BF_RS +
+                                   ((lane >> 3) & 1) * 16 + (lane >> 4) * 32;
+#pragma unroll
+            for (int ks = 0; ks < 16; ks += 2) {
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(b0, b1, b2, b3, kbase + ks * 32);
+                mma_bf16(sacc[0], qa[ks], b0, b1);
+                mma_bf16(sacc[1], qa[ks + 1], b2, b3);
+            }
+        }
+        const bool v0 = tk0 < n, v1 = tk0 + 1 < n;
+        const bool row8 = r < 4; // head r + 8 is a real head (8..11)
+        const float ninf = -INFINITY;
+        float x[4];
+        x[0] = v0 ? (sacc[0][0] + sacc[1][0]) * cs_base * skr[0] : ninf;
+        x[1] = v1 ? (sacc[0][1] + sacc[1][1]) * cs_base * skr[1] : ninf;
+        x[2] = (v0 && row8) ? (sacc[0][2] + sacc[1][2]) * cs_base * skr[0] : ninf;
+        x[3] = (v1 && row8) ? (sacc[0][3] + sacc[1][3]) * cs_base * skr[1] : ninf;
+        float ma = fmaxf(x[0], x[1]), mb = fmaxf(x[2], x[3]);
+        ma = fmaxf(ma, __shfl_xor_sync(0xFFFFFFFFu, ma, 1));
+        ma = fmaxf(ma, __shfl_xor_sync(0xFFFFFFFFu, ma, 2));
+        mb = fmaxf(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 1));
+        mb = fmaxf(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 2));
+        float* const redb = red + buf * NW * 16;
+        if (c == 0) {
+            redb[warp * 16 + r] = ma;
+            redb[warp * 16 + r + 8] = mb;
+        }
+        const float* const mrefv = mref + v * 16;
+        float mo_a = first ? ninf : mrefv[r];
+        float mo_b = first ? ninf : mrefv[r + 8];
+
+        uint8_t* const Pb = smem + Ly::off_p + buf * 24 * PRS;
+        float pr[4];
+        auto compute_p = [&](float ra, float rb) {
+            pr[0] = x[0] == ninf ? 0.f : ex2(x[0] - ra);
+            pr[1] = x[1] == ninf ? 0.f : ex2(x[1] - ra);
+            pr[2] = x[2] == ninf ? 0.f : ex2(x[2] - rb);
+            pr[3] = x[3] == ninf ? 0.f : ex2(x[3] - rb);
+        };
+        auto write_p = [&]() {
+            float pv[4] = {pr[0] * svr[0], pr[1] * svr[1], pr[2] * svr[0], pr[3] * svr[1]};
+            pv[0] = v0 ? pv[0] : 0.f;
+            pv[1] = v1 ? pv[1] : 0.f;
+            pv[2] = v0 ? pv[2] : 0.f;
+            pv[3] = v1 ? pv[3] : 0.f;
+            const uint32_t hi_a = pack_bf16x2(pv[0], pv[1]);
+            const uint32_t lo_a = pack_bf16x2(pv[0] - bf16_lo(hi_a), pv[1] - bf16_hi(hi_a));
+            *reinterpret_cast<uint32_t*>(Pb + r * PRS + tk0 * 2) = hi_a;
+            *reinterpret_cast<uint32_t*>(Pb + (8 + r) * PRS + tk0 * 2) = lo_a;
+            if (row8) {
+                const uint32_t hi_b = pack_bf16x2(pv[2], pv[3]);
+                const uint32_t lo_b = pack_bf16x2(pv[2] - bf16_lo(hi_b), pv[3] - bf16_hi(hi_b));
+                *reinterpret_cast<uint32_t*>(Pb + (16 + r) * PRS + tk0 * 2) = hi_b;
+                *reinterpret_cast<uint32_t*>(Pb + (20 + r) * PRS + tk0 * 2) = lo_b;
+            }
+        };
+        compute_p(mo_a, mo_b);
+        write_p();
+        consumer_sync();
+
+        // stage maximum per head vs the running reference
+        auto stage_max = [&](int h) {
+            float m = redb[h];
+#pragma unroll
+            for (int w = 1; w < NW; ++w) m = fmaxf(m, redb[w * 16 + h]);
+            return m;
+        };
+        auto old_ref = [&](int h) { return first ? ninf : mrefv[h]; };
+        bool nd = first || stage_max(r) > mo_a + TAU || (row8 && stage_max(r + 8) > mo_b + TAU);
+        if (__any_sync(0xFFFFFFFFu, nd)) {
+            // slow path (uniform over the four warps): raise the reference max
+            auto new_ref = [&](int h) { return fmaxf(old_ref(h), stage_max(h)); };
+            auto alpha = [&](int h) {
+                const float mo = old_ref(h);
+                return mo == ninf ? 0.f : ex2(mo - new_ref(h));
+            };
+            const float na = new_ref(r), nb = row8 ? new_ref(r + 8) : 0.f;
+            l0 *= alpha(r);
+            l1 *= row8 ? alpha(r + 8) : 0.f;
+            compute_p(na, nb);
+            write_p();
+            const float a0 = alpha(2 * c), a1 = alpha(2 * c + 1);
+            const float a2 = alpha(8 + ((2 * c) & 3)), a3 = alpha(8 + ((2 * c + 1) & 3));
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    o[mt][j][0] *= a0;
+                    o[mt][j][1] *= a1;
+                    o[mt][j][2] *= a0;
+                    o[mt][j][3] *= a1;
+                }
+                o[mt][2][0] *= a2;
+                o[mt][2][1] *= a3;
+                o[mt][2][2] *= a2;
+                o[mt][2][3] *= a3;
+            }
+            if (warp == 0 && lane < GROUP) mref[(v ^ 1) * 16 + lane] = new_ref(lane);
+            v ^= 1;
+            consumer_sync();
+        }
+        l0 += pr[0] + pr[1];
+        l1 += pr[2] + pr[3];
+
+        // ---------------------------------------------------------------- PV
+        {
+            uint32_t pb[2][3][2];
+            const uint32_t pbase = smem_u32(Pb);
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk) {
+                const uint32_t a4 = pbase + ((lane >> 4) * 8 + (lane & 7)) * PRS +
+                                    (kk * 16 + ((lane >> 3) & 1) * 8) * 2;
+                ldsm_x4(pb[kk][0][0], pb[kk][0][1], pb[kk][1][0], pb[kk][1][1], a4);
+                const uint32_t a2 =
+                    pbase + (16 + (lane & 7)) * PRS + (kk * 16 + ((lane >> 3) & 1) * 8) * 2;
+                ldsm_x2(pb[kk][2][0], pb[kk][2][1], a2);
+            }
+            const uint32_t vbase = smem_u32(Vb) + ((lane >> 4) * 8 + (lane & 7)) * BF_RS +
+                                   (warp * (D / NW) + ((lane >> 3) & 1) * 8) * 2;
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk) {
+                    uint32_t a[4];
+                    ldsm_x4_t(a[0], a[1], a[2], a[3], vbase + kk * 16 * BF_RS + mt * 32);
+#pragma unroll
+                    for (int j = 0; j < 3; ++j) mma_bf16(o[mt][j], a, pb[kk][j][0], pb[kk][j][1]);
+                }
+            }
+        }
+        if constexpr (!Tr::DEQ) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty_bar(s));
+        }
+
+        // ------------------------------------------------------------ epilogue
+        if (last) {
+            const int L = segL[b];
+            const bool complete = (seg_j0 == 0) && (cc.j1 == L);
+            const int sid = b * Hkv + g;
+            float la = l0, lb = l1;
+            la += __shfl_xor_sync(0xFFFFFFFFu, la, 1);
+            la += __shfl_xor_sync(0xFFFFFFFFu, la, 2);
+            lb += __shfl_xor_sync(0xFFFFFFFFu, lb, 1);
+            lb += __shfl_xor_sync(0xFFFFFFFFu, lb, 2);
+            if (c == 0) {
+                lred[warp * 16 + r] = la;
+                lred[warp * 16 + r + 8] = lb;
+            }
+            consumer_sync();
+            auto ltot = [&](int h) {
+                float t = 0.f;
+#pragma unroll
+                for (int w = 0; w < NW; ++w) t += lred[w * 16 + h];
+                return t;
+            };
+            const int hA = 2 * c, hB = 2 * c + 1, hC = 8 + 2 * c, hD = 9 + 2 * c;
+            const float fA = complete ? out_scale / ltot(hA) : 1.f;
+            const float fB = complete ? out_scale / ltot(hB) : 1.f;
+            const float fC = (complete && c < 2) ? out_scale / ltot(hC) : 1.f;
+            const float fD = (complete && c < 2) ? out_scale / ltot(hD) : 1.f;
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                const int dA = warp * (D / NW) + mt * 16 + r, dB = dA + 8;
+                Os[hA * OS_STRIDE + dA] = (o[mt][0][0] + o[mt][1][0]) * fA;
+                Os[hB * OS_STRIDE + dA] = (o[mt][0][1] + o[mt][1][1]) * fB;
+                Os[hA * OS_STRIDE + dB] = (o[mt][0][2] + o[mt][1][2]) * fA;
+                Os[hB * OS_STRIDE + dB] = (o[mt][0][3] + o[mt][1][3]) * fB;
+                float u[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) u[e] = __shfl_xor_sync(0xFFFFFFFFu, o[mt][2][e], 2);
+                if (c < 2) {
+                    Os[hC * OS_STRIDE + dA] = (o[mt][2][0] + u[0]) * fC;
+                    Os[hD * OS_STRIDE + dA] = (o[mt][2][1] + u[1]) * fD;
+                    Os[hC * OS_STRIDE + dB] = (o[mt][2][2] + u[2]) * fC;
+                    Os[hD * OS_STRIDE + dB] = (o[mt][2][3] + u[3]) * fD;
+                }
+            }
+            consumer_sync();
+            __nv_bfloat16* const outb = p.out + b * p.o_sb + (long long)(g * GROUP) * p.o_sh;
+            if (complete) {
+                for (int ch = tid; ch < GROUP * (D / 8); ch += NCT) {
+                    const int h = ch / (D / 8), d0 = (ch % (D / 8)) * 8;
+                    const float4 x0 = *reinterpret_cast<const float4*>(Os + h * OS_STRIDE + d0);
+                    const float4 x1 = *reinterpret_cast<const float4*>(Os + h * OS_STRIDE + d0 + 4);
+                    *reinterpret_cast<uint4*>(outb + h * p.o_sh + d0) =
+                        make_uint4(pack_bf16x2(x0.x, x0.y), pack_bf16x2(x0.z, x0.w),
+                                   pack_bf16x2(x1.x, x1.y), pack_bf16x2(x1.z, x1.w));
+                }
+            } else {
+                const float* const mfin = mref + v * 16;
+                uint8_t* const part =
+                    p.part + ((long long)blockIdx.x * 2 + (cc.kseg == 0 ? 0 : 1)) * PART_BYTES;
+                for (int ch = tid; ch < GROUP * (D / 4); ch += NCT) {
+                    const int h = ch / (D / 4), d0 = (ch % (D / 4)) * 4;
+                    *reinterpret_cast<float4*>(part + (h * D + d0) * 4) =
+                        *reinterpret_cast<const float4*>(Os + h * OS_STRIDE + d0);
+                }
+                if (tid < GROUP) {
+                    reinterpret_cast<float*>(part + PART_O_BYTES)[tid] = mfin[tid];
+                    reinterpret_cast<float*>(part + PART_O_BYTES + GROUP * 4)[tid] = ltot(tid);
+                }
+                __threadfence();
+                consumer_sync();
+                const long long Fs = (long long)Hkv * segP[b] + (long long)g * L;
+                const long long c_first = cta_of(Fs, N, G);
+                const long long c_last = cta_of(Fs + L - 1, N, G);
+                if (tid == 0) {
+                    const int old = atomicAdd(p.cnt + sid, 1);
+                    misc[1] = (old == static_cast<int>(c_last - c_first)) ? 1 : 0;
+                }
+                consumer_sync();
+                if (misc[1]) {
+                    __threadfence();
+                    auto part_of = [&](long long cta) -> const uint8_t* {
+                        const int slot = (cta == c_first && cta_begin(cta, N, G) < Fs) ? 1 : 0;
+                        return p.part + (cta * 2 + slot) * PART_BYTES;
+                    };
+                    if (tid < GROUP) {
+                        float M = ninf;
+                        for (long long k = c_first; k <= c_last; ++k)
+                            M = fmaxf(M, __ldcg(reinterpret_cast<const float*>(part_of(k) +
+                                                                               PART_O_BYTES) + tid));
+                        float den = 0.f;
+                        for (long long k = c_first; k <= c_last; ++k) {
+                            const float* mk = reinterpret_cast<const float*>(part_of(k) + PART_O_BYTES);
+                            const float mv = __ldcg(mk + tid);
+                            if (mv != ninf) den += __ldcg(mk + GROUP + tid) * ex2(mv - M);
+                        }
+                        mergeM[tid] = M;
+                        mergeDen[tid] = den;
+                    }
+                    consumer_sync();
+                    for (int ch = tid; ch < GROUP * (D / 4); ch += NCT) {
+                        const int h = ch / (D / 4), d0 = (ch % (D / 4)) * 4;
+                        const float M = mergeM[h];
+                        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                        for (long long k = c_first; k <= c_last; ++k) {
+                            const uint8_t* pk = part_of(k);
+                            const float mv = __ldcg(reinterpret_cast<const float*>(pk + PART_O_BYTES) + h);
+                            if (mv == ninf) continue;
+                            const float w = ex2(mv - M);
+                            const float4 ov = __ldcg(reinterpret_cast<const float4*>(pk + (h * D + d0) * 4));
+                            acc.x += w * ov.x;
+                            acc.y += w * ov.y;
+                            acc.z += w * ov.z;
+                            acc.w += w * ov.w;
+                        }
+                        const float f = out_scale / mergeDen[h];
+                        *reinterpret_cast<uint2*>(outb + h * p.o_sh + d0) =
+                            make_uint2(pack_bf16x2(acc.x * f, acc.y * f), pack_bf16x2(acc.z * f, acc.w * f));
+                    }
+                    if (tid == 0) atomicExch(p.cnt + sid, 0);
+                }
+            }
+            consumer_sync();
+        }
+        cursor_advance(cc, t_end, segL, Hkv);
+        buf ^= 1;
+    }
+}
+
+} // namespace qsa
+
+// ====================================================================== host
+
+namespace {
+
+using namespace qsa;
+
+thread_local std::string g_last_error;
+
+int fail(int code, const char* fmt, ...) {
+    char msg[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(msg, sizeof msg, fmt, ap);
+    va_end(ap);
+    g_last_error = msg;
+    return code;
+}
+
+struct DeviceState {
+    int sms = 0;
+    bool smem_set[4] = {false, false, false, false};
+};
+
+std::mutex g_mu;
+DeviceState g_dev[64];
+
+int current_device(int* dev, int* sms) {
+    cudaError_t e = cudaGetDevice(dev);
+    if (e != cudaSuccess) return fail(QSA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (*dev < 0 || *dev >= 64) return fail(QSA_ERR_CUDA, "device ordinal %d out of range", *dev);
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState& st = g_dev[*dev];
+    if (st.sms == 0) {
+        e = cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, *dev);
+        if (e != cudaSuccess)
+            return fail(QSA_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
+    }
+    *sms = st.sms;
+    return QSA_OK;
+}
+
+int check_sizes(int32_t bs, int32_t num_q_heads, int32_t capacity) {
+    if (bs < 1 || bs > MAX_BS)
+        return fail(QSA_ERR_UNSUPPORTED, "batch size %d outside the supported 1..%d", bs, MAX_BS);
+    if (num_q_heads != 12 && num_q_heads != 24)
+        return fail(QSA_ERR_UNSUPPORTED,
+                    "%d query heads: the decode contract is 24 (TP1, 2 KV heads) or 12 (TP2, 1 KV head)",
+                    num_q_heads);
+    if (capacity < 1 || capacity > MAX_CAPACITY)
+        return fail(QSA_ERR_UNSUPPORTED, "selected-KV capacity %d outside the supported 1..%d",
+                    capacity, MAX_CAPACITY);
+    return QSA_OK;
+}
+
+long long grid_for(int32_t bs, int32_t num_q_heads, int32_t capacity, int32_t max_ctas, int sms) {
+    const long long hkv = num_q_heads / GROUP;
+    const long long work = (long long)bs * hkv * capacity;
+    long long g = (work + MIN_TOKENS_PER_CTA - 1) / MIN_TOKENS_PER_CTA;
+    if (g > sms) g = sms;
+    if (max_ctas > 0 && g > max_ctas) g = max_ctas;
+    return g < 1 ? 1 : g;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+void layout_for(int32_t bs, int32_t num_q_heads, long long grid, qsa_scratch_layout* ly) {
+    const size_t hkv = num_q_heads / GROUP;
+    ly->error_word_offset = 0;
+    ly->counters_offset = 256;
+    ly->counters_count = (size_t)bs * hkv;
+    ly->partials_offset = 256 + align_up(ly->counters_count * 4, 256);
+    ly->partial_slot_bytes = PART_BYTES;
+    ly->total_bytes = ly->partials_offset + (size_t)grid * 2 * PART_BYTES;
+}
+
+bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+int check_row_tensor(const qsa_tensor* t, const char* name, int bs, int hq) {
+    if (t->dtype != QSA_DTYPE_BF16)
+        return fail(QSA_ERR_UNSUPPORTED, "%s must be bf16 (dtype %d given)", name, t->dtype);
+    if (t->ndim != 3 || t->shape[0] != bs || t->shape[1] != hq || t->shape[2] != D)
+        return fail(QSA_ERR_INVALID_ARGUMENT, "%s must be [bs=%d, Hq=%d, 256]", name, bs, hq);
+    if (t->stride[2] != 1)
+        return fail(QSA_ERR_INVALID_ARGUMENT, "%s must be contiguous along the head dimension", name);
+    if (t->stride[0] % 8 != 0 || t->stride[1] % 8 != 0 || t->stride[0] < 0 || t->stride[1] < 0)
+        return fail(QSA_ERR_MISALIGNED, "%s strides must be non-negative multiples of 8 elements",
+                    name);
+    if (t->data == nullptr) return fail(QSA_ERR_INVALID_ARGUMENT, "%s data is NULL", name);
+    if (!aligned16(t->data)) return fail(QSA_ERR_MISALIGNED, "%s must be 16-byte aligned", name);
+    return QSA_OK;
+}
+
+template <int FMT> const void* kernel_ptr() { return reinterpret_cast<const void*>(&qsa_decode_kernel<FMT>); }
+
+template <int FMT>
+int launch(const Params& prm, int grid, int dev, cudaStream_t stream) {
+    constexpr int smem = Layout<FMT>::TOTAL;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!g_dev[dev].smem_set[FMT]) {
+            cudaError_t e = cudaFuncSetAttribute(qsa_decode_kernel<FMT>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            if (e != cudaSuccess)
+                return fail(QSA_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+            g_dev[dev].smem_set[FMT] = true;
+        }
+    }
+    qsa_decode_kernel<FMT><<<grid, NTHREADS, smem, stream>>>(prm);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(QSA_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
+    return QSA_OK;
+}
+
+} // namespace
+
+extern "C" {
+
+int qsa_version(void) { return 100; }
+
+const char* qsa_strerror(int code) {
+    switch (code) {
+    case QSA_OK: return "success";
+    case QSA_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case QSA_ERR_UNSUPPORTED: return "outside the packed QSA decode contract";
+    case QSA_ERR_SCRATCH_TOO_SMALL: return "scratch buffer too small";
+    case QSA_ERR_MISALIGNED: return "misaligned pointer or stride";
+    case QSA_ERR_CUDA: return "CUDA runtime error";
+    default: return "unknown error";
+    }
+}
+
+const char* qsa_last_error_message(void) { return g_last_error.c_str(); }
+
+int32_t qsa_decode_grid(int32_t bs, int32_t num_q_heads, int32_t capacity, int32_t max_ctas) {
+    int rc = check_sizes(bs, num_q_heads, capacity);
+    if (rc != QSA_OK) return rc;
+    int dev, sms;
+    rc = current_device(&dev, &sms);
+    if (rc != QSA_OK) return rc;
+    return static_cast<int32_t>(grid_for(bs, num_q_heads, capacity, max_ctas, sms));
+}
+
+int qsa_decode_scratch_layout(int32_t bs, int32_t num_q_heads, int32_t capacity,
+                              qsa_scratch_layout* layout) {
+    if (layout == nullptr) return fail(QSA_ERR_INVALID_ARGUMENT, "layout is NULL");
+    int rc = check_sizes(bs, num_q_heads, capacity);
+    if (rc != QSA_OK) return rc;
+    int dev, sms;
+    rc = current_device(&dev, &sms);
+    if (rc != QSA_OK) return rc;
+    layout_for(bs, num_q_heads, grid_for(bs, num_q_heads, capacity, 0, sms), layout);
+    return QSA_OK;
+}
+
+size_t qsa_decode_scratch_bytes(int32_t bs, int32_t num_q_heads, int32_t capacity) {
+    qsa_scratch_layout ly;
+    if (qsa_decode_scratch_layout(bs, num_q_heads, capacity, &ly) != QSA_OK) return 0;
+    return ly.total_bytes;
+}
+
+int qsa_scratch_init(void* scratch, size_t scratch_bytes, void* stream) {
+    if (scratch == nullptr) return fail(QSA_ERR_INVALID_ARGUMENT, "scratch is NULL");
+    cudaError_t e = cudaMemsetAsync(scratch, 0, scratch_bytes, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(QSA_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(e));
+    return QSA_OK;
+}
+
+int qsa_scratch_error(const void* scratch, int32_t* flags, int32_t clear, void* stream) {
+    if (scratch == nullptr || flags == nullptr)
+        return fail(QSA_ERR_INVALID_ARGUMENT, "scratch and flags must be non-NULL");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int32_t host = 0;
+    cudaError_t e = cudaMemcpyAsync(&host, scratch, sizeof host, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess && clear)
+        e = cudaMemsetAsync(const_cast<void*>(scratch), 0, sizeof(int32_t), st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return fail(QSA_ERR_CUDA, "error-word readback: %s", cudaGetErrorString(e));
+    *flags = host;
+    return QSA_OK;
+}
+
+int qsa_decode(const qsa_tensor* q, const qsa_tensor* k_pool, const qsa_tensor* v_pool,
+               const qsa_kv_quant_meta* meta, const qsa_tensor* sel, const qsa_tensor* cu,
+               const qsa_tensor* out, void* scratch, size_t scratch_bytes, void* stream) {
+    if (!q || !k_pool || !v_pool || !meta || !sel || !cu || !out)
+        return fail(QSA_ERR_INVALID_ARGUMENT, "a descriptor pointer is NULL");
+    const int fmt = meta->format;
+    if (fmt < QSA_KV_BF16 || fmt > QSA_KV_INT4)
+        return fail(QSA_ERR_UNSUPPORTED, "unknown K/V pool format %d", fmt);
+    if (q->ndim != 3) return fail(QSA_ERR_INVALID_ARGUMENT, "q must be [bs, Hq, 256]");
+    const int64_t bs64 = q->shape[0], hq64 = q->shape[1];
+    if (q->shape[2] != D)
+        return fail(QSA_ERR_UNSUPPORTED, "head dim %lld: the decode contract is D = 256",
+                    (long long)q->shape[2]);
+    if (bs64 < 1 || bs64 > MAX_BS)
+        return fail(QSA_ERR_UNSUPPORTED, "batch size %lld outside the supported 1..%d",
+                    (long long)bs64, MAX_BS);
+    if (hq64 != 12 && hq64 != 24)
+        return fail(QSA_ERR_UNSUPPORTED,
+                    "%lld query heads: the decode contract is 24 (TP1, 2 KV heads) or 12 (TP2, 1 KV head)",
+                    (long long)hq64);
+    const int bs = (int)bs64, hq = (int)hq64, hkv = hq / GROUP;
+    int rc = check_sizes(bs, hq, meta->capacity);
+    if (rc != QSA_OK) return rc;
+    if ((rc = check_row_tensor(q, "q", bs, hq)) != QSA_OK) return rc;
+    if ((rc = check_row_tensor(out, "out", bs, hq)) != QSA_OK) return rc;
+
+    const int want_dtype = fmt == QSA_KV_BF16 ? QSA_DTYPE_BF16
+                           : fmt == QSA_KV_INT8 ? QSA_DTYPE_INT8
+                                                : QSA_DTYPE_UINT8;
+    const int64_t row_elems = fmt == QSA_KV_INT4 ? D / 2 : D;
+    for (const qsa_tensor* pool : {k_pool, v_pool}) {
+        const char* nm = pool == k_pool ? "k_pool" : "v_pool";
+        if (pool->dtype != want_dtype)
+            return fail(QSA_ERR_INVALID_ARGUMENT, "%s dtype %d does not match pool format %d", nm,
+                        pool->dtype, fmt);
+        if (pool->ndim != 3 || pool->shape[1] != hkv || pool->shape[2] != row_elems ||
+            pool->shape[0] < 1)
+            return fail(QSA_ERR_INVALID_ARGUMENT, "%s must be [num_slots, Hkv=%d, %lld]", nm, hkv,
+                        (long long)row_elems);
+        if (pool->stride[2] != 1 || pool->stride[1] != row_elems ||
+            pool->stride[0] != hkv * row_elems)
+            return fail(QSA_ERR_INVALID_ARGUMENT, "%s must be contiguous", nm);
+        if (pool->data == nullptr) return fail(QSA_ERR_INVALID_ARGUMENT, "%s data is NULL", nm);
+        if (!aligned16(pool->data)) return fail(QSA_ERR_MISALIGNED, "%s must be 16-byte aligned", nm);
+    }
+    if (k_pool->shape[0] != v_pool->shape[0])
+        return fail(QSA_ERR_INVALID_ARGUMENT, "k_pool and v_pool hold different slot counts");
+    if (sel->dtype != QSA_DTYPE_INT32 || sel->ndim != 1 || (sel->shape[0] > 1 && sel->stride[0] != 1) ||
+        sel->shape[0] < 0)
+        return fail(QSA_ERR_INVALID_ARGUMENT, "sel_indices must be a contiguous int32 vector");
+    if (sel->shape[0] > 0 && sel->data == nullptr)
+        return fail(QSA_ERR_INVALID_ARGUMENT, "sel_indices data is NULL");
+    if (sel->shape[0] > INT32_MAX)
+        return fail(QSA_ERR_UNSUPPORTED, "sel_indices longer than 2^31 - 1");
+    if (cu->dtype != QSA_DTYPE_INT32 || cu->ndim != 1 || cu->shape[0] != bs + 1 ||
+        cu->stride[0] != 1 || cu->data == nullptr)
+        return fail(QSA_ERR_INVALID_ARGUMENT, "cu_seqlens must be a contiguous int32 [bs + 1]");
+    if (!std::isfinite(meta->softmax_scale))
+        return fail(QSA_ERR_INVALID_ARGUMENT, "softmax_scale must be finite");
+    if (fmt != QSA_KV_BF16) {
+        if (meta->k_scale == nullptr || meta->v_scale == nullptr)
+            return fail(QSA_ERR_INVALID_ARGUMENT, "quantised pools need k_scale and v_scale");
+        if ((reinterpret_cast<uintptr_t>(meta->k_scale) & 3u) ||
+            (reinterpret_cast<uintptr_t>(meta->v_scale) & 3u))
+            return fail(QSA_ERR_MISALIGNED, "scales must be 4-byte aligned");
+    }
+    if (scratch == nullptr) return fail(QSA_ERR_INVALID_ARGUMENT, "scratch is NULL");
+    if (reinterpret_cast<uintptr_t>(scratch) & 255u)
+        return fail(QSA_ERR_MISALIGNED, "scratch must be 256-byte aligned");
+
+    int dev, sms;
+    if ((rc = current_device(&dev, &sms)) != QSA_OK) return rc;
+    const long long grid = grid_for(bs, hq, meta->capacity, meta->max_ctas, sms);
+    qsa_scratch_layout ly;
+    layout_for(bs, hq, grid, &ly);
+    if (scratch_bytes < ly.total_bytes)
+        return fail(QSA_ERR_SCRATCH_TOO_SMALL, "scratch holds %zu bytes, this call needs %zu",
+                    scratch_bytes, ly.total_bytes);
+
+    Params prm;
+    prm.q = static_cast<const __nv_bfloat16*>(q->data);
+    prm.q_sb = q->stride[0];
+    prm.q_sh = q->stride[1];
+    prm.kpool = static_cast<const uint8_t*>(k_pool->data);
+    prm.vpool = static_cast<const uint8_t*>(v_pool->data);
+    prm.num_slots = k_pool->shape[0];
+    prm.k_scale = meta->k_scale;
+    prm.v_scale = meta->v_scale;
+    prm.sel = static_cast<const int*>(sel->data);
+    prm.n_sel = sel->shape[0];
+    prm.cu = static_cast<const int*>(cu->data);
+    prm.out = static_cast<__nv_bfloat16*>(out->data);
+    prm.o_sb = out->stride[0];
+    prm.o_sh = out->stride[1];
+    uint8_t* base = static_cast<uint8_t*>(scratch);
+    prm.err = reinterpret_cast<int*>(base + ly.error_word_offset);
+    prm.cnt = reinterpret_cast<int*>(base + ly.counters_offset);
+    prm.part = base + ly.partials_offset;
+    prm.bs = bs;
+    prm.Hkv = hkv;
+    prm.capacity = meta->capacity;
+    prm.scale_log2 = meta->softmax_scale * 1.4426950408889634f;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    switch (fmt) {
+    case QSA_KV_BF16: rc = launch<QSA_KV_BF16>(prm, (int)grid, dev, st); break;
+    case QSA_KV_FP8_E4M3: rc = launch<QSA_KV_FP8_E4M3>(prm, (int)grid, dev, st); break;
+    case QSA_KV_INT8: rc = launch<QSA_KV_INT8>(prm, (int)grid, dev, st); break;
+    default: rc = launch<QSA_KV_INT4>(prm, (int)grid, dev, st); break;
+    }
+    if (rc == QSA_OK) g_last_error.clear();
+    return rc;
+}
+
+} // extern "C"

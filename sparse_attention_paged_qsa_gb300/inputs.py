@@ -276,3 +276,28 @@ def replay_inputs(seed: int, replay: torch.Tensor, bs: int, band: str, capacity:
     ids = hash_key(seed, replay, b, j) % num_slots
     live = pos < cu[bs]
     sel_out.copy_(torch.where(live, ids, torch.zeros_like(ids)).to(torch.int32))
+
+
+# ----------------------------------------------------------- host subsets
+
+def host_subset(w: Workload, rows) -> Workload:
+    """Host workload holding only `rows` of a device workload, with the pool
+    rows those sequences select copied to the host (slot ids remapped)."""
+    rows = [int(r) for r in rows]
+    cu = w.cu.cpu().long()
+    sel = w.sel.cpu().long()
+    parts = [sel[cu[b]:cu[b + 1]] for b in rows]
+    flat = torch.cat(parts) if parts else torch.zeros(0, dtype=torch.long)
+    uniq, inv = torch.unique(flat, return_inverse=True)
+    dev_idx = uniq.to(w.k_pool.device)
+    k = w.k_pool.index_select(0, dev_idx).cpu()
+    v = w.v_pool.index_select(0, dev_idx).cpu()
+    ks = vs = None
+    if w.fmt in ("int8", "int4"):
+        ks = w.k_scale.index_select(0, dev_idx).cpu()
+        vs = w.v_scale.index_select(0, dev_idx).cpu()
+    elif w.fmt == "fp8_e4m3":
+        ks, vs = w.k_scale.cpu(), w.v_scale.cpu()
+    lens = [int(cu[b + 1] - cu[b]) for b in rows]
+    return Workload(w.q.cpu()[rows], k, v, inv.to(torch.int32), cu_from_lengths(lens), w.fmt,
+                      ks, vs, w.softmax_scale, w.capacity, w.name + "_subset")

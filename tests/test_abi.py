@@ -1,0 +1,130 @@
+"""The C ABI without a GPU: the library loads, exports every declared
+symbol, the binding's structs match the header, and contract violations are
+rejected on the host before any CUDA call."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+import torch
+
+from sparse_attention_paged_qsa_gb300 import binding as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qsa.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(qsa_\w+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = B.load()
+    names = declared_functions()
+    assert names, "no declarations parsed"
+    for name in names:
+        assert hasattr(lib, name), f"{name} declared in qsa.h but not exported"
+    assert sorted(B.EXPORTED) == names
+    out = subprocess.run(["nm", "-D", "--defined-only", B.LIB_PATH], capture_output=True,
+                         text=True).stdout
+    for name in names:
+        assert re.search(rf"\bT {name}$", out, flags=re.M), name
+
+
+def test_struct_layouts_match_header(tmp_path):
+    src = tmp_path / "sizes.c"
+    src.write_text(
+        '#include <stdio.h>\n#include <stddef.h>\n#include "qsa.h"\n'
+        "int main(void){printf(\"%zu %zu %zu %zu %zu %zu\\n\", sizeof(qsa_tensor),"
+        " sizeof(qsa_kv_quant_meta), offsetof(qsa_kv_quant_meta, softmax_scale),"
+        " offsetof(qsa_kv_quant_meta, max_ctas), sizeof(qsa_scratch_layout),"
+        " offsetof(qsa_tensor, stride));return 0;}\n")
+    exe = tmp_path / "sizes"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
+                   check=True)
+    got = list(map(int, subprocess.run([str(exe)], capture_output=True, text=True).stdout.split()))
+    assert got == [ctypes.sizeof(B.QsaTensor), ctypes.sizeof(B.QsaKvQuantMeta),
+                   B.QsaKvQuantMeta.softmax_scale.offset, B.QsaKvQuantMeta.max_ctas.offset,
+                   ctypes.sizeof(B.QsaScratchLayout), B.QsaTensor.stride.offset]
+
+
+def test_version_and_strerror():
+    lib = B.load()
+    assert lib.qsa_version() >= 100
+    for code in (0, -1, -2, -3, -4, -5):
+        assert lib.qsa_strerror(code)
+    assert lib.qsa_strerror(-99) == b"unknown error"
+
+
+def _host_call(q_shape=(2, 24, 256), pool_shape=(64, 2, 256), fmt="bf16", pool_dtype=None,
+               capacity=100, q_offset=0, scales=False, scratch=True, cu_len=None):
+    """Describe host tensors (never dereferenced) and call qsa_decode."""
+    pd = pool_dtype or {"bf16": torch.bfloat16, "fp8_e4m3": torch.uint8, "int8": torch.int8,
+                        "int4": torch.uint8}[fmt]
+    qbuf = torch.zeros(int(torch.tensor(q_shape).prod()) + 64, dtype=torch.bfloat16)
+    q = qbuf[q_offset:q_offset + int(torch.tensor(q_shape).prod())].view(q_shape)
+    k = torch.zeros(pool_shape, dtype=pd)
+    v = torch.zeros(pool_shape, dtype=pd)
+    bs = q_shape[0]
+    sel = torch.zeros(10, dtype=torch.int32)
+    cu = torch.zeros(cu_len or (bs + 1), dtype=torch.int32)
+    out = torch.zeros(q_shape, dtype=torch.bfloat16)
+    sc = torch.ones(pool_shape[0] * pool_shape[1], dtype=torch.float32)
+    meta = B.KVQuantMeta(fmt, capacity, sc if scales else None, sc if scales else None, 1 / 16)
+    scr = torch.zeros(1 << 16, dtype=torch.uint8)
+    lib = B.load()
+    d = [B.describe(t) for t in (q, k, v)]
+    m = meta.to_c()
+    sd, cd, od = B.describe(sel), B.describe(cu), B.describe(out)
+    base = scr.data_ptr()
+    aligned = (base + 255) // 256 * 256
+    rc = lib.qsa_decode(ctypes.byref(d[0]), ctypes.byref(d[1]), ctypes.byref(d[2]),
+                        ctypes.byref(m), ctypes.byref(sd), ctypes.byref(cd), ctypes.byref(od),
+                        aligned if scratch else None, 1 << 15, None)
+    return rc, lib.qsa_last_error_message().decode()
+
+
+@pytest.mark.parametrize("kw, code, text", [
+    (dict(q_shape=(0, 24, 256)), B.ERR_UNSUPPORTED, "batch size"),
+    (dict(q_shape=(129, 24, 256)), B.ERR_UNSUPPORTED, "batch size"),
+    (dict(q_shape=(2, 16, 256)), B.ERR_UNSUPPORTED, "query heads"),
+    (dict(q_shape=(2, 24, 128)), B.ERR_UNSUPPORTED, "D = 256"),
+    (dict(capacity=2056), B.ERR_UNSUPPORTED, "capacity"),
+    (dict(capacity=0), B.ERR_UNSUPPORTED, "capacity"),
+    (dict(pool_dtype=torch.float32), B.ERR_INVALID_ARGUMENT, "dtype"),
+    (dict(pool_shape=(64, 1, 256)), B.ERR_INVALID_ARGUMENT, "Hkv=2"),
+    (dict(fmt="int4", pool_shape=(64, 2, 256)), B.ERR_INVALID_ARGUMENT, "128"),
+    (dict(fmt="int8"), B.ERR_INVALID_ARGUMENT, "scale"),
+    (dict(q_offset=1), B.ERR_MISALIGNED, "aligned"),
+    (dict(scratch=False), B.ERR_INVALID_ARGUMENT, "scratch"),
+    (dict(cu_len=2), B.ERR_INVALID_ARGUMENT, "cu_seqlens"),
+])
+def test_contract_rejections_on_host(kw, code, text):
+    rc, msg = _host_call(**kw)
+    assert rc == code, msg
+    assert text in msg
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(B, "_lib", None)
+    monkeypatch.setattr(B, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        B.load()
+
+
+def test_oracle_and_product_share_no_code():
+    pkg = os.path.join(ROOT, "sparse_attention_paged_qsa_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", text, flags=re.M), f
+                assert "qsa_oracle" not in text and "liboracle" not in text, f
+    for f in os.listdir(os.path.join(ROOT, "oracle")):
+        if f.endswith((".py", ".c", ".h")):
+            text = open(os.path.join(ROOT, "oracle", f)).read()
+            assert "sparse_attention_paged_qsa_gb300" not in text, f
+            assert "qsa.h" not in text, f

@@ -1,0 +1,172 @@
+"""GPU parity: the CUDA path (through the C ABI) against the FP64 oracle.
+
+Every comparison is per (sequence, head) relative L2 over the 256 output
+dims, against the oracle rounded to bf16, with a 2e-3 bound.
+"""
+import numpy as np
+import pytest
+import torch
+
+import sparse_attention_paged_qsa_gb300 as qsa
+from sparse_attention_paged_qsa_gb300 import inputs as I
+from tests.helpers import compare, counters, gather_subset, run_cuda, run_oracle
+
+pytestmark = pytest.mark.gpu
+
+
+def _parity(w, dev, max_ctas=0):
+    wd = w.to(dev)
+    out, scratch = run_cuda(wd, max_ctas)
+    torch.cuda.synchronize()
+    ref = run_oracle(w)
+    eb, eu = compare(out, ref, w.lengths().numpy())
+    assert qsa.qsa_scratch_error(scratch) == 0
+    assert (counters(scratch, w.bs, w.num_q_heads, w.capacity) == 0).all()
+    return out, eb, eu
+
+
+@pytest.mark.parametrize("fmt", I.FORMATS)
+@pytest.mark.parametrize("length", [1, 31, 32, 33, 64, 77, 2055])
+def test_tiny_tp2(cuda_device, fmt, length):
+    w = I.tiny_tp2(seed=0, length=length, fmt=fmt)
+    _parity(w, cuda_device)
+
+
+@pytest.mark.parametrize("fmt", I.FORMATS)
+def test_tp1_mixed_lengths(cuda_device, fmt):
+    w = I.tp1_mixed(seed=1, bs=16, fmt=fmt)
+    _parity(w, cuda_device)
+
+
+@pytest.mark.parametrize("max_ctas", [1, 2, 3, 7, 0])
+def test_split_count_invariance(cuda_device, max_ctas):
+    """Forcing one CTA (no split) or several gives the same answer within rounding."""
+    w = I.tp1_mixed(seed=5, bs=6, num_slots=8192, lengths=[2055, 1, 700, 0, 64, 1500])
+    out, _, _ = _parity(w, cuda_device, max_ctas)
+    wd = w.to(cuda_device)
+    base, _ = run_cuda(wd, 1)
+    torch.cuda.synchronize()
+    a = out.float().cpu().double().numpy()
+    b = base.float().cpu().double().numpy()
+    num = np.sqrt(((a - b) ** 2).sum(-1))
+    den = np.sqrt((b ** 2).sum(-1))
+    live = den > 0
+    # both are bf16 roundings of nearly equal FP32 results: at most isolated 1-ulp flips
+    assert (num[live] / den[live]).max() <= 2e-3
+
+
+def test_edge_lengths_and_empty_rows(cuda_device):
+    lengths = [0, 1, 2055, 0, 5, 64, 65, 0, 33, 2054]
+    w = I.tp1_mixed(seed=6, bs=len(lengths), num_slots=16384, lengths=lengths)
+    _parity(w, cuda_device)
+
+
+def test_all_empty(cuda_device):
+    w = I.tp1_mixed(seed=6, bs=4, num_slots=1024, lengths=[0, 0, 0, 0])
+    w.capacity = 16
+    wd = w.to(cuda_device)
+    out, scratch = run_cuda(wd)
+    torch.cuda.synchronize()
+    assert (out == 0).all()
+    assert qsa.qsa_scratch_error(scratch) == 0
+
+
+def test_single_index_is_bitwise_the_v_row(cuda_device):
+    w = I.tp1_mixed(seed=7, bs=32, num_slots=4096, lengths=[1] * 32)
+    wd = w.to(cuda_device)
+    out, _ = run_cuda(wd)
+    torch.cuda.synchronize()
+    ref = torch.stack([w.v_pool[int(w.sel[b])].repeat_interleave(12, 0) for b in range(32)])
+    assert torch.equal(out.cpu(), ref)
+
+
+def test_duplicates_only(cuda_device):
+    """A selection of one slot repeated n times equals that slot's V row."""
+    w = I.tp1_mixed(seed=8, bs=3, num_slots=4096, lengths=[5, 300, 2055])
+    w.sel[:] = 1234
+    wd = w.to(cuda_device)
+    out, _ = run_cuda(wd)
+    torch.cuda.synchronize()
+    ref = w.v_pool[1234].repeat_interleave(12, 0)
+    for b in range(3):
+        assert torch.equal(out[b].cpu(), ref)
+
+
+def test_bs128_tiny_lengths(cuda_device):
+    g = torch.Generator().manual_seed(9)
+    lengths = torch.randint(0, 4, (128,), generator=g)
+    w = I.tp1_mixed(seed=9, bs=128, num_slots=4096, lengths=lengths)
+    _parity(w, cuda_device)
+
+
+def test_repeat_launches_deterministic_and_counters_reset(cuda_device):
+    w = I.tp1_mixed(seed=10, bs=17, num_slots=65536, max_len=2055)
+    wd = w.to(cuda_device)
+    out0, scratch = run_cuda(wd)
+    outs = torch.empty_like(out0)
+    for _ in range(200):
+        run_cuda(wd, out=outs, scratch=scratch)
+    torch.cuda.synchronize()
+    assert torch.equal(out0, outs)
+    assert (counters(scratch, w.bs, w.num_q_heads, w.capacity) == 0).all()
+    assert qsa.qsa_scratch_error(scratch) == 0
+
+
+def test_device_error_flags(cuda_device):
+    w = I.tp1_mixed(seed=11, bs=4, num_slots=2048, lengths=[10, 20, 30, 40])
+    wd = w.to(cuda_device)
+    bad = wd.sel.clone()
+    bad[15] = w.num_slots + 5
+    bad[16] = -3
+    out = torch.empty_like(wd.q)
+    scratch = qsa.alloc_scratch(w.bs, w.num_q_heads, w.capacity, cuda_device)
+    meta = qsa.KVQuantMeta("bf16", w.capacity, None, None, w.softmax_scale)
+    qsa.qsa_decode(wd.q, wd.k_pool, wd.v_pool, meta, bad, wd.cu, out, scratch)
+    assert qsa.qsa_scratch_error(scratch, clear=True) == qsa.binding.DEVERR_SLOT_RANGE
+    assert qsa.qsa_scratch_error(scratch) == 0
+    # decreasing cu_seqlens and a length above capacity
+    cu = wd.cu.clone()
+    cu[2] = cu[1] - 1
+    qsa.qsa_decode(wd.q, wd.k_pool, wd.v_pool, meta, wd.sel, cu, out, scratch)
+    assert qsa.qsa_scratch_error(scratch, clear=True) & qsa.binding.DEVERR_CU_SEQLENS
+    meta_small = qsa.KVQuantMeta("bf16", 25, None, None, w.softmax_scale)
+    qsa.qsa_decode(wd.q, wd.k_pool, wd.v_pool, meta_small, wd.sel, wd.cu, out, scratch)
+    assert qsa.qsa_scratch_error(scratch, clear=True) & qsa.binding.DEVERR_CU_SEQLENS
+    # the library keeps working afterwards
+    out2, _ = run_cuda(wd, scratch=scratch)
+    torch.cuda.synchronize()
+    compare(out2, run_oracle(w), w.lengths().numpy())
+    assert (counters(scratch, w.bs, w.num_q_heads, w.capacity) == 0).all()
+
+
+def test_strided_q_and_out(cuda_device):
+    """q and out may be views with padded batch/head strides."""
+    w = I.tp1_mixed(seed=12, bs=5, num_slots=4096, lengths=[3, 100, 2055, 40, 1])
+    wd = w.to(cuda_device)
+    qbig = torch.zeros(5, 30, 264, dtype=torch.bfloat16, device=cuda_device)
+    qv = qbig[:, 3:27, 8:]
+    qv.copy_(wd.q)
+    obig = torch.zeros(5, 26, 272, dtype=torch.bfloat16, device=cuda_device)
+    ov = obig[:, 1:25, 16:]
+    wd.q = qv
+    run_cuda(wd, out=ov)
+    torch.cuda.synchronize()
+    compare(ov, run_oracle(w), w.lengths().numpy())
+    assert (obig[:, 0] == 0).all() and (obig[:, :, :16] == 0).all()
+
+
+@pytest.mark.parametrize("fmt", I.FORMATS)
+def test_headline_saturated_sampled(cuda_device, fmt):
+    """bs=128, L=2055, 24Q/2KV over a 1M-slot pool: sampled sequences vs the oracle."""
+    w = I.tp1_saturated(seed=2, device=cuda_device, fmt=fmt)
+    out, scratch = run_cuda(w)
+    torch.cuda.synchronize()
+    rows = [0, 1, 37, 64, 100, 127]
+    sub = gather_subset(w, rows)
+    ref = run_oracle(sub)
+    compare(out[rows], ref, [2055] * len(rows))
+    assert qsa.qsa_scratch_error(scratch) == 0
+    assert (counters(scratch, w.bs, w.num_q_heads, w.capacity) == 0).all()
+    # every row is finite and non-degenerate
+    o = out.float()
+    assert torch.isfinite(o).all() and (o.abs().sum(-1) > 0).all()
