@@ -208,6 +208,7 @@ def run_native(args):
         raise RuntimeError(f"device error flags {err}")
 
     # e2e: host (pinned) q / slot ids / cu_seqlens -> device, decode, output -> host
+    e2e_steps = args.steps if not args.no_e2e else 0
     hq_ = [w.q.cpu().pin_memory() for w in works]
     hsel = [w.sel.cpu().pin_memory() for w in works]
     hcu = [w.cu.cpu().pin_memory() for w in works]
@@ -222,16 +223,18 @@ def run_native(args):
         qsa.qsa_decode(dq, w0.k_pool, w0.v_pool, meta, dsel, dcu, out, scratch, stream)
         hout.copy_(out, non_blocking=True)
 
-    for k in range(args.warmup):
-        e2e_step(k)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for k in range(args.steps):
-        e2e_step(k)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.steps
+    e2e_ms = float("nan")
+    if e2e_steps:
+        for k in range(args.warmup):
+            e2e_step(k)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for k in range(e2e_steps):
+            e2e_step(k)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / e2e_steps
     h2d = hq_[0].numel() * 2 + hsel[0].numel() * 4 + hcu[0].numel() * 4
     d2h = hout.numel() * 2
 
@@ -242,7 +245,7 @@ def run_native(args):
         step_ms, e2e_ms = float(t[0]), float(t[1])
     abytes = algorithmic_bytes(fmt)
     value = ws * abytes / (step_ms * 1e-3) / 1e9
-    e2e_val = ws * abytes / (e2e_ms * 1e-3) / 1e9
+    e2e_val = ws * abytes / (e2e_ms * 1e-3) / 1e9 if e2e_steps else None
     kernel_ms = sum(per) / len(per)
     achieved = abytes / (kernel_ms * 1e-3) / 1e9
     peak, peak_kind = measured_peaks()
@@ -277,7 +280,7 @@ def run_native(args):
                          "peak_source": f"{peak_kind} hbm_gbs",
                          "bytes_per_launch": abytes, "kernel_ms": kernel_ms},
             "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms} if e2e_steps else None,
             "gpu_launches": args.steps,
             "clocks": clk.summary(),
             "cpu_baseline": cpu,
@@ -297,6 +300,7 @@ def main():
     ap.add_argument("--index-sets", type=int, default=3)
     ap.add_argument("--cpu-rows", type=int, default=128,
                     help="sequences of the oracle CPU-baseline sample (0 disables)")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--ref-rows", type=int, default=8,
                     help="sequences per step of the --impl reference sample")
     args = ap.parse_args()

@@ -17,14 +17,18 @@
 //    a fixed (graph-captured) grid balances any length mix. A CTA whose range
 //    covers a whole (sequence, KV head) segment writes the output directly;
 //    segments cut between CTAs are merged by the last arriving CTA.
-//  * One producer warp gathers whole K/V rows with per-row bulk async copies
-//    (cp.async.bulk, the TMA engine) into a multi-stage shared-memory ring
-//    completed on mbarriers; slot ids are prefetched several stages ahead.
-//  * Four consumer warps: QK on mma.m16n8k16 (12 heads padded to 16 rows,
-//    8 tokens per warp), a per-stage max exchange with lazy rescaling, and
-//    PV computed transposed (O^T = V^T P^T) with P split into bf16 hi + lo
-//    columns (24 columns: 12 heads x {hi, lo}), each warp owning 64 of the
-//    256 output dims.
+//  * Warp-specialised CTA (one per SM): four producer warps, one per SM
+//    sub-partition, gather whole K/V rows with 16-byte cp.async into a
+//    multi-stage shared-memory ring of 64-token stages, completing each stage
+//    on an mbarrier; slot ids are prefetched a ring's depth ahead. Rows are
+//    stored with a 16-byte-chunk XOR swizzle (chunk ^ row % 8) so the
+//    ldmatrix reads below are bank-conflict free without padding.
+//  * Eight consumer warps (two per sub-partition): QK on mma.m16n8k16 with
+//    the 12 heads padded to 16 rows, 8 tokens per warp; a per-stage max
+//    exchange with lazy rescaling (the reference max only moves when a score
+//    exceeds it by 2^8); PV computed transposed, O^T = V^T P^T, with P split
+//    into bf16 hi + lo columns (24 columns: 12 heads x {hi, lo}) so P keeps
+//    ~16 significant bits; each warp owns 32 of the 256 output dims.
 //  * Quantised pools are converted exactly to bf16 in shared memory by the
 //    warp that consumes them; per-slot scales scale the scores (K) and the
 //    probabilities (V) in FP32, per-pool fp8 scales fold into constants.
@@ -47,56 +51,61 @@
 namespace qsa {
 
 constexpr int D = 256;
-constexpr int GROUP = 12;               // query heads per KV head
-constexpr int T = 32;                   // tokens per pipeline stage
-constexpr int NW = 4;                   // consumer warps
-constexpr int NTHREADS = (NW + 1) * 32; // + one producer warp
-constexpr int NCT = NW * 32;            // consumer threads
-constexpr int MT = D / NW / 16;         // 16-dim m-tiles per consumer warp in PV
-constexpr int BF_RS = 528;              // smem row stride of bf16 rows (512 + 16 pad)
-constexpr int PRS = T * 2 + 16;         // smem row stride of P^T rows (bytes)
-constexpr int OS_STRIDE = D + 4;        // epilogue rows (floats)
-constexpr float TAU = 8.0f;             // lazy-rescale threshold (log2 units)
+constexpr int GROUP = 12;                   // query heads per KV head
+constexpr int T = 64;                       // tokens per pipeline stage
+constexpr int NW = 8;                       // consumer warps
+constexpr int NP = 4;                       // producer warps
+constexpr int NCT = NW * 32;                // consumer threads
+constexpr int NTHREADS = (NW + NP) * 32;
+constexpr int TPW = T / NW;                 // QK tokens per consumer warp (one n8 tile)
+constexpr int DPW = D / NW;                 // PV output dims per consumer warp
+constexpr int MT = DPW / 16;                // 16-dim m-tiles per consumer warp
+constexpr int KK = T / 16;                  // PV k-steps per stage
+constexpr int TPP = T / NP;                 // tokens gathered per producer warp
+constexpr int BF_ROW = D * 2;               // bf16 row bytes (swizzled, unpadded)
+constexpr int Q_RS = 528;                   // Q tile row stride (512 + 16 pad)
+constexpr int PRS = T * 2 + 16;             // P^T row stride (bytes)
+constexpr float TAU = 8.0f;                 // lazy-rescale threshold (log2 units)
 constexpr int MAX_BS = 128;
 constexpr int MAX_CAPACITY = 2055;
 constexpr int MIN_TOKENS_PER_CTA = 64;
-constexpr int PART_O_BYTES = GROUP * D * 4;           // unnormalised O, fp32
-constexpr int PART_BYTES = 12416;                     // O + m[12] + l[12], 128-byte multiple
-constexpr long long WAIT_NS = 2000000000LL;           // bounded-wait limit (2 s)
-constexpr int BAR_CONSUMERS = 1;                      // named barrier id
+constexpr int PART_BYTES = 12416;           // fp32 O[12][256] + m[12] + l[12], 128-byte multiple
+constexpr long long WAIT_NS = 2000000000LL; // bounded-wait limit (2 s)
+constexpr int BAR_CONSUMERS = 1;            // named barrier id
+static_assert(TPW == 8 && MT >= 1 && TPP <= 32, "tile shape");
+static_assert(PART_BYTES >= (GROUP * D + 2 * GROUP) * 4, "partial slot size");
 
 template <int FMT> struct Traits;
 template <> struct Traits<QSA_KV_BF16> {
-    static constexpr int ROWB = 512, RS = 528, STAGES = 4;
+    static constexpr int ROWB = 512, STAGES = 3;
     static constexpr bool DEQ = false, SCALES = false;
 };
 template <> struct Traits<QSA_KV_FP8_E4M3> {
-    static constexpr int ROWB = 256, RS = 272, STAGES = 8;
+    static constexpr int ROWB = 256, STAGES = 4;
     static constexpr bool DEQ = true, SCALES = false;
 };
 template <> struct Traits<QSA_KV_INT8> {
-    static constexpr int ROWB = 256, RS = 272, STAGES = 8;
+    static constexpr int ROWB = 256, STAGES = 4;
     static constexpr bool DEQ = true, SCALES = true;
 };
 template <> struct Traits<QSA_KV_INT4> {
-    static constexpr int ROWB = 128, RS = 144, STAGES = 12;
+    static constexpr int ROWB = 128, STAGES = 6;
     static constexpr bool DEQ = true, SCALES = true;
 };
 
 template <int FMT> struct Layout {
     using Tr = Traits<FMT>;
-    static constexpr int STAGE_KV = T * Tr::RS;
+    static constexpr int STAGE_KV = T * Tr::ROWB;
     static constexpr int STAGE_SC = Tr::SCALES ? 2 * T * 4 : 0;
     static constexpr int STAGE_BYTES = 2 * STAGE_KV + STAGE_SC;
     static constexpr int PF = Tr::STAGES;       // slot-id prefetch distance (stages)
     static constexpr int R = PF + 1;            // slot-id ring entries
     static constexpr int off_stage = 0;
     static constexpr int off_kbf = off_stage + Tr::STAGES * STAGE_BYTES;
-    static constexpr int kbf_bytes = Tr::DEQ ? 2 * T * BF_RS : 0;
+    static constexpr int kbf_bytes = Tr::DEQ ? 2 * T * BF_ROW : 0;
     static constexpr int off_q = off_kbf + kbf_bytes;
-    static constexpr int off_p = off_q + 2 * 16 * BF_RS;
-    static constexpr int off_os = off_p + 2 * 24 * PRS;
-    static constexpr int off_red = off_os + GROUP * OS_STRIDE * 4;
+    static constexpr int off_p = off_q + 2 * 16 * Q_RS;
+    static constexpr int off_red = off_p + 2 * 24 * PRS;
     static constexpr int off_mref = off_red + 2 * NW * 16 * 4;
     static constexpr int off_lred = off_mref + 2 * 16 * 4;
     static constexpr int off_ring = off_lred + NW * 16 * 4;
@@ -108,7 +117,7 @@ template <int FMT> struct Layout {
     static constexpr int n_bars = 2 * Tr::STAGES + 4;
     static constexpr int TOTAL = off_bar + n_bars * 8;
     static_assert(TOTAL <= 227 * 1024, "shared memory budget");
-    static_assert(STAGE_BYTES % 16 == 0 && off_kbf % 16 == 0 && off_q % 16 == 0, "alignment");
+    static_assert(STAGE_BYTES % 128 == 0 && off_kbf % 128 == 0 && off_q % 16 == 0, "alignment");
 };
 
 struct Params {
@@ -130,6 +139,12 @@ struct Params {
     int bs, Hkv, capacity;
     float scale_log2; // softmax_scale * log2(e)
 };
+
+// Byte offset of 16-byte chunk `chunk` of row `row` in a swizzled row buffer.
+template <int ROWB>
+__device__ __forceinline__ int swz(int row, int chunk) {
+    return row * ROWB + ((chunk ^ (row & 7)) << 4);
+}
 
 // ------------------------------------------------------------------ PTX helpers
 
@@ -208,6 +223,9 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
 __device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() {
     asm volatile("cp.async.commit_group;" ::: "memory");
 }
@@ -282,7 +300,7 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
     return (b & 0x80u) ? -v : v;
 }
 
-// 16 raw bytes (8-bit formats) -> 16 bf16, stored as two uint4.
+// 16 raw bytes (8-bit formats) -> 16 bf16, as two 16-byte chunks.
 template <int FMT>
 __device__ __forceinline__ void dequant16_8bit(const uint4 raw, uint4& o0, uint4& o1) {
     const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
@@ -305,7 +323,8 @@ __device__ __forceinline__ void dequant16_8bit(const uint4 raw, uint4& o0, uint4
     o1 = make_uint4(r[4], r[5], r[6], r[7]);
 }
 
-// 16 raw bytes of int4 (32 nibbles, element 2i in the low nibble) -> 32 bf16.
+// 16 raw bytes of int4 (32 nibbles, element 2i in the low nibble) -> 32 bf16
+// as four 16-byte chunks.
 __device__ __forceinline__ void dequant32_int4(const uint4 raw, uint4* o) {
     const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
@@ -388,7 +407,7 @@ template <int FMT>
 __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p) {
     using Tr = Traits<FMT>;
     using Ly = Layout<FMT>;
-    extern __shared__ __align__(128) uint8_t smem[];
+    extern __shared__ __align__(1024) uint8_t smem[];
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -408,7 +427,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
     // ---------------------------------------------------------------- setup
     if (tid == 0) {
         for (int s = 0; s < Tr::STAGES; ++s) {
-            mbar_init(full_bar(s), Tr::SCALES ? 64 : 32);
+            // every producer lane arrives twice: once when its cp.async copies land
+            // (noinc), once in program order after its shared-memory stores
+            mbar_init(full_bar(s), NP * 64);
             mbar_init(empty_bar(s), NW);
         }
         for (int i = 0; i < 2; ++i) {
@@ -418,13 +439,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
         misc[0] = 0;
         fence_mbarrier_init();
     }
-    // zero the padding rows 12..15 of both Q buffers (rows of the 16-row MMA tile)
-    for (int i = tid; i < 2 * 4 * (BF_RS / 16); i += NTHREADS) {
-        const int buf = i / (4 * (BF_RS / 16));
-        const int rem = i % (4 * (BF_RS / 16));
-        uint4* dst = reinterpret_cast<uint4*>(smem + Ly::off_q + buf * 16 * BF_RS +
-                                              (12 + rem / (BF_RS / 16)) * BF_RS) +
-                     rem % (BF_RS / 16);
+    // zero the padding rows 12..15 of both Q tiles (rows of the 16-row MMA tile)
+    for (int i = tid; i < 2 * 4 * (Q_RS / 16); i += NTHREADS) {
+        const int buf = i / (4 * (Q_RS / 16));
+        const int rem = i % (4 * (Q_RS / 16));
+        uint4* dst = reinterpret_cast<uint4*>(smem + Ly::off_q + buf * 16 * Q_RS +
+                                              (12 + rem / (Q_RS / 16)) * Q_RS) +
+                     rem % (Q_RS / 16);
         *dst = make_uint4(0, 0, 0, 0);
     }
     // sanitised lengths, index offsets and prefix sums (warp 0; bs <= 128)
@@ -498,15 +519,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
     uint8_t* const stage0 = smem + Ly::off_stage;
     int* const ring = reinterpret_cast<int*>(smem + Ly::off_ring);
 
-    if (warp == NW) {
-        // ============================================================ producer
+    if (warp >= NW) {
+        // ============================================================ producers
+        // Producer warp pw gathers tokens [pw*TPP, (pw+1)*TPP) of every stage.
+        const int pw = warp - NW;
+        const int mytok = pw * TPP + lane;
         Cursor pc, ic;
         cursor_init(pc, t_begin, t_end, segL, segP, p.bs, Hkv);
         ic = pc;
         auto prefetch = [&](const Cursor& c, int entry) {
-            const int n = cursor_n(c);
-            if (lane < n)
-                cp_async4(smem_u32(ring + entry * T + lane), p.sel + segSrc[c.b] + c.j + lane);
+            if (lane < TPP && mytok < cursor_n(c))
+                cp_async4(smem_u32(ring + entry * T + mytok), p.sel + segSrc[c.b] + c.j + mytok);
         };
 #pragma unroll 1
         for (int i = 0; i < Ly::PF; ++i) {
@@ -516,6 +539,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
             }
             cp_async_commit();
         }
+        constexpr int CPR = Tr::ROWB / 16; // 16-byte chunks per row
+        constexpr int RPI = 32 / CPR;      // rows per warp-wide copy instruction
+        const int toff = lane / CPR, chunk = lane % CPR;
 #pragma unroll 1
         for (int i = 0; ic.t < t_end; ++i) {
             if (pc.t < t_end) {
@@ -527,51 +553,52 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
             __syncwarp();
             const int n = cursor_n(ic);
             const int b = ic.b, g = ic.g;
-            if (ic.segfirst) {
+            if (ic.segfirst && pw == 0) {
                 const int qb = ic.kseg & 1;
                 if (!mbar_wait(qempty_bar(qb), ((ic.kseg >> 1) & 1) ^ 1, p.err, abort_flag)) break;
                 if (lane == 0) mbar_arrive_expect_tx(qfull_bar(qb), GROUP * D * 2);
                 __syncwarp();
                 if (lane < GROUP)
-                    bulk_g2s(smem_u32(smem + Ly::off_q + qb * 16 * BF_RS + lane * BF_RS),
+                    bulk_g2s(smem_u32(smem + Ly::off_q + qb * 16 * Q_RS + lane * Q_RS),
                              p.q + b * p.q_sb + (g * GROUP + lane) * p.q_sh, D * 2, qfull_bar(qb));
             }
             const int s = i % Tr::STAGES;
             if (!mbar_wait(empty_bar(s), ((i / Tr::STAGES) & 1) ^ 1, p.err, abort_flag)) break;
-            uint8_t* Ks = stage0 + s * Ly::STAGE_BYTES;
-            uint8_t* Vs = Ks + Ly::STAGE_KV;
-            const bool valid = lane < n;
-            long long row = 0;
+            uint8_t* const Ks = stage0 + s * Ly::STAGE_BYTES;
+            uint8_t* const Vs = Ks + Ly::STAGE_KV;
+            long long myrow = 0;
+            const bool valid = lane < TPP && mytok < n;
             if (valid) {
-                int slot = ring[(i % Ly::R) * T + lane];
+                int slot = ring[(i % Ly::R) * T + mytok];
                 if (slot < 0 || (long long)slot >= p.num_slots) {
                     atomicOr(p.err, QSA_DEVERR_SLOT_RANGE);
                     slot = 0;
                 }
-                row = (long long)slot * Hkv + g;
-            } else {
-                uint4* z = reinterpret_cast<uint4*>(Vs + lane * Tr::RS);
-#pragma unroll
-                for (int k = 0; k < Tr::ROWB / 16; ++k) z[k] = make_uint4(0, 0, 0, 0);
-                fence_proxy_async();
+                myrow = (long long)slot * Hkv + g;
             }
-            __syncwarp();
-            if (lane == 0) mbar_expect_tx(full_bar(s), n * 2 * Tr::ROWB);
-            __syncwarp();
-            if (valid) {
-                bulk_g2s(smem_u32(Ks + lane * Tr::RS), p.kpool + row * Tr::ROWB, Tr::ROWB,
-                         full_bar(s));
-                bulk_g2s(smem_u32(Vs + lane * Tr::RS), p.vpool + row * Tr::ROWB, Tr::ROWB,
-                         full_bar(s));
+#pragma unroll
+            for (int t0 = 0; t0 < TPP; t0 += RPI) {
+                const int tl = t0 + toff;
+                const long long row = __shfl_sync(0xFFFFFFFFu, myrow, tl);
+                const int t = pw * TPP + tl;
+                if (t < n) {
+                    cp_async16(smem_u32(Ks + swz<Tr::ROWB>(t, chunk)),
+                               p.kpool + row * Tr::ROWB + chunk * 16);
+                    cp_async16(smem_u32(Vs + swz<Tr::ROWB>(t, chunk)),
+                               p.vpool + row * Tr::ROWB + chunk * 16);
+                } else {
+                    // rows past the live length hold zeros (P is 0 there, V must be finite)
+                    *reinterpret_cast<uint4*>(Vs + swz<Tr::ROWB>(t, chunk)) = make_uint4(0, 0, 0, 0);
+                }
             }
             if constexpr (Tr::SCALES) {
                 float* sc = reinterpret_cast<float*>(Vs + Ly::STAGE_KV);
                 if (valid) {
-                    cp_async4(smem_u32(sc + lane), p.k_scale + row);
-                    cp_async4(smem_u32(sc + T + lane), p.v_scale + row);
+                    cp_async4(smem_u32(sc + mytok), p.k_scale + myrow);
+                    cp_async4(smem_u32(sc + T + mytok), p.v_scale + myrow);
                 }
-                cp_async_arrive_noinc(full_bar(s));
             }
+            cp_async_arrive_noinc(full_bar(s));
             mbar_arrive(full_bar(s));
             cursor_advance(ic, t_end, segL, Hkv);
         }
@@ -590,7 +617,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
     float* const red = reinterpret_cast<float*>(smem + Ly::off_red);    // [2][NW][16]
     float* const mref = reinterpret_cast<float*>(smem + Ly::off_mref);  // [2][16]
     float* const lred = reinterpret_cast<float*>(smem + Ly::off_lred);  // [NW][16]
-    float* const Os = reinterpret_cast<float*>(smem + Ly::off_os);      // [12][OS_STRIDE]
     float* const mergeM = reinterpret_cast<float*>(misc + 16);
     float* const mergeDen = reinterpret_cast<float*>(misc + 32);
 
@@ -598,8 +624,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
     float o[MT][3][4];
     float l0 = 0.f, l1 = 0.f;
     int v = 0, buf = 0, seg_j0 = 0;
-    const int tok_base = warp * 8;
+    const int tok_base = warp * TPW;
     const int tk0 = tok_base + 2 * c;
+    const int xs = lane & 7;                 // row % 8 of every row this lane addresses
+    // QK B-fragment chunk pattern: matrix (lane >> 3) covers chunk 2*ks + cb
+    const int kx = ((((lane >> 3) & 1) + (lane >> 4) * 2) ^ xs) << 4;
+    // PV A-fragment chunk pattern: chunk 4*warp + 2*mt + ((lane >> 3) & 1)
+    const int vx = ((((lane >> 3) & 1)) ^ xs) << 4;
 
     Cursor cc;
     cursor_init(cc, t_begin, t_end, segL, segP, p.bs, Hkv);
@@ -613,12 +644,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
             seg_j0 = cc.j;
             const int qb = cc.kseg & 1;
             if (!mbar_wait(qfull_bar(qb), (cc.kseg >> 1) & 1, p.err, abort_flag)) break;
-            const uint32_t qbase = smem_u32(smem + Ly::off_q + qb * 16 * BF_RS);
+            const uint32_t qbase = smem_u32(smem + Ly::off_q + qb * 16 * Q_RS);
 #pragma unroll
             for (int ks = 0; ks < 16; ++ks) {
                 const int mi = lane >> 3;
                 const uint32_t addr =
-                    qbase + ((mi & 1) * 8 + (lane & 7)) * BF_RS + (ks * 16 + (mi >> 1) * 8) * 2;
+                    qbase + ((mi & 1) * 8 + (lane & 7)) * Q_RS + (ks * 16 + (mi >> 1) * 8) * 2;
                 ldsm_x4(qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], addr);
             }
             __syncwarp();
@@ -635,62 +666,59 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
         if (!mbar_wait(full_bar(s), (i / Tr::STAGES) & 1, p.err, abort_flag)) break;
         uint8_t* const Ks = stage0 + s * Ly::STAGE_BYTES;
         uint8_t* const Vs = Ks + Ly::STAGE_KV;
-        const uint8_t* Kb = Ks;   // bf16 rows [T][BF_RS] used by the MMAs
+        const uint8_t* Kb = Ks;   // bf16 rows [T][BF_ROW] (swizzled) used by the MMAs
         const uint8_t* Vb = Vs;
         float skr[2] = {1.f, 1.f}, svr[2] = {1.f, 1.f};
 
         if constexpr (Tr::DEQ) {
             uint8_t* const kbf = smem + Ly::off_kbf;
-            uint8_t* const vbf = kbf + T * BF_RS;
+            uint8_t* const vbf = kbf + T * BF_ROW;
             const int tt = lane & 7, ch = lane >> 3;
+            const int t = tok_base + tt;
             if constexpr (FMT == QSA_KV_INT4) {
-                // K: this warp's 8 tokens, 8 chunks of 16 bytes each
+                // K: this warp's 8 tokens; 8 raw chunks per row, 32 values each
 #pragma unroll
                 for (int it = 0; it < 2; ++it) {
-                    const int chunk = ch + 4 * it;
-                    const uint4 raw =
-                        *reinterpret_cast<const uint4*>(Ks + (tok_base + tt) * Tr::RS + chunk * 16);
+                    const int rc = ch + 4 * it;
+                    const uint4 raw = *reinterpret_cast<const uint4*>(Ks + swz<Tr::ROWB>(t, rc));
                     uint4 ov[4];
                     dequant32_int4(raw, ov);
-                    uint4* dst = reinterpret_cast<uint4*>(kbf + (tok_base + tt) * BF_RS + chunk * 64);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) dst[k] = ov[k];
+                    for (int k = 0; k < 4; ++k)
+                        *reinterpret_cast<uint4*>(kbf + swz<BF_ROW>(t, 4 * rc + k)) = ov[k];
                 }
-                // V: this warp's 64 dims (32 bytes) of all T tokens
-                const int t16 = lane & 15, ch2 = lane >> 4;
+                // V: this warp's 32 dims = raw chunk `warp` of every token
 #pragma unroll
                 for (int it = 0; it < 2; ++it) {
-                    const int tok = t16 + 16 * it;
-                    const uint4 raw = *reinterpret_cast<const uint4*>(Vs + tok * Tr::RS + warp * 32 +
-                                                                      ch2 * 16);
+                    const int tv = lane + 32 * it;
+                    const uint4 raw = *reinterpret_cast<const uint4*>(Vs + swz<Tr::ROWB>(tv, warp));
                     uint4 ov[4];
                     dequant32_int4(raw, ov);
-                    uint4* dst = reinterpret_cast<uint4*>(vbf + tok * BF_RS + (warp * 64 + ch2 * 32) * 2);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) dst[k] = ov[k];
+                    for (int k = 0; k < 4; ++k)
+                        *reinterpret_cast<uint4*>(vbf + swz<BF_ROW>(tv, 4 * warp + k)) = ov[k];
                 }
             } else {
+                // K: this warp's 8 tokens; 16 raw chunks per row, 16 values each
 #pragma unroll
                 for (int it = 0; it < 4; ++it) {
-                    const int chunk = ch + 4 * it;
-                    const uint4 raw =
-                        *reinterpret_cast<const uint4*>(Ks + (tok_base + tt) * Tr::RS + chunk * 16);
+                    const int rc = ch + 4 * it;
+                    const uint4 raw = *reinterpret_cast<const uint4*>(Ks + swz<Tr::ROWB>(t, rc));
                     uint4 o0, o1;
                     dequant16_8bit<FMT>(raw, o0, o1);
-                    uint4* dst = reinterpret_cast<uint4*>(kbf + (tok_base + tt) * BF_RS + chunk * 32);
-                    dst[0] = o0;
-                    dst[1] = o1;
+                    *reinterpret_cast<uint4*>(kbf + swz<BF_ROW>(t, 2 * rc)) = o0;
+                    *reinterpret_cast<uint4*>(kbf + swz<BF_ROW>(t, 2 * rc + 1)) = o1;
                 }
+                // V: this warp's 32 dims = raw chunks 2*warp, 2*warp+1 of every token
 #pragma unroll
                 for (int it = 0; it < 4; ++it) {
-                    const int tok = tt + 8 * it;
-                    const uint4 raw =
-                        *reinterpret_cast<const uint4*>(Vs + tok * Tr::RS + warp * 64 + ch * 16);
+                    const int task = it * 32 + lane;
+                    const int tv = task >> 1, rc = 2 * warp + (task & 1);
+                    const uint4 raw = *reinterpret_cast<const uint4*>(Vs + swz<Tr::ROWB>(tv, rc));
                     uint4 o0, o1;
                     dequant16_8bit<FMT>(raw, o0, o1);
-                    uint4* dst = reinterpret_cast<uint4*>(vbf + tok * BF_RS + (warp * 64 + ch * 16) * 2);
-                    dst[0] = o0;
-                    dst[1] = o1;
+                    *reinterpret_cast<uint4*>(vbf + swz<BF_ROW>(tv, 2 * rc)) = o0;
+                    *reinterpret_cast<uint4*>(vbf + swz<BF_ROW>(tv, 2 * rc + 1)) = o1;
                 }
             }
             if constexpr (Tr::SCALES) {
@@ -709,12 +737,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
         // ---------------------------------------------------------------- QK
         float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         {
-            const uint32_t kbase = smem_u32(Kb) + (tok_base + (lane & 7)) * BF_RS +
-                                   ((lane >> 3) & 1) * 16 + (lane >> 4) * 32;
+            const uint32_t krow = smem_u32(Kb) + (tok_base + (lane & 7)) * BF_ROW;
 #pragma unroll
             for (int ks = 0; ks < 16; ks += 2) {
                 uint32_t b0, b1, b2, b3;
-                ldsm_x4(b0, b1, b2, b3, kbase + ks * 32);
+                ldsm_x4(b0, b1, b2, b3, krow + ((ks * 32) ^ kx));
                 mma_bf16(sacc[0], qa[ks], b0, b1);
                 mma_bf16(sacc[1], qa[ks + 1], b2, b3);
             }
@@ -738,8 +765,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
             redb[warp * 16 + r + 8] = mb;
         }
         const float* const mrefv = mref + v * 16;
-        float mo_a = first ? ninf : mrefv[r];
-        float mo_b = first ? ninf : mrefv[r + 8];
+        const float mo_a = first ? ninf : mrefv[r];
+        const float mo_b = first ? ninf : mrefv[r + 8];
 
         uint8_t* const Pb = smem + Ly::off_p + buf * 24 * PRS;
         float pr[4];
@@ -778,9 +805,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
             return m;
         };
         auto old_ref = [&](int h) { return first ? ninf : mrefv[h]; };
-        bool nd = first || stage_max(r) > mo_a + TAU || (row8 && stage_max(r + 8) > mo_b + TAU);
+        const bool nd = first || stage_max(r) > mo_a + TAU || (row8 && stage_max(r + 8) > mo_b + TAU);
         if (__any_sync(0xFFFFFFFFu, nd)) {
-            // slow path (uniform over the four warps): raise the reference max
+            // slow path (uniform over the consumer warps): raise the reference max
             auto new_ref = [&](int h) { return fmaxf(old_ref(h), stage_max(h)); };
             auto alpha = [&](int h) {
                 const float mo = old_ref(h);
@@ -816,27 +843,23 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
 
         // ---------------------------------------------------------------- PV
         {
-            uint32_t pb[2][3][2];
             const uint32_t pbase = smem_u32(Pb);
+            const uint32_t vrow = smem_u32(Vb) + ((lane >> 4) * 8 + (lane & 7)) * BF_ROW;
 #pragma unroll
-            for (int kk = 0; kk < 2; ++kk) {
-                const uint32_t a4 = pbase + ((lane >> 4) * 8 + (lane & 7)) * PRS +
-                                    (kk * 16 + ((lane >> 3) & 1) * 8) * 2;
-                ldsm_x4(pb[kk][0][0], pb[kk][0][1], pb[kk][1][0], pb[kk][1][1], a4);
-                const uint32_t a2 =
-                    pbase + (16 + (lane & 7)) * PRS + (kk * 16 + ((lane >> 3) & 1) * 8) * 2;
-                ldsm_x2(pb[kk][2][0], pb[kk][2][1], a2);
-            }
-            const uint32_t vbase = smem_u32(Vb) + ((lane >> 4) * 8 + (lane & 7)) * BF_RS +
-                                   (warp * (D / NW) + ((lane >> 3) & 1) * 8) * 2;
+            for (int kk = 0; kk < KK; ++kk) {
+                uint32_t pb[3][2];
+                ldsm_x4(pb[0][0], pb[0][1], pb[1][0], pb[1][1],
+                        pbase + ((lane >> 4) * 8 + (lane & 7)) * PRS +
+                            (kk * 16 + ((lane >> 3) & 1) * 8) * 2);
+                ldsm_x2(pb[2][0], pb[2][1],
+                        pbase + (16 + (lane & 7)) * PRS + (kk * 16 + ((lane >> 3) & 1) * 8) * 2);
 #pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
-#pragma unroll
-                for (int kk = 0; kk < 2; ++kk) {
+                for (int mt = 0; mt < MT; ++mt) {
                     uint32_t a[4];
-                    ldsm_x4_t(a[0], a[1], a[2], a[3], vbase + kk * 16 * BF_RS + mt * 32);
+                    ldsm_x4_t(a[0], a[1], a[2], a[3],
+                              vrow + kk * 16 * BF_ROW + (((4 * warp + 2 * mt) << 4) ^ vx));
 #pragma unroll
-                    for (int j = 0; j < 3; ++j) mma_bf16(o[mt][j], a, pb[kk][j][0], pb[kk][j][1]);
+                    for (int j = 0; j < 3; ++j) mma_bf16(o[mt][j], a, pb[j][0], pb[j][1]);
                 }
             }
         }
@@ -871,46 +894,36 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
             const float fB = complete ? out_scale / ltot(hB) : 1.f;
             const float fC = (complete && c < 2) ? out_scale / ltot(hC) : 1.f;
             const float fD = (complete && c < 2) ? out_scale / ltot(hD) : 1.f;
+            __nv_bfloat16* const outb = p.out + b * p.o_sb + (long long)(g * GROUP) * p.o_sh;
+            float* const part = reinterpret_cast<float*>(
+                p.part + ((long long)blockIdx.x * 2 + (cc.kseg == 0 ? 0 : 1)) * PART_BYTES);
+            auto put = [&](int h, int d, float val) {
+                if (complete)
+                    outb[h * p.o_sh + d] = __float2bfloat16_rn(val);
+                else
+                    part[h * D + d] = val;
+            };
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt) {
-                const int dA = warp * (D / NW) + mt * 16 + r, dB = dA + 8;
-                Os[hA * OS_STRIDE + dA] = (o[mt][0][0] + o[mt][1][0]) * fA;
-                Os[hB * OS_STRIDE + dA] = (o[mt][0][1] + o[mt][1][1]) * fB;
-                Os[hA * OS_STRIDE + dB] = (o[mt][0][2] + o[mt][1][2]) * fA;
-                Os[hB * OS_STRIDE + dB] = (o[mt][0][3] + o[mt][1][3]) * fB;
+                const int dA = warp * DPW + mt * 16 + r, dB = dA + 8;
+                put(hA, dA, (o[mt][0][0] + o[mt][1][0]) * fA);
+                put(hB, dA, (o[mt][0][1] + o[mt][1][1]) * fB);
+                put(hA, dB, (o[mt][0][2] + o[mt][1][2]) * fA);
+                put(hB, dB, (o[mt][0][3] + o[mt][1][3]) * fB);
                 float u[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) u[e] = __shfl_xor_sync(0xFFFFFFFFu, o[mt][2][e], 2);
                 if (c < 2) {
-                    Os[hC * OS_STRIDE + dA] = (o[mt][2][0] + u[0]) * fC;
-                    Os[hD * OS_STRIDE + dA] = (o[mt][2][1] + u[1]) * fD;
-                    Os[hC * OS_STRIDE + dB] = (o[mt][2][2] + u[2]) * fC;
-                    Os[hD * OS_STRIDE + dB] = (o[mt][2][3] + u[3]) * fD;
+                    put(hC, dA, (o[mt][2][0] + u[0]) * fC);
+                    put(hD, dA, (o[mt][2][1] + u[1]) * fD);
+                    put(hC, dB, (o[mt][2][2] + u[2]) * fC);
+                    put(hD, dB, (o[mt][2][3] + u[3]) * fD);
                 }
             }
-            consumer_sync();
-            __nv_bfloat16* const outb = p.out + b * p.o_sb + (long long)(g * GROUP) * p.o_sh;
-            if (complete) {
-                for (int ch = tid; ch < GROUP * (D / 8); ch += NCT) {
-                    const int h = ch / (D / 8), d0 = (ch % (D / 8)) * 8;
-                    const float4 x0 = *reinterpret_cast<const float4*>(Os + h * OS_STRIDE + d0);
-                    const float4 x1 = *reinterpret_cast<const float4*>(Os + h * OS_STRIDE + d0 + 4);
-                    *reinterpret_cast<uint4*>(outb + h * p.o_sh + d0) =
-                        make_uint4(pack_bf16x2(x0.x, x0.y), pack_bf16x2(x0.z, x0.w),
-                                   pack_bf16x2(x1.x, x1.y), pack_bf16x2(x1.z, x1.w));
-                }
-            } else {
-                const float* const mfin = mref + v * 16;
-                uint8_t* const part =
-                    p.part + ((long long)blockIdx.x * 2 + (cc.kseg == 0 ? 0 : 1)) * PART_BYTES;
-                for (int ch = tid; ch < GROUP * (D / 4); ch += NCT) {
-                    const int h = ch / (D / 4), d0 = (ch % (D / 4)) * 4;
-                    *reinterpret_cast<float4*>(part + (h * D + d0) * 4) =
-                        *reinterpret_cast<const float4*>(Os + h * OS_STRIDE + d0);
-                }
+            if (!complete) {
                 if (tid < GROUP) {
-                    reinterpret_cast<float*>(part + PART_O_BYTES)[tid] = mfin[tid];
-                    reinterpret_cast<float*>(part + PART_O_BYTES + GROUP * 4)[tid] = ltot(tid);
+                    part[GROUP * D + tid] = mref[v * 16 + tid];
+                    part[GROUP * D + GROUP + tid] = ltot(tid);
                 }
                 __threadfence();
                 consumer_sync();
@@ -924,18 +937,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
                 consumer_sync();
                 if (misc[1]) {
                     __threadfence();
-                    auto part_of = [&](long long cta) -> const uint8_t* {
+                    auto part_of = [&](long long cta) -> const float* {
                         const int slot = (cta == c_first && cta_begin(cta, N, G) < Fs) ? 1 : 0;
-                        return p.part + (cta * 2 + slot) * PART_BYTES;
+                        return reinterpret_cast<const float*>(p.part + (cta * 2 + slot) * PART_BYTES);
                     };
                     if (tid < GROUP) {
                         float M = ninf;
                         for (long long k = c_first; k <= c_last; ++k)
-                            M = fmaxf(M, __ldcg(reinterpret_cast<const float*>(part_of(k) +
-                                                                               PART_O_BYTES) + tid));
+                            M = fmaxf(M, __ldcg(part_of(k) + GROUP * D + tid));
                         float den = 0.f;
                         for (long long k = c_first; k <= c_last; ++k) {
-                            const float* mk = reinterpret_cast<const float*>(part_of(k) + PART_O_BYTES);
+                            const float* mk = part_of(k) + GROUP * D;
                             const float mv = __ldcg(mk + tid);
                             if (mv != ninf) den += __ldcg(mk + GROUP + tid) * ex2(mv - M);
                         }
@@ -948,11 +960,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
                         const float M = mergeM[h];
                         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
                         for (long long k = c_first; k <= c_last; ++k) {
-                            const uint8_t* pk = part_of(k);
-                            const float mv = __ldcg(reinterpret_cast<const float*>(pk + PART_O_BYTES) + h);
+                            const float* pk = part_of(k);
+                            const float mv = __ldcg(pk + GROUP * D + h);
                             if (mv == ninf) continue;
                             const float w = ex2(mv - M);
-                            const float4 ov = __ldcg(reinterpret_cast<const float4*>(pk + (h * D + d0) * 4));
+                            const float4 ov = __ldcg(reinterpret_cast<const float4*>(pk + h * D + d0));
                             acc.x += w * ov.x;
                             acc.y += w * ov.y;
                             acc.z += w * ov.z;
