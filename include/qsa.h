@@ -165,6 +165,39 @@ const char* qsa_strerror(int code);
 /* Descriptive message of the last failing call on this host thread ("" if none). */
 const char* qsa_last_error_message(void);
 
+/*
+ * qsa_decode_static_scratch -- qsa_decode without a caller-provided scratch
+ * buffer. The pages have no counterpart to this entry point.
+ *
+ * For callers that cannot allocate device memory when they call: code whose
+ * memory is fixed up front and that may not call cudaMalloc (or a framework
+ * allocator) on the call path, e.g. an inference-engine plugin with a preset
+ * memory budget or a host loop where an allocation would synchronise the
+ * device, and bindings that hold pointers to tensors but own no allocator.
+ * It allocates nothing: its scratch is one file-scope device array of
+ * 3,974,400 bytes (256-byte aligned) that every GPU which loads libqsa holds
+ * until the process exits.
+ *
+ * Arguments as for qsa_decode, minus scratch. The grid is capped at 160 CTAs
+ * so the split-KV partials fit the array; kv_quant_meta->max_ctas may lower
+ * that cap. Every size the decode contract admits fits; anything else is
+ * rejected like qsa_decode does (QSA_ERR_UNSUPPORTED, QSA_ERR_SCRATCH_TOO_SMALL,
+ * ... with qsa_last_error_message()).
+ *
+ * The first call on each device (with that device current) looks up the
+ * array's device address; make that first call before any stream capture.
+ * Each call enqueues a 1,280-byte memset that clears the array's error word
+ * and counters, then the decode kernel, both on `stream`. All calls on a
+ * device share the one array, which keeps the last call's contents: calls
+ * that overlap on the GPU (unordered streams, concurrent host threads) race
+ * on it and must be serialised by the caller. The device error word is not
+ * readable through this entry point.
+ */
+int qsa_decode_static_scratch(const qsa_tensor* q, const qsa_tensor* k_pool,
+                              const qsa_tensor* v_pool, const qsa_kv_quant_meta* kv_quant_meta,
+                              const qsa_tensor* sel_indices, const qsa_tensor* cu_seqlens,
+                              const qsa_tensor* out, void* stream);
+
 /* Library version, major * 10000 + minor * 100 + patch. */
 int qsa_version(void);
 

@@ -35,7 +35,7 @@ _TORCH_DTYPES = {
 EXPORTED = (
     "qsa_decode", "qsa_decode_scratch_bytes", "qsa_decode_grid", "qsa_decode_scratch_layout",
     "qsa_scratch_init", "qsa_scratch_error", "qsa_strerror", "qsa_last_error_message",
-    "qsa_version",
+    "qsa_version", "qsa_decode_static_scratch",
 )
 
 
@@ -79,6 +79,10 @@ def load() -> ctypes.CDLL:
     lib.qsa_decode.argtypes = [P(QsaTensor), P(QsaTensor), P(QsaTensor), P(QsaKvQuantMeta),
                                P(QsaTensor), P(QsaTensor), P(QsaTensor), ctypes.c_void_p,
                                ctypes.c_size_t, ctypes.c_void_p]
+    lib.qsa_decode_static_scratch.restype = ctypes.c_int
+    lib.qsa_decode_static_scratch.argtypes = [P(QsaTensor), P(QsaTensor), P(QsaTensor),
+                                              P(QsaKvQuantMeta), P(QsaTensor), P(QsaTensor),
+                                              P(QsaTensor), ctypes.c_void_p]
     lib.qsa_decode_scratch_bytes.restype = ctypes.c_size_t
     lib.qsa_decode_scratch_bytes.argtypes = [ctypes.c_int32] * 3
     lib.qsa_decode_grid.restype = ctypes.c_int32

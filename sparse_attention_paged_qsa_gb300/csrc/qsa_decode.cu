@@ -1282,3 +1282,61 @@ int qsa_decode(const qsa_tensor* q, const qsa_tensor* k_pool, const qsa_tensor* 
 }
 
 } // extern "C"
+
+// ============================================ decode without caller-provided scratch
+//
+// qsa_decode_static_scratch is qsa_decode for callers that cannot allocate
+// device memory at call time. Its scratch is one file-scope device array of
+// fixed size, created when the library is loaded and held by every GPU that
+// loads it until the process exits.
+
+namespace {
+
+constexpr int STATIC_MAX_CTAS = 160;                 // grid cap of this entry point
+constexpr size_t STATIC_HEADER_BYTES = 256 + 1024;   // error word + 256 counters
+constexpr size_t STATIC_SCRATCH_BYTES =
+    STATIC_HEADER_BYTES + (size_t)STATIC_MAX_CTAS * 2 * PART_BYTES; // 3,974,400 bytes
+
+void* g_static_ptr[64] = {nullptr};                  // per-device address, under g_mu
+
+} // namespace
+
+static __device__ __align__(256) unsigned char g_static_scratch[STATIC_SCRATCH_BYTES];
+
+extern "C" int qsa_decode_static_scratch(const qsa_tensor* q, const qsa_tensor* k_pool,
+                                         const qsa_tensor* v_pool,
+                                         const qsa_kv_quant_meta* kv_quant_meta,
+                                         const qsa_tensor* sel_indices,
+                                         const qsa_tensor* cu_seqlens, const qsa_tensor* out,
+                                         void* stream) {
+    if (kv_quant_meta == nullptr) return fail(QSA_ERR_INVALID_ARGUMENT, "kv_quant_meta is NULL");
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(QSA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= 64) return fail(QSA_ERR_CUDA, "device ordinal %d out of range", dev);
+    void* ptr = nullptr;
+    {
+        // Set-up, once per device, with that device current: the array's name is
+        // only a host-side stand-in, so look up its device address.
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (g_static_ptr[dev] == nullptr) {
+            void* addr = nullptr;
+            e = cudaGetSymbolAddress(&addr, g_static_scratch);
+            if (e != cudaSuccess)
+                return fail(QSA_ERR_CUDA, "cudaGetSymbolAddress(static scratch): %s",
+                            cudaGetErrorString(e));
+            g_static_ptr[dev] = addr;
+        }
+        ptr = g_static_ptr[dev];
+    }
+    // Cap the grid so the partial results fit the fixed array; any size the
+    // decode contract admits then fits, and qsa_decode rejects the rest.
+    qsa_kv_quant_meta meta = *kv_quant_meta;
+    if (meta.max_ctas <= 0 || meta.max_ctas > STATIC_MAX_CTAS) meta.max_ctas = STATIC_MAX_CTAS;
+    // The array keeps the previous call's contents: the error word and the
+    // arrival counters must start at zero.
+    e = cudaMemsetAsync(ptr, 0, STATIC_HEADER_BYTES, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(QSA_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(e));
+    return qsa_decode(q, k_pool, v_pool, &meta, sel_indices, cu_seqlens, out, ptr,
+                      STATIC_SCRATCH_BYTES, stream);
+}
