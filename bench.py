@@ -61,6 +61,22 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+def measured_traffic(fmt: str):
+    """DRAM bytes per launch from profiles/traffic.txt, if taken on the current kernel source."""
+    import hashlib
+
+    src = os.path.join(ROOT, "sparse_attention_paged_qsa_gb300", "csrc", "qsa_decode.cu")
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    for line in open(path):
+        parts = line.split()
+        if len(parts) == 3 and not line.startswith("#") and parts[0] == fmt and parts[2] == sha:
+            return int(parts[1])
+    return None
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle sampling during the timed region."""
 
@@ -259,11 +275,7 @@ def run_native(args):
         cpu = cpu_baseline(fmt, args.cpu_rows, works[0])
 
     if rank == 0:
-        traffic = None
-        tpath = os.path.join(ROOT, "profiles", f"traffic_{fmt}.json")
-        if os.path.exists(tpath):
-            with open(tpath) as f:
-                traffic = json.load(f).get("bytes_per_launch")
+        traffic = measured_traffic(fmt)
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
