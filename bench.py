@@ -52,6 +52,22 @@ def dist_env():
     return ws, rank, local
 
 
+def reduce_max(values, device):
+    """Element-wise max of a list of floats over all ranks (identity when not distributed)."""
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def whole_job_gbs(world: int, bytes_per_rank_step: int, step_ms: float) -> float:
+    """Aggregate GB/s: every rank moves its own bytes per step; time is the slowest rank's."""
+    return world * bytes_per_rank_step / (step_ms * 1e-3) / 1e9
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -255,13 +271,10 @@ def run_native(args):
     d2h = hout.numel() * 2
 
     step_ms = total_ms / args.steps
-    if ws > 1:
-        t = torch.tensor([step_ms, e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        step_ms, e2e_ms = float(t[0]), float(t[1])
+    step_ms, e2e_ms = reduce_max([step_ms, e2e_ms if e2e_steps else 0.0], dev)
     abytes = algorithmic_bytes(fmt)
-    value = ws * abytes / (step_ms * 1e-3) / 1e9
-    e2e_val = ws * abytes / (e2e_ms * 1e-3) / 1e9 if e2e_steps else None
+    value = whole_job_gbs(ws, abytes, step_ms)
+    e2e_val = whole_job_gbs(ws, abytes, e2e_ms) if e2e_steps else None
     kernel_ms = sum(per) / len(per)
     achieved = abytes / (kernel_ms * 1e-3) / 1e9
     peak, peak_kind = measured_peaks()
