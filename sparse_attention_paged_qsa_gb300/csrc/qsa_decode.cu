@@ -29,14 +29,18 @@
 //    exceeds it by 2^8); PV computed transposed, O^T = V^T P^T, with P split
 //    into bf16 hi + lo columns (24 columns: 12 heads x {hi, lo}) so P keeps
 //    ~16 significant bits; each warp owns 32 of the 256 output dims.
-//  * Quantised pools are converted exactly to bf16 in shared memory by the
-//    warp that consumes them; per-slot scales scale the scores (K) and the
-//    probabilities (V) in FP32, per-pool fp8 scales fold into constants.
+//  * Quantised pools are converted exactly, in shared memory, by the warp
+//    that consumes them: codes become f16 for QK (Q is rescaled per head by a
+//    power of two so it converts to f16 exactly) and f16 (fp8) or bf16
+//    (int8/int4) for PV, with magic-number integer conversions and the
+//    hardware e4m3 conversion. Per-slot scales scale the scores (K) and the
+//    probabilities (V) in FP32; per-pool fp8 scales fold into constants.
 //  * Every wait is bounded; bad slot ids / cu_seqlens set a sticky error
 //    word and are clamped, never trapped.
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include <cmath>
 #include <cstdarg>
@@ -75,22 +79,26 @@ constexpr int BAR_CONSUMERS = 1;            // named barrier id
 static_assert(TPW == 8 && MT >= 1 && TPP <= 32, "tile shape");
 static_assert(PART_BYTES >= (GROUP * D + 2 * GROUP) * 4, "partial slot size");
 
+// ROWB: pool row bytes; DEQ: rows are converted in shared memory; SCALES:
+// per-(slot, KV head) fp32 scales; QK_F16: QK runs on f16 operands (exact
+// integer / e4m3 codes, Q rescaled per head by a power of two); PV_F16: PV runs
+// on f16 operands (only when no per-slot scale enters P).
 template <int FMT> struct Traits;
 template <> struct Traits<QSA_KV_BF16> {
     static constexpr int ROWB = 512, STAGES = 3;
-    static constexpr bool DEQ = false, SCALES = false;
+    static constexpr bool DEQ = false, SCALES = false, QK_F16 = false, PV_F16 = false;
 };
 template <> struct Traits<QSA_KV_FP8_E4M3> {
     static constexpr int ROWB = 256, STAGES = 4;
-    static constexpr bool DEQ = true, SCALES = false;
+    static constexpr bool DEQ = true, SCALES = false, QK_F16 = true, PV_F16 = true;
 };
 template <> struct Traits<QSA_KV_INT8> {
     static constexpr int ROWB = 256, STAGES = 4;
-    static constexpr bool DEQ = true, SCALES = true;
+    static constexpr bool DEQ = true, SCALES = true, QK_F16 = true, PV_F16 = false;
 };
 template <> struct Traits<QSA_KV_INT4> {
     static constexpr int ROWB = 128, STAGES = 6;
-    static constexpr bool DEQ = true, SCALES = true;
+    static constexpr bool DEQ = true, SCALES = true, QK_F16 = true, PV_F16 = false;
 };
 
 template <int FMT> struct Layout {
@@ -274,6 +282,23 @@ __device__ __forceinline__ void mma_bf16(float* d, const uint32_t* a, uint32_t b
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// D += A(16x16, row) * B(16x8, col), f16 inputs, fp32 accumulators.
+__device__ __forceinline__ void mma_f16(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+template <bool F16>
+__device__ __forceinline__ void mma16816(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+    if constexpr (F16)
+        mma_f16(d, a, b0, b1);
+    else
+        mma_bf16(d, a, b0, b1);
+}
+
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -286,56 +311,114 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
-
-// ------------------------------------------------------------ exact dequant
-
-// OCP e4m3fn byte -> float, exactly. The 7 magnitude bits placed at binary32
-// bits [26:20] encode value * 2^-120 for normals and subnormals alike
-// (exponent bias 127 vs 7); multiplying by 2^120 restores the value. The
-// all-ones magnitude is NaN in e4m3fn.
-__device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
-    const uint32_t m = b & 0x7Fu;
-    float v = __uint_as_float(m << 20) * 0x1p120f;
-    v = (m == 0x7Fu) ? __uint_as_float(0x7FC00000u) : v;
-    return (b & 0x80u) ? -v : v;
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ float f16_lo(uint32_t v) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(v & 0xFFFFu)));
+}
+__device__ __forceinline__ float f16_hi(uint32_t v) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(v >> 16)));
+}
+// Two probabilities as a packed pair of the PV operand type, plus the
+// rounding residual pair (the "lo" term of the hi + lo split).
+template <bool F16>
+__device__ __forceinline__ void split_pair(float a, float b, uint32_t& hi, uint32_t& lo) {
+    if constexpr (F16) {
+        hi = pack_f16x2(a, b);
+        lo = pack_f16x2(a - f16_lo(hi), b - f16_hi(hi));
+    } else {
+        hi = pack_bf16x2(a, b);
+        lo = pack_bf16x2(a - bf16_lo(hi), b - bf16_hi(hi));
+    }
 }
 
-// 16 raw bytes (8-bit formats) -> 16 bf16, as two 16-byte chunks.
-template <int FMT>
-__device__ __forceinline__ void dequant16_8bit(const uint4 raw, uint4& o0, uint4& o1) {
+// ------------------------------------------------------------ exact dequant
+//
+// Every conversion below is exact: the codes (|int8| <= 128, |int4| <= 8,
+// e4m3 with 4 significant bits and |x| <= 448) are representable in f16 and
+// bf16. Integers use the magic-number construction: a byte u placed in the
+// low mantissa bits of a float whose exponent gives a mantissa step of 1 reads
+// as (magic + u); subtracting (magic + offset) leaves the code.
+
+__device__ __forceinline__ uint32_t sub_f16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t sub_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// 4 int8 codes -> 2 f16x2: 0x64uu is 1024 + u; u = code ^ 0x80 = code + 128.
+__device__ __forceinline__ void i8x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    const uint32_t x = w ^ 0x80808080u;
+    lo = sub_f16x2(__byte_perm(x, 0x64646464u, 0x4140), 0x64806480u); // - 1152
+    hi = sub_f16x2(__byte_perm(x, 0x64646464u, 0x4342), 0x64806480u);
+}
+
+// 4 int8 codes -> 2 bf16x2. bf16 has 7 stored mantissa bits, so the sign bit
+// is handled apart: 0x43 0b0mmmmmmm is 128 + (code & 127) and 0x43 0bs0000000
+// is 128 or 256 by the sign bit; their difference is the two's-complement code.
+__device__ __forceinline__ void i8x4_to_bf16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    const uint32_t t0 = __byte_perm(w, 0u, 0x4140), t1 = __byte_perm(w, 0u, 0x4342);
+    lo = sub_bf16x2((t0 & 0x007F007Fu) | 0x43004300u, (t0 & 0x00800080u) | 0x43004300u);
+    hi = sub_bf16x2((t1 & 0x007F007Fu) | 0x43004300u, (t1 & 0x00800080u) | 0x43004300u);
+}
+
+// 8 int4 codes (channel 2i in the low nibble) -> 4 packed pairs, f16 or bf16:
+// nibble u = code ^ 8 = code + 8 under the magic 1024 (f16) or 128 (bf16).
+template <bool F16>
+__device__ __forceinline__ void i4x8_to(uint32_t w, uint32_t* o) {
+    constexpr uint32_t MAGIC = F16 ? 0x64006400u : 0x43004300u;
+    constexpr uint32_t BIAS = F16 ? 0x64086408u : 0x43084308u; // 1032 / 136
+    const uint32_t x = w ^ 0x88888888u;
+    const uint32_t hs = x >> 4;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t t = __byte_perm(x, hs, k | ((4 + k) << 8));
+        const uint32_t v = (t & 0x000F000Fu) | MAGIC;
+        o[k] = F16 ? sub_f16x2(v, BIAS) : sub_bf16x2(v, BIAS);
+    }
+}
+
+// 4 e4m3fn codes -> 2 f16x2 with the hardware conversion (exact).
+__device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
+}
+
+// 16 raw bytes of an 8-bit row -> 16 values as two 16-byte chunks (f16 or bf16).
+template <int FMT, bool F16>
+__device__ __forceinline__ void convert16(const uint4 raw, uint4& o0, uint4& o1) {
     const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
     uint32_t r[8];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        float f[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const uint32_t byte = (w[k] >> (8 * e)) & 0xFFu;
-            if constexpr (FMT == QSA_KV_FP8_E4M3)
-                f[e] = e4m3_to_f32(byte);
-            else
-                f[e] = static_cast<float>(static_cast<int8_t>(byte));
-        }
-        r[2 * k] = pack_bf16x2(f[0], f[1]);
-        r[2 * k + 1] = pack_bf16x2(f[2], f[3]);
+        if constexpr (FMT == QSA_KV_FP8_E4M3)
+            e4m3x4_to_f16(w[k], r[2 * k], r[2 * k + 1]);
+        else if constexpr (F16)
+            i8x4_to_f16(w[k], r[2 * k], r[2 * k + 1]);
+        else
+            i8x4_to_bf16(w[k], r[2 * k], r[2 * k + 1]);
     }
     o0 = make_uint4(r[0], r[1], r[2], r[3]);
     o1 = make_uint4(r[4], r[5], r[6], r[7]);
 }
 
-// 16 raw bytes of int4 (32 nibbles, element 2i in the low nibble) -> 32 bf16
-// as four 16-byte chunks.
-__device__ __forceinline__ void dequant32_int4(const uint4 raw, uint4* o) {
+// 16 raw bytes of an int4 row (32 codes) -> four 16-byte chunks.
+template <bool F16>
+__device__ __forceinline__ void convert32_int4(const uint4 raw, uint4* o) {
     const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
         uint32_t r[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int lo = static_cast<int>(w[k] << (28 - 8 * e)) >> 28;
-            const int hi = static_cast<int>(w[k] << (24 - 8 * e)) >> 28;
-            r[e] = pack_bf16x2(static_cast<float>(lo), static_cast<float>(hi));
-        }
+        i4x8_to<F16>(w[k], r);
         o[k] = make_uint4(r[0], r[1], r[2], r[3]);
     }
 }
@@ -621,6 +704,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
     float* const mergeDen = reinterpret_cast<float*>(misc + 32);
 
     uint32_t qa[16][4];
+    float qmul_a = 1.f, qmul_b = 1.f; // undo the per-head Q scaling of f16 QK
     float o[MT][3][4];
     float l0 = 0.f, l1 = 0.f;
     int v = 0, buf = 0, seg_j0 = 0;
@@ -654,6 +738,39 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(qempty_bar(qb));
+            if constexpr (Tr::QK_F16) {
+                // Q to f16, exactly: scale each head (row) by a power of two that
+                // brings its largest |q| into [2^14, 2^15); undo it on the scores.
+                float mr = 0.f, mr8 = 0.f;
+#pragma unroll
+                for (int ks = 0; ks < 16; ++ks) {
+                    mr = fmaxf(mr, fmaxf(fmaxf(fabsf(bf16_lo(qa[ks][0])), fabsf(bf16_hi(qa[ks][0]))),
+                                         fmaxf(fabsf(bf16_lo(qa[ks][2])), fabsf(bf16_hi(qa[ks][2])))));
+                    mr8 = fmaxf(mr8, fmaxf(fmaxf(fabsf(bf16_lo(qa[ks][1])), fabsf(bf16_hi(qa[ks][1]))),
+                                           fmaxf(fabsf(bf16_lo(qa[ks][3])), fabsf(bf16_hi(qa[ks][3])))));
+                }
+                mr = fmaxf(mr, __shfl_xor_sync(0xFFFFFFFFu, mr, 1));
+                mr = fmaxf(mr, __shfl_xor_sync(0xFFFFFFFFu, mr, 2));
+                mr8 = fmaxf(mr8, __shfl_xor_sync(0xFFFFFFFFu, mr8, 1));
+                mr8 = fmaxf(mr8, __shfl_xor_sync(0xFFFFFFFFu, mr8, 2));
+                auto shift_of = [](float m) {
+                    const int e = static_cast<int>((__float_as_uint(m) >> 23) & 0xFFu) - 127;
+                    const int sh = m > 0.f ? e - 14 : 0;
+                    return sh < -100 ? -100 : (sh > 100 ? 100 : sh);
+                };
+                const int sa = shift_of(mr), sb = shift_of(mr8);
+                const float da = __uint_as_float(static_cast<uint32_t>(127 - sa) << 23);
+                const float db = __uint_as_float(static_cast<uint32_t>(127 - sb) << 23);
+                qmul_a = __uint_as_float(static_cast<uint32_t>(127 + sa) << 23);
+                qmul_b = __uint_as_float(static_cast<uint32_t>(127 + sb) << 23);
+#pragma unroll
+                for (int ks = 0; ks < 16; ++ks) {
+                    qa[ks][0] = pack_f16x2(bf16_lo(qa[ks][0]) * da, bf16_hi(qa[ks][0]) * da);
+                    qa[ks][2] = pack_f16x2(bf16_lo(qa[ks][2]) * da, bf16_hi(qa[ks][2]) * da);
+                    qa[ks][1] = pack_f16x2(bf16_lo(qa[ks][1]) * db, bf16_hi(qa[ks][1]) * db);
+                    qa[ks][3] = pack_f16x2(bf16_lo(qa[ks][3]) * db, bf16_hi(qa[ks][3]) * db);
+                }
+            }
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -682,7 +799,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
                     const int rc = ch + 4 * it;
                     const uint4 raw = *reinterpret_cast<const uint4*>(Ks + swz<Tr::ROWB>(t, rc));
                     uint4 ov[4];
-                    dequant32_int4(raw, ov);
+                    convert32_int4<Tr::QK_F16>(raw, ov);
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
                         *reinterpret_cast<uint4*>(kbf + swz<BF_ROW>(t, 4 * rc + k)) = ov[k];
@@ -693,7 +810,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
                     const int tv = lane + 32 * it;
                     const uint4 raw = *reinterpret_cast<const uint4*>(Vs + swz<Tr::ROWB>(tv, warp));
                     uint4 ov[4];
-                    dequant32_int4(raw, ov);
+                    convert32_int4<Tr::PV_F16>(raw, ov);
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
                         *reinterpret_cast<uint4*>(vbf + swz<BF_ROW>(tv, 4 * warp + k)) = ov[k];
@@ -705,7 +822,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
                     const int rc = ch + 4 * it;
                     const uint4 raw = *reinterpret_cast<const uint4*>(Ks + swz<Tr::ROWB>(t, rc));
                     uint4 o0, o1;
-                    dequant16_8bit<FMT>(raw, o0, o1);
+                    convert16<FMT, Tr::QK_F16>(raw, o0, o1);
                     *reinterpret_cast<uint4*>(kbf + swz<BF_ROW>(t, 2 * rc)) = o0;
                     *reinterpret_cast<uint4*>(kbf + swz<BF_ROW>(t, 2 * rc + 1)) = o1;
                 }
@@ -716,7 +833,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
                     const int tv = task >> 1, rc = 2 * warp + (task & 1);
                     const uint4 raw = *reinterpret_cast<const uint4*>(Vs + swz<Tr::ROWB>(tv, rc));
                     uint4 o0, o1;
-                    dequant16_8bit<FMT>(raw, o0, o1);
+                    convert16<FMT, Tr::PV_F16>(raw, o0, o1);
                     *reinterpret_cast<uint4*>(vbf + swz<BF_ROW>(tv, 2 * rc)) = o0;
                     *reinterpret_cast<uint4*>(vbf + swz<BF_ROW>(tv, 2 * rc + 1)) = o1;
                 }
@@ -742,18 +859,19 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
             for (int ks = 0; ks < 16; ks += 2) {
                 uint32_t b0, b1, b2, b3;
                 ldsm_x4(b0, b1, b2, b3, krow + ((ks * 32) ^ kx));
-                mma_bf16(sacc[0], qa[ks], b0, b1);
-                mma_bf16(sacc[1], qa[ks + 1], b2, b3);
+                mma16816<Tr::QK_F16>(sacc[0], qa[ks], b0, b1);
+                mma16816<Tr::QK_F16>(sacc[1], qa[ks + 1], b2, b3);
             }
         }
         const bool v0 = tk0 < n, v1 = tk0 + 1 < n;
         const bool row8 = r < 4; // head r + 8 is a real head (8..11)
         const float ninf = -INFINITY;
         float x[4];
-        x[0] = v0 ? (sacc[0][0] + sacc[1][0]) * cs_base * skr[0] : ninf;
-        x[1] = v1 ? (sacc[0][1] + sacc[1][1]) * cs_base * skr[1] : ninf;
-        x[2] = (v0 && row8) ? (sacc[0][2] + sacc[1][2]) * cs_base * skr[0] : ninf;
-        x[3] = (v1 && row8) ? (sacc[0][3] + sacc[1][3]) * cs_base * skr[1] : ninf;
+        const float csa = cs_base * qmul_a, csb = cs_base * qmul_b;
+        x[0] = v0 ? (sacc[0][0] + sacc[1][0]) * csa * skr[0] : ninf;
+        x[1] = v1 ? (sacc[0][1] + sacc[1][1]) * csa * skr[1] : ninf;
+        x[2] = (v0 && row8) ? (sacc[0][2] + sacc[1][2]) * csb * skr[0] : ninf;
+        x[3] = (v1 && row8) ? (sacc[0][3] + sacc[1][3]) * csb * skr[1] : ninf;
         float ma = fmaxf(x[0], x[1]), mb = fmaxf(x[2], x[3]);
         ma = fmaxf(ma, __shfl_xor_sync(0xFFFFFFFFu, ma, 1));
         ma = fmaxf(ma, __shfl_xor_sync(0xFFFFFFFFu, ma, 2));
@@ -782,13 +900,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
             pv[1] = v1 ? pv[1] : 0.f;
             pv[2] = v0 ? pv[2] : 0.f;
             pv[3] = v1 ? pv[3] : 0.f;
-            const uint32_t hi_a = pack_bf16x2(pv[0], pv[1]);
-            const uint32_t lo_a = pack_bf16x2(pv[0] - bf16_lo(hi_a), pv[1] - bf16_hi(hi_a));
+            uint32_t hi_a, lo_a;
+            split_pair<Tr::PV_F16>(pv[0], pv[1], hi_a, lo_a);
             *reinterpret_cast<uint32_t*>(Pb + r * PRS + tk0 * 2) = hi_a;
             *reinterpret_cast<uint32_t*>(Pb + (8 + r) * PRS + tk0 * 2) = lo_a;
             if (row8) {
-                const uint32_t hi_b = pack_bf16x2(pv[2], pv[3]);
-                const uint32_t lo_b = pack_bf16x2(pv[2] - bf16_lo(hi_b), pv[3] - bf16_hi(hi_b));
+                uint32_t hi_b, lo_b;
+                split_pair<Tr::PV_F16>(pv[2], pv[3], hi_b, lo_b);
                 *reinterpret_cast<uint32_t*>(Pb + (16 + r) * PRS + tk0 * 2) = hi_b;
                 *reinterpret_cast<uint32_t*>(Pb + (20 + r) * PRS + tk0 * 2) = lo_b;
             }
@@ -859,7 +977,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
                     ldsm_x4_t(a[0], a[1], a[2], a[3],
                               vrow + kk * 16 * BF_ROW + (((4 * warp + 2 * mt) << 4) ^ vx));
 #pragma unroll
-                    for (int j = 0; j < 3; ++j) mma_bf16(o[mt][j], a, pb[j][0], pb[j][1]);
+                    for (int j = 0; j < 3; ++j) mma16816<Tr::PV_F16>(o[mt][j], a, pb[j][0], pb[j][1]);
                 }
             }
         }

@@ -170,3 +170,32 @@ def test_headline_saturated_sampled(cuda_device, fmt):
     # every row is finite and non-degenerate
     o = out.float()
     assert torch.isfinite(o).all() and (o.abs().sum(-1) > 0).all()
+
+
+@pytest.mark.parametrize("fmt", ["fp8_e4m3", "int8", "int4"])
+def test_every_code_dequantises_exactly(cuda_device, fmt):
+    """A single selected slot whose V row holds every code of the format, with a
+    unit scale: the output row is exactly the decoded codes (NaN codes give NaN)."""
+    w = I.tiny_tp2(seed=40, length=1, fmt=fmt)
+    slot = int(w.sel[0])
+    if fmt == "int4":
+        codes = torch.arange(256, dtype=torch.int32) % 16
+        row = (codes[0::2] | (codes[1::2] << 4)).to(torch.uint8)
+        vals = torch.where(codes >= 8, codes - 16, codes).float()
+    elif fmt == "int8":
+        row = torch.arange(-128, 128, dtype=torch.int32).to(torch.int8)
+        vals = row.float()
+    else:
+        row = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+        vals = row.view(torch.float8_e4m3fn).float()
+    w.v_pool[slot, 0] = row
+    w.v_scale = torch.ones_like(w.v_scale)
+    wd = w.to(cuda_device)
+    out, _ = run_cuda(wd)
+    torch.cuda.synchronize()
+    ref = vals.to(torch.bfloat16).float()
+    got = out[0].float().cpu()
+    for h in range(12):
+        nan = torch.isnan(ref)
+        assert torch.equal(torch.isnan(got[h]), nan)
+        assert torch.equal(got[h][~nan], ref[~nan])
