@@ -251,6 +251,18 @@ __device__ __forceinline__ void fence_mbarrier_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
+// Named barrier over the consumer warps that also ORs a predicate across them.
+__device__ __forceinline__ bool consumer_sync_or(bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "n"(BAR_CONSUMERS), "n"(NCT)
+        : "memory");
+    return r != 0;
+}
+
 __device__ __forceinline__ void consumer_sync() {
     asm volatile("bar.sync %0, %1;" ::"n"(BAR_CONSUMERS), "n"(NCT) : "memory");
 }
@@ -275,7 +287,7 @@ __device__ __forceinline__ void ldsm_x2(uint32_t& r0, uint32_t& r1, uint32_t add
 
 // D += A(16x16, row) * B(16x8, col), bf16 inputs, fp32 accumulators.
 __device__ __forceinline__ void mma_bf16(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
         "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -284,7 +296,7 @@ __device__ __forceinline__ void mma_bf16(float* d, const uint32_t* a, uint32_t b
 
 // D += A(16x16, row) * B(16x8, col), f16 inputs, fp32 accumulators.
 __device__ __forceinline__ void mma_f16(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
         "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -476,11 +488,13 @@ __device__ __forceinline__ void cursor_advance(Cursor& c, long long t_end, const
     }
 }
 
-// CTA index whose range holds flattened token t; first token of CTA c.
-__device__ __forceinline__ long long cta_of(long long t, long long N, long long G) {
-    return ((t + 1) * G - 1) / N;
+// CTA index whose range holds flattened token t; first token of CTA c. All
+// operands stay below 2^28 (N <= 128 * 2 * 2055 tokens, G <= #SMs), so 32-bit
+// unsigned arithmetic is exact.
+__device__ __forceinline__ unsigned cta_of(unsigned t, unsigned N, unsigned G) {
+    return ((t + 1u) * G - 1u) / N;
 }
-__device__ __forceinline__ long long cta_begin(long long c, long long N, long long G) {
+__device__ __forceinline__ unsigned cta_begin(unsigned c, unsigned N, unsigned G) {
     return c * N / G;
 }
 
@@ -578,7 +592,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
     __syncthreads();
 
     const int Hkv = p.Hkv;
-    const long long N = (long long)Hkv * segP[p.bs];
+    const unsigned N = static_cast<unsigned>(Hkv) * static_cast<unsigned>(segP[p.bs]);
 
     // empty selections -> zero rows (spread over all CTAs)
     if (warp < NW) {
@@ -593,9 +607,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
         }
     }
     if (N == 0) return;
-    long long G = (N + MIN_TOKENS_PER_CTA - 1) / MIN_TOKENS_PER_CTA;
-    G = G < (long long)gridDim.x ? G : (long long)gridDim.x;
-    if ((long long)blockIdx.x >= G) return;
+    unsigned G = (N + MIN_TOKENS_PER_CTA - 1) / MIN_TOKENS_PER_CTA;
+    G = G < gridDim.x ? G : gridDim.x;
+    if (blockIdx.x >= G) return;
     const long long t_begin = cta_begin(blockIdx.x, N, G);
     const long long t_end = cta_begin(blockIdx.x + 1, N, G);
 
@@ -700,14 +714,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
     float* const red = reinterpret_cast<float*>(smem + Ly::off_red);    // [2][NW][16]
     float* const mref = reinterpret_cast<float*>(smem + Ly::off_mref);  // [2][16]
     float* const lred = reinterpret_cast<float*>(smem + Ly::off_lred);  // [NW][16]
-    float* const mergeM = reinterpret_cast<float*>(misc + 16);
-    float* const mergeDen = reinterpret_cast<float*>(misc + 32);
 
     uint32_t qa[16][4];
     float qmul_a = 1.f, qmul_b = 1.f; // undo the per-head Q scaling of f16 QK
     float o[MT][3][4];
     float l0 = 0.f, l1 = 0.f;
     int v = 0, buf = 0, seg_j0 = 0;
+    int pend0 = -1, pend1 = -1;     // split segments whose partial this CTA wrote
     const int tok_base = warp * TPW;
     const int tk0 = tok_base + 2 * c;
     const int xs = lane & 7;                 // row % 8 of every row this lane addresses
@@ -852,26 +865,29 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
         }
 
         // ---------------------------------------------------------------- QK
-        float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        float sacc[4][4] = {};
         {
             const uint32_t krow = smem_u32(Kb) + (tok_base + (lane & 7)) * BF_ROW;
 #pragma unroll
             for (int ks = 0; ks < 16; ks += 2) {
                 uint32_t b0, b1, b2, b3;
                 ldsm_x4(b0, b1, b2, b3, krow + ((ks * 32) ^ kx));
-                mma16816<Tr::QK_F16>(sacc[0], qa[ks], b0, b1);
-                mma16816<Tr::QK_F16>(sacc[1], qa[ks + 1], b2, b3);
+                float* acc = sacc[(ks >> 1) & 1];
+                mma16816<Tr::QK_F16>(acc, qa[ks], b0, b1);
+                mma16816<Tr::QK_F16>(sacc[2 + ((ks >> 1) & 1)], qa[ks + 1], b2, b3);
             }
         }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sacc[0][e] += sacc[1][e] + sacc[2][e] + sacc[3][e];
         const bool v0 = tk0 < n, v1 = tk0 + 1 < n;
         const bool row8 = r < 4; // head r + 8 is a real head (8..11)
         const float ninf = -INFINITY;
         float x[4];
         const float csa = cs_base * qmul_a, csb = cs_base * qmul_b;
-        x[0] = v0 ? (sacc[0][0] + sacc[1][0]) * csa * skr[0] : ninf;
-        x[1] = v1 ? (sacc[0][1] + sacc[1][1]) * csa * skr[1] : ninf;
-        x[2] = (v0 && row8) ? (sacc[0][2] + sacc[1][2]) * csb * skr[0] : ninf;
-        x[3] = (v1 && row8) ? (sacc[0][3] + sacc[1][3]) * csb * skr[1] : ninf;
+        x[0] = v0 ? sacc[0][0] * csa * skr[0] : ninf;
+        x[1] = v1 ? sacc[0][1] * csa * skr[1] : ninf;
+        x[2] = (v0 && row8) ? sacc[0][2] * csb * skr[0] : ninf;
+        x[3] = (v1 && row8) ? sacc[0][3] * csb * skr[1] : ninf;
         float ma = fmaxf(x[0], x[1]), mb = fmaxf(x[2], x[3]);
         ma = fmaxf(ma, __shfl_xor_sync(0xFFFFFFFFu, ma, 1));
         ma = fmaxf(ma, __shfl_xor_sync(0xFFFFFFFFu, ma, 2));
@@ -913,18 +929,18 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
         };
         compute_p(mo_a, mo_b);
         write_p();
-        consumer_sync();
-
-        // stage maximum per head vs the running reference
-        auto stage_max = [&](int h) {
-            float m = redb[h];
+        // One barrier publishes P and the per-warp maxima and ORs "some score of
+        // this stage exceeds its head's reference by more than TAU" over all warps.
+        const bool nd_local = first || ma > mo_a + TAU || (row8 && mb > mo_b + TAU);
+        if (consumer_sync_or(nd_local)) {
+            // stage maximum per head vs the running reference
+            auto stage_max = [&](int h) {
+                float m = redb[h];
 #pragma unroll
-            for (int w = 1; w < NW; ++w) m = fmaxf(m, redb[w * 16 + h]);
-            return m;
-        };
-        auto old_ref = [&](int h) { return first ? ninf : mrefv[h]; };
-        const bool nd = first || stage_max(r) > mo_a + TAU || (row8 && stage_max(r + 8) > mo_b + TAU);
-        if (__any_sync(0xFFFFFFFFu, nd)) {
+                for (int w = 1; w < NW; ++w) m = fmaxf(m, redb[w * 16 + h]);
+                return m;
+            };
+            auto old_ref = [&](int h) { return first ? ninf : mrefv[h]; };
             // slow path (uniform over the consumer warps): raise the reference max
             auto new_ref = [&](int h) { return fmaxf(old_ref(h), stage_max(h)); };
             auto alpha = [&](int h) {
@@ -1008,10 +1024,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
                 return t;
             };
             const int hA = 2 * c, hB = 2 * c + 1, hC = 8 + 2 * c, hD = 9 + 2 * c;
-            const float fA = complete ? out_scale / ltot(hA) : 1.f;
-            const float fB = complete ? out_scale / ltot(hB) : 1.f;
-            const float fC = (complete && c < 2) ? out_scale / ltot(hC) : 1.f;
-            const float fD = (complete && c < 2) ? out_scale / ltot(hD) : 1.f;
+            const float fA = complete ? __fdividef(out_scale, ltot(hA)) : 1.f;
+            const float fB = complete ? __fdividef(out_scale, ltot(hB)) : 1.f;
+            const float fC = (complete && c < 2) ? __fdividef(out_scale, ltot(hC)) : 1.f;
+            const float fD = (complete && c < 2) ? __fdividef(out_scale, ltot(hD)) : 1.f;
             __nv_bfloat16* const outb = p.out + b * p.o_sb + (long long)(g * GROUP) * p.o_sh;
             float* const part = reinterpret_cast<float*>(
                 p.part + ((long long)blockIdx.x * 2 + (cc.kseg == 0 ? 0 : 1)) * PART_BYTES);
@@ -1039,66 +1055,111 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
                 }
             }
             if (!complete) {
+                // split segment: leave the partial (m, l next to O) for the merge; the
+                // arrival ticket is taken after this CTA's whole range is streamed
                 if (tid < GROUP) {
                     part[GROUP * D + tid] = mref[v * 16 + tid];
                     part[GROUP * D + GROUP + tid] = ltot(tid);
                 }
-                __threadfence();
-                consumer_sync();
-                const long long Fs = (long long)Hkv * segP[b] + (long long)g * L;
-                const long long c_first = cta_of(Fs, N, G);
-                const long long c_last = cta_of(Fs + L - 1, N, G);
-                if (tid == 0) {
-                    const int old = atomicAdd(p.cnt + sid, 1);
-                    misc[1] = (old == static_cast<int>(c_last - c_first)) ? 1 : 0;
-                }
-                consumer_sync();
-                if (misc[1]) {
-                    __threadfence();
-                    auto part_of = [&](long long cta) -> const float* {
-                        const int slot = (cta == c_first && cta_begin(cta, N, G) < Fs) ? 1 : 0;
-                        return reinterpret_cast<const float*>(p.part + (cta * 2 + slot) * PART_BYTES);
-                    };
-                    if (tid < GROUP) {
-                        float M = ninf;
-                        for (long long k = c_first; k <= c_last; ++k)
-                            M = fmaxf(M, __ldcg(part_of(k) + GROUP * D + tid));
-                        float den = 0.f;
-                        for (long long k = c_first; k <= c_last; ++k) {
-                            const float* mk = part_of(k) + GROUP * D;
-                            const float mv = __ldcg(mk + tid);
-                            if (mv != ninf) den += __ldcg(mk + GROUP + tid) * ex2(mv - M);
-                        }
-                        mergeM[tid] = M;
-                        mergeDen[tid] = den;
-                    }
-                    consumer_sync();
-                    for (int ch = tid; ch < GROUP * (D / 4); ch += NCT) {
-                        const int h = ch / (D / 4), d0 = (ch % (D / 4)) * 4;
-                        const float M = mergeM[h];
-                        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                        for (long long k = c_first; k <= c_last; ++k) {
-                            const float* pk = part_of(k);
-                            const float mv = __ldcg(pk + GROUP * D + h);
-                            if (mv == ninf) continue;
-                            const float w = ex2(mv - M);
-                            const float4 ov = __ldcg(reinterpret_cast<const float4*>(pk + h * D + d0));
-                            acc.x += w * ov.x;
-                            acc.y += w * ov.y;
-                            acc.z += w * ov.z;
-                            acc.w += w * ov.w;
-                        }
-                        const float f = out_scale / mergeDen[h];
-                        *reinterpret_cast<uint2*>(outb + h * p.o_sh + d0) =
-                            make_uint2(pack_bf16x2(acc.x * f, acc.y * f), pack_bf16x2(acc.z * f, acc.w * f));
-                    }
-                    if (tid == 0) atomicExch(p.cnt + sid, 0);
-                }
+                if (cc.kseg == 0)
+                    pend0 = sid;
+                else
+                    pend1 = sid;
             }
-            consumer_sync();
+            // no trailing barrier: lred is next written in a later epilogue, and
+            // every stage in between passes the per-stage consumer barrier
         }
         cursor_advance(cc, t_end, segL, Hkv);
         buf ^= 1;
+    }
+
+    // ------------------------------------------------ deferred split merges
+    // Each split segment's partials are merged by the CTA that arrives last on
+    // its counter; the merger resets the counter to zero. The partial stores of
+    // all consumer threads precede thread 0's acq_rel ticket through the
+    // barrier (release), and the merger's reads follow its ticket (acquire).
+    if (pend0 >= 0 || pend1 >= 0) {
+        // contributors of a split segment: CTAs c_first..c_last; c_first's partial
+        // sits in its slot 1 when its range began before the segment
+        auto seg_range = [&](int sid, unsigned& Fs, unsigned& c_first, unsigned& c_last) {
+            const int b = sid / Hkv, g = sid - (sid / Hkv) * Hkv, L = segL[b];
+            Fs = static_cast<unsigned>(Hkv * segP[b] + g * L);
+            c_first = cta_of(Fs, N, G);
+            c_last = cta_of(Fs + static_cast<unsigned>(L) - 1u, N, G);
+        };
+        if (tid == 0) {
+            int last[2] = {0, 0};
+            __threadfence(); // release: every consumer's partial stores precede the tickets
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const int sid = q == 0 ? pend0 : pend1;
+                if (sid < 0) continue;
+                unsigned Fs, cf, cl;
+                seg_range(sid, Fs, cf, cl);
+                last[q] = atomicAdd(p.cnt + sid, 1) == static_cast<int>(cl - cf) ? 1 : 0;
+            }
+            __threadfence(); // acquire: the merge reads below follow the tickets
+            misc[2] = last[0];
+            misc[3] = last[1];
+        }
+        consumer_sync();
+        const float ninf = -INFINITY;
+#pragma unroll 1
+        for (int q = 0; q < 2; ++q) {
+            const int sid = q == 0 ? pend0 : pend1;
+            if (sid < 0 || !misc[2 + q]) continue;
+            unsigned Fs, c_first, c_last;
+            seg_range(sid, Fs, c_first, c_last);
+            const int b = sid / Hkv, g = sid - b * Hkv;
+            __nv_bfloat16* const outb = p.out + b * p.o_sb + (long long)(g * GROUP) * p.o_sh;
+            constexpr int CH = GROUP * (D / 4) / NCT; // float4 chunks per thread (3)
+            static_assert(GROUP * (D / 4) % NCT == 0, "merge chunking");
+            float M[CH], den[CH];
+            float4 acc[CH];
+#pragma unroll
+            for (int e = 0; e < CH; ++e) {
+                M[e] = ninf;
+                den[e] = 0.f;
+                acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll 1
+            for (unsigned cta = c_first; cta <= c_last; ++cta) {
+                const unsigned slot = (cta == c_first && cta_begin(cta, N, G) < Fs) ? 1u : 0u;
+                const float* pk = reinterpret_cast<const float*>(
+                    p.part + static_cast<size_t>(cta * 2u + slot) * PART_BYTES);
+                float mv[CH], lv[CH];
+                float4 ov[CH];
+#pragma unroll
+                for (int e = 0; e < CH; ++e) {
+                    const int ch = tid + e * NCT, h = ch / (D / 4), d0 = (ch % (D / 4)) * 4;
+                    mv[e] = __ldcg(pk + GROUP * D + h);
+                    lv[e] = __ldcg(pk + GROUP * D + GROUP + h);
+                    ov[e] = __ldcg(reinterpret_cast<const float4*>(pk + h * D + d0));
+                }
+#pragma unroll
+                for (int e = 0; e < CH; ++e) {
+                    if (mv[e] == ninf) continue;
+                    const float Mn = fmaxf(M[e], mv[e]);
+                    const float r0 = M[e] == ninf ? 0.f : ex2(M[e] - Mn);
+                    const float w = ex2(mv[e] - Mn);
+                    den[e] = den[e] * r0 + w * lv[e];
+                    acc[e].x = acc[e].x * r0 + w * ov[e].x;
+                    acc[e].y = acc[e].y * r0 + w * ov[e].y;
+                    acc[e].z = acc[e].z * r0 + w * ov[e].z;
+                    acc[e].w = acc[e].w * r0 + w * ov[e].w;
+                    M[e] = Mn;
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < CH; ++e) {
+                const int ch = tid + e * NCT, h = ch / (D / 4), d0 = (ch % (D / 4)) * 4;
+                const float f = __fdividef(out_scale, den[e]);
+                *reinterpret_cast<uint2*>(outb + h * p.o_sh + d0) =
+                    make_uint2(pack_bf16x2(acc[e].x * f, acc[e].y * f),
+                               pack_bf16x2(acc[e].z * f, acc[e].w * f));
+            }
+            if (tid == 0) atomicExch(p.cnt + sid, 0);
+        }
     }
 }
 
