@@ -13,6 +13,9 @@ sequence b and query head h with KV head g = h // (Hq // Hkv),
 ``I = sel[cu[b]:cu[b+1]]`` in order, duplicates kept; an empty selection
 gives zeros. Khat/Vhat are the exactly dequantised pool rows.
 
+It also holds the quantising KV write (``quantize_rows``): the codes and
+scales the pools' write path produces, in binary32.
+
 Pins: every function here is checked in ``tests/test_oracle_pins.py``
 against closed forms, library routines and brute force (see that file).
 """
@@ -74,6 +77,11 @@ def _load():
         ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,  # rows, n_rows, out, threads
     ]
     lib.orc_max_threads.restype = ctypes.c_int
+    lib.orc_e4m3fn_encode.restype = ctypes.c_uint8
+    lib.orc_e4m3fn_encode.argtypes = [ctypes.c_float]
+    lib.orc_quantize_rows.restype = ctypes.c_int
+    lib.orc_quantize_rows.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                      ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p]
     _lib = lib
     return lib
 
@@ -188,6 +196,38 @@ def round_bf16(x: np.ndarray) -> np.ndarray:
     """float64 values of round_bf16_bits(x)."""
     bits = round_bf16_bits(x).astype(np.uint32) << 16
     return bits.view(np.float32).astype(np.float64)
+
+
+def e4m3fn_encode(v: float) -> int:
+    """e4m3fn code of a binary32 value (nearest-even, saturating at +-448)."""
+    return _load().orc_e4m3fn_encode(float(v))
+
+
+def quantize_rows(x, fmt: str, fp8_scale: float = 1.0):
+    """Quantise bf16 rows [n, D] as the KV write path does.
+
+    Returns (codes, scales): codes uint8 [n, D] (bf16: uint16 bits [n, D];
+    int8: int8 [n, D]; int4: uint8 [n, D/2]); scales float32 [n] for int8/int4,
+    else None."""
+    lib = _load()
+    xn = _np(x)
+    if xn.dtype != np.uint16 or xn.ndim != 2:
+        raise ValueError("x must be bf16 [n, D]")
+    n, D = xn.shape
+    f = FORMATS[fmt]
+    if fmt == "bf16":
+        codes = np.empty((n, D), dtype=np.uint16)
+    elif fmt == "int4":
+        codes = np.zeros((n, D // 2), dtype=np.uint8)
+    else:
+        codes = np.empty((n, D), dtype=np.uint8)
+    scales = np.zeros(n, dtype=np.float32) if fmt in ("int8", "int4") else None
+    rc = lib.orc_quantize_rows(_ptr(xn), n, D, f, float(fp8_scale), _ptr(codes), _ptr(scales))
+    if rc != 0:
+        raise ValueError("bad format or shape")
+    if fmt == "int8":
+        codes = codes.view(np.int8)
+    return codes, scales
 
 
 def max_threads() -> int:

@@ -211,6 +211,97 @@ int orc_decode(const uint16_t* q, int64_t q_sb, int64_t q_sh,
     return 0;
 }
 
+/* ------------------------------------------------------------------ KV write
+ *
+ * The quantising write that fills the pools (sglang PR #37798, "Modifications":
+ * one fused quantise + scatter per write; part 1, mem_cache/memory_pool.py: the
+ * fp8 write saturates to +-448 before the e4m3 cast). Everything here is
+ * binary32 arithmetic, as the write path computes it, so a code decided by
+ * rounding is decided the same way on both sides.
+ */
+
+/* e4m3fn encoding of a binary32 value: round to nearest, ties to even, values
+ * of magnitude >= 448 (and infinities) saturate to +-448; NaN -> 0x7F. */
+uint8_t orc_e4m3fn_encode(float v) {
+    if (isnan(v)) return 0x7F;
+    const uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    const double a = fabs((double)v);
+    if (a >= 448.0) return sign | 0x7E;
+    if (a < ldexp(1.0, -6)) {
+        /* subnormals m * 2^-9, m = 0..7; m = 8 is the smallest normal 0x08 */
+        const double m = nearbyint(a / ldexp(1.0, -9));
+        return sign | (uint8_t)m;
+    }
+    int e2;
+    frexp(a, &e2);
+    int E = e2 - 1; /* a in [2^E, 2^(E+1)) */
+    double m = nearbyint((a / ldexp(1.0, E) - 1.0) * 8.0);
+    if (m == 8.0) {
+        m = 0.0;
+        E += 1;
+    }
+    return sign | (uint8_t)(((E + 7) << 3) | (int)m);
+}
+
+/* Quantise n rows of D bf16 values:
+ *   bf16 (0): codes are the input bits (2 bytes per value)
+ *   fp8  (1): codes[d] = e4m3fn(x[d] / s), s = fp8_scale (one per pool)
+ *   int8 (2): s = absmax / 127, codes[d] = clamp(rint(x[d] / s), -127, 127)
+ *   int4 (3): s = absmax / 7,   codes[d] = clamp(rint(x[d] / s), -8, 7), two per
+ *             byte, channel 2i in the low nibble
+ * An all-zero row gets s = 0 and zero codes. rint is round-half-to-even.
+ * codes: n * D bytes (2n * D for bf16, n * D / 2 for int4); scales: n floats
+ * (int8 / int4 only). Returns 0, or -1 for a bad format or odd D with int4. */
+int orc_quantize_rows(const uint16_t* x, int64_t n, int D, int format, float fp8_scale,
+                      uint8_t* codes, float* scales) {
+    if (format < ORC_BF16 || format > ORC_INT4 || D <= 0 || (format == ORC_INT4 && (D & 1)))
+        return -1;
+    for (int64_t r = 0; r < n; ++r) {
+        const uint16_t* xr = x + r * D;
+        if (format == ORC_BF16) {
+            memcpy(codes + r * D * 2, xr, (size_t)D * 2);
+            continue;
+        }
+        if (format == ORC_FP8_E4M3) {
+            for (int d = 0; d < D; ++d) {
+                const float xf = (float)orc_bf16_to_double(xr[d]);
+                const float y = xf / fp8_scale;
+                codes[r * D + d] = orc_e4m3fn_encode(y);
+            }
+            continue;
+        }
+        const float qmax = format == ORC_INT8 ? 127.0f : 7.0f;
+        const float qmin = format == ORC_INT8 ? -127.0f : -8.0f;
+        float amax = 0.0f;
+        for (int d = 0; d < D; ++d) {
+            const float a = fabsf((float)orc_bf16_to_double(xr[d]));
+            if (a > amax) amax = a;
+        }
+        const float s = amax / qmax;
+        scales[r] = s;
+        for (int d = 0; d < D; ++d) {
+            int q = 0;
+            if (s > 0.0f) {
+                const float y = (float)orc_bf16_to_double(xr[d]) / s;
+                float qf = rintf(y);
+                if (qf > qmax) qf = qmax;
+                if (qf < qmin) qf = qmin;
+                q = (int)qf;
+            }
+            if (format == ORC_INT8) {
+                codes[r * D + d] = (uint8_t)(int8_t)q;
+            } else {
+                uint8_t* byte = codes + r * (D / 2) + d / 2;
+                if ((d & 1) == 0)
+                    *byte = (uint8_t)(q & 0xF);
+                else
+                    *byte |= (uint8_t)((q & 0xF) << 4);
+            }
+        }
+    }
+    return 0;
+}
+
 /* Threads the OpenMP runtime would use (1 without OpenMP). */
 int orc_max_threads(void) {
 #ifdef _OPENMP

@@ -103,16 +103,16 @@ def quantize_pool(x: torch.Tensor, fmt: str):
     if fmt == "fp8_e4m3":
         amax = x.abs().max().to(torch.float32)
         s = (amax / FP8_E4M3_MAX).reshape(1)
-        inv = torch.where(s > 0, 1.0 / s, torch.zeros_like(s))
-        y = (x * inv).clamp(-FP8_E4M3_MAX, FP8_E4M3_MAX)
+        y = torch.where(s > 0, x / s, torch.zeros_like(x)).clamp(-FP8_E4M3_MAX, FP8_E4M3_MAX)
         return y.to(torch.float8_e4m3fn).view(torch.uint8), s.to(torch.float32)
     if fmt in ("int8", "int4"):
         qmax = 127.0 if fmt == "int8" else 7.0
         qmin = -127.0 if fmt == "int8" else -8.0
         amax = x.abs().amax(dim=-1)
         s = (amax / qmax).to(torch.float32)
-        inv = torch.where(s > 0, 1.0 / s, torch.zeros_like(s))
-        qv = torch.round(x * inv.unsqueeze(-1)).clamp(qmin, qmax).to(torch.int8)
+        safe = torch.where(s > 0, s, torch.ones_like(s)).unsqueeze(-1)
+        qv = torch.where(s.unsqueeze(-1) > 0, torch.round(x / safe), torch.zeros_like(x))
+        qv = qv.clamp(qmin, qmax).to(torch.int8)
         if fmt == "int8":
             return qv, s
         lo = (qv[..., 0::2].to(torch.int16) & 0xF)

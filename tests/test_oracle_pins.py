@@ -318,3 +318,61 @@ def test_thread_count_does_not_change_results():
     a = _run(w, threads=1)
     b = _run(w, threads=4)
     assert np.array_equal(a, b)
+
+
+# ---------------------------------------------------------- quantising KV write
+
+def test_e4m3fn_encode_matches_torch_cast_and_saturates():
+    g = torch.Generator().manual_seed(21)
+    x = torch.randn(50000, generator=g) * torch.exp(torch.randn(50000, generator=g) * 3)
+    x = torch.cat([x, torch.tensor([0.0, -0.0, 448.0, -448.0, 2.0 ** -9, 2.0 ** -10, 3 * 2.0 ** -11])])
+    inside = x.clamp(-448, 448)
+    ref = inside.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.e4m3fn_encode(float(v)) for v in inside])
+    assert np.array_equal(ref, got)
+    # beyond the largest finite value the write saturates (the cast alone would give NaN)
+    for v, code in ((449.0, 0x7E), (1e6, 0x7E), (-500.0, 0xFE), (float("inf"), 0x7E)):
+        assert oracle.e4m3fn_encode(v) == code
+    assert oracle.e4m3fn_encode(float("nan")) == 0x7F
+
+
+@pytest.mark.parametrize("fmt", ["int8", "int4", "fp8_e4m3"])
+def test_quantize_rows_matches_the_torch_quantiser(fmt):
+    """Two independent implementations of the write-side quantiser agree bit for bit."""
+    x = I.normal_values((300, 1, 256), 22).to(torch.bfloat16)
+    xf = x.float()
+    codes_t, s_t = I.quantize_pool(xf, fmt)
+    scale = float(s_t[0]) if fmt == "fp8_e4m3" else 1.0
+    codes, scales = oracle.quantize_rows(x[:, 0], fmt, fp8_scale=scale)
+    assert np.array_equal(codes.view(np.uint8), codes_t[:, 0].view(torch.uint8).numpy())
+    if fmt != "fp8_e4m3":
+        assert np.array_equal(scales, s_t[:, 0].numpy())
+
+
+def test_quantize_rows_ties_zero_rows_and_clamps():
+    # absmax 127 -> scale exactly 1; halves round to even
+    row = torch.zeros(256)
+    row[0], row[1], row[2], row[3], row[4] = 127.0, 2.5, 3.5, -2.5, 100.5
+    zero = torch.zeros(256)
+    x = torch.stack([row, zero]).to(torch.bfloat16)
+    codes, scales = oracle.quantize_rows(x, "int8")
+    assert scales[0] == 1.0 and scales[1] == 0.0
+    assert codes[0, :5].tolist() == [127, 2, 4, -2, 100]
+    assert not codes[1].any()
+    # int4: absmax 7 -> scale 1; channel 2i in the low nibble; halves to even
+    row4 = torch.zeros(256)
+    row4[0], row4[1], row4[2], row4[3] = 7.0, -3.5, 2.5, 0.5
+    c4, s4 = oracle.quantize_rows(row4[None].to(torch.bfloat16), "int4")
+    assert s4[0] == 1.0
+    assert c4[0, 0] == 0xC7 and c4[0, 1] == 0x02 and not c4[0, 2:].any()
+
+
+def test_quantize_then_dequantize_round_trip():
+    x = I.normal_values((64, 1, 256), 23, std=2.0).to(torch.bfloat16)
+    xd = x[:, 0].double().numpy()
+    for fmt, qmax in (("int8", 127), ("int4", 7)):
+        codes, scales = oracle.quantize_rows(x[:, 0], fmt)
+        pool = torch.from_numpy(codes.view(np.uint8) if fmt == "int4" else codes)[:, None]
+        back = oracle.dequant_rows(pool, fmt, range(64), 0, torch.from_numpy(scales)[:, None])
+        # |rint(fl(x / s)) - x / s| <= 1/2 + |fl(x / s) - x / s|, the second term below qmax * 2^-24
+        assert (np.abs(back - xd) <= (0.5 + qmax * 2.0 ** -23) * scales[:, None]).all()
