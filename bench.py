@@ -315,6 +315,64 @@ def run_native(args):
         torch.distributed.destroy_process_group()
 
 
+KVW_TOKENS = 131072  # one prefill chunk: 128 sequences x 1024 new tokens
+
+
+def kv_write_bytes(fmt: str, n: int = KVW_TOKENS, hkv: int = HKV) -> int:
+    """Bytes one qsa_kv_write call must move: the new bf16 K and V rows, the slot
+    ids, the written codes and (int8/int4) the written per-row scales."""
+    read = 2 * n * hkv * 512 + n * 4 + (8 if fmt == "fp8_e4m3" else 0)
+    write = 2 * n * hkv * (ROW_BYTES[fmt] + SCALE_BYTES[fmt])
+    return read + write
+
+
+def run_kv_write(args):
+    """Secondary measurement: the quantising KV write (one call per step)."""
+    import sparse_attention_paged_qsa_gb300 as qsa
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    fmt = args.fmt
+    kc, vc, ks, vs = I.make_pools(SLOTS, HKV, fmt, seed=2, device=dev)
+    g = torch.Generator(device=dev).manual_seed(7)
+    xs = [torch.randn(KVW_TOKENS, HKV, 256, generator=g, device=dev).to(torch.bfloat16)
+          for _ in range(4)]
+    slots = [torch.randperm(SLOTS, generator=g, device=dev)[:KVW_TOKENS].to(torch.int32)
+             for _ in range(2)]
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(k):
+        qsa.qsa_kv_write(fmt, xs[k % 4], xs[(k + 1) % 4], slots[k % 2], kc, vc, ks, vs, err, stream)
+
+    for k in range(args.warmup):
+        step(k)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0) as clk:
+        e0.record(stream)
+        for k in range(args.steps):
+            step(k)
+        e1.record(stream)
+        torch.cuda.synchronize()
+    if int(err.item()):
+        raise RuntimeError("device error flag set")
+    ms = e0.elapsed_time(e1) / args.steps
+    b = kv_write_bytes(fmt)
+    gbs = b / (ms * 1e-3) / 1e9
+    peak, kind = measured_peaks()
+    print(json.dumps({
+        "metric": "quantising KV write HBM GB/s (128 x 1024 new tokens, 24Q/2KV, D=256)",
+        "op": "kv_write", "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "dtype": fmt,
+        "data": "synthetic", "tokens_per_s": KVW_TOKENS / (ms * 1e-3),
+        "config": {"workload": f"kv write of {KVW_TOKENS} tokens x 2 KV heads into a "
+                               f"{SLOTS}-slot {fmt} pool, random distinct slots"},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                     "frac": gbs / peak, "peak_source": f"{kind} hbm_gbs", "bytes_per_launch": b},
+        "gpu_launches": args.steps, "clocks": clk.summary()}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -322,6 +380,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--fmt", default="bf16", choices=list(I.FORMATS))
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--op", default="decode", choices=["decode", "kv_write"],
+                    help="decode (the headline) or the quantising KV write")
     ap.add_argument("--index-sets", type=int, default=3)
     ap.add_argument("--cpu-rows", type=int, default=128,
                     help="sequences of the oracle CPU-baseline sample (0 disables)")
@@ -333,6 +393,8 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.op == "kv_write":
+        run_kv_write(args)
     else:
         run_native(args)
 

@@ -127,6 +127,36 @@ int qsa_decode(const qsa_tensor* q, const qsa_tensor* k_pool, const qsa_tensor* 
                const qsa_tensor* cu_seqlens, const qsa_tensor* out, void* scratch,
                size_t scratch_bytes, void* stream);
 
+/*
+ * qsa_kv_write -- quantise new K/V rows and scatter them into the pools: the
+ * write that fills what qsa_decode gathers (sglang PR #37798, "Modifications":
+ * one fused quantise + scatter launch per write; part 1, mem_cache/memory_pool.py:
+ * the fp8 write saturates to +-448 before the e4m3 cast).
+ *
+ *  format      QSA_KV_* of the pools.
+ *  k_new,      bf16 [n, Hkv, 256] (Hkv 1 or 2); stride[2] == 1, other strides
+ *  v_new       non-negative multiples of 8; base 16-byte aligned. n may be 0.
+ *  slots       int32 [n], contiguous: destination slot of token i. Slots should be
+ *              distinct within a call; for a repeated slot one of the writes wins.
+ *  k_pool,     pools as for qsa_decode; row slot[i] * Hkv + g receives token i, head g.
+ *  v_pool
+ *  k_scale,    fp8: the pool's fp32 scale [1] (read; must be finite and > 0);
+ *  v_scale     int8/int4: fp32 [num_slots * Hkv], entry of each written row set to
+ *              absmax(row) / 127 (int8) or / 7 (int4); bf16: unused (may be NULL).
+ *  device_error  optional int32 device word: QSA_DEVERR_SLOT_RANGE is OR-ed in when a
+ *              slot is outside [0, num_slots); that row is skipped. May be NULL.
+ *  stream      cudaStream_t.
+ *
+ * Codes, in binary32 with IEEE division and round-to-nearest-even: bf16 rows are
+ * copied; fp8 = e4m3fn(x / s) saturating at +-448; int8 = clamp(rint(x / s), -127, 127);
+ * int4 = clamp(rint(x / s), -8, 7), two's-complement nibbles, channel 2i in the low
+ * nibble; an all-zero row gets scale 0 and zero codes. Inputs must be finite.
+ * Validates on the host, enqueues one kernel, allocates nothing.
+ */
+int qsa_kv_write(int32_t format, const qsa_tensor* k_new, const qsa_tensor* v_new,
+                 const qsa_tensor* slots, const qsa_tensor* k_pool, const qsa_tensor* v_pool,
+                 float* k_scale, float* v_scale, int32_t* device_error, void* stream);
+
 /* Scratch bytes a qsa_decode call with these sizes needs on the current
  * device (0 when the sizes are outside the contract). Split-KV partials take
  * two 12 KiB slots per CTA of the grid the library would choose. */

@@ -35,7 +35,7 @@ _TORCH_DTYPES = {
 EXPORTED = (
     "qsa_decode", "qsa_decode_scratch_bytes", "qsa_decode_grid", "qsa_decode_scratch_layout",
     "qsa_scratch_init", "qsa_scratch_error", "qsa_strerror", "qsa_last_error_message",
-    "qsa_version", "qsa_decode_static_scratch",
+    "qsa_version", "qsa_decode_static_scratch", "qsa_kv_write",
 )
 
 
@@ -83,6 +83,10 @@ def load() -> ctypes.CDLL:
     lib.qsa_decode_static_scratch.argtypes = [P(QsaTensor), P(QsaTensor), P(QsaTensor),
                                               P(QsaKvQuantMeta), P(QsaTensor), P(QsaTensor),
                                               P(QsaTensor), ctypes.c_void_p]
+    lib.qsa_kv_write.restype = ctypes.c_int
+    lib.qsa_kv_write.argtypes = [ctypes.c_int32, P(QsaTensor), P(QsaTensor), P(QsaTensor),
+                                 P(QsaTensor), P(QsaTensor), ctypes.c_void_p, ctypes.c_void_p,
+                                 ctypes.c_void_p, ctypes.c_void_p]
     lib.qsa_decode_scratch_bytes.restype = ctypes.c_size_t
     lib.qsa_decode_scratch_bytes.argtypes = [ctypes.c_int32] * 3
     lib.qsa_decode_grid.restype = ctypes.c_int32
@@ -168,6 +172,17 @@ def qsa_decode(q, k_pool, v_pool, kv_quant_meta: KVQuantMeta, sel_indices, cu_se
                         ctypes.byref(out_d), scratch.data_ptr() if scratch is not None else None,
                         scratch.numel() * scratch.element_size() if scratch is not None else 0,
                         _stream_handle(stream))
+    _check(rc)
+
+
+def qsa_kv_write(fmt: str, k_new, v_new, slots, k_pool, v_pool, k_scale=None, v_scale=None,
+                 error_word=None, stream=None) -> None:
+    """Enqueue one quantise + scatter write of new K/V rows (see include/qsa.h)."""
+    lib = load()
+    d = [describe(t) for t in (k_new, v_new, slots, k_pool, v_pool)]
+    ptr = lambda t: t.data_ptr() if t is not None else None
+    rc = lib.qsa_kv_write(KV_FORMATS[fmt], *(ctypes.byref(x) for x in d), ptr(k_scale),
+                          ptr(v_scale), ptr(error_word), _stream_handle(stream))
     _check(rc)
 
 

@@ -7,7 +7,7 @@ import subprocess
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
-SOURCES = [os.path.join(PKG, "csrc", "qsa_decode.cu")]
+SOURCES = [os.path.join(PKG, "csrc", "qsa_decode.cu"), os.path.join(PKG, "csrc", "qsa_kv_write.cu")]
 HEADERS = [os.path.join(ROOT, "include", "qsa.h")]
 LIB = os.path.join(PKG, "libqsa.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -1167,11 +1167,23 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
 
 // ====================================================================== host
 
+// Shared with the other translation units of libqsa (not exported): record the
+// message qsa_last_error_message() returns on this thread.
+__attribute__((visibility("hidden"))) void qsa_detail_set_error(const char* msg);
+
 namespace {
 
 using namespace qsa;
 
 thread_local std::string g_last_error;
+
+} // namespace
+
+__attribute__((visibility("hidden"))) void qsa_detail_set_error(const char* msg) {
+    g_last_error = msg ? msg : "";
+}
+
+namespace {
 
 int fail(int code, const char* fmt, ...) {
     char msg[512];

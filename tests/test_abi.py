@@ -128,3 +128,25 @@ def test_oracle_and_product_share_no_code():
             text = open(os.path.join(ROOT, "oracle", f)).read()
             assert "sparse_attention_paged_qsa_gb300" not in text, f
             assert "qsa.h" not in text, f
+
+
+def test_kv_write_rejections_on_host():
+    lib = B.load()
+    x = torch.zeros(4, 2, 256, dtype=torch.bfloat16)
+    slots = torch.zeros(4, dtype=torch.int32)
+    pool = torch.zeros(16, 2, 256, dtype=torch.int8)
+    sc = torch.zeros(32)
+    d = lambda t: ctypes.byref(B.describe(t))
+    rc = lib.qsa_kv_write(2, d(x), d(x), d(slots), d(pool), d(pool), None, None, None, None)
+    assert rc == B.ERR_INVALID_ARGUMENT and b"scale" in lib.qsa_last_error_message()
+    rc = lib.qsa_kv_write(1, d(x), d(x), d(slots), d(pool), d(pool), sc.data_ptr(), sc.data_ptr(),
+                          None, None)
+    assert rc == B.ERR_INVALID_ARGUMENT and b"dtype" in lib.qsa_last_error_message()
+    x3 = torch.zeros(4, 3, 256, dtype=torch.bfloat16)
+    rc = lib.qsa_kv_write(2, d(x3), d(x3), d(slots), d(pool), d(pool), sc.data_ptr(), sc.data_ptr(),
+                          None, None)
+    assert rc == B.ERR_UNSUPPORTED
+    empty = torch.zeros(0, 2, 256, dtype=torch.bfloat16)
+    rc = lib.qsa_kv_write(2, d(empty), d(empty), d(torch.zeros(0, dtype=torch.int32)), d(pool),
+                          d(pool), sc.data_ptr(), sc.data_ptr(), None, None)
+    assert rc == B.OK  # nothing to write, nothing enqueued
