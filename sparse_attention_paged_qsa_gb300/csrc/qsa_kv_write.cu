@@ -15,6 +15,7 @@
 // One warp per (token, head, K-or-V) row: a 16-byte load per lane covers the
 // row, the absmax is a warp reduction, and each lane stores its codes with one
 // 16/8/4-byte store, so a row is one coalesced read and one coalesced write.
+// Each warp issues the loads of its RPW rows before converting any of them.
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
@@ -57,23 +58,31 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
     return r;
 }
 
-// Codes are defined on fl(x / s), the correctly rounded binary32 quotient. With
-// r = fl(1 / s), r_lo = fl(r * (1 - 2^-20)) and r_hi = fl(r * (1 + 2^-20)), the
-// exact products x * r_lo and x * r_hi lie on either side of fl(x / s) (their
-// distance from x / s is at least |x / s| * 2^-21, the rounding of fl(x / s)
-// and r at most |x / s| * 2^-23). Rounding is monotone, so where the codes of
-// both products agree that is the code of fl(x / s); only the rare lane where
-// they differ divides.
+// Codes are defined on q = fl(x / s), the correctly rounded binary32 quotient.
+//
+// fp8 (s is any pool scale): with r = fl(1 / s), r_lo = fl(r * (1 - 2^-20)) and
+// r_hi = fl(r * (1 + 2^-20)), fl(x * r_lo) and fl(x * r_hi) lie on either side
+// of q (each is at least |x / s| * 2^-21 away from x / s, q at most
+// |x / s| * 2^-24). The conversion is monotone, so where both give the same code
+// that is the code of q; pairs where they differ divide.
+//
+// int8 / int4 (s = fl(a / qmax), a = absmax, a bf16 value): q comes from
+// Markstein's correction (P. Markstein, "Computation of elementary functions on
+// the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990):
+// q0 = fl(x * r), e = fma(-q0, s, x), q = fma(e, r, q0) with r = fl(1 / s). For
+// a in [1, 2) it was checked against exact rational arithmetic for every bf16
+// x with 2^-11 a <= |x| <= a and every a (smaller |x| gives code 0 either way);
+// the steps commute with scaling by 2^E while all terms stay normal, which holds
+// for a >= 2^-60. s and r for a = m * 2^E are those of m (a 128-entry table of
+// the bf16 mantissas) with the exponent moved by E.
 
-// fma(x, c, 1.5 * 2^23) rounds x * c + 1.5 * 2^23 once, to an integer (the
-// spacing of binary32 in [2^23, 2^24)), ties to even: its bit pattern is
-// 0x4B400000 + rint(x * c) for |x * c| < 2^22, so the low byte is the two's
-// complement byte of rint(x * c).
+// x + 1.5 * 2^23 rounds once, to an integer (the spacing of binary32 in
+// [2^23, 2^24)), ties to even: its bit pattern is 0x4B400000 + rint(x) for
+// |x| < 2^22, so the low byte is the two's complement byte of rint(x).
 constexpr float RINT_MAGIC = 12582912.0f;
+constexpr float FAST_MIN_ABSMAX = 0x1p-60f;
 
-__device__ __forceinline__ uint32_t rint_bits(float x, float c) {
-    return __float_as_uint(__fmaf_rn(x, c, RINT_MAGIC));
-}
+__device__ __forceinline__ uint32_t rint_bits(float q) { return __float_as_uint(__fadd_rn(q, RINT_MAGIC)); }
 
 // Low bytes of four words packed into one (a in the lowest byte).
 __device__ __forceinline__ uint32_t low_bytes(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
@@ -86,125 +95,193 @@ __device__ __forceinline__ uint32_t low_nibbles(uint32_t w) {
     return __byte_perm(t, 0u, 0x4420);
 }
 
-template <int FMT>
-__device__ __forceinline__ void write_row(const Params& p, const uint4 raw, long long row, bool isv,
-                                          int lane, float fr_lo, float fr_hi) {
-    uint8_t* const pool = isv ? p.vpool : p.kpool;
-    if constexpr (FMT == QSA_KV_BF16) {
-        reinterpret_cast<uint4*>(pool + row * (D * 2))[lane] = raw;
-    } else {
-        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-        float x[8];
+__device__ __forceinline__ void unpack(const uint4 raw, float x[8]) {
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            x[2 * k] = __uint_as_float(w[k] << 16);
-            x[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
-        }
-        if constexpr (FMT == QSA_KV_FP8_E4M3) {
-            uint32_t c[4];
-            bool same = true;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const uint32_t lo = e4m3x2(x[2 * k] * fr_lo, x[2 * k + 1] * fr_lo);
-                const uint32_t hi = e4m3x2(x[2 * k] * fr_hi, x[2 * k + 1] * fr_hi);
-                same &= lo == hi;
-                c[k] = lo;
-            }
-            if (!same) {
-                const float s = __ldg(isv ? p.vscale : p.kscale);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) c[k] = e4m3x2(x[2 * k] / s, x[2 * k + 1] / s);
-            }
-            reinterpret_cast<uint2*>(pool + row * D)[lane] =
-                make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
-        } else {
-            constexpr float qmax = FMT == QSA_KV_INT8 ? 127.0f : 7.0f;
-            constexpr float qmin = FMT == QSA_KV_INT8 ? -127.0f : -8.0f;
-            float a = 0.0f;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) a = fmaxf(a, fabsf(x[k]));
-            // a >= 0, so its bit pattern orders like its value
-            a = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(a)));
-            const float s = __fdiv_rn(a, qmax);
-            uint32_t b0, b1;
-            bool same = false;
-            // Below 2^-100 the scale or its reciprocal leaves the normal range (and
-            // codes can need the clamp); above, |x / s| <= qmax * (1 + 2^-19).
-            if (a >= 0x1p-100f) {
-                const float r = __frcp_rn(s);
-                const float r_lo = r * (1.0f - 0x1p-20f), r_hi = r * (1.0f + 0x1p-20f);
-                uint32_t lo[8], hi[8];
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    lo[k] = rint_bits(x[k], r_lo);
-                    hi[k] = rint_bits(x[k], r_hi);
-                }
-                b0 = low_bytes(lo[0], lo[1], lo[2], lo[3]);
-                b1 = low_bytes(lo[4], lo[5], lo[6], lo[7]);
-                same = b0 == low_bytes(hi[0], hi[1], hi[2], hi[3]) &&
-                       b1 == low_bytes(hi[4], hi[5], hi[6], hi[7]);
-            }
-            if (!same) {
-                int q[8];
-#pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    q[k] = s > 0.0f ? static_cast<int>(fminf(fmaxf(rintf(x[k] / s), qmin), qmax)) : 0;
-                b0 = low_bytes(q[0], q[1], q[2], q[3]);
-                b1 = low_bytes(q[4], q[5], q[6], q[7]);
-            }
-            if constexpr (FMT == QSA_KV_INT8) {
-                reinterpret_cast<uint2*>(pool + row * D)[lane] = make_uint2(b0, b1);
-            } else {
-                reinterpret_cast<uint32_t*>(pool + row * (D / 2))[lane] =
-                    low_nibbles(b0) | (low_nibbles(b1) << 16);
-            }
-            if (lane == 0) (isv ? p.vscale : p.kscale)[row] = s;
-        }
+    for (int k = 0; k < 4; ++k) {
+        x[2 * k] = __uint_as_float(w[k] << 16);
+        x[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
     }
 }
 
-// Each warp takes RPW consecutive (token, head, K-or-V) rows and issues all their
-// loads before converting any, so a warp keeps RPW row reads in flight.
+__device__ __forceinline__ uint8_t* row_ptr(const Params& p, bool isv, long long row, int row_bytes) {
+    return (isv ? p.vpool : p.kpool) + row * row_bytes;
+}
+
+// POW2: the scale is a power of two, so x * (1 / s) is the exact quotient and
+// its code needs no bracket (fr_lo = fr_hi = 1 / s).
+template <bool POW2>
+__device__ __forceinline__ void store_fp8(const Params& p, const uint4 raw, long long row, bool isv,
+                                          int lane, float fr_lo, float fr_hi) {
+    float x[8];
+    unpack(raw, x);
+    uint32_t c[4];
+    if constexpr (POW2) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) c[k] = e4m3x2(x[2 * k] * fr_lo, x[2 * k + 1] * fr_lo);
+    } else {
+        uint32_t d[4];
+        bool same = true;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            c[k] = e4m3x2(x[2 * k] * fr_lo, x[2 * k + 1] * fr_lo);
+            d[k] = e4m3x2(x[2 * k] * fr_hi, x[2 * k + 1] * fr_hi);
+            same &= c[k] == d[k];
+        }
+        if (!same) {
+            const float s = __ldg(isv ? p.vscale : p.kscale);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                if (c[k] != d[k]) c[k] = e4m3x2(x[2 * k] / s, x[2 * k + 1] / s);
+        }
+    }
+    reinterpret_cast<uint2*>(row_ptr(p, isv, row, D))[lane] =
+        make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+}
+
+// Codes of one lane's 8 values, as low bytes of z (int8: -127..127, int4: -8..7).
 template <int FMT>
-__global__ void __launch_bounds__(WARPS * 32) kv_write_kernel(const Params p) {
+__device__ __forceinline__ void codes_markstein(const float x[8], float s, float r, uint32_t z[8]) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const float q0 = __fmul_rn(x[k], r);
+        const float e = __fmaf_rn(-q0, s, x[k]);
+        z[k] = rint_bits(__fmaf_rn(e, r, q0));
+    }
+}
+
+// The definition as it stands, for absmax below 2^-60 (subnormal or zero scales).
+template <int FMT>
+__device__ __forceinline__ void codes_divide(const float x[8], float s, uint32_t z[8]) {
+    constexpr float qmax = FMT == QSA_KV_INT8 ? 127.0f : 7.0f;
+    constexpr float qmin = FMT == QSA_KV_INT8 ? -127.0f : -8.0f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        z[k] = static_cast<uint32_t>(s > 0.0f ? static_cast<int>(fminf(fmaxf(rintf(x[k] / s), qmin), qmax)) : 0);
+}
+
+template <int FMT>
+__device__ __forceinline__ void store_codes(const Params& p, long long row, bool isv, int lane, float s,
+                                            const uint32_t z[8]) {
+    const uint32_t b0 = low_bytes(z[0], z[1], z[2], z[3]);
+    const uint32_t b1 = low_bytes(z[4], z[5], z[6], z[7]);
+    if constexpr (FMT == QSA_KV_INT8)
+        reinterpret_cast<uint2*>(row_ptr(p, isv, row, D))[lane] = make_uint2(b0, b1);
+    else
+        reinterpret_cast<uint32_t*>(row_ptr(p, isv, row, D / 2))[lane] = low_nibbles(b0) | (low_nibbles(b1) << 16);
+    if (lane == 0) (isv ? p.vscale : p.kscale)[row] = s;
+}
+
+// One row's conversion and store; rows are resolved from the task index
+// t in [0, 2 n Hkv): K rows first, token-major, then V rows.
+template <int FMT> struct Converter {
+    float k_lo, k_hi, v_lo, v_hi;     // fp8: 1 / pool scale times 1 -+ 2^-20 (or 1)
+    const uint32_t* s_tab;            // int8/int4: s and 1 / s for a = 1 + t / 128
+    const uint32_t* r_tab;
+
+    __device__ __forceinline__ void operator()(const Params& p, const uint4 raw, long long row, bool isv,
+                                               int lane) const {
+        if constexpr (FMT == QSA_KV_BF16) {
+            reinterpret_cast<uint4*>(row_ptr(p, isv, row, 2 * D))[lane] = raw;
+        } else if constexpr (FMT == QSA_KV_FP8_E4M3) {
+            const float lo = isv ? v_lo : k_lo, hi = isv ? v_hi : k_hi;
+            if (lo == hi) // uniform across the grid
+                store_fp8<true>(p, raw, row, isv, lane, lo, hi);
+            else
+                store_fp8<false>(p, raw, row, isv, lane, lo, hi);
+        } else {
+            constexpr float qmax = FMT == QSA_KV_INT8 ? 127.0f : 7.0f;
+            float x[8];
+            unpack(raw, x);
+            float m = 0.0f;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(x[k]));
+            // m >= 0, so its bit pattern orders like its value
+            const float a = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(m)));
+            uint32_t z[8];
+            float sc;
+            if (a >= FAST_MIN_ABSMAX) { // uniform across the warp
+                // a = (1 + t / 128) * 2^E exactly: move the table entries' exponents by E
+                const uint32_t ab = __float_as_uint(a);
+                const int t = (ab >> 16) & 0x7F;
+                const uint32_t e = (ab & 0x7F800000u) - (127u << 23);
+                sc = __uint_as_float(s_tab[t] + e);
+                codes_markstein<FMT>(x, sc, __uint_as_float(r_tab[t] - e), z);
+            } else {
+                sc = __fdiv_rn(a, qmax);
+                codes_divide<FMT>(x, sc, z);
+            }
+            store_codes<FMT>(p, row, isv, lane, sc, z);
+        }
+    }
+};
+
+// Task t -> source row and destination pool row; false for t past the end or a
+// slot outside the pool (then *bad).
+__device__ __forceinline__ bool resolve(const Params& p, int rows, int t, const __nv_bfloat16** src,
+                                        long long* dst, bool* isv, bool* bad) {
+    *bad = false;
+    if (t >= 2 * rows) return false;
+    *isv = t >= rows;
+    const int r = *isv ? t - rows : t;
+    const int i = p.Hkv == 2 ? r >> 1 : r, g = p.Hkv == 2 ? r & 1 : 0;
+    const int slot = __ldg(p.slots + i);
+    if (slot < 0 || (long long)slot >= p.num_slots) {
+        *bad = true;
+        return false;
+    }
+    *src = *isv ? p.vx + i * p.v_st + g * p.v_sh : p.kx + i * p.k_st + g * p.k_sh;
+    *dst = (long long)slot * p.Hkv + g;
+    return true;
+}
+
+// Bracket factors for an fp8 pool scale s: both 1 / s when s is a power of two
+// (then x / s = x * (1 / s) exactly), else 1 / s times 1 -+ 2^-20.
+__device__ __forceinline__ void fp8_factors(float s, float* lo, float* hi) {
+    const float r = __frcp_rn(s);
+    const bool pow2 = (__float_as_uint(s) & 0x007FFFFFu) == 0 && s > 0x1p-126f && s < 0x1p126f;
+    *lo = pow2 ? r : r * (1.0f - 0x1p-20f);
+    *hi = pow2 ? r : r * (1.0f + 0x1p-20f);
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(WARPS * 32, 5) kv_write_kernel(const Params p) {
+    constexpr bool INTQ = FMT == QSA_KV_INT8 || FMT == QSA_KV_INT4;
+    constexpr float qmax = FMT == QSA_KV_INT8 ? 127.0f : 7.0f;
+    __shared__ uint32_t s_tab[INTQ ? 128 : 1], r_tab[INTQ ? 128 : 1];
+    Converter<FMT> conv{0.0f, 0.0f, 0.0f, 0.0f, s_tab, r_tab};
+    if constexpr (INTQ) {
+        if (threadIdx.x < 128) {
+            const float s0 = __fdiv_rn(1.0f + threadIdx.x * 0x1p-7f, qmax);
+            s_tab[threadIdx.x] = __float_as_uint(s0);
+            r_tab[threadIdx.x] = __float_as_uint(__frcp_rn(s0));
+        }
+        __syncthreads();
+    }
+    if constexpr (FMT == QSA_KV_FP8_E4M3) {
+        fp8_factors(__ldg(p.kscale), &conv.k_lo, &conv.k_hi);
+        fp8_factors(__ldg(p.vscale), &conv.v_lo, &conv.v_hi);
+    }
     const int lane = threadIdx.x & 31;
     const int rows = p.n * p.Hkv; // n <= 2^28 and Hkv <= 2: every task index fits in 32 bits
     const int first = (blockIdx.x * WARPS + (threadIdx.x >> 5)) * RPW;
-    float kr_lo = 0.0f, kr_hi = 0.0f, vr_lo = 0.0f, vr_hi = 0.0f;
-    if constexpr (FMT == QSA_KV_FP8_E4M3) {
-        const float kr = __frcp_rn(__ldg(p.kscale)), vr = __frcp_rn(__ldg(p.vscale));
-        kr_lo = kr * (1.0f - 0x1p-20f);
-        kr_hi = kr * (1.0f + 0x1p-20f);
-        vr_lo = vr * (1.0f - 0x1p-20f);
-        vr_hi = vr * (1.0f + 0x1p-20f);
-    }
     uint4 raw[RPW];
     long long dst[RPW];
+    bool isv[RPW];
 #pragma unroll
     for (int u = 0; u < RPW; ++u) {
-        const int task = first + u;
+        const __nv_bfloat16* src;
+        bool bad;
         dst[u] = -1;
         raw[u] = make_uint4(0u, 0u, 0u, 0u);
-        if (task >= 2 * rows) continue;
-        const bool isv = task >= rows;
-        const int r = isv ? task - rows : task;
-        const int i = p.Hkv == 2 ? r >> 1 : r, g = p.Hkv == 2 ? r & 1 : 0;
-        const int slot = __ldg(p.slots + i);
-        if (slot < 0 || (long long)slot >= p.num_slots) {
-            if (lane == 0 && p.err) atomicOr(p.err, QSA_DEVERR_SLOT_RANGE);
-            continue;
-        }
-        const __nv_bfloat16* src =
-            isv ? p.vx + i * p.v_st + g * p.v_sh : p.kx + i * p.k_st + g * p.k_sh;
-        raw[u] = __ldg(reinterpret_cast<const uint4*>(src) + lane); // dims 8*lane .. +7
-        dst[u] = (long long)slot * p.Hkv + g;
+        if (resolve(p, rows, first + u, &src, &dst[u], &isv[u], &bad))
+            raw[u] = __ldg(reinterpret_cast<const uint4*>(src) + lane); // dims 8 lane .. 8 lane + 7
+        else if (bad && lane == 0 && p.err)
+            atomicOr(p.err, QSA_DEVERR_SLOT_RANGE);
     }
 #pragma unroll
-    for (int u = 0; u < RPW; ++u) {
-        const bool isv = first + u >= rows;
-        if (dst[u] >= 0)
-            write_row<FMT>(p, raw[u], dst[u], isv, lane, isv ? vr_lo : kr_lo, isv ? vr_hi : kr_hi);
-    }
+    for (int u = 0; u < RPW; ++u)
+        if (dst[u] >= 0) conv(p, raw[u], dst[u], isv[u], lane);
 }
 
 namespace {
