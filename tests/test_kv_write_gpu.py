@@ -144,3 +144,67 @@ def test_write_then_decode(cuda_device, fmt):
                       None if wd.k_scale is None else wd.k_scale.cpu(),
                       None if wd.v_scale is None else wd.v_scale.cpu(), w.softmax_scale, w.capacity)
     compare(out, run_oracle(host), w.lengths().numpy())
+
+
+def _ratio_rows(exponent: int) -> torch.Tensor:
+    """Rows whose absmax a = (1 + t/128) 2^exponent takes every bf16 mantissa t and
+    whose other values are every bf16 x with 2^-11 a <= |x| <= a (both signs): every
+    ratio x / a that can give a nonzero code, so the rounding of every such x / s is
+    checked."""
+    rows = []
+    for t in range(128):
+        a = (1 + t / 128) * 2.0 ** exponent
+        xs = [m / 128 * 2.0 ** (exponent + e) for e in range(0, -12, -1) for m in range(128, 256)]
+        xs = [v for v in xs if v <= a]
+        xs = torch.tensor(xs + [-v for v in xs], dtype=torch.float64)
+        for k in range(0, xs.numel(), 255):
+            chunk = xs[k:k + 255]
+            row = torch.zeros(256, dtype=torch.float64)
+            row[0] = a
+            row[1:1 + chunk.numel()] = chunk
+            rows.append(row)
+    return torch.stack(rows).to(torch.bfloat16)
+
+
+def _write_and_compare(dev, fmt, x, fp8_scale=None):
+    n = x.shape[0]
+    xk = x.reshape(n, 1, 256)
+    slots = torch.arange(n, dtype=torch.int32)
+    kp, vp = _pools(fmt, n, 1, dev, 70)
+    if fmt == "fp8_e4m3":
+        ks = torch.tensor([fp8_scale], device=dev)
+        vs = ks.clone()
+    else:
+        ks = torch.zeros(n, 1, device=dev)
+        vs = torch.zeros(n, 1, device=dev)
+    xd = xk.to(dev)
+    qsa.qsa_kv_write(fmt, xd, xd, slots.to(dev), kp, vp, ks, vs)
+    torch.cuda.synchronize()
+    codes, scales = oracle.quantize_rows(x, fmt, fp8_scale=1.0 if fp8_scale is None else fp8_scale)
+    for pool, sc in ((kp, ks), (vp, vs)):
+        got = pool.cpu().reshape(n, -1).view(torch.uint8).numpy()
+        assert np.array_equal(got, codes.view(np.uint8)), (fmt, fp8_scale)
+        if scales is not None:
+            assert np.array_equal(sc.cpu().reshape(-1).numpy(), scales)
+
+
+@pytest.mark.parametrize("fmt", ["int8", "int4"])
+def test_every_quotient_rounds_like_the_oracle(cuda_device, fmt):
+    """All reachable (x, absmax) bf16 mantissa pairs, at absmax exponents from the
+    smallest of the table path (2^-60) to the largest bf16 binade."""
+    for e in (-60, -59, -20, -1, 0, 1, 37, 100, 127):
+        _write_and_compare(cuda_device, fmt, _ratio_rows(e))
+    # below 2^-60 (subnormal scales, clamped codes) the kernel divides
+    _write_and_compare(cuda_device, fmt, _ratio_rows(-61))
+    _write_and_compare(cuda_device, fmt, _ratio_rows(-126)[::7])
+
+
+@pytest.mark.parametrize("scale", [1.0, 0.0625, 2.0 ** -20, 0.05, 0.0112, 3.0, 448.0 / 3])
+def test_every_bf16_value_fp8(cuda_device, scale):
+    """Every finite bf16 bit pattern through the fp8 write, power-of-two and other scales."""
+    bits = torch.arange(65536, dtype=torch.int32).to(torch.int16)
+    vals = bits.view(torch.bfloat16)
+    vals = vals[torch.isfinite(vals.float())]
+    pad = (-vals.numel()) % 256
+    x = torch.cat([vals, torch.zeros(pad, dtype=torch.bfloat16)]).reshape(-1, 256)
+    _write_and_compare(cuda_device, "fp8_e4m3", x, fp8_scale=scale)
