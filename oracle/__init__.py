@@ -31,7 +31,9 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "qsa_oracle.c")
 _LIB = os.path.join(_HERE, "liboracle.so")
 
-FORMATS = {"bf16": 0, "fp8_e4m3": 1, "int8": 2, "int4": 3}
+FORMATS = {"bf16": 0, "fp8_e4m3": 1, "int8": 2, "int4": 3, "int8_g64": 4, "int4_g32": 5}
+GROUP = {"int8_g64": 64, "int4_g32": 32}     # channels per binary16 scale
+NIBBLE = ("int4", "int4_g32")              # two 4-bit codes per byte
 
 _lib = None
 
@@ -59,6 +61,12 @@ def _load():
     lib.orc_e4m3fn_to_double.argtypes = [ctypes.c_uint8]
     lib.orc_int4_value.restype = ctypes.c_int
     lib.orc_int4_value.argtypes = [ctypes.c_uint8, ctypes.c_int]
+    lib.orc_fp16_to_double.restype = ctypes.c_double
+    lib.orc_fp16_to_double.argtypes = [ctypes.c_uint16]
+    lib.orc_round_fp16.restype = ctypes.c_uint16
+    lib.orc_round_fp16.argtypes = [ctypes.c_float]
+    lib.orc_int4_offset_value.restype = ctypes.c_int
+    lib.orc_int4_offset_value.argtypes = [ctypes.c_uint8, ctypes.c_int]
     lib.orc_round_bf16.restype = ctypes.c_uint16
     lib.orc_round_bf16.argtypes = [ctypes.c_double]
     lib.orc_round_bf16_array.restype = None
@@ -102,6 +110,8 @@ def _np(a, dtype=None):
             t = t.view(torch.int16).view(torch.uint16) if hasattr(torch, "uint16") else t.view(torch.int16)
         elif t.dtype == torch.float8_e4m3fn:
             t = t.view(torch.uint8)
+        elif t.dtype == torch.float16:
+            t = t.view(torch.int16)
         a = t.contiguous().numpy()
         if a.dtype == np.int16:
             a = a.view(np.uint16)
@@ -115,13 +125,29 @@ def _ptr(a):
     return a.ctypes.data_as(ctypes.c_void_p) if a is not None else None
 
 
+def _scales(a, fmt: str):
+    """Scales as the C side reads them: float32, or binary16 bits for the grouped formats."""
+    if a is None:
+        return None
+    if fmt in GROUP:
+        n = _np(a)
+        if n.dtype == np.float16:
+            n = n.view(np.uint16)
+        if n.dtype != np.uint16:
+            raise ValueError("grouped formats take binary16 scales")
+        return np.ascontiguousarray(n)
+    return _np(a, np.float32)
+
+
 def decode(q, k_pool, v_pool, fmt: str, sel, cu, softmax_scale: float,
            k_scale=None, v_scale=None, rows=None, threads: int = 0) -> np.ndarray:
     """Oracle decode. Returns float64 [len(rows) or bs, Hq, D].
 
     q: bf16 [bs, Hq, D] (torch bf16 tensor or uint16 bits); k_pool/v_pool:
     [num_slots, Hkv, D] (bf16 bits / uint8 e4m3 / int8) or [num_slots, Hkv, D/2]
-    uint8 (int4); sel int32 [n_sel]; cu int32 [bs+1]; scales float32.
+    uint8 (4-bit formats); sel int32 [n_sel]; cu int32 [bs+1]; scales float32
+    (fp8 [1], int8/int4 [num_slots, Hkv]) or binary16 [num_slots, Hkv, D/group]
+    for the grouped formats.
     """
     lib = _load()
     f = FORMATS[fmt]
@@ -131,17 +157,16 @@ def decode(q, k_pool, v_pool, fmt: str, sel, cu, softmax_scale: float,
     bs, Hq, D = qn.shape
     kn, vn = _np(k_pool), _np(v_pool)
     num_slots, Hkv = kn.shape[0], kn.shape[1]
-    if f == 3:
+    if fmt in NIBBLE:
         if kn.shape[2] * 2 != D:
-            raise ValueError("int4 pool rows must hold D/2 bytes")
+            raise ValueError("4-bit pool rows must hold D/2 bytes")
     elif kn.shape[2] != D:
         raise ValueError("pool rows must hold D elements")
     sn = _np(sel, np.int32)
     cn = _np(cu, np.int32)
     if cn.shape[0] != bs + 1:
         raise ValueError("cu_seqlens must have bs+1 entries")
-    ks = _np(k_scale, np.float32) if k_scale is not None else None
-    vs = _np(v_scale, np.float32) if v_scale is not None else None
+    ks, vs = _scales(k_scale, fmt), _scales(v_scale, fmt)
     if f != 0 and (ks is None or vs is None):
         raise ValueError("quantised pools need k_scale and v_scale")
     rn = _np(rows, np.int32) if rows is not None else None
@@ -161,8 +186,8 @@ def dequant_rows(pool, fmt: str, slots, g: int, scale=None) -> np.ndarray:
     lib = _load()
     pn = _np(pool)
     Hkv = pn.shape[1]
-    D = pn.shape[2] * (2 if fmt == "int4" else 1)
-    sc = _np(scale, np.float32) if scale is not None else None
+    D = pn.shape[2] * (2 if fmt in NIBBLE else 1)
+    sc = _scales(scale, fmt)
     out = np.zeros((len(slots), D), dtype=np.float64)
     for i, s in enumerate(slots):
         row = out[i]
@@ -177,6 +202,19 @@ def e4m3fn_to_double(byte: int) -> float:
 
 def int4_value(byte: int, hi: int) -> int:
     return _load().orc_int4_value(int(byte), int(hi))
+
+
+def int4_offset_value(byte: int, hi: int) -> int:
+    return _load().orc_int4_offset_value(int(byte), int(hi))
+
+
+def fp16_to_double(bits: int) -> float:
+    return _load().orc_fp16_to_double(int(bits))
+
+
+def round_fp16_bits(v: float) -> int:
+    """binary16 bits of a binary32 value rounded to nearest, ties to even."""
+    return _load().orc_round_fp16(float(v))
 
 
 def bf16_to_double(bits: int) -> float:
@@ -207,7 +245,8 @@ def quantize_rows(x, fmt: str, fp8_scale: float = 1.0):
     """Quantise bf16 rows [n, D] as the KV write path does.
 
     Returns (codes, scales): codes uint8 [n, D] (bf16: uint16 bits [n, D];
-    int8: int8 [n, D]; int4: uint8 [n, D/2]); scales float32 [n] for int8/int4,
+    int8 / int8_g64: int8 [n, D]; int4 / int4_g32: uint8 [n, D/2]); scales
+    float32 [n] for int8/int4, float16 [n, D/group] for the grouped formats,
     else None."""
     lib = _load()
     xn = _np(x)
@@ -217,16 +256,23 @@ def quantize_rows(x, fmt: str, fp8_scale: float = 1.0):
     f = FORMATS[fmt]
     if fmt == "bf16":
         codes = np.empty((n, D), dtype=np.uint16)
-    elif fmt == "int4":
+    elif fmt in NIBBLE:
         codes = np.zeros((n, D // 2), dtype=np.uint8)
     else:
         codes = np.empty((n, D), dtype=np.uint8)
-    scales = np.zeros(n, dtype=np.float32) if fmt in ("int8", "int4") else None
+    if fmt in GROUP:
+        scales = np.zeros((n, D // GROUP[fmt]), dtype=np.uint16)
+    elif fmt in ("int8", "int4"):
+        scales = np.zeros(n, dtype=np.float32)
+    else:
+        scales = None
     rc = lib.orc_quantize_rows(_ptr(xn), n, D, f, float(fp8_scale), _ptr(codes), _ptr(scales))
     if rc != 0:
         raise ValueError("bad format or shape")
-    if fmt == "int8":
+    if fmt in ("int8", "int8_g64"):
         codes = codes.view(np.int8)
+    if fmt in GROUP:
+        scales = scales.view(np.float16)
     return codes, scales
 
 

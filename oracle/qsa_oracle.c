@@ -24,6 +24,12 @@
  *   int8    : int8 * s[slot, g]                  (fp32 per (slot, KV head))
  *   int4    : sext4(nibble) * s[slot, g]; two per byte, element 2i in the
  *             low nibble (two's-complement nibbles)
+ *   int8_g64: int8 * s16[slot, g, d / 64]       (IEEE binary16 per 64-channel
+ *             group; group 0 holds the rotary dims)
+ *   int4_g32: (nibble - 8) * s16[slot, g, d / 32] (offset-binary nibbles, element
+ *             2i in the low nibble; binary16 per 32-channel group)
+ * (the grouped formats: sglang PR #37798, "Modifications", the int8 and int4
+ * KV pool modules)
  *
  * Every step is written as the definition states it: no tiling, no
  * online softmax, no split, no merge. The scores use one exact max
@@ -37,7 +43,15 @@
 #include <omp.h>
 #endif
 
-enum { ORC_BF16 = 0, ORC_FP8_E4M3 = 1, ORC_INT8 = 2, ORC_INT4 = 3 };
+enum { ORC_BF16 = 0, ORC_FP8_E4M3 = 1, ORC_INT8 = 2, ORC_INT4 = 3, ORC_INT8_G64 = 4, ORC_INT4_G32 = 5 };
+
+/* Channels per scale group: 64 / 32 for the grouped formats, 0 otherwise. */
+static int group_size(int format) {
+    return format == ORC_INT8_G64 ? 64 : format == ORC_INT4_G32 ? 32 : 0;
+}
+
+/* Pool rows hold D / 2 bytes (two 4-bit codes per byte). */
+static int is_nibble_format(int format) { return format == ORC_INT4 || format == ORC_INT4_G32; }
 
 /* bf16 -> double: a bf16 is the upper half of an IEEE binary32. */
 double orc_bf16_to_double(uint16_t h) {
@@ -61,6 +75,47 @@ double orc_e4m3fn_to_double(uint8_t b) {
     else
         v = ldexp(1.0 + (double)m / 8.0, e - 7);
     return sign ? -v : v;
+}
+
+/* IEEE 754 binary16: 1 sign, 5 exponent bits with bias 15, 10 fraction bits;
+ * exponent field 0 encodes subnormals f/1024 * 2^-14, field 31 inf / NaN. */
+double orc_fp16_to_double(uint16_t h) {
+    int sign = h >> 15;
+    int e = (h >> 10) & 0x1F;
+    int f = h & 0x3FF;
+    double v;
+    if (e == 0x1F) v = f ? NAN : INFINITY;
+    else if (e == 0) v = ldexp((double)f / 1024.0, -14);
+    else v = ldexp(1.0 + (double)f / 1024.0, e - 15);
+    return sign ? -v : v;
+}
+
+/* Round a binary32 value to the nearest binary16 (ties to even), returning its
+ * bits; magnitudes that round beyond 65504 give infinity. */
+uint16_t orc_round_fp16(float x) {
+    if (isnan(x)) return 0x7E00;
+    uint16_t sign = signbit(x) ? 0x8000 : 0;
+    double a = fabs((double)x);
+    if (a == 0.0) return sign;
+    if (isinf(a)) return sign | 0x7C00;
+    int e2;
+    frexp(a, &e2);
+    int E = e2 - 1;              /* floor(log2 a) */
+    if (E < -14) E = -14;        /* subnormal quantum is 2^-24 */
+    double quantum = ldexp(1.0, E - 10);
+    double r = nearbyint(a / quantum) * quantum; /* ties to even */
+    if (r > 65504.0) return sign | 0x7C00;
+    if (r < ldexp(1.0, -14)) return sign | (uint16_t)(r / ldexp(1.0, -24));
+    frexp(r, &e2);
+    E = e2 - 1;
+    uint16_t frac = (uint16_t)((r / ldexp(1.0, E) - 1.0) * 1024.0);
+    return sign | (uint16_t)((E + 15) << 10) | frac;
+}
+
+/* Offset-binary 4-bit value held in bits [4*hi, 4*hi+3] of `byte`: u - 8. */
+int orc_int4_offset_value(uint8_t byte, int hi) {
+    int n = hi ? (byte >> 4) & 0xF : byte & 0xF;
+    return n - 8;
 }
 
 /* Two's-complement 4-bit value held in bits [4*hi, 4*hi+3] of `byte`. */
@@ -100,7 +155,8 @@ typedef struct {
     int format;
     int Hkv;
     int D;
-    const float* scale; /* fp8: [1]; int8/int4: [num_slots * Hkv]; bf16: unused */
+    const void* scale; /* fp8: float [1]; int8/int4: float [num_slots * Hkv];
+                          grouped: binary16 bits [num_slots * Hkv * D / group]; bf16: unused */
 } orc_pool;
 
 /* Dequantised element d of pool row (slot, g), exactly in FP64. */
@@ -111,19 +167,30 @@ static double pool_elem(const orc_pool* p, int64_t slot, int g, int d) {
         return orc_bf16_to_double(((const uint16_t*)p->pool)[row * p->D + d]);
     case ORC_FP8_E4M3:
         return orc_e4m3fn_to_double(((const uint8_t*)p->pool)[row * p->D + d]) *
-               (double)p->scale[0];
+               (double)((const float*)p->scale)[0];
     case ORC_INT8:
-        return (double)((const int8_t*)p->pool)[row * p->D + d] * (double)p->scale[row];
+        return (double)((const int8_t*)p->pool)[row * p->D + d] * (double)((const float*)p->scale)[row];
     case ORC_INT4: {
         uint8_t byte = ((const uint8_t*)p->pool)[row * (p->D / 2) + d / 2];
-        return (double)orc_int4_value(byte, d & 1) * (double)p->scale[row];
+        return (double)orc_int4_value(byte, d & 1) * (double)((const float*)p->scale)[row];
+    }
+    case ORC_INT8_G64: {
+        const int groups = p->D / 64;
+        const uint16_t s16 = ((const uint16_t*)p->scale)[row * groups + d / 64];
+        return (double)((const int8_t*)p->pool)[row * p->D + d] * orc_fp16_to_double(s16);
+    }
+    case ORC_INT4_G32: {
+        const int groups = p->D / 32;
+        const uint16_t s16 = ((const uint16_t*)p->scale)[row * groups + d / 32];
+        uint8_t byte = ((const uint8_t*)p->pool)[row * (p->D / 2) + d / 2];
+        return (double)orc_int4_offset_value(byte, d & 1) * orc_fp16_to_double(s16);
     }
     }
     return NAN;
 }
 
 /* Dequantise one pool row into `dst` (D doubles). */
-void orc_dequant_row(const void* pool, int format, int Hkv, int D, const float* scale,
+void orc_dequant_row(const void* pool, int format, int Hkv, int D, const void* scale,
                      int64_t slot, int g, double* dst) {
     orc_pool p = {pool, format, Hkv, D, scale};
     for (int d = 0; d < D; ++d) dst[d] = pool_elem(&p, slot, g, d);
@@ -133,7 +200,8 @@ void orc_dequant_row(const void* pool, int format, int Hkv, int D, const float* 
  * Full decode. Returns 0 on success and a negative value when the input
  * breaks the contract the pages define (the oracle refuses such inputs
  * instead of guessing an answer):
- *   -1  bad geometry (Hq not a multiple of Hkv, D odd for int4, unknown format)
+ *   -1  bad geometry (Hq not a multiple of Hkv, D odd for int4, D not a
+ *       multiple of the scale group, unknown format)
  *   -2  cu_seqlens not monotone, negative, or beyond the index buffer
  *   -3  a selected slot outside [0, num_slots)
  *
@@ -145,12 +213,13 @@ void orc_dequant_row(const void* pool, int format, int Hkv, int D, const float* 
 int orc_decode(const uint16_t* q, int64_t q_sb, int64_t q_sh,
                const void* k_pool, const void* v_pool, int format,
                int64_t num_slots, int Hkv, int D,
-               const float* k_scale, const float* v_scale, double softmax_scale,
+               const void* k_scale, const void* v_scale, double softmax_scale,
                const int32_t* sel, int64_t n_sel, const int32_t* cu, int bs, int Hq,
                const int32_t* rows, int n_rows, double* out, int nthreads) {
     if (Hkv <= 0 || Hq <= 0 || Hq % Hkv != 0 || D <= 0) return -1;
-    if (format < ORC_BF16 || format > ORC_INT4) return -1;
-    if (format == ORC_INT4 && (D & 1)) return -1;
+    if (format < ORC_BF16 || format > ORC_INT4_G32) return -1;
+    if (is_nibble_format(format) && (D & 1)) return -1;
+    if (group_size(format) && D % group_size(format)) return -1;
     if (rows == NULL) n_rows = bs;
     for (int i = 0; i < n_rows; ++i) {
         int b = rows ? rows[i] : i;
@@ -249,12 +318,35 @@ uint8_t orc_e4m3fn_encode(float v) {
  *   int8 (2): s = absmax / 127, codes[d] = clamp(rint(x[d] / s), -127, 127)
  *   int4 (3): s = absmax / 7,   codes[d] = clamp(rint(x[d] / s), -8, 7), two per
  *             byte, channel 2i in the low nibble
- * An all-zero row gets s = 0 and zero codes. rint is round-half-to-even.
- * codes: n * D bytes (2n * D for bf16, n * D / 2 for int4); scales: n floats
- * (int8 / int4 only). Returns 0, or -1 for a bad format or odd D with int4. */
+ *   int8_g64 (4), int4_g32 (5): per group of 64 / 32 channels, the binary32
+ *             absmax / 127 (/ 7) clamped to 65504 and rounded to binary16 is
+ *             the group's scale s16; codes[d] = clamp(rint(x[d] / s16), -q, q)
+ *             with q = 127 (7); int4_g32 stores nibbles q + 8 (offset binary),
+ *             channel 2i in the low nibble. The codes divide by the stored
+ *             binary16 scale, the one the reader multiplies by.
+ * An all-zero row or group (or a scale that rounds to 0) gets s = 0 and zero
+ * codes (offset-binary 8 for int4_g32). rint is round-half-to-even. codes: n * D
+ * bytes (2n * D for bf16, n * D / 2 for the 4-bit formats); scales: n floats
+ * (int8 / int4) or n * D / group binary16 bits (grouped). Returns 0, or -1 for a
+ * bad format or a D the format cannot hold. */
+static void put_code(uint8_t* codes, int64_t r, int D, int format, int d, int q) {
+    if (format == ORC_INT8 || format == ORC_INT8_G64) {
+        codes[r * D + d] = (uint8_t)(int8_t)q;
+        return;
+    }
+    const int u = format == ORC_INT4_G32 ? q + 8 : q & 0xF;
+    uint8_t* byte = codes + r * (D / 2) + d / 2;
+    if ((d & 1) == 0)
+        *byte = (uint8_t)u;
+    else
+        *byte |= (uint8_t)(u << 4);
+}
+
 int orc_quantize_rows(const uint16_t* x, int64_t n, int D, int format, float fp8_scale,
-                      uint8_t* codes, float* scales) {
-    if (format < ORC_BF16 || format > ORC_INT4 || D <= 0 || (format == ORC_INT4 && (D & 1)))
+                      uint8_t* codes, void* scales) {
+    if (format < ORC_BF16 || format > ORC_INT4_G32 || D <= 0 ||
+        (is_nibble_format(format) && (D & 1)) ||
+        (group_size(format) && D % group_size(format)))
         return -1;
     for (int64_t r = 0; r < n; ++r) {
         const uint16_t* xr = x + r * D;
@@ -270,32 +362,35 @@ int orc_quantize_rows(const uint16_t* x, int64_t n, int D, int format, float fp8
             }
             continue;
         }
-        const float qmax = format == ORC_INT8 ? 127.0f : 7.0f;
-        const float qmin = format == ORC_INT8 ? -127.0f : -8.0f;
-        float amax = 0.0f;
-        for (int d = 0; d < D; ++d) {
-            const float a = fabsf((float)orc_bf16_to_double(xr[d]));
-            if (a > amax) amax = a;
-        }
-        const float s = amax / qmax;
-        scales[r] = s;
-        for (int d = 0; d < D; ++d) {
-            int q = 0;
-            if (s > 0.0f) {
-                const float y = (float)orc_bf16_to_double(xr[d]) / s;
-                float qf = rintf(y);
-                if (qf > qmax) qf = qmax;
-                if (qf < qmin) qf = qmin;
-                q = (int)qf;
+        const int grouped = group_size(format) != 0;
+        const int gs = grouped ? group_size(format) : D;
+        const float qmax = (format == ORC_INT8 || format == ORC_INT8_G64) ? 127.0f : 7.0f;
+        const float qmin = format == ORC_INT4 ? -8.0f : -qmax;
+        for (int k = 0; k < D / gs; ++k) {
+            float amax = 0.0f;
+            for (int d = k * gs; d < (k + 1) * gs; ++d) {
+                const float a = fabsf((float)orc_bf16_to_double(xr[d]));
+                if (a > amax) amax = a;
             }
-            if (format == ORC_INT8) {
-                codes[r * D + d] = (uint8_t)(int8_t)q;
+            float s = amax / qmax;
+            if (grouped) {
+                if (s > 65504.0f) s = 65504.0f;
+                const uint16_t s16 = orc_round_fp16(s);
+                ((uint16_t*)scales)[r * (D / gs) + k] = s16;
+                s = (float)orc_fp16_to_double(s16);
             } else {
-                uint8_t* byte = codes + r * (D / 2) + d / 2;
-                if ((d & 1) == 0)
-                    *byte = (uint8_t)(q & 0xF);
-                else
-                    *byte |= (uint8_t)((q & 0xF) << 4);
+                ((float*)scales)[r] = s;
+            }
+            for (int d = k * gs; d < (k + 1) * gs; ++d) {
+                int q = 0;
+                if (s > 0.0f) {
+                    const float y = (float)orc_bf16_to_double(xr[d]) / s;
+                    float qf = rintf(y);
+                    if (qf > qmax) qf = qmax;
+                    if (qf < qmin) qf = qmin;
+                    q = (int)qf;
+                }
+                put_code(codes, r, D, format, d, q);
             }
         }
     }

@@ -26,8 +26,11 @@ PAGE = 64               # slots per page
 MAX_CAPACITY = 2055     # largest selected-KV length of the contract
 SOFTMAX_SCALE = 1.0 / 16.0
 
-FORMATS = ("bf16", "fp8_e4m3", "int8", "int4")
+FORMATS = ("bf16", "fp8_e4m3", "int8", "int4", "int8_g64", "int4_g32")
+GROUPED = {"int8_g64": 64, "int4_g32": 32}   # channels per binary16 scale
+NIBBLE_FORMATS = ("int4", "int4_g32")        # two 4-bit codes per byte
 FP8_E4M3_MAX = 448.0    # largest finite e4m3fn value; the fp8 write saturates here
+FP16_MAX = 65504.0      # the grouped formats' scale clamp (largest finite binary16)
 
 
 @dataclass
@@ -40,7 +43,8 @@ class Workload:
     sel: torch.Tensor                # int32 [n_sel], packed by cu
     cu: torch.Tensor                 # int32 [bs+1]
     fmt: str = "bf16"
-    k_scale: Optional[torch.Tensor] = None   # fp8: [1]; int8/int4: [slots, Hkv] float32
+    k_scale: Optional[torch.Tensor] = None   # fp8: [1]; int8/int4: [slots, Hkv] float32;
+                                             # grouped: [slots, Hkv, 256 / group] float16
     v_scale: Optional[torch.Tensor] = None
     softmax_scale: float = SOFTMAX_SCALE
     capacity: int = MAX_CAPACITY
@@ -96,6 +100,10 @@ def quantize_pool(x: torch.Tensor, fmt: str):
     int8: fp32 scale per (slot, KV head) = absmax(row) / 127; codes = clamp(rint(x/s), -127, 127).
     int4: fp32 scale per (slot, KV head) = absmax(row) / 7; codes = clamp(rint(x/s), -8, 7),
           two's-complement nibbles, two per byte, element 2i in the low nibble.
+    int8_g64 / int4_g32 (sglang PR #37798, "Modifications", the int8 and int4 KV
+          pool modules): per 64 / 32-channel group a binary16 scale
+          s16 = fp16(min(absmax / q, 65504)), q = 127 / 7; codes = clamp(rint(x / s16), -q, q);
+          int4_g32 stores offset-binary nibbles code + 8, element 2i in the low nibble.
     rint is round-half-to-even (torch.round). A zero row gets scale 0 and zero codes.
     """
     if fmt == "bf16":
@@ -118,6 +126,20 @@ def quantize_pool(x: torch.Tensor, fmt: str):
         lo = (qv[..., 0::2].to(torch.int16) & 0xF)
         hi = (qv[..., 1::2].to(torch.int16) & 0xF)
         return (lo | (hi << 4)).to(torch.uint8), s
+    if fmt in GROUPED:
+        gs = GROUPED[fmt]
+        qmax = 127.0 if fmt == "int8_g64" else 7.0
+        xg = x.reshape(*x.shape[:-1], x.shape[-1] // gs, gs)
+        amax = xg.abs().amax(dim=-1)
+        s16 = (amax / qmax).to(torch.float32).clamp(max=FP16_MAX).to(torch.float16)
+        s32 = s16.to(torch.float32).unsqueeze(-1)
+        safe = torch.where(s32 > 0, s32, torch.ones_like(s32))
+        qv = torch.where(s32 > 0, torch.round(xg / safe), torch.zeros_like(xg))
+        qv = qv.clamp(-qmax, qmax).to(torch.int8).reshape(x.shape)
+        if fmt == "int8_g64":
+            return qv, s16
+        u = qv.to(torch.int16) + 8
+        return (u[..., 0::2] | (u[..., 1::2] << 4)).to(torch.uint8), s16
     raise ValueError(f"unknown pool format {fmt!r}")
 
 
@@ -293,7 +315,7 @@ def host_subset(w: Workload, rows) -> Workload:
     k = w.k_pool.index_select(0, dev_idx).cpu()
     v = w.v_pool.index_select(0, dev_idx).cpu()
     ks = vs = None
-    if w.fmt in ("int8", "int4"):
+    if w.fmt in ("int8", "int4") or w.fmt in GROUPED:
         ks = w.k_scale.index_select(0, dev_idx).cpu()
         vs = w.v_scale.index_select(0, dev_idx).cpu()
     elif w.fmt == "fp8_e4m3":

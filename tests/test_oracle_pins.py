@@ -194,6 +194,14 @@ def test_single_index_returns_that_v_row(fmt):
                        * float(w.v_scale[0])).numpy()
             elif fmt == "int8":
                 ref = (w.v_pool[slot, gkv].to(torch.float64) * float(w.v_scale[slot, gkv])).numpy()
+            elif fmt == "int8_g64":
+                sc = w.v_scale[slot, gkv].to(torch.float64).repeat_interleave(64)
+                ref = (w.v_pool[slot, gkv].to(torch.float64) * sc).numpy()
+            elif fmt == "int4_g32":
+                byts = w.v_pool[slot, gkv].numpy().astype(np.int64)
+                vals = np.stack([(byts & 0xF) - 8, (byts >> 4) - 8], 1).reshape(-1)
+                sc = w.v_scale[slot, gkv].to(torch.float64).repeat_interleave(32).numpy()
+                ref = vals * sc
             else:
                 byts = w.v_pool[slot, gkv].numpy()
                 lo = (byts.astype(np.int16) << 12).astype(np.int16) >> 12
@@ -376,3 +384,156 @@ def test_quantize_then_dequantize_round_trip():
         back = oracle.dequant_rows(pool, fmt, range(64), 0, torch.from_numpy(scales)[:, None])
         # |rint(fl(x / s)) - x / s| <= 1/2 + |fl(x / s) - x / s|, the second term below qmax * 2^-24
         assert (np.abs(back - xd) <= (0.5 + qmax * 2.0 ** -23) * scales[:, None]).all()
+
+
+# ------------------------------------------------------- grouped pool formats
+
+def _golden_grouped():
+    nib, groups, clamp = [], {}, None
+    for line in open(os.path.join(GOLDEN, "grouped_formats.txt")):
+        if line.startswith("#") or not line.strip():
+            continue
+        f = line.split()
+        if f[0] == "nibble":
+            nib.append((int(f[1], 16), int(f[2]), int(f[3])))
+        elif f[0] == "group":
+            pairs = [(int(f[i + 1]), int(f[i + 3])) for i in range(3, len(f), 4)]
+            groups[f[1]] = (int(f[2]), pairs)
+        elif f[0] == "clamp":
+            clamp = float(f[1])
+    return nib, groups, clamp
+
+
+def test_fp16_decode_matches_numpy_for_all_patterns():
+    bits = np.arange(1 << 16, dtype=np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = np.array([oracle.fp16_to_double(int(b)) for b in bits])
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    fin = ~np.isnan(ref)
+    assert np.array_equal(got[fin], ref[fin])
+
+
+def test_round_fp16_matches_numpy_including_ties_and_overflow():
+    rng = np.random.default_rng(5)
+    x = (rng.standard_normal(20000) * 10.0 ** rng.integers(-9, 6, 20000)).astype(np.float32)
+    base = rng.standard_normal(2000).astype(np.float16).astype(np.float32)
+    m, e = np.frexp(base)
+    half_ulp = np.ldexp(np.ones_like(base), e - 12).astype(np.float32)  # ties between neighbours
+    edges = np.array([65504, 65519.996, 65520, 70000, 2.0 ** -14, 2.0 ** -24, 2.0 ** -25,
+                      3 * 2.0 ** -25, 1e-9, 0.0, -0.0], dtype=np.float32)
+    x = np.concatenate([x, base + half_ulp, base - half_ulp, edges, -edges])
+    with np.errstate(over="ignore"):
+        ref = x.astype(np.float16).view(np.uint16)
+    got = np.array([oracle.round_fp16_bits(float(v)) for v in x], dtype=np.uint16)
+    assert np.array_equal(got, ref)
+    # closed forms: 1 + 2^-11 is halfway between 1 and 1 + 2^-10 -> 1 (even)
+    assert oracle.round_fp16_bits(1 + 2 ** -11) == 0x3C00
+    assert oracle.round_fp16_bits(1 + 3 * 2 ** -11) == 0x3C02
+
+
+def test_grouped_golden_nibbles_groups_and_clamp():
+    nib, groups, clamp = _golden_grouped()
+    for byte, even, odd in nib:
+        assert oracle.int4_offset_value(byte, 0) == even
+        assert oracle.int4_offset_value(byte, 1) == odd
+    for fmt, (size, pairs) in groups.items():
+        # codes 1 everywhere, scale of group k = 2^k: a channel reads its group's scale
+        G = 256 // size
+        codes = torch.full((1, 1, 128 if fmt == "int4_g32" else 256),
+                           0x99 if fmt == "int4_g32" else 1, dtype=torch.uint8)
+        if fmt == "int8_g64":
+            codes = codes.view(torch.int8)
+        sc = torch.tensor([[[2.0 ** k for k in range(G)]]], dtype=torch.float16)
+        row = oracle.dequant_rows(codes, fmt, [0], 0, sc)[0]
+        assert oracle.GROUP[fmt] == size
+        for ch, grp in pairs:
+            assert row[ch] == 2.0 ** grp
+    for fmt in ("int8_g64", "int4_g32"):
+        x = torch.zeros(1, 256)
+        x[0, 0] = 3.0e38  # absmax / q far above the binary16 range
+        x[0, 1] = -1.0e10
+        _, s = oracle.quantize_rows(x.to(torch.bfloat16), fmt)
+        assert float(s[0, 0]) == clamp and float(s[0, 1]) == 0.0
+
+
+@pytest.mark.parametrize("fmt", ["int8_g64", "int4_g32"])
+def test_grouped_decode_equals_bf16_pool_with_the_same_values(fmt):
+    """Codes times power-of-two binary16 scales are exact bf16 values: decoding the
+    grouped pool must equal decoding a bf16 pool that holds those values."""
+    gs = oracle.GROUP[fmt]
+    slots, Hkv, G = 64, 2, 256 // gs
+    g = torch.Generator().manual_seed(31)
+    if fmt == "int8_g64":
+        codes = torch.randint(-127, 128, (2, slots, Hkv, 256), generator=g)
+        packed = codes.to(torch.int8)
+    else:
+        codes = torch.randint(-7, 8, (2, slots, Hkv, 256), generator=g)
+        u = (codes + 8).to(torch.int16)
+        packed = (u[..., 0::2] | (u[..., 1::2] << 4)).to(torch.uint8)
+    exps = torch.randint(-6, 4, (2, slots, Hkv, G), generator=g).to(torch.float32)
+    scales = torch.pow(2.0, exps).to(torch.float16)
+    values = codes.to(torch.float64) * scales.to(torch.float64).repeat_interleave(gs, -1)
+    bf = values.to(torch.bfloat16)
+    assert torch.equal(bf.to(torch.float64), values)
+    q = I.make_query(3, 12 * Hkv, 32)
+    sel = I.uniform_indices(3 * 40, slots, g)
+    cu = I.cu_from_lengths([40, 40, 40])
+    got = oracle.decode(q, packed[0], packed[1], fmt, sel, cu, 1 / 16, scales[0], scales[1])
+    ref = oracle.decode(q, bf[0], bf[1], "bf16", sel, cu, 1 / 16)
+    assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("fmt", ["int8_g64", "int4_g32"])
+def test_grouped_quantisers_agree_and_round_trip(fmt):
+    """The oracle's write-side quantiser and the input generator's torch one agree
+    bit for bit, and dequant(quantise(x)) is within half a step of x."""
+    x = I.normal_values((200, 1, 256), 33, std=3.0).to(torch.bfloat16)
+    x[0] = 0.0
+    x[1, 0, :40] = 0.0           # an all-zero group
+    x[2, 0, 5] = 2.0e9           # a group whose scale clamps
+    codes, scales = oracle.quantize_rows(x[:, 0], fmt)
+    codes_t, s_t = I.quantize_pool(x.float(), fmt)
+    assert np.array_equal(codes.view(np.uint8), codes_t[:, 0].view(torch.uint8).numpy())
+    assert np.array_equal(scales.view(np.uint16), s_t[:, 0].view(torch.int16).numpy().view(np.uint16))
+    back = oracle.dequant_rows(torch.from_numpy(codes.view(np.uint8) if fmt == "int4_g32" else codes)[:, None],
+                               fmt, range(200), 0, torch.from_numpy(scales)[:, None])
+    xd = x[:, 0].double().numpy()
+    s = scales.astype(np.float64).repeat(oracle.GROUP[fmt], -1)
+    qmax = 127 if fmt == "int8_g64" else 7
+    ok = np.ones_like(xd, dtype=bool)
+    ok[2] = False  # the clamped group saturates
+    assert (np.abs(back - xd)[ok] <= ((0.5 + qmax * 2.0 ** -23) * s)[ok]).all()
+    assert back[2, 5] == qmax * 65504.0
+
+
+def test_grouped_error_bands_from_the_pages():
+    """Relative RMS error bands of the pages' pool tests (sglang PR #37798, "Accuracy
+    Tests"): int8 with 64-channel groups below 1.2 %, int4 with 32-channel groups in
+    8-11.5 %; measured on N(0, 1) draws."""
+    def rel_rms(fmt):
+        x = I.normal_values((256, 2, 256), 34)
+        codes, s = I.quantize_pool(x, fmt)
+        xr = np.stack([oracle.dequant_rows(codes, fmt, range(256), g, s) for g in range(2)], 1)
+        xd = x.double().numpy()
+        return math.sqrt(((xr - xd) ** 2).mean() / (xd ** 2).mean())
+
+    assert rel_rms("int8_g64") < 0.012
+    assert 0.08 < rel_rms("int4_g32") < 0.115
+
+
+def test_grouped_quantiser_ties_and_zero_groups():
+    row = torch.zeros(256)
+    row[0], row[1], row[2], row[3] = 127.0, 2.5, 3.5, -2.5     # group 0: s16 = 1
+    row[64], row[65] = 7.0, 0.5                                 # group 1: s16 = 7/127 rounded
+    codes, s = oracle.quantize_rows(row[None].to(torch.bfloat16), "int8_g64")
+    assert float(s[0, 0]) == 1.0 and codes[0, :4].tolist() == [127, 2, 4, -2]
+    assert float(s[0, 2]) == 0.0 and not codes[0, 128:].any()
+    s1 = np.float16(np.float32(7.0) / np.float32(127.0))
+    assert s[0, 1] == s1 and codes[0, 64] == np.rint(np.float32(7.0) / np.float32(s1))
+    row4 = torch.zeros(256)
+    row4[0], row4[1], row4[2], row4[3] = 7.0, -3.5, 2.5, 0.5    # group 0: s16 = 1
+    c4, s4 = oracle.quantize_rows(row4[None].to(torch.bfloat16), "int4_g32")
+    assert float(s4[0, 0]) == 1.0
+    # offset binary, even channel low: (7 + 8, -4 + 8) -> 0x4f; (2 + 8, 0 + 8) -> 0x8a
+    assert c4[0, 0] == 0x4F and c4[0, 1] == 0x8A
+    assert (c4[0, 2:] == 0x88).all()                            # zero codes read 8
