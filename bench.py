@@ -3,7 +3,7 @@
 One step = one qsa_decode call over one batch (every selected K/V row
 gathered, QK, softmax, PV, split merge). Prints one JSON line.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--fmt bf16|fp8_e4m3|int8|int4]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--fmt bf16|fp8_e4m3|int8|int4|int8_g64|int4_g32]
                   [--impl native|reference]
 
 --impl reference times the FP64 CPU oracle on the host cores on a bounded
@@ -29,8 +29,10 @@ from sparse_attention_paged_qsa_gb300 import inputs as I  # noqa: E402
 
 METRIC = "selected-KV HBM GB/s (% of GB300 peak) & qsa_decode calls/s at bs=128, L=2055"
 BS, L, HQ, HKV, SLOTS = 128, I.MAX_CAPACITY, 24, 2, 1048576
-ROW_BYTES = {"bf16": 512, "fp8_e4m3": 256, "int8": 256, "int4": 128}
-SCALE_BYTES = {"bf16": 0, "fp8_e4m3": 0, "int8": 4, "int4": 4}
+ROW_BYTES = {"bf16": 512, "fp8_e4m3": 256, "int8": 256, "int4": 128, "int8_g64": 256,
+             "int4_g32": 128}
+# per-row scale bytes: fp32 per (slot, KV head), or binary16 per channel group
+SCALE_BYTES = {"bf16": 0, "fp8_e4m3": 0, "int8": 4, "int4": 4, "int8_g64": 8, "int4_g32": 16}
 
 
 def algorithmic_bytes(fmt: str, bs: int = BS, length: int = L, hq: int = HQ) -> int:

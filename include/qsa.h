@@ -57,8 +57,13 @@ enum {
     QSA_KV_BF16 = 0,     /* [slots, Hkv, 256] bf16 */
     QSA_KV_FP8_E4M3 = 1, /* [slots, Hkv, 256] uint8 e4m3fn codes, one fp32 scale per pool */
     QSA_KV_INT8 = 2,     /* [slots, Hkv, 256] int8, fp32 scale per (slot, KV head) */
-    QSA_KV_INT4 = 3      /* [slots, Hkv, 128] uint8: two's-complement nibbles, channel 2i
+    QSA_KV_INT4 = 3,     /* [slots, Hkv, 128] uint8: two's-complement nibbles, channel 2i
                             in the low nibble, fp32 scale per (slot, KV head) */
+    QSA_KV_INT8_G64 = 4, /* [slots, Hkv, 256] int8, binary16 scale per (slot, KV head,
+                            64-channel group): [slots, Hkv, 4]; group 0 = the rotary dims */
+    QSA_KV_INT4_G32 = 5  /* [slots, Hkv, 128] uint8: offset-binary nibbles (code + 8,
+                            code in [-7, 7]), channel 2i in the low nibble, binary16 scale
+                            per (slot, KV head, 32-channel group): [slots, Hkv, 8] */
 };
 
 /* Return codes. Nothing is enqueued when a call returns an error. */
@@ -96,8 +101,10 @@ typedef struct {
 typedef struct {
     int32_t format;       /* QSA_KV_* */
     int32_t capacity;     /* max selected slots per sequence, 1..2055; bounds the split plan */
-    const float* k_scale; /* device; fp8: [1]; int8/int4: [slots * Hkv]; bf16: NULL */
-    const float* v_scale; /* same layout as k_scale */
+    const void* k_scale;  /* device; fp8: float [1]; int8/int4: float [slots * Hkv];
+                             int8_g64 / int4_g32: binary16 [slots * Hkv * 4 / 8], 8- / 16-byte
+                             aligned; bf16: NULL */
+    const void* v_scale;  /* same layout as k_scale */
     float softmax_scale;  /* finite; 1/16 = 1/sqrt(256) for the pages' model */
     int32_t max_ctas;     /* 0: library chooses the grid; > 0: cap on CTAs (e.g. 1 forces
                              one CTA to do all the work, which tests the no-split path) */
@@ -109,8 +116,9 @@ typedef struct {
  *  q           bf16 [bs, Hq, 256]; stride[2] == 1; stride[0], stride[1] multiples of 8;
  *              base 16-byte aligned.
  *  k_pool,     [num_slots, Hkv, row] contiguous; row = 256 elements (bf16, fp8 as
- *  v_pool      uint8, int8) or 128 bytes (int4 as uint8); identical shapes; base 16-byte
- *              aligned. Row (slot, g) is read whole, once per selecting (sequence, g).
+ *  v_pool      uint8, int8 and int8_g64 as int8) or 128 bytes (int4 / int4_g32 as uint8);
+ *              identical shapes; base 16-byte aligned. Row (slot, g) is read whole, once
+ *              per selecting (sequence, g), with its scales.
  *  kv_quant_meta  format, scales, softmax scale, capacity, optional CTA cap.
  *  sel_indices int32 [n_sel], contiguous: the packed selected slot ids.
  *  cu_seqlens  int32 [bs + 1], device, read on the device only.

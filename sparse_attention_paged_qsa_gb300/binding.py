@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_PKG, "libqsa.so")
 
 # include/qsa.h enums
 DTYPE_BF16, DTYPE_UINT8, DTYPE_INT8, DTYPE_INT32, DTYPE_FLOAT32 = 1, 2, 3, 4, 5
-KV_FORMATS = {"bf16": 0, "fp8_e4m3": 1, "int8": 2, "int4": 3}
+KV_FORMATS = {"bf16": 0, "fp8_e4m3": 1, "int8": 2, "int4": 3, "int8_g64": 4, "int4_g32": 5}
 OK, ERR_INVALID_ARGUMENT, ERR_UNSUPPORTED, ERR_SCRATCH_TOO_SMALL, ERR_MISALIGNED, ERR_CUDA = (
     0, -1, -2, -3, -4, -5)
 DEVERR_SLOT_RANGE, DEVERR_CU_SEQLENS, DEVERR_TIMEOUT = 1, 2, 4

@@ -35,6 +35,10 @@
 //    (int8/int4) for PV, with magic-number integer conversions and the
 //    hardware e4m3 conversion. Per-slot scales scale the scores (K) and the
 //    probabilities (V) in FP32; per-pool fp8 scales fold into constants.
+//    Grouped pools (binary16 scale per 64 / 32 channels): QK accumulates each
+//    channel group's k-steps apart and adds them with the token's group scale;
+//    each consumer warp's 32 PV dims lie in one group, so the warp rebuilds its
+//    own P^T with that group's per-token V scales from an FP32 copy of P.
 //  * Every wait is bounded; bad slot ids / cu_seqlens set a sticky error
 //    word and are clamped, never trapped.
 
@@ -80,31 +84,48 @@ static_assert(TPW == 8 && MT >= 1 && TPP <= 32, "tile shape");
 static_assert(PART_BYTES >= (GROUP * D + 2 * GROUP) * 4, "partial slot size");
 
 // ROWB: pool row bytes; DEQ: rows are converted in shared memory; SCALES:
-// per-(slot, KV head) fp32 scales; QK_F16: QK runs on f16 operands (exact
+// per-slot scales (fp32 per (slot, KV head), or binary16 per (slot, KV head,
+// channel group) when GROUPS > 0); QK_F16: QK runs on f16 operands (exact
 // integer / e4m3 codes, Q rescaled per head by a power of two); PV_F16: PV runs
-// on f16 operands (only when no per-slot scale enters P).
+// on f16 operands (only when no per-slot scale enters P); NIB4: 4-bit codes,
+// NIB_OFFSET: stored as code + 8 (else two's complement).
 template <int FMT> struct Traits;
 template <> struct Traits<QSA_KV_BF16> {
-    static constexpr int ROWB = 512, STAGES = 3;
+    static constexpr int ROWB = 512, STAGES = 3, GROUPS = 0;
     static constexpr bool DEQ = false, SCALES = false, QK_F16 = false, PV_F16 = false;
+    static constexpr bool NIB4 = false, NIB_OFFSET = false;
 };
 template <> struct Traits<QSA_KV_FP8_E4M3> {
-    static constexpr int ROWB = 256, STAGES = 4;
+    static constexpr int ROWB = 256, STAGES = 4, GROUPS = 0;
     static constexpr bool DEQ = true, SCALES = false, QK_F16 = true, PV_F16 = true;
+    static constexpr bool NIB4 = false, NIB_OFFSET = false;
 };
 template <> struct Traits<QSA_KV_INT8> {
-    static constexpr int ROWB = 256, STAGES = 4;
+    static constexpr int ROWB = 256, STAGES = 4, GROUPS = 0;
     static constexpr bool DEQ = true, SCALES = true, QK_F16 = true, PV_F16 = false;
+    static constexpr bool NIB4 = false, NIB_OFFSET = false;
 };
 template <> struct Traits<QSA_KV_INT4> {
-    static constexpr int ROWB = 128, STAGES = 6;
+    static constexpr int ROWB = 128, STAGES = 6, GROUPS = 0;
     static constexpr bool DEQ = true, SCALES = true, QK_F16 = true, PV_F16 = false;
+    static constexpr bool NIB4 = true, NIB_OFFSET = false;
+};
+template <> struct Traits<QSA_KV_INT8_G64> {
+    static constexpr int ROWB = 256, STAGES = 3, GROUPS = 4;
+    static constexpr bool DEQ = true, SCALES = true, QK_F16 = true, PV_F16 = false;
+    static constexpr bool NIB4 = false, NIB_OFFSET = false;
+};
+template <> struct Traits<QSA_KV_INT4_G32> {
+    static constexpr int ROWB = 128, STAGES = 6, GROUPS = 8;
+    static constexpr bool DEQ = true, SCALES = true, QK_F16 = true, PV_F16 = false;
+    static constexpr bool NIB4 = true, NIB_OFFSET = true;
 };
 
 template <int FMT> struct Layout {
     using Tr = Traits<FMT>;
     static constexpr int STAGE_KV = T * Tr::ROWB;
-    static constexpr int STAGE_SC = Tr::SCALES ? 2 * T * 4 : 0;
+    static constexpr int SC_TOK = Tr::GROUPS ? Tr::GROUPS * 2 : 4; // scale bytes per token
+    static constexpr int STAGE_SC = Tr::SCALES ? 2 * T * SC_TOK : 0;
     static constexpr int STAGE_BYTES = 2 * STAGE_KV + STAGE_SC;
     static constexpr int PF = Tr::STAGES;       // slot-id prefetch distance (stages)
     static constexpr int R = PF + 1;            // slot-id ring entries
@@ -113,7 +134,10 @@ template <int FMT> struct Layout {
     static constexpr int kbf_bytes = Tr::DEQ ? 2 * T * BF_ROW : 0;
     static constexpr int off_q = off_kbf + kbf_bytes;
     static constexpr int off_p = off_q + 2 * 16 * Q_RS;
-    static constexpr int off_red = off_p + 2 * 24 * PRS;
+    // P^T hi/lo (two buffers); grouped pools: FP32 P [2][12][T] then one P^T per warp
+    static constexpr int off_pw = off_p + 2 * GROUP * T * 4;
+    static constexpr int p_bytes = Tr::GROUPS ? 2 * GROUP * T * 4 + NW * 24 * PRS : 2 * 24 * PRS;
+    static constexpr int off_red = off_p + p_bytes;
     static constexpr int off_mref = off_red + 2 * NW * 16 * 4;
     static constexpr int off_lred = off_mref + 2 * 16 * 4;
     static constexpr int off_ring = off_lred + NW * 16 * 4;
@@ -126,6 +150,8 @@ template <int FMT> struct Layout {
     static constexpr int TOTAL = off_bar + n_bars * 8;
     static_assert(TOTAL <= 227 * 1024, "shared memory budget");
     static_assert(STAGE_BYTES % 128 == 0 && off_kbf % 128 == 0 && off_q % 16 == 0, "alignment");
+    static_assert(off_p % 16 == 0 && off_pw % 16 == 0 && off_red % 16 == 0 && off_bar % 8 == 0,
+                  "alignment");
 };
 
 struct Params {
@@ -134,8 +160,8 @@ struct Params {
     const uint8_t* kpool;
     const uint8_t* vpool;
     long long num_slots;
-    const float* k_scale;
-    const float* v_scale;
+    const void* k_scale; // fp32 (fp8: [1]; int8/int4: [slots * Hkv]) or binary16 [slots * Hkv * GROUPS]
+    const void* v_scale;
     const int* sel;
     long long n_sel;
     const int* cu;
@@ -230,6 +256,9 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
 
 __device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
@@ -382,12 +411,13 @@ __device__ __forceinline__ void i8x4_to_bf16(uint32_t w, uint32_t& lo, uint32_t&
 }
 
 // 8 int4 codes (channel 2i in the low nibble) -> 4 packed pairs, f16 or bf16:
-// nibble u = code ^ 8 = code + 8 under the magic 1024 (f16) or 128 (bf16).
-template <bool F16>
+// nibble u = code + 8 (offset-binary storage as it is; two's complement
+// code ^ 8) under the magic 1024 (f16) or 128 (bf16).
+template <bool F16, bool OFFSET>
 __device__ __forceinline__ void i4x8_to(uint32_t w, uint32_t* o) {
     constexpr uint32_t MAGIC = F16 ? 0x64006400u : 0x43004300u;
     constexpr uint32_t BIAS = F16 ? 0x64086408u : 0x43084308u; // 1032 / 136
-    const uint32_t x = w ^ 0x88888888u;
+    const uint32_t x = OFFSET ? w : w ^ 0x88888888u;
     const uint32_t hs = x >> 4;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -423,14 +453,14 @@ __device__ __forceinline__ void convert16(const uint4 raw, uint4& o0, uint4& o1)
     o1 = make_uint4(r[4], r[5], r[6], r[7]);
 }
 
-// 16 raw bytes of an int4 row (32 codes) -> four 16-byte chunks.
-template <bool F16>
+// 16 raw bytes of a 4-bit row (32 codes) -> four 16-byte chunks.
+template <bool F16, bool OFFSET>
 __device__ __forceinline__ void convert32_int4(const uint4 raw, uint4* o) {
     const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
         uint32_t r[4];
-        i4x8_to<F16>(w[k], r);
+        i4x8_to<F16, OFFSET>(w[k], r);
         o[k] = make_uint4(r[0], r[1], r[2], r[3]);
     }
 }
@@ -689,10 +719,28 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
                 }
             }
             if constexpr (Tr::SCALES) {
-                float* sc = reinterpret_cast<float*>(Vs + Ly::STAGE_KV);
+                uint8_t* sc = Vs + Ly::STAGE_KV; // K scales [T][SC_TOK], then V scales
+                const uint32_t ks = smem_u32(sc + mytok * Ly::SC_TOK);
+                const uint32_t vs = ks + T * Ly::SC_TOK;
+                const uint8_t* kg = static_cast<const uint8_t*>(p.k_scale) + myrow * Ly::SC_TOK;
+                const uint8_t* vg = static_cast<const uint8_t*>(p.v_scale) + myrow * Ly::SC_TOK;
                 if (valid) {
-                    cp_async4(smem_u32(sc + mytok), p.k_scale + myrow);
-                    cp_async4(smem_u32(sc + T + mytok), p.v_scale + myrow);
+                    if constexpr (Ly::SC_TOK == 4) {
+                        cp_async4(ks, kg);
+                        cp_async4(vs, vg);
+                    } else if constexpr (Ly::SC_TOK == 8) {
+                        cp_async8(ks, kg);
+                        cp_async8(vs, vg);
+                    } else {
+                        cp_async16(ks, kg);
+                        cp_async16(vs, vg);
+                    }
+                } else if (Tr::GROUPS && lane < TPP) {
+                    // past the live length: zero V scales keep 0 * scale finite in P
+                    if constexpr (Ly::SC_TOK == 8)
+                        *reinterpret_cast<uint2*>(sc + T * Ly::SC_TOK + mytok * 8) = make_uint2(0, 0);
+                    else if constexpr (Ly::SC_TOK == 16)
+                        *reinterpret_cast<uint4*>(sc + T * Ly::SC_TOK + mytok * 16) = make_uint4(0, 0, 0, 0);
                 }
             }
             cp_async_arrive_noinc(full_bar(s));
@@ -707,8 +755,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
     const int r = lane >> 2, c = lane & 3;
     float kscale_g = 1.0f, out_scale = 1.0f;
     if constexpr (FMT == QSA_KV_FP8_E4M3) {
-        kscale_g = __ldg(p.k_scale);
-        out_scale = __ldg(p.v_scale);
+        kscale_g = __ldg(static_cast<const float*>(p.k_scale));
+        out_scale = __ldg(static_cast<const float*>(p.v_scale));
     }
     const float cs_base = p.scale_log2 * kscale_g;
     float* const red = reinterpret_cast<float*>(smem + Ly::off_red);    // [2][NW][16]
@@ -799,20 +847,25 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
         const uint8_t* Kb = Ks;   // bf16 rows [T][BF_ROW] (swizzled) used by the MMAs
         const uint8_t* Vb = Vs;
         float skr[2] = {1.f, 1.f}, svr[2] = {1.f, 1.f};
+        // grouped pools: K scales (binary16 pairs) of tokens tk0, tk0 + 1, and V
+        // scales of tokens 2 lane, 2 lane + 1 in this warp's channel group
+        constexpr int GP = Tr::GROUPS ? Tr::GROUPS / 2 : 1;
+        uint32_t ksw[2][GP];
+        float svw[2] = {0.f, 0.f};
 
         if constexpr (Tr::DEQ) {
             uint8_t* const kbf = smem + Ly::off_kbf;
             uint8_t* const vbf = kbf + T * BF_ROW;
             const int tt = lane & 7, ch = lane >> 3;
             const int t = tok_base + tt;
-            if constexpr (FMT == QSA_KV_INT4) {
+            if constexpr (Tr::NIB4) {
                 // K: this warp's 8 tokens; 8 raw chunks per row, 32 values each
 #pragma unroll
                 for (int it = 0; it < 2; ++it) {
                     const int rc = ch + 4 * it;
                     const uint4 raw = *reinterpret_cast<const uint4*>(Ks + swz<Tr::ROWB>(t, rc));
                     uint4 ov[4];
-                    convert32_int4<Tr::QK_F16>(raw, ov);
+                    convert32_int4<Tr::QK_F16, Tr::NIB_OFFSET>(raw, ov);
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
                         *reinterpret_cast<uint4*>(kbf + swz<BF_ROW>(t, 4 * rc + k)) = ov[k];
@@ -823,7 +876,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
                     const int tv = lane + 32 * it;
                     const uint4 raw = *reinterpret_cast<const uint4*>(Vs + swz<Tr::ROWB>(tv, warp));
                     uint4 ov[4];
-                    convert32_int4<Tr::PV_F16>(raw, ov);
+                    convert32_int4<Tr::PV_F16, Tr::NIB_OFFSET>(raw, ov);
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
                         *reinterpret_cast<uint4*>(vbf + swz<BF_ROW>(tv, 4 * warp + k)) = ov[k];
@@ -835,7 +888,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
                     const int rc = ch + 4 * it;
                     const uint4 raw = *reinterpret_cast<const uint4*>(Ks + swz<Tr::ROWB>(t, rc));
                     uint4 o0, o1;
-                    convert16<FMT, Tr::QK_F16>(raw, o0, o1);
+                    convert16<FMT == QSA_KV_FP8_E4M3 ? FMT : QSA_KV_INT8, Tr::QK_F16>(raw, o0, o1);
                     *reinterpret_cast<uint4*>(kbf + swz<BF_ROW>(t, 2 * rc)) = o0;
                     *reinterpret_cast<uint4*>(kbf + swz<BF_ROW>(t, 2 * rc + 1)) = o1;
                 }
@@ -846,17 +899,30 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
                     const int tv = task >> 1, rc = 2 * warp + (task & 1);
                     const uint4 raw = *reinterpret_cast<const uint4*>(Vs + swz<Tr::ROWB>(tv, rc));
                     uint4 o0, o1;
-                    convert16<FMT, Tr::PV_F16>(raw, o0, o1);
+                    convert16<FMT == QSA_KV_FP8_E4M3 ? FMT : QSA_KV_INT8, Tr::PV_F16>(raw, o0, o1);
                     *reinterpret_cast<uint4*>(vbf + swz<BF_ROW>(tv, 2 * rc)) = o0;
                     *reinterpret_cast<uint4*>(vbf + swz<BF_ROW>(tv, 2 * rc + 1)) = o1;
                 }
             }
-            if constexpr (Tr::SCALES) {
+            if constexpr (Tr::SCALES && !Tr::GROUPS) {
                 const float* sc = reinterpret_cast<const float*>(Vs + Ly::STAGE_KV);
                 skr[0] = sc[tk0];
                 skr[1] = sc[tk0 + 1];
                 svr[0] = sc[T + tk0];
                 svr[1] = sc[T + tk0 + 1];
+            }
+            if constexpr (Tr::GROUPS) { // read before the stage is released below
+                constexpr int G = Tr::GROUPS;
+                const uint32_t* sk = reinterpret_cast<const uint32_t*>(Vs + Ly::STAGE_KV);
+#pragma unroll
+                for (int k = 0; k < GP; ++k) {
+                    ksw[0][k] = sk[tk0 * GP + k];
+                    ksw[1][k] = sk[(tk0 + 1) * GP + k];
+                }
+                const __half* sv = reinterpret_cast<const __half*>(Vs + Ly::STAGE_KV + T * Ly::SC_TOK);
+                const int gv = warp * G / NW;
+                svw[0] = __half2float(sv[(2 * lane) * G + gv]);
+                svw[1] = __half2float(sv[(2 * lane + 1) * G + gv]);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(empty_bar(s));
@@ -866,7 +932,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
 
         // ---------------------------------------------------------------- QK
         float sacc[4][4] = {};
-        {
+        if constexpr (Tr::GROUPS == 0) {
             const uint32_t krow = smem_u32(Kb) + (tok_base + (lane & 7)) * BF_ROW;
 #pragma unroll
             for (int ks = 0; ks < 16; ks += 2) {
@@ -876,9 +942,37 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
                 mma16816<Tr::QK_F16>(acc, qa[ks], b0, b1);
                 mma16816<Tr::QK_F16>(sacc[2 + ((ks >> 1) & 1)], qa[ks + 1], b2, b3);
             }
-        }
 #pragma unroll
-        for (int e = 0; e < 4; ++e) sacc[0][e] += sacc[1][e] + sacc[2][e] + sacc[3][e];
+            for (int e = 0; e < 4; ++e) sacc[0][e] += sacc[1][e] + sacc[2][e] + sacc[3][e];
+        } else {
+            // score = sum over channel groups of (group dot product) * K scale of
+            // (token, group); each group is KPG k-steps of 16 channels
+            constexpr int G = Tr::GROUPS, KPG = 16 / G;
+            const uint32_t krow = smem_u32(Kb) + (tok_base + (lane & 7)) * BF_ROW;
+#pragma unroll
+            for (int gi = 0; gi < G; ++gi) {
+                float acc[KPG][4] = {};
+#pragma unroll
+                for (int kk = 0; kk < KPG; kk += 2) {
+                    const int ks = gi * KPG + kk;
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(b0, b1, b2, b3, krow + ((ks * 32) ^ kx));
+                    mma16816<Tr::QK_F16>(acc[kk], qa[ks], b0, b1);
+                    mma16816<Tr::QK_F16>(acc[kk + 1], qa[ks + 1], b2, b3);
+                }
+#pragma unroll
+                for (int kk = 1; kk < KPG; ++kk)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) acc[0][e] += acc[kk][e];
+                const uint32_t w0 = ksw[0][gi >> 1], w1 = ksw[1][gi >> 1];
+                const float s0 = __half2float(__ushort_as_half(static_cast<unsigned short>(gi & 1 ? w0 >> 16 : w0)));
+                const float s1 = __half2float(__ushort_as_half(static_cast<unsigned short>(gi & 1 ? w1 >> 16 : w1)));
+                sacc[0][0] += acc[0][0] * s0;
+                sacc[0][1] += acc[0][1] * s1;
+                sacc[0][2] += acc[0][2] * s0;
+                sacc[0][3] += acc[0][3] * s1;
+            }
+        }
         const bool v0 = tk0 < n, v1 = tk0 + 1 < n;
         const bool row8 = r < 4; // head r + 8 is a real head (8..11)
         const float ninf = -INFINITY;
@@ -910,12 +1004,18 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
             pr[2] = x[2] == ninf ? 0.f : ex2(x[2] - rb);
             pr[3] = x[3] == ninf ? 0.f : ex2(x[3] - rb);
         };
+        float* const Pf = reinterpret_cast<float*>(smem + Ly::off_p) + buf * GROUP * T;
         auto write_p = [&]() {
             float pv[4] = {pr[0] * svr[0], pr[1] * svr[1], pr[2] * svr[0], pr[3] * svr[1]};
             pv[0] = v0 ? pv[0] : 0.f;
             pv[1] = v1 ? pv[1] : 0.f;
             pv[2] = v0 ? pv[2] : 0.f;
             pv[3] = v1 ? pv[3] : 0.f;
+            if constexpr (Tr::GROUPS) { // FP32 P; each warp scales and splits its own copy
+                *reinterpret_cast<float2*>(Pf + r * T + tk0) = make_float2(pv[0], pv[1]);
+                if (row8) *reinterpret_cast<float2*>(Pf + (8 + r) * T + tk0) = make_float2(pv[2], pv[3]);
+                return;
+            }
             uint32_t hi_a, lo_a;
             split_pair<Tr::PV_F16>(pv[0], pv[1], hi_a, lo_a);
             *reinterpret_cast<uint32_t*>(Pb + r * PRS + tk0 * 2) = hi_a;
@@ -976,8 +1076,28 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
         l1 += pr[2] + pr[3];
 
         // ---------------------------------------------------------------- PV
+        const uint8_t* Pt = Pb;
+        if constexpr (Tr::GROUPS) {
+            // this warp's dims lie in one channel group: P^T columns scaled per token
+            // by that group's V scale (read into svw above), split into bf16 hi + lo
+            uint8_t* const Pw = smem + Ly::off_pw + warp * 24 * PRS;
+            const int t = 2 * lane;
+            const float sv0 = svw[0], sv1 = svw[1];
+            __syncwarp(); // the previous stage's reads of Pw are done
+#pragma unroll
+            for (int h = 0; h < GROUP; ++h) {
+                const float2 pp = *reinterpret_cast<const float2*>(Pf + h * T + t);
+                uint32_t hi, lo;
+                split_pair<false>(pp.x * sv0, pp.y * sv1, hi, lo);
+                const int rh = h < 8 ? h : 8 + h, rl = h < 8 ? 8 + h : 12 + h;
+                *reinterpret_cast<uint32_t*>(Pw + rh * PRS + t * 2) = hi;
+                *reinterpret_cast<uint32_t*>(Pw + rl * PRS + t * 2) = lo;
+            }
+            __syncwarp();
+            Pt = Pw;
+        }
         {
-            const uint32_t pbase = smem_u32(Pb);
+            const uint32_t pbase = smem_u32(Pt);
             const uint32_t vrow = smem_u32(Vb) + ((lane >> 4) * 8 + (lane & 7)) * BF_ROW;
 #pragma unroll
             for (int kk = 0; kk < KK; ++kk) {
@@ -1197,7 +1317,7 @@ int fail(int code, const char* fmt, ...) {
 
 struct DeviceState {
     int sms = 0;
-    bool smem_set[4] = {false, false, false, false};
+    bool smem_set[QSA_KV_INT4_G32 + 1] = {};
 };
 
 std::mutex g_mu;
@@ -1364,7 +1484,7 @@ int qsa_decode(const qsa_tensor* q, const qsa_tensor* k_pool, const qsa_tensor* 
     if (!q || !k_pool || !v_pool || !meta || !sel || !cu || !out)
         return fail(QSA_ERR_INVALID_ARGUMENT, "a descriptor pointer is NULL");
     const int fmt = meta->format;
-    if (fmt < QSA_KV_BF16 || fmt > QSA_KV_INT4)
+    if (fmt < QSA_KV_BF16 || fmt > QSA_KV_INT4_G32)
         return fail(QSA_ERR_UNSUPPORTED, "unknown K/V pool format %d", fmt);
     if (q->ndim != 3) return fail(QSA_ERR_INVALID_ARGUMENT, "q must be [bs, Hq, 256]");
     const int64_t bs64 = q->shape[0], hq64 = q->shape[1];
@@ -1384,10 +1504,10 @@ int qsa_decode(const qsa_tensor* q, const qsa_tensor* k_pool, const qsa_tensor* 
     if ((rc = check_row_tensor(q, "q", bs, hq)) != QSA_OK) return rc;
     if ((rc = check_row_tensor(out, "out", bs, hq)) != QSA_OK) return rc;
 
-    const int want_dtype = fmt == QSA_KV_BF16 ? QSA_DTYPE_BF16
-                           : fmt == QSA_KV_INT8 ? QSA_DTYPE_INT8
-                                                : QSA_DTYPE_UINT8;
-    const int64_t row_elems = fmt == QSA_KV_INT4 ? D / 2 : D;
+    const int want_dtype = fmt == QSA_KV_BF16                              ? QSA_DTYPE_BF16
+                           : (fmt == QSA_KV_INT8 || fmt == QSA_KV_INT8_G64) ? QSA_DTYPE_INT8
+                                                                            : QSA_DTYPE_UINT8;
+    const int64_t row_elems = (fmt == QSA_KV_INT4 || fmt == QSA_KV_INT4_G32) ? D / 2 : D;
     for (const qsa_tensor* pool : {k_pool, v_pool}) {
         const char* nm = pool == k_pool ? "k_pool" : "v_pool";
         if (pool->dtype != want_dtype)
@@ -1420,9 +1540,11 @@ int qsa_decode(const qsa_tensor* q, const qsa_tensor* k_pool, const qsa_tensor* 
     if (fmt != QSA_KV_BF16) {
         if (meta->k_scale == nullptr || meta->v_scale == nullptr)
             return fail(QSA_ERR_INVALID_ARGUMENT, "quantised pools need k_scale and v_scale");
-        if ((reinterpret_cast<uintptr_t>(meta->k_scale) & 3u) ||
-            (reinterpret_cast<uintptr_t>(meta->v_scale) & 3u))
-            return fail(QSA_ERR_MISALIGNED, "scales must be 4-byte aligned");
+        // grouped pools read a token's binary16 scales with one 8- or 16-byte copy
+        const uintptr_t al = fmt == QSA_KV_INT8_G64 ? 8 : fmt == QSA_KV_INT4_G32 ? 16 : 4;
+        if ((reinterpret_cast<uintptr_t>(meta->k_scale) & (al - 1)) ||
+            (reinterpret_cast<uintptr_t>(meta->v_scale) & (al - 1)))
+            return fail(QSA_ERR_MISALIGNED, "scales must be %d-byte aligned for this format", (int)al);
     }
     if (scratch == nullptr) return fail(QSA_ERR_INVALID_ARGUMENT, "scratch is NULL");
     if (reinterpret_cast<uintptr_t>(scratch) & 255u)
@@ -1466,7 +1588,9 @@ int qsa_decode(const qsa_tensor* q, const qsa_tensor* k_pool, const qsa_tensor* 
     case QSA_KV_BF16: rc = launch<QSA_KV_BF16>(prm, (int)grid, dev, st); break;
     case QSA_KV_FP8_E4M3: rc = launch<QSA_KV_FP8_E4M3>(prm, (int)grid, dev, st); break;
     case QSA_KV_INT8: rc = launch<QSA_KV_INT8>(prm, (int)grid, dev, st); break;
-    default: rc = launch<QSA_KV_INT4>(prm, (int)grid, dev, st); break;
+    case QSA_KV_INT4: rc = launch<QSA_KV_INT4>(prm, (int)grid, dev, st); break;
+    case QSA_KV_INT8_G64: rc = launch<QSA_KV_INT8_G64>(prm, (int)grid, dev, st); break;
+    default: rc = launch<QSA_KV_INT4_G32>(prm, (int)grid, dev, st); break;
     }
     if (rc == QSA_OK) g_last_error.clear();
     return rc;

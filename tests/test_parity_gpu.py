@@ -172,17 +172,20 @@ def test_headline_saturated_sampled(cuda_device, fmt):
     assert torch.isfinite(o).all() and (o.abs().sum(-1) > 0).all()
 
 
-@pytest.mark.parametrize("fmt", ["fp8_e4m3", "int8", "int4"])
+@pytest.mark.parametrize("fmt", ["fp8_e4m3", "int8", "int4", "int8_g64", "int4_g32"])
 def test_every_code_dequantises_exactly(cuda_device, fmt):
     """A single selected slot whose V row holds every code of the format, with a
     unit scale: the output row is exactly the decoded codes (NaN codes give NaN)."""
     w = I.tiny_tp2(seed=40, length=1, fmt=fmt)
     slot = int(w.sel[0])
-    if fmt == "int4":
+    if fmt in ("int4", "int4_g32"):
         codes = torch.arange(256, dtype=torch.int32) % 16
         row = (codes[0::2] | (codes[1::2] << 4)).to(torch.uint8)
-        vals = torch.where(codes >= 8, codes - 16, codes).float()
-    elif fmt == "int8":
+        if fmt == "int4":
+            vals = torch.where(codes >= 8, codes - 16, codes).float()
+        else:
+            vals = (codes - 8).float()        # offset binary
+    elif fmt in ("int8", "int8_g64"):
         row = torch.arange(-128, 128, dtype=torch.int32).to(torch.int8)
         vals = row.float()
     else:
@@ -199,3 +202,20 @@ def test_every_code_dequantises_exactly(cuda_device, fmt):
         nan = torch.isnan(ref)
         assert torch.equal(torch.isnan(got[h]), nan)
         assert torch.equal(got[h][~nan], ref[~nan])
+
+
+@pytest.mark.parametrize("fmt", ["int8_g64", "int4_g32"])
+def test_group_scales_reach_their_channels(cuda_device, fmt):
+    """One selected slot, V codes all 1 (int4_g32: nibble 9), V scale of group k
+    = 2^k: output channel d reads exactly the scale of its group."""
+    w = I.tiny_tp2(seed=41, length=1, fmt=fmt)
+    slot = int(w.sel[0])
+    G = I.HEAD_DIM // I.GROUPED[fmt]
+    w.v_pool[slot, 0] = 0x99 if fmt == "int4_g32" else 1
+    w.v_scale[slot, 0] = torch.tensor([2.0 ** k for k in range(G)], dtype=torch.float16)
+    wd = w.to(cuda_device)
+    out, _ = run_cuda(wd)
+    torch.cuda.synchronize()
+    ref = torch.tensor([2.0 ** (d // I.GROUPED[fmt]) for d in range(256)])
+    for h in range(12):
+        assert torch.equal(out[0, h].float().cpu(), ref)
