@@ -150,7 +150,10 @@ int qsa_decode(const qsa_tensor* q, const qsa_tensor* k_pool, const qsa_tensor* 
  *  v_pool
  *  k_scale,    fp8: the pool's fp32 scale [1] (read; must be finite and > 0);
  *  v_scale     int8/int4: fp32 [num_slots * Hkv], entry of each written row set to
- *              absmax(row) / 127 (int8) or / 7 (int4); bf16: unused (may be NULL).
+ *              absmax(row) / 127 (int8) or / 7 (int4); int8_g64 / int4_g32: binary16
+ *              [num_slots * Hkv * 4 / 8] (8- / 16-byte aligned), the written row's
+ *              group entries set to binary16(min(absmax(group) / 127 or / 7, 65504));
+ *              bf16: unused (may be NULL).
  *  device_error  optional int32 device word: QSA_DEVERR_SLOT_RANGE is OR-ed in when a
  *              slot is outside [0, num_slots); that row is skipped. May be NULL.
  *  stream      cudaStream_t.
@@ -158,12 +161,14 @@ int qsa_decode(const qsa_tensor* q, const qsa_tensor* k_pool, const qsa_tensor* 
  * Codes, in binary32 with IEEE division and round-to-nearest-even: bf16 rows are
  * copied; fp8 = e4m3fn(x / s) saturating at +-448; int8 = clamp(rint(x / s), -127, 127);
  * int4 = clamp(rint(x / s), -8, 7), two's-complement nibbles, channel 2i in the low
- * nibble; an all-zero row gets scale 0 and zero codes. Inputs must be finite.
+ * nibble; int8_g64 / int4_g32 = clamp(rint(x / s16), -127, 127) / (-7, 7) with the
+ * group's binary16 scale s16, int4_g32 as offset-binary nibbles code + 8; an all-zero
+ * row (group) gets scale 0 and zero codes. Inputs must be finite.
  * Validates on the host, enqueues one kernel, allocates nothing.
  */
 int qsa_kv_write(int32_t format, const qsa_tensor* k_new, const qsa_tensor* v_new,
                  const qsa_tensor* slots, const qsa_tensor* k_pool, const qsa_tensor* v_pool,
-                 float* k_scale, float* v_scale, int32_t* device_error, void* stream);
+                 void* k_scale, void* v_scale, int32_t* device_error, void* stream);
 
 /* Scratch bytes a qsa_decode call with these sizes needs on the current
  * device (0 when the sizes are outside the contract). Split-KV partials take

@@ -10,6 +10,10 @@
 //   int8 : s = absmax(x) / 127 -> scale[row]; codes clamp(rint(x / s), -127, 127)
 //   int4 : s = absmax(x) / 7   -> scale[row]; codes clamp(rint(x / s), -8, 7),
 //          two per byte, channel 2i in the low nibble
+//   int8_g64 / int4_g32 (the int8 and int4 KV pool modules of the same PR):
+//          per 64 / 32-channel group s16 = binary16(min(absmax / q, 65504)),
+//          q = 127 / 7, -> scale[row][group]; codes clamp(rint(x / s16), -q, q);
+//          int4_g32 stores offset-binary nibbles code + 8
 // all in binary32 with IEEE division; an all-zero row gets s = 0 and zero codes.
 //
 // One warp per (token, head, K-or-V) row: a 16-byte load per lane covers the
@@ -45,8 +49,8 @@ struct Params {
     uint8_t* kpool;
     uint8_t* vpool;
     long long num_slots;
-    float* kscale;
-    float* vscale;
+    void* kscale; // fp32 (fp8: [1]; int8/int4: [slots * Hkv]) or binary16 [slots * Hkv * groups]
+    void* vscale;
     int* err;
 };
 
@@ -66,7 +70,8 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
 // |x / s| * 2^-24). The conversion is monotone, so where both give the same code
 // that is the code of q; pairs where they differ divide.
 //
-// int8 / int4 (s = fl(a / qmax), a = absmax, a bf16 value): q comes from
+// int8 / int4 (s = fl(a / qmax), a = absmax, a bf16 value; the grouped formats
+// round s to binary16 first, s16 = fl16(fl(a / qmax))): q comes from
 // Markstein's correction (P. Markstein, "Computation of elementary functions on
 // the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990):
 // q0 = fl(x * r), e = fma(-q0, s, x), q = fma(e, r, q0) with r = fl(1 / s). For
@@ -74,7 +79,9 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
 // x with 2^-11 a <= |x| <= a and every a (smaller |x| gives code 0 either way);
 // the steps commute with scaling by 2^E while all terms stay normal, which holds
 // for a >= 2^-60. s and r for a = m * 2^E are those of m (a 128-entry table of
-// the bf16 mantissas) with the exponent moved by E.
+// the bf16 mantissas) with the exponent moved by E. The same check holds for the
+// binary16 scales s16 of every mantissa, which scale the same way while
+// fl(a / qmax) is a normal binary16 value (2^-14 .. 65504).
 
 // x + 1.5 * 2^23 rounds once, to an integer (the spacing of binary32 in
 // [2^23, 2^24)), ties to even: its bit pattern is 0x4B400000 + rint(x) for
@@ -129,7 +136,7 @@ __device__ __forceinline__ void store_fp8(const Params& p, const uint4 raw, long
             same &= c[k] == d[k];
         }
         if (!same) {
-            const float s = __ldg(isv ? p.vscale : p.kscale);
+            const float s = __ldg(static_cast<const float*>(isv ? p.vscale : p.kscale));
 #pragma unroll
             for (int k = 0; k < 4; ++k)
                 if (c[k] != d[k]) c[k] = e4m3x2(x[2 * k] / s, x[2 * k + 1] / s);
@@ -153,8 +160,8 @@ __device__ __forceinline__ void codes_markstein(const float x[8], float s, float
 // The definition as it stands, for absmax below 2^-60 (subnormal or zero scales).
 template <int FMT>
 __device__ __forceinline__ void codes_divide(const float x[8], float s, uint32_t z[8]) {
-    constexpr float qmax = FMT == QSA_KV_INT8 ? 127.0f : 7.0f;
-    constexpr float qmin = FMT == QSA_KV_INT8 ? -127.0f : -8.0f;
+    constexpr float qmax = (FMT == QSA_KV_INT8 || FMT == QSA_KV_INT8_G64) ? 127.0f : 7.0f;
+    constexpr float qmin = FMT == QSA_KV_INT4 ? -8.0f : -qmax;
 #pragma unroll
     for (int k = 0; k < 8; ++k)
         z[k] = static_cast<uint32_t>(s > 0.0f ? static_cast<int>(fminf(fmaxf(rintf(x[k] / s), qmin), qmax)) : 0);
@@ -169,15 +176,15 @@ __device__ __forceinline__ void store_codes(const Params& p, long long row, bool
         reinterpret_cast<uint2*>(row_ptr(p, isv, row, D))[lane] = make_uint2(b0, b1);
     else
         reinterpret_cast<uint32_t*>(row_ptr(p, isv, row, D / 2))[lane] = low_nibbles(b0) | (low_nibbles(b1) << 16);
-    if (lane == 0) (isv ? p.vscale : p.kscale)[row] = s;
+    if (lane == 0) static_cast<float*>(isv ? p.vscale : p.kscale)[row] = s;
 }
 
 // One row's conversion and store; rows are resolved from the task index
 // t in [0, 2 n Hkv): K rows first, token-major, then V rows.
 template <int FMT> struct Converter {
     float k_lo, k_hi, v_lo, v_hi;     // fp8: 1 / pool scale times 1 -+ 2^-20 (or 1)
-    const uint32_t* s_tab;            // int8/int4: s and 1 / s for a = 1 + t / 128
-    const uint32_t* r_tab;
+    const uint32_t* s_tab;            // int8/int4: s and 1 / s for a = 1 + t / 128;
+    const uint32_t* r_tab;            // grouped: s16 and 1 / s16
 
     __device__ __forceinline__ void operator()(const Params& p, const uint4 raw, long long row, bool isv,
                                                int lane) const {
@@ -189,6 +196,42 @@ template <int FMT> struct Converter {
                 store_fp8<true>(p, raw, row, isv, lane, lo, hi);
             else
                 store_fp8<false>(p, raw, row, isv, lane, lo, hi);
+        } else if constexpr (FMT == QSA_KV_INT8_G64 || FMT == QSA_KV_INT4_G32) {
+            constexpr int GS = FMT == QSA_KV_INT8_G64 ? 64 : 32; // channels per scale
+            constexpr int LPG = GS / 8;                           // lanes per group
+            constexpr float qmax = FMT == QSA_KV_INT8_G64 ? 127.0f : 7.0f;
+            float x[8];
+            unpack(raw, x);
+            float a = 0.0f;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) a = fmaxf(a, fabsf(x[k]));
+#pragma unroll
+            for (int off = 1; off < LPG; off <<= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, off));
+            // a = (1 + t / 128) * 2^E: fl(a / qmax) from the table, exponent moved by E
+            const uint32_t ab = __float_as_uint(a);
+            const int t = (ab >> 16) & 0x7F;
+            const uint32_t e = (ab & 0x7F800000u) - (127u << 23);
+            const float s32 = __uint_as_float(s_tab[2 * t] + e);
+            uint32_t z[8];
+            float sc;
+            if (a >= FAST_MIN_ABSMAX && s32 >= 0x1p-14f && s32 <= 65504.0f) { // uniform per group
+                sc = __uint_as_float(s_tab[2 * t + 1] + e);
+                codes_markstein<FMT>(x, sc, __uint_as_float(r_tab[t] - e), z);
+            } else {
+                sc = __half2float(__float2half_rn(fminf(__fdiv_rn(a, qmax), 65504.0f)));
+                codes_divide<FMT>(x, sc, z);
+            }
+            const uint32_t b0 = low_bytes(z[0], z[1], z[2], z[3]);
+            const uint32_t b1 = low_bytes(z[4], z[5], z[6], z[7]);
+            if constexpr (FMT == QSA_KV_INT8_G64)
+                reinterpret_cast<uint2*>(row_ptr(p, isv, row, D))[lane] = make_uint2(b0, b1);
+            else // offset binary: code + 8 is code ^ 8 on a two's-complement nibble
+                reinterpret_cast<uint32_t*>(row_ptr(p, isv, row, D / 2))[lane] =
+                    (low_nibbles(b0) | (low_nibbles(b1) << 16)) ^ 0x88888888u;
+            // the group leaders' 2-byte stores fill one 8- / 16-byte block per row
+            if (lane % LPG == 0)
+                static_cast<__half*>(isv ? p.vscale : p.kscale)[row * (D / GS) + lane / LPG] =
+                    __float2half_rn(sc);
         } else {
             constexpr float qmax = FMT == QSA_KV_INT8 ? 127.0f : 7.0f;
             float x[8];
@@ -246,21 +289,31 @@ __device__ __forceinline__ void fp8_factors(float s, float* lo, float* hi) {
 
 template <int FMT>
 __global__ void __launch_bounds__(WARPS * 32, 5) kv_write_kernel(const Params p) {
-    constexpr bool INTQ = FMT == QSA_KV_INT8 || FMT == QSA_KV_INT4;
-    constexpr float qmax = FMT == QSA_KV_INT8 ? 127.0f : 7.0f;
-    __shared__ uint32_t s_tab[INTQ ? 128 : 1], r_tab[INTQ ? 128 : 1];
+    constexpr bool GROUPED = FMT == QSA_KV_INT8_G64 || FMT == QSA_KV_INT4_G32;
+    constexpr bool INTQ = FMT == QSA_KV_INT8 || FMT == QSA_KV_INT4 || GROUPED;
+    constexpr float qmax = (FMT == QSA_KV_INT8 || FMT == QSA_KV_INT8_G64) ? 127.0f : 7.0f;
+    // per bf16 mantissa t: s = fl((1 + t / 128) / qmax) and fl(1 / s); grouped:
+    // (s, s16 = fl16(s)) pairs and fl(1 / s16)
+    __shared__ uint32_t s_tab[INTQ ? (GROUPED ? 256 : 128) : 1], r_tab[INTQ ? 128 : 1];
     Converter<FMT> conv{0.0f, 0.0f, 0.0f, 0.0f, s_tab, r_tab};
     if constexpr (INTQ) {
         if (threadIdx.x < 128) {
             const float s0 = __fdiv_rn(1.0f + threadIdx.x * 0x1p-7f, qmax);
-            s_tab[threadIdx.x] = __float_as_uint(s0);
-            r_tab[threadIdx.x] = __float_as_uint(__frcp_rn(s0));
+            if constexpr (GROUPED) {
+                const float s16 = __half2float(__float2half_rn(s0));
+                s_tab[2 * threadIdx.x] = __float_as_uint(s0);
+                s_tab[2 * threadIdx.x + 1] = __float_as_uint(s16);
+                r_tab[threadIdx.x] = __float_as_uint(__frcp_rn(s16));
+            } else {
+                s_tab[threadIdx.x] = __float_as_uint(s0);
+                r_tab[threadIdx.x] = __float_as_uint(__frcp_rn(s0));
+            }
         }
         __syncthreads();
     }
     if constexpr (FMT == QSA_KV_FP8_E4M3) {
-        fp8_factors(__ldg(p.kscale), &conv.k_lo, &conv.k_hi);
-        fp8_factors(__ldg(p.vscale), &conv.v_lo, &conv.v_hi);
+        fp8_factors(__ldg(static_cast<const float*>(p.kscale)), &conv.k_lo, &conv.k_hi);
+        fp8_factors(__ldg(static_cast<const float*>(p.vscale)), &conv.v_lo, &conv.v_hi);
     }
     const int lane = threadIdx.x & 31;
     const int rows = p.n * p.Hkv; // n <= 2^28 and Hkv <= 2: every task index fits in 32 bits
@@ -312,12 +365,12 @@ template <int FMT> int launch(const Params& prm, cudaStream_t st) {
 
 extern "C" int qsa_kv_write(int32_t format, const qsa_tensor* k_new, const qsa_tensor* v_new,
                             const qsa_tensor* slots, const qsa_tensor* k_pool,
-                            const qsa_tensor* v_pool, float* k_scale, float* v_scale,
+                            const qsa_tensor* v_pool, void* k_scale, void* v_scale,
                             int32_t* device_error, void* stream) {
     using namespace qsakv;
     if (!k_new || !v_new || !slots || !k_pool || !v_pool)
         return fail(QSA_ERR_INVALID_ARGUMENT, "a descriptor pointer is NULL");
-    if (format < QSA_KV_BF16 || format > QSA_KV_INT4)
+    if (format < QSA_KV_BF16 || format > QSA_KV_INT4_G32)
         return fail(QSA_ERR_UNSUPPORTED, "unknown K/V pool format %d", format);
     if (k_new->ndim != 3 || v_new->ndim != 3)
         return fail(QSA_ERR_INVALID_ARGUMENT, "k_new and v_new must be [n, Hkv, 256]");
@@ -341,10 +394,10 @@ extern "C" int qsa_kv_write(int32_t format, const qsa_tensor* k_new, const qsa_t
     if (slots->dtype != QSA_DTYPE_INT32 || slots->ndim != 1 || slots->shape[0] != n ||
         (n > 1 && slots->stride[0] != 1) || (n > 0 && slots->data == nullptr))
         return fail(QSA_ERR_INVALID_ARGUMENT, "slots must be a contiguous int32 [n]");
-    const int want_dtype = format == QSA_KV_BF16   ? QSA_DTYPE_BF16
-                           : format == QSA_KV_INT8 ? QSA_DTYPE_INT8
-                                                   : QSA_DTYPE_UINT8;
-    const long long row_elems = format == QSA_KV_INT4 ? D / 2 : D;
+    const int want_dtype = format == QSA_KV_BF16                                    ? QSA_DTYPE_BF16
+                           : (format == QSA_KV_INT8 || format == QSA_KV_INT8_G64) ? QSA_DTYPE_INT8
+                                                                                  : QSA_DTYPE_UINT8;
+    const long long row_elems = (format == QSA_KV_INT4 || format == QSA_KV_INT4_G32) ? D / 2 : D;
     for (const qsa_tensor* pool : {k_pool, v_pool}) {
         const char* nm = pool == k_pool ? "k_pool" : "v_pool";
         if (pool->dtype != want_dtype)
@@ -363,8 +416,11 @@ extern "C" int qsa_kv_write(int32_t format, const qsa_tensor* k_new, const qsa_t
     if (format != QSA_KV_BF16) {
         if (k_scale == nullptr || v_scale == nullptr)
             return fail(QSA_ERR_INVALID_ARGUMENT, "quantised pools need k_scale and v_scale");
-        if ((reinterpret_cast<uintptr_t>(k_scale) & 3u) || (reinterpret_cast<uintptr_t>(v_scale) & 3u))
-            return fail(QSA_ERR_MISALIGNED, "scales must be 4-byte aligned");
+        // the alignment qsa_decode reads these scales with
+        const uintptr_t al = format == QSA_KV_INT8_G64 ? 8 : format == QSA_KV_INT4_G32 ? 16 : 4;
+        if ((reinterpret_cast<uintptr_t>(k_scale) & (al - 1)) ||
+            (reinterpret_cast<uintptr_t>(v_scale) & (al - 1)))
+            return fail(QSA_ERR_MISALIGNED, "scales must be %d-byte aligned for this format", (int)al);
     }
     if (n > (1LL << 28)) return fail(QSA_ERR_UNSUPPORTED, "more than 2^28 new tokens in one call");
     qsa_detail_set_error("");
@@ -391,6 +447,8 @@ extern "C" int qsa_kv_write(int32_t format, const qsa_tensor* k_new, const qsa_t
     case QSA_KV_BF16: return launch<QSA_KV_BF16>(prm, st);
     case QSA_KV_FP8_E4M3: return launch<QSA_KV_FP8_E4M3>(prm, st);
     case QSA_KV_INT8: return launch<QSA_KV_INT8>(prm, st);
-    default: return launch<QSA_KV_INT4>(prm, st);
+    case QSA_KV_INT4: return launch<QSA_KV_INT4>(prm, st);
+    case QSA_KV_INT8_G64: return launch<QSA_KV_INT8_G64>(prm, st);
+    default: return launch<QSA_KV_INT4_G32>(prm, st);
     }
 }

@@ -60,10 +60,10 @@ def test_version_and_strerror():
 
 
 def _host_call(q_shape=(2, 24, 256), pool_shape=(64, 2, 256), fmt="bf16", pool_dtype=None,
-               capacity=100, q_offset=0, scales=False, scratch=True, cu_len=None):
+               capacity=100, q_offset=0, scales=False, scratch=True, cu_len=None, scale_offset=0):
     """Describe host tensors (never dereferenced) and call qsa_decode."""
     pd = pool_dtype or {"bf16": torch.bfloat16, "fp8_e4m3": torch.uint8, "int8": torch.int8,
-                        "int4": torch.uint8}[fmt]
+                        "int4": torch.uint8, "int8_g64": torch.int8, "int4_g32": torch.uint8}[fmt]
     qbuf = torch.zeros(int(torch.tensor(q_shape).prod()) + 64, dtype=torch.bfloat16)
     q = qbuf[q_offset:q_offset + int(torch.tensor(q_shape).prod())].view(q_shape)
     k = torch.zeros(pool_shape, dtype=pd)
@@ -72,7 +72,8 @@ def _host_call(q_shape=(2, 24, 256), pool_shape=(64, 2, 256), fmt="bf16", pool_d
     sel = torch.zeros(10, dtype=torch.int32)
     cu = torch.zeros(cu_len or (bs + 1), dtype=torch.int32)
     out = torch.zeros(q_shape, dtype=torch.bfloat16)
-    sc = torch.ones(pool_shape[0] * pool_shape[1], dtype=torch.float32)
+    sc = torch.ones(pool_shape[0] * pool_shape[1] * 8 + 64, dtype=torch.float16)
+    sc = sc[(-sc.data_ptr() // 2) % 8 + scale_offset:]   # 16-byte aligned, then offset
     meta = B.KVQuantMeta(fmt, capacity, sc if scales else None, sc if scales else None, 1 / 16)
     scr = torch.zeros(1 << 16, dtype=torch.uint8)
     lib = B.load()
@@ -98,6 +99,12 @@ def _host_call(q_shape=(2, 24, 256), pool_shape=(64, 2, 256), fmt="bf16", pool_d
     (dict(pool_shape=(64, 1, 256)), B.ERR_INVALID_ARGUMENT, "Hkv=2"),
     (dict(fmt="int4", pool_shape=(64, 2, 256)), B.ERR_INVALID_ARGUMENT, "128"),
     (dict(fmt="int8"), B.ERR_INVALID_ARGUMENT, "scale"),
+    (dict(fmt="int8_g64", pool_dtype=torch.uint8, scales=True), B.ERR_INVALID_ARGUMENT, "dtype"),
+    (dict(fmt="int4_g32", pool_shape=(64, 2, 256), scales=True), B.ERR_INVALID_ARGUMENT, "128"),
+    (dict(fmt="int4_g32", pool_shape=(64, 2, 128)), B.ERR_INVALID_ARGUMENT, "scale"),
+    (dict(fmt="int8_g64", scales=True, scale_offset=2), B.ERR_MISALIGNED, "8-byte"),
+    (dict(fmt="int4_g32", pool_shape=(64, 2, 128), scales=True, scale_offset=4), B.ERR_MISALIGNED,
+     "16-byte"),
     (dict(q_offset=1), B.ERR_MISALIGNED, "aligned"),
     (dict(scratch=False), B.ERR_INVALID_ARGUMENT, "scratch"),
     (dict(cu_len=2), B.ERR_INVALID_ARGUMENT, "cu_seqlens"),
@@ -146,6 +153,19 @@ def test_kv_write_rejections_on_host():
     rc = lib.qsa_kv_write(2, d(x3), d(x3), d(slots), d(pool), d(pool), sc.data_ptr(), sc.data_ptr(),
                           None, None)
     assert rc == B.ERR_UNSUPPORTED
+    # grouped pools: binary16 scales, 8- (int8_g64) / 16-byte (int4_g32) aligned
+    h = torch.zeros(16 * 2 * 8 + 16, dtype=torch.float16)
+    h = h[(-h.data_ptr() // 2) % 8:]
+    rc = lib.qsa_kv_write(4, d(x), d(x), d(slots), d(pool), d(pool), h.data_ptr() + 4,
+                          h.data_ptr(), None, None)
+    assert rc == B.ERR_MISALIGNED and b"8-byte" in lib.qsa_last_error_message()
+    pool4 = torch.zeros(16, 2, 128, dtype=torch.uint8)
+    rc = lib.qsa_kv_write(5, d(x), d(x), d(slots), d(pool4), d(pool4), h.data_ptr() + 8,
+                          h.data_ptr(), None, None)
+    assert rc == B.ERR_MISALIGNED and b"16-byte" in lib.qsa_last_error_message()
+    rc = lib.qsa_kv_write(5, d(x), d(x), d(slots), d(pool), d(pool), h.data_ptr(), h.data_ptr(),
+                          None, None)
+    assert rc == B.ERR_INVALID_ARGUMENT and b"dtype" in lib.qsa_last_error_message()
     empty = torch.zeros(0, 2, 256, dtype=torch.bfloat16)
     rc = lib.qsa_kv_write(2, d(empty), d(empty), d(torch.zeros(0, dtype=torch.int32)), d(pool),
                           d(pool), sc.data_ptr(), sc.data_ptr(), None, None)

@@ -16,8 +16,22 @@ from tests.helpers import compare, run_cuda, run_oracle
 
 pytestmark = pytest.mark.gpu
 
-ROW = {"bf16": 256, "fp8_e4m3": 256, "int8": 256, "int4": 128}
-DT = {"bf16": torch.bfloat16, "fp8_e4m3": torch.uint8, "int8": torch.int8, "int4": torch.uint8}
+ROW = {"bf16": 256, "fp8_e4m3": 256, "int8": 256, "int4": 128, "int8_g64": 256, "int4_g32": 128}
+DT = {"bf16": torch.bfloat16, "fp8_e4m3": torch.uint8, "int8": torch.int8, "int4": torch.uint8,
+      "int8_g64": torch.int8, "int4_g32": torch.uint8}
+
+
+def _scales(fmt, slots_n, hkv, dev, fill):
+    """Scale buffers of a pool: fp32 per (slot, head), binary16 per group, fp8 [1]."""
+    if fmt in I.GROUPED:
+        return torch.full((slots_n, hkv, 256 // I.GROUPED[fmt]), fill, dtype=torch.float16, device=dev)
+    return torch.full((slots_n, hkv), fill, device=dev)
+
+
+def _bits(t):
+    """Scales as comparable integer bits (float32 or binary16)."""
+    a = t.numpy() if hasattr(t, "numpy") else t
+    return a.view(np.uint16 if a.dtype == np.float16 else np.uint32).reshape(-1)
 
 
 def _new_rows(n, hkv, seed):
@@ -70,9 +84,9 @@ def test_kv_write_matches_oracle(cuda_device, fmt, hkv, fp8_scales):
     if fmt == "fp8_e4m3":
         ks = torch.tensor([fp8_scales[0]], device=cuda_device)
         vs = torch.tensor([fp8_scales[1]], device=cuda_device)
-    elif fmt in ("int8", "int4"):
-        ks = torch.full((slots_n, hkv), -1.0, device=cuda_device)
-        vs = torch.full((slots_n, hkv), -1.0, device=cuda_device)
+    elif fmt != "bf16":
+        ks = _scales(fmt, slots_n, hkv, cuda_device, -1.0)
+        vs = _scales(fmt, slots_n, hkv, cuda_device, -1.0)
     err = torch.zeros(1, dtype=torch.int32, device=cuda_device)
     qsa.qsa_kv_write(fmt, x_k.to(cuda_device), x_v.to(cuda_device), slots.to(cuda_device),
                      kp, vp, ks, vs, err)
@@ -89,7 +103,7 @@ def test_kv_write_matches_oracle(cuda_device, fmt, hkv, fp8_scales):
         else:
             assert np.array_equal(got.view(torch.uint8).numpy(), codes.view(np.uint8))
         if scales is not None:
-            assert np.array_equal(sc.cpu()[slots.long()].reshape(-1).numpy(), scales)
+            assert np.array_equal(_bits(sc.cpu()[slots.long()]), _bits(scales))
             assert (sc.cpu()[~written] == -1.0).all()
         assert torch.equal(pool.cpu()[~written], pool0.cpu()[~written])
 
@@ -129,7 +143,7 @@ def test_kv_write_strided_input(cuda_device):
     assert np.array_equal(ks.cpu()[slots.cpu().long()].reshape(-1).numpy(), scales)
 
 
-@pytest.mark.parametrize("fmt", ["int8", "fp8_e4m3", "int4"])
+@pytest.mark.parametrize("fmt", ["int8", "fp8_e4m3", "int4", "int8_g64", "int4_g32"])
 def test_write_then_decode(cuda_device, fmt):
     """Rows written by qsa_kv_write decode like the oracle says they should."""
     w = I.tp1_mixed(seed=63, bs=4, num_slots=4096, lengths=[100, 2055, 1, 640], fmt=fmt)
@@ -146,22 +160,24 @@ def test_write_then_decode(cuda_device, fmt):
     compare(out, run_oracle(host), w.lengths().numpy())
 
 
-def _ratio_rows(exponent: int) -> torch.Tensor:
-    """Rows whose absmax a = (1 + t/128) 2^exponent takes every bf16 mantissa t and
-    whose other values are every bf16 x with 2^-11 a <= |x| <= a (both signs): every
-    ratio x / a that can give a nonzero code, so the rounding of every such x / s is
-    checked."""
+def _ratio_rows(exponent: int, gs: int = 256) -> torch.Tensor:
+    """Rows whose every scale group (gs channels) has absmax a = (1 + t/128) 2^exponent
+    in its first channel, t taking every bf16 mantissa, and whose other values are
+    every bf16 x with 2^-11 a <= |x| <= a (both signs): every ratio x / a that can give
+    a nonzero code, so the rounding of every such x / s is checked."""
+    per = gs - 1
     rows = []
     for t in range(128):
         a = (1 + t / 128) * 2.0 ** exponent
         xs = [m / 128 * 2.0 ** (exponent + e) for e in range(0, -12, -1) for m in range(128, 256)]
         xs = [v for v in xs if v <= a]
         xs = torch.tensor(xs + [-v for v in xs], dtype=torch.float64)
-        for k in range(0, xs.numel(), 255):
-            chunk = xs[k:k + 255]
+        groups = [xs[k:k + per] for k in range(0, xs.numel(), per)]
+        for r0 in range(0, len(groups), 256 // gs):
             row = torch.zeros(256, dtype=torch.float64)
-            row[0] = a
-            row[1:1 + chunk.numel()] = chunk
+            for j, chunk in enumerate(groups[r0:r0 + 256 // gs]):
+                row[j * gs] = a
+                row[j * gs + 1:j * gs + 1 + chunk.numel()] = chunk
             rows.append(row)
     return torch.stack(rows).to(torch.bfloat16)
 
@@ -175,8 +191,8 @@ def _write_and_compare(dev, fmt, x, fp8_scale=None):
         ks = torch.tensor([fp8_scale], device=dev)
         vs = ks.clone()
     else:
-        ks = torch.zeros(n, 1, device=dev)
-        vs = torch.zeros(n, 1, device=dev)
+        ks = _scales(fmt, n, 1, dev, 0.0)
+        vs = _scales(fmt, n, 1, dev, 0.0)
     xd = xk.to(dev)
     qsa.qsa_kv_write(fmt, xd, xd, slots.to(dev), kp, vp, ks, vs)
     torch.cuda.synchronize()
@@ -185,7 +201,7 @@ def _write_and_compare(dev, fmt, x, fp8_scale=None):
         got = pool.cpu().reshape(n, -1).view(torch.uint8).numpy()
         assert np.array_equal(got, codes.view(np.uint8)), (fmt, fp8_scale)
         if scales is not None:
-            assert np.array_equal(sc.cpu().reshape(-1).numpy(), scales)
+            assert np.array_equal(_bits(sc.cpu()), _bits(scales))
 
 
 @pytest.mark.parametrize("fmt", ["int8", "int4"])
@@ -197,6 +213,16 @@ def test_every_quotient_rounds_like_the_oracle(cuda_device, fmt):
     # below 2^-60 (subnormal scales, clamped codes) the kernel divides
     _write_and_compare(cuda_device, fmt, _ratio_rows(-61))
     _write_and_compare(cuda_device, fmt, _ratio_rows(-126)[::7])
+
+
+@pytest.mark.parametrize("fmt", ["int8_g64", "int4_g32"])
+def test_every_group_quotient_rounds_like_the_oracle(cuda_device, fmt):
+    """Grouped formats: every (x, group absmax) bf16 mantissa pair, with the group
+    absmax in binary16's subnormal range, across its normal range, at the 65504 clamp
+    boundary and beyond it, and at the extremes of bf16."""
+    gs = I.GROUPED[fmt]
+    for e in (-126, -40, -20, -14, -9, -8, -1, 0, 5, 15, 18, 19, 22, 23, 30, 127):
+        _write_and_compare(cuda_device, fmt, _ratio_rows(e, gs))
 
 
 @pytest.mark.parametrize("scale", [1.0, 0.0625, 2.0 ** -20, 0.05, 0.0112, 3.0, 448.0 / 3])
