@@ -14,7 +14,12 @@ sequence b and query head h with KV head g = h // (Hq // Hkv),
 gives zeros. Khat/Vhat are the exactly dequantised pool rows.
 
 It also holds the quantising KV write (``quantize_rows``): the codes and
-scales the pools' write path produces, in binary32.
+scales the pools' write path produces, in binary32; and the tiered
+``int8ring_int4`` pool (``decode_tiered``, ``write_tiered``; sglang PR #37798,
+"Modifications", the tiered KV pool module): every token is written as an
+int4_g32 row of its slot and as an int8_g64 row of the ring position
+``slot & (R - 1)``, whose owner entry becomes the slot; a reader takes the ring
+row when ``owner[slot & (R - 1)] == slot`` and the int4_g32 row otherwise.
 
 Pins: every function here is checked in ``tests/test_oracle_pins.py``
 against closed forms, library routines and brute force (see that file).
@@ -80,6 +85,18 @@ def _load():
         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,           # k_pool, v_pool, format
         ctypes.c_int64, ctypes.c_int, ctypes.c_int,               # num_slots, Hkv, D
         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_double,        # k_scale, v_scale, scale
+        ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,         # sel, n_sel, cu
+        ctypes.c_int, ctypes.c_int,                               # bs, Hq
+        ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,  # rows, n_rows, out, threads
+    ]
+    lib.orc_decode_tiered.restype = ctypes.c_int
+    lib.orc_decode_tiered.argtypes = [
+        ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,          # q, q_sb, q_sh
+        ctypes.c_void_p, ctypes.c_void_p,                         # k_pool, v_pool (int4_g32)
+        ctypes.c_int64, ctypes.c_int, ctypes.c_int,               # num_slots, Hkv, D
+        ctypes.c_void_p, ctypes.c_void_p,                         # k_scale, v_scale
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,  # rings + scales
+        ctypes.c_void_p, ctypes.c_int64, ctypes.c_double,         # owner, R, scale
         ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,         # sel, n_sel, cu
         ctypes.c_int, ctypes.c_int,                               # bs, Hq
         ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,  # rows, n_rows, out, threads
@@ -179,6 +196,68 @@ def decode(q, k_pool, v_pool, fmt: str, sel, cu, softmax_scale: float,
         raise OracleRefused({-1: "bad geometry", -2: "bad cu_seqlens",
                              -3: "slot id out of range"}.get(rc, str(rc)))
     return out
+
+
+def decode_tiered(q, k_pool, v_pool, sel, cu, softmax_scale: float, k_scale, v_scale,
+                  k_ring, v_ring, k_ring_scale, v_ring_scale, owner, rows=None,
+                  threads: int = 0) -> np.ndarray:
+    """Oracle decode over a tiered int8ring_int4 pool. Returns float64 [rows, Hq, D].
+
+    k_pool/v_pool: int4_g32 rows [num_slots, Hkv, D/2] uint8 with binary16 scales
+    [num_slots, Hkv, D/32]; k_ring/v_ring: int8_g64 rows [R, Hkv, D] with binary16
+    scales [R, Hkv, D/64]; owner: int32 [R] (R a power of two; -1 = no owner)."""
+    lib = _load()
+    qn = _np(q)
+    bs, Hq, D = qn.shape
+    kn, vn = _np(k_pool), _np(v_pool)
+    num_slots, Hkv = kn.shape[0], kn.shape[1]
+    kr, vr = _np(k_ring).view(np.int8), _np(v_ring).view(np.int8)
+    on = _np(owner, np.int32)
+    R = on.shape[0]
+    if kr.shape != (R, Hkv, D) or kn.shape[2] * 2 != D:
+        raise ValueError("ring rows must be [R, Hkv, D] int8 and pool rows [slots, Hkv, D/2]")
+    sn, cn = _np(sel, np.int32), _np(cu, np.int32)
+    rn = _np(rows, np.int32) if rows is not None else None
+    n_rows = bs if rn is None else rn.shape[0]
+    out = np.zeros((n_rows, Hq, D), dtype=np.float64)
+    ks, vs = _scales(k_scale, "int4_g32"), _scales(v_scale, "int4_g32")
+    krs, vrs = _scales(k_ring_scale, "int8_g64"), _scales(v_ring_scale, "int8_g64")
+    rc = lib.orc_decode_tiered(_ptr(qn), Hq * D, D, _ptr(kn), _ptr(vn), num_slots, Hkv, D,
+                               _ptr(ks), _ptr(vs), _ptr(kr), _ptr(vr), _ptr(krs), _ptr(vrs),
+                               _ptr(on), R, float(softmax_scale), _ptr(sn), sn.shape[0], _ptr(cn),
+                               bs, Hq, _ptr(rn), n_rows, _ptr(out), int(threads))
+    if rc != 0:
+        raise OracleRefused({-1: "bad geometry", -2: "bad cu_seqlens",
+                             -3: "slot id out of range"}.get(rc, str(rc)))
+    return out
+
+
+def write_tiered(x_k, x_v, slots, pools: dict) -> None:
+    """The tiered write, in token order (a later token of the same write takes a
+    ring row over an earlier one): for token i with slot s and ring position
+    p = s & (R - 1), every head g gets the int4_g32 row (s, g) and the int8_g64
+    ring row (p, g), and owner[p] = s. `pools` holds numpy arrays, updated in
+    place: k_pool, v_pool (uint8 [slots, Hkv, D/2]), k_scale, v_scale (float16
+    [slots, Hkv, D/32]), k_ring, v_ring (int8 [R, Hkv, D]), k_ring_scale,
+    v_ring_scale (float16 [R, Hkv, D/64]), owner (int32 [R])."""
+    xk, xv = _np(x_k), _np(x_v)
+    n, Hkv, D = xk.shape
+    sl = _np(slots, np.int32)
+    R = pools["owner"].shape[0]
+    for x, pool, sc, ring, rsc in ((xk, "k_pool", "k_scale", "k_ring", "k_ring_scale"),
+                                   (xv, "v_pool", "v_scale", "v_ring", "v_ring_scale")):
+        c4, s4 = quantize_rows(x.reshape(n * Hkv, D), "int4_g32")
+        c8, s8 = quantize_rows(x.reshape(n * Hkv, D), "int8_g64")
+        c4, s4 = c4.reshape(n, Hkv, -1), s4.reshape(n, Hkv, -1)
+        c8, s8 = c8.reshape(n, Hkv, -1), s8.reshape(n, Hkv, -1)
+        for i in range(n):
+            s, pos = int(sl[i]), int(sl[i]) & (R - 1)
+            pools[pool][s] = c4[i]
+            pools[sc][s] = s4[i]
+            pools[ring][pos] = c8[i]
+            pools[rsc][pos] = s8[i]
+    for i in range(n):
+        pools["owner"][int(sl[i]) & (R - 1)] = sl[i]
 
 
 def dequant_rows(pool, fmt: str, slots, g: int, scale=None) -> np.ndarray:

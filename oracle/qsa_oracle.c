@@ -30,6 +30,10 @@
  *             2i in the low nibble; binary16 per 32-channel group)
  * (the grouped formats: sglang PR #37798, "Modifications", the int8 and int4
  * KV pool modules)
+ *   int8ring_int4: a row (slot, g) reads the int8_g64 ring row
+ *             (slot & (R - 1), g) when owner[slot & (R - 1)] == slot (hot),
+ *             else the int4_g32 pool row (slot, g) (cold)  (same PR, the
+ *             tiered KV pool module: every token is written to both)
  *
  * Every step is written as the definition states it: no tiling, no
  * online softmax, no split, no merge. The scores use one exact max
@@ -43,7 +47,8 @@
 #include <omp.h>
 #endif
 
-enum { ORC_BF16 = 0, ORC_FP8_E4M3 = 1, ORC_INT8 = 2, ORC_INT4 = 3, ORC_INT8_G64 = 4, ORC_INT4_G32 = 5 };
+enum { ORC_BF16 = 0, ORC_FP8_E4M3 = 1, ORC_INT8 = 2, ORC_INT4 = 3, ORC_INT8_G64 = 4, ORC_INT4_G32 = 5,
+       ORC_INT8RING_INT4 = 6 };
 
 /* Channels per scale group: 64 / 32 for the grouped formats, 0 otherwise. */
 static int group_size(int format) {
@@ -51,7 +56,9 @@ static int group_size(int format) {
 }
 
 /* Pool rows hold D / 2 bytes (two 4-bit codes per byte). */
-static int is_nibble_format(int format) { return format == ORC_INT4 || format == ORC_INT4_G32; }
+static int is_nibble_format(int format) {
+    return format == ORC_INT4 || format == ORC_INT4_G32 || format == ORC_INT8RING_INT4;
+}
 
 /* bf16 -> double: a bf16 is the upper half of an IEEE binary32. */
 double orc_bf16_to_double(uint16_t h) {
@@ -157,11 +164,27 @@ typedef struct {
     int D;
     const void* scale; /* fp8: float [1]; int8/int4: float [num_slots * Hkv];
                           grouped: binary16 bits [num_slots * Hkv * D / group]; bf16: unused */
+    /* int8ring_int4 only: the hot ring (int8_g64 rows [R, Hkv, D] and binary16
+     * scales [R, Hkv, D / 64]) and its owner table [R]; pool / scale above are
+     * the int4_g32 rows and scales of every slot */
+    const int8_t* ring;
+    const uint16_t* ring_scale;
+    const int32_t* owner;
+    int64_t R;
 } orc_pool;
 
 /* Dequantised element d of pool row (slot, g), exactly in FP64. */
 static double pool_elem(const orc_pool* p, int64_t slot, int g, int d) {
     int64_t row = slot * p->Hkv + g;
+    if (p->format == ORC_INT8RING_INT4) {
+        const int64_t pos = slot & (p->R - 1);
+        if ((int64_t)p->owner[pos] == slot) { /* hot: the ring row */
+            orc_pool hot = {p->ring, ORC_INT8_G64, p->Hkv, p->D, p->ring_scale, 0, 0, 0, 0};
+            return pool_elem(&hot, pos, g, d);
+        }
+        orc_pool cold = {p->pool, ORC_INT4_G32, p->Hkv, p->D, p->scale, 0, 0, 0, 0};
+        return pool_elem(&cold, slot, g, d);
+    }
     switch (p->format) {
     case ORC_BF16:
         return orc_bf16_to_double(((const uint16_t*)p->pool)[row * p->D + d]);
@@ -192,7 +215,7 @@ static double pool_elem(const orc_pool* p, int64_t slot, int g, int d) {
 /* Dequantise one pool row into `dst` (D doubles). */
 void orc_dequant_row(const void* pool, int format, int Hkv, int D, const void* scale,
                      int64_t slot, int g, double* dst) {
-    orc_pool p = {pool, format, Hkv, D, scale};
+    orc_pool p = {pool, format, Hkv, D, scale, 0, 0, 0, 0};
     for (int d = 0; d < D; ++d) dst[d] = pool_elem(&p, slot, g, d);
 }
 
@@ -210,6 +233,11 @@ void orc_dequant_row(const void* pool, int format, int Hkv, int D, const void* s
  *           output row i holds sequence rows[i]
  * out     : double [n_rows][Hq][D]
  */
+static int decode_impl(const uint16_t* q, int64_t q_sb, int64_t q_sh, orc_pool kp, orc_pool vp,
+                       int64_t num_slots, double softmax_scale, const int32_t* sel, int64_t n_sel,
+                       const int32_t* cu, int bs, int Hq, const int32_t* rows, int n_rows,
+                       double* out, int nthreads);
+
 int orc_decode(const uint16_t* q, int64_t q_sb, int64_t q_sh,
                const void* k_pool, const void* v_pool, int format,
                int64_t num_slots, int Hkv, int D,
@@ -220,6 +248,37 @@ int orc_decode(const uint16_t* q, int64_t q_sb, int64_t q_sh,
     if (format < ORC_BF16 || format > ORC_INT4_G32) return -1;
     if (is_nibble_format(format) && (D & 1)) return -1;
     if (group_size(format) && D % group_size(format)) return -1;
+    orc_pool kp = {k_pool, format, Hkv, D, k_scale, 0, 0, 0, 0};
+    orc_pool vp = {v_pool, format, Hkv, D, v_scale, 0, 0, 0, 0};
+    return decode_impl(q, q_sb, q_sh, kp, vp, num_slots, softmax_scale, sel, n_sel, cu, bs, Hq,
+                       rows, n_rows, out, nthreads);
+}
+
+/* Decode over a tiered pool: int4_g32 rows + scales of every slot (k_pool,
+ * k_scale, ...), the int8_g64 ring [R, Hkv, D] with binary16 scales
+ * [R, Hkv, D / 64], and the owner table [R] (R a power of two). Same return
+ * codes as orc_decode. */
+int orc_decode_tiered(const uint16_t* q, int64_t q_sb, int64_t q_sh,
+                      const void* k_pool, const void* v_pool, int64_t num_slots, int Hkv, int D,
+                      const void* k_scale, const void* v_scale,
+                      const int8_t* k_ring, const int8_t* v_ring,
+                      const uint16_t* k_ring_scale, const uint16_t* v_ring_scale,
+                      const int32_t* owner, int64_t R, double softmax_scale,
+                      const int32_t* sel, int64_t n_sel, const int32_t* cu, int bs, int Hq,
+                      const int32_t* rows, int n_rows, double* out, int nthreads) {
+    if (Hkv <= 0 || Hq <= 0 || Hq % Hkv != 0 || D <= 0 || D % 64) return -1;
+    if (R <= 0 || (R & (R - 1))) return -1;
+    orc_pool kp = {k_pool, ORC_INT8RING_INT4, Hkv, D, k_scale, k_ring, k_ring_scale, owner, R};
+    orc_pool vp = {v_pool, ORC_INT8RING_INT4, Hkv, D, v_scale, v_ring, v_ring_scale, owner, R};
+    return decode_impl(q, q_sb, q_sh, kp, vp, num_slots, softmax_scale, sel, n_sel, cu, bs, Hq,
+                       rows, n_rows, out, nthreads);
+}
+
+static int decode_impl(const uint16_t* q, int64_t q_sb, int64_t q_sh, orc_pool kp, orc_pool vp,
+                       int64_t num_slots, double softmax_scale, const int32_t* sel, int64_t n_sel,
+                       const int32_t* cu, int bs, int Hq, const int32_t* rows, int n_rows,
+                       double* out, int nthreads) {
+    const int Hkv = kp.Hkv, D = kp.D;
     if (rows == NULL) n_rows = bs;
     for (int i = 0; i < n_rows; ++i) {
         int b = rows ? rows[i] : i;
@@ -230,8 +289,6 @@ int orc_decode(const uint16_t* q, int64_t q_sb, int64_t q_sh,
             if (sel[t] < 0 || (int64_t)sel[t] >= num_slots) return -3;
     }
     const int group = Hq / Hkv;
-    orc_pool kp = {k_pool, format, Hkv, D, k_scale};
-    orc_pool vp = {v_pool, format, Hkv, D, v_scale};
     const int64_t tasks = (int64_t)n_rows * Hq;
 #ifdef _OPENMP
     if (nthreads > 0) omp_set_num_threads(nthreads);

@@ -27,6 +27,9 @@ MAX_CAPACITY = 2055     # largest selected-KV length of the contract
 SOFTMAX_SCALE = 1.0 / 16.0
 
 FORMATS = ("bf16", "fp8_e4m3", "int8", "int4", "int8_g64", "int4_g32")
+TIERED = "int8ring_int4"   # int4_g32 pool of every slot + int8_g64 ring with an owner table
+RING_SLOTS = 8192          # the pages' default ring size
+TIER_KEYS = ("k_ring", "v_ring", "k_ring_scale", "v_ring_scale", "owner")
 GROUPED = {"int8_g64": 64, "int4_g32": 32}   # channels per binary16 scale
 NIBBLE_FORMATS = ("int4", "int4_g32")        # two 4-bit codes per byte
 FP8_E4M3_MAX = 448.0    # largest finite e4m3fn value; the fp8 write saturates here
@@ -69,9 +72,10 @@ class Workload:
 
     def to(self, device) -> "Workload":
         mv = lambda t: None if t is None else t.to(device)
+        extra = {k: (v.to(device) if isinstance(v, torch.Tensor) else v) for k, v in self.extra.items()}
         return Workload(mv(self.q), mv(self.k_pool), mv(self.v_pool), mv(self.sel), mv(self.cu),
                         self.fmt, mv(self.k_scale), mv(self.v_scale), self.softmax_scale,
-                        self.capacity, self.name, dict(self.extra))
+                        self.capacity, self.name, extra)
 
     def lengths(self) -> torch.Tensor:
         return (self.cu[1:] - self.cu[:-1]).cpu()
@@ -157,6 +161,42 @@ def make_pools(num_slots: int, num_kv_heads: int, fmt: str, seed: int, device="c
     return kc, vc, ks, vs
 
 
+def make_tiered_pools(num_slots: int, num_kv_heads: int, ring_slots: int, seed: int, device="cpu",
+                      unowned: float = 0.1):
+    """A tiered int8ring_int4 pool as a run of writes leaves it (sglang PR #37798,
+    "Modifications", the tiered KV pool module): every slot holds its int4_g32 row;
+    slots were written in a seeded random order, so ring position p holds the int8_g64
+    row of the last slot written with slot & (R - 1) == p, and owner[p] is that slot.
+    A share `unowned` of ring positions was never written (owner -1, ring rows zero).
+
+    Returns (k_pool, v_pool, k_scale, v_scale, tier) with tier a dict of TIER_KEYS."""
+    if ring_slots <= 0 or ring_slots & (ring_slots - 1):
+        raise ValueError("the ring size must be a power of two")
+    shape = (num_slots, num_kv_heads, HEAD_DIM)
+    g = torch.Generator().manual_seed(seed * 1000 + 7)
+    order = torch.randperm(num_slots, generator=g)
+    pos = order & (ring_slots - 1)
+    last = torch.full((ring_slots,), -1, dtype=torch.int64)
+    last.scatter_reduce_(0, pos, torch.arange(num_slots), reduce="amax")   # latest write per position
+    owner = torch.where(last >= 0, order[last.clamp(min=0)], torch.full_like(last, -1))
+    drop = torch.rand(ring_slots, generator=g) < unowned
+    owner = torch.where(drop, torch.full_like(owner, -1), owner).to(torch.int32)
+    out = {}
+    for name, sub in (("k", 1), ("v", 2)):
+        x = normal_values(shape, seed * 1000 + sub, device)
+        codes4, s4 = quantize_pool(x, "int4_g32")
+        own = owner.to(device).long()
+        rows = x.index_select(0, own.clamp(min=0))
+        codes8, s8 = quantize_pool(rows, "int8_g64")
+        live = (own >= 0).view(-1, 1, 1)
+        out[name] = (codes4, s4, torch.where(live, codes8, torch.zeros_like(codes8)),
+                     torch.where(live, s8, torch.zeros_like(s8)))
+        del x, rows
+    tier = {"k_ring": out["k"][2], "v_ring": out["v"][2], "k_ring_scale": out["k"][3],
+            "v_ring_scale": out["v"][3], "owner": owner.to(device)}
+    return out["k"][0], out["v"][0], out["k"][1], out["v"][1], tier
+
+
 def make_query(bs: int, num_q_heads: int, seed: int, device="cpu") -> torch.Tensor:
     return normal_values((bs, num_q_heads, HEAD_DIM), seed * 1000 + 3, device).to(torch.bfloat16)
 
@@ -230,6 +270,36 @@ def tp1_saturated(seed: int = 2, device="cpu", bs: int = 128, num_slots: int = 1
     return Workload(make_query(bs, 24, seed if index_seed is None else index_seed, device),
                     kc, vc, sel.to(device), cu_from_lengths([length] * bs).to(device), fmt, ks, vs,
                     capacity=length, name=f"tp1_saturated_bs{bs}_L{length}_{fmt}")
+
+
+def tiered(seed: int = 4, device="cpu", bs: int = 16, num_slots: int = 16384,
+           ring_slots: int = 4096, num_kv_heads: int = 2, lengths=None, max_len: int = MAX_CAPACITY,
+           hot_share: float = 0.5, pools=None) -> Workload:
+    """A tiered int8ring_int4 workload: each sequence's ids are a `hot_share` of
+    slots that own their ring row (read from the int8_g64 ring) and uniform slots
+    (mostly read from the int4_g32 pool), interleaved in a seeded order."""
+    if pools is None:
+        pools = make_tiered_pools(num_slots, num_kv_heads, ring_slots, seed, device)
+    kc, vc, ks, vs, tier = pools
+    g = _gen(seed, "cpu")
+    if lengths is None:
+        lengths = torch.randint(1, max_len + 1, (bs,), generator=g, dtype=torch.int64)
+    lengths = torch.as_tensor(lengths, dtype=torch.int64)
+    owner = tier["owner"].cpu().long()
+    hot_slots = owner[owner >= 0]
+    parts = []
+    for L in lengths.tolist():
+        nh = int(round(L * hot_share)) if hot_slots.numel() else 0
+        hot = hot_slots[torch.randint(0, max(hot_slots.numel(), 1), (nh,), generator=g)]
+        uni = torch.randint(0, kc.shape[0], (L - nh,), generator=g, dtype=torch.int64)
+        ids = torch.cat([hot, uni])
+        parts.append(ids[torch.randperm(L, generator=g)])
+    sel = (torch.cat(parts) if parts else torch.zeros(0, dtype=torch.int64)).to(torch.int32)
+    hq = 12 * num_kv_heads
+    return Workload(make_query(bs, hq, seed, device), kc, vc, sel.to(device),
+                    cu_from_lengths(lengths).to(device), TIERED, ks, vs,
+                    capacity=max(int(lengths.max()), 1) if lengths.numel() else 1,
+                    name=f"tiered_bs{bs}_R{ring_slots}", extra=dict(tier))
 
 
 # ------------------------------------------- counter-based generator (replays)
@@ -314,6 +384,8 @@ def host_subset(w: Workload, rows) -> Workload:
     dev_idx = uniq.to(w.k_pool.device)
     k = w.k_pool.index_select(0, dev_idx).cpu()
     v = w.v_pool.index_select(0, dev_idx).cpu()
+    if w.fmt == TIERED:
+        return _tiered_subset(w, rows, cu, sel, uniq, inv)
     ks = vs = None
     if w.fmt in ("int8", "int4") or w.fmt in GROUPED:
         ks = w.k_scale.index_select(0, dev_idx).cpu()
@@ -323,3 +395,34 @@ def host_subset(w: Workload, rows) -> Workload:
     lens = [int(cu[b + 1] - cu[b]) for b in rows]
     return Workload(w.q.cpu()[rows], k, v, inv.to(torch.int32), cu_from_lengths(lens), w.fmt,
                       ks, vs, w.softmax_scale, w.capacity, w.name + "_subset")
+
+
+def _tiered_subset(w: Workload, rows, cu, sel, uniq, inv) -> Workload:
+    """host_subset of a tiered workload: the selected slots become ids 0..n-1 of a
+    tiered pool whose ring has one position per id (a power of two at least n), so
+    id k owns ring row k exactly when its original slot owned its ring row."""
+    tier = w.extra
+    R = tier["owner"].shape[0]
+    dev_idx = uniq.to(w.k_pool.device)
+    pos = dev_idx & (R - 1)
+    owner = tier["owner"].index_select(0, pos)
+    hot = owner == dev_idx.to(owner.dtype)
+    n = uniq.numel()
+    R2 = 1
+    while R2 < max(n, 1):
+        R2 *= 2
+    new_tier = {}
+    for key in ("k_ring", "v_ring", "k_ring_scale", "v_ring_scale"):
+        src = tier[key].index_select(0, pos)
+        pad = torch.zeros((R2 - n,) + tuple(src.shape[1:]), dtype=src.dtype, device=src.device)
+        new_tier[key] = torch.cat([src, pad]).cpu()
+    new_owner = torch.full((R2,), -1, dtype=torch.int32)
+    new_owner[:n] = torch.where(hot.cpu(), torch.arange(n, dtype=torch.int32),
+                                torch.full((n,), -1, dtype=torch.int32))
+    new_tier["owner"] = new_owner
+    lens = [int(cu[b + 1] - cu[b]) for b in rows]
+    return Workload(w.q.cpu()[rows], w.k_pool.index_select(0, dev_idx).cpu(),
+                    w.v_pool.index_select(0, dev_idx).cpu(), inv.to(torch.int32),
+                    cu_from_lengths(lens), w.fmt, w.k_scale.index_select(0, dev_idx).cpu(),
+                    w.v_scale.index_select(0, dev_idx).cpu(), w.softmax_scale, w.capacity,
+                    w.name + "_subset", new_tier)

@@ -537,3 +537,103 @@ def test_grouped_quantiser_ties_and_zero_groups():
     # offset binary, even channel low: (7 + 8, -4 + 8) -> 0x4f; (2 + 8, 0 + 8) -> 0x8a
     assert c4[0, 0] == 0x4F and c4[0, 1] == 0x8A
     assert (c4[0, 2:] == 0x88).all()                            # zero codes read 8
+
+
+# ------------------------------------------------ tiered int8ring_int4 pools
+
+def _tiered_run(w, owner=None, **kw):
+    t = w.extra
+    return oracle.decode_tiered(w.q, w.k_pool, w.v_pool, w.sel, w.cu, w.softmax_scale, w.k_scale,
+                                w.v_scale, t["k_ring"], t["v_ring"], t["k_ring_scale"],
+                                t["v_ring_scale"], t["owner"] if owner is None else owner, **kw)
+
+
+def test_tiered_all_hot_is_int8_g64_and_all_cold_is_int4_g32():
+    """The pages' tiered tests: all-hot equals the int8 kernel, all-cold the int4 one;
+    a stale owner (another slot of the same ring row) reads the int4 row."""
+    slots, R = 1024, 1024
+    w = I.tiered(seed=40, bs=3, num_slots=slots, ring_slots=R, lengths=[7, 300, 64])
+    t = w.extra
+    all_hot = torch.arange(R, dtype=torch.int32)
+    # owner[p] = p with R = slots: every slot is hot and its ring row is ring[slot]
+    hot = _tiered_run(w, owner=all_hot)
+    ref8 = oracle.decode(w.q, t["k_ring"], t["v_ring"], "int8_g64", w.sel, w.cu, w.softmax_scale,
+                         t["k_ring_scale"], t["v_ring_scale"])
+    assert np.array_equal(hot, ref8)
+    cold = _tiered_run(w, owner=torch.full((R,), -1, dtype=torch.int32))
+    ref4 = oracle.decode(w.q, w.k_pool, w.v_pool, "int4_g32", w.sel, w.cu, w.softmax_scale,
+                         w.k_scale, w.v_scale)
+    assert np.array_equal(cold, ref4)
+    stale = _tiered_run(w, owner=all_hot + R)          # same positions, other slots
+    assert np.array_equal(stale, ref4)
+
+
+def test_tiered_reads_the_ring_row_exactly_when_the_owner_matches():
+    """Exact values (power-of-two scales, small codes) in both tiers: the tiered
+    decode equals a bf16 pool holding, per slot, the ring value when
+    owner[slot & (R-1)] == slot and the int4_g32 value otherwise."""
+    slots, R, Hkv = 512, 128, 2
+    g = torch.Generator().manual_seed(41)
+    c8 = torch.randint(-127, 128, (2, R, Hkv, 256), generator=g)
+    c4 = torch.randint(-7, 8, (2, slots, Hkv, 256), generator=g)
+    s8 = torch.pow(2.0, torch.randint(-5, 3, (2, R, Hkv, 4), generator=g).float()).to(torch.float16)
+    s4 = torch.pow(2.0, torch.randint(-5, 3, (2, slots, Hkv, 8), generator=g).float()).to(torch.float16)
+    owner = torch.randint(-1, slots, (R,), generator=g).to(torch.int32)
+    owner[::3] = (torch.arange(R, dtype=torch.int32) + R * torch.randint(0, slots // R, (R,), generator=g).to(torch.int32))[::3]
+    u = (c4 + 8).to(torch.int16)
+    packed4 = (u[..., 0::2] | (u[..., 1::2] << 4)).to(torch.uint8)
+    v8 = c8.double() * s8.double().repeat_interleave(64, -1)
+    v4 = c4.double() * s4.double().repeat_interleave(32, -1)
+    sl = torch.arange(slots)
+    is_hot = owner.long()[sl & (R - 1)] == sl
+    assert 0 < int(is_hot.sum()) < slots
+    vals = torch.where(is_hot.view(1, -1, 1, 1), v8[:, sl & (R - 1)], v4)
+    bf = vals.to(torch.bfloat16)
+    assert torch.equal(bf.double(), vals)
+    q = I.make_query(2, 12 * Hkv, 42)
+    sel = torch.randint(0, slots, (2 * 200,), generator=g).to(torch.int32)
+    cu = I.cu_from_lengths([200, 200])
+    got = oracle.decode_tiered(q, packed4[0], packed4[1], sel, cu, 1 / 16, s4[0], s4[1],
+                               c8[0].to(torch.int8), c8[1].to(torch.int8), s8[0], s8[1], owner)
+    ref = oracle.decode(q, bf[0], bf[1], "bf16", sel, cu, 1 / 16)
+    assert np.array_equal(got, ref)
+
+
+def test_tiered_write_in_token_order_with_ring_wrap_and_collisions():
+    """R = 64 over 4096 slots (the pages' ring-wrap test): after a write of 500
+    tokens, each touched ring row belongs to the last token of the write with that
+    ring position, holds that token's int8_g64 row, and every written slot holds its
+    int4_g32 row; untouched ring rows and slots keep their contents."""
+    slots, R, Hkv, n = 4096, 64, 2, 500
+    g = torch.Generator().manual_seed(43)
+    pools = {
+        "k_pool": np.full((slots, Hkv, 128), 0x5A, np.uint8), "v_pool": np.full((slots, Hkv, 128), 0xA5, np.uint8),
+        "k_scale": np.full((slots, Hkv, 8), 3.0, np.float16), "v_scale": np.full((slots, Hkv, 8), 5.0, np.float16),
+        "k_ring": np.full((R, Hkv, 256), 9, np.int8), "v_ring": np.full((R, Hkv, 256), -9, np.int8),
+        "k_ring_scale": np.full((R, Hkv, 4), 7.0, np.float16), "v_ring_scale": np.full((R, Hkv, 4), 11.0, np.float16),
+        "owner": np.full(R, -1, np.int32),
+    }
+    sl = torch.randperm(slots, generator=g)[:n].to(torch.int32)   # 500 slots over 64 ring rows
+    xk = I.normal_values((n, Hkv, 256), 44).to(torch.bfloat16)
+    xv = I.normal_values((n, Hkv, 256), 45).to(torch.bfloat16)
+    before = {k: v.copy() for k, v in pools.items()}
+    oracle.write_tiered(xk, xv, sl, pools)
+    c8k, s8k = oracle.quantize_rows(xk.reshape(n * Hkv, 256), "int8_g64")
+    c4k, s4k = oracle.quantize_rows(xk.reshape(n * Hkv, 256), "int4_g32")
+    last = {}
+    for i, s in enumerate(sl.tolist()):
+        last[s % R] = i                                  # the later token wins
+    for p in range(R):
+        if p in last:
+            i = last[p]
+            assert pools["owner"][p] == sl[i]
+            assert np.array_equal(pools["k_ring"][p], c8k.reshape(n, Hkv, 256)[i])
+            assert np.array_equal(pools["k_ring_scale"][p], s8k.reshape(n, Hkv, 4)[i])
+        else:
+            assert pools["owner"][p] == -1 and np.array_equal(pools["k_ring"][p], before["k_ring"][p])
+    for i, s in enumerate(sl.tolist()):
+        assert np.array_equal(pools["k_pool"][s], c4k.reshape(n, Hkv, 128)[i])
+        assert np.array_equal(pools["k_scale"][s], s4k.reshape(n, Hkv, 8)[i])
+    untouched = np.setdiff1d(np.arange(slots), sl.numpy())
+    assert np.array_equal(pools["v_pool"][untouched], before["v_pool"][untouched])
+    assert len(last) < n                                  # collisions happened
