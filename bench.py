@@ -3,7 +3,7 @@
 One step = one qsa_decode call over one batch (every selected K/V row
 gathered, QK, softmax, PV, split merge). Prints one JSON line.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--fmt bf16|fp8_e4m3|int8|int4|int8_g64|int4_g32]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--fmt bf16|fp8_e4m3|int8|int4|int8_g64|int4_g32|int8ring_int4]
                   [--impl native|reference]
 
 --impl reference times the FP64 CPU oracle on the host cores on a bounded
@@ -45,6 +45,49 @@ def algorithmic_bytes(fmt: str, bs: int = BS, length: int = L, hq: int = HQ) -> 
     cu = (bs + 1) * 4
     extra = 8 if fmt == "fp8_e4m3" else 0
     return kv + idx + q + out + cu + extra
+
+
+TIER_HOT_SHARE = 0.25   # share of each selection drawn from slots that own their ring row
+
+
+def tiered_bytes(work) -> int:
+    """Bytes one tiered call must move: per selected (id, KV head) the owner entry
+    (4 B) and, for K and V, the ring row with its 4 binary16 scales (264 B) when the
+    slot owns its ring position, else the int4_g32 row with its 8 scales (144 B);
+    plus slot ids, q, out and cu_seqlens."""
+    sel = work.sel.long()
+    owner = work.extra["owner"].long()
+    hot = int((owner[sel & (owner.numel() - 1)] == sel).sum())
+    n = sel.numel()
+    hkv = work.num_kv_heads
+    kv = hkv * (hot * 2 * 264 + (n - hot) * 2 * 144 + n * 4)
+    return kv + n * 4 + 2 * work.bs * work.num_q_heads * 512 + (work.bs + 1) * 4
+
+
+def oracle_decode(w, threads: int = 0):
+    import oracle
+
+    if w.fmt == I.TIERED:
+        t = w.extra
+        return oracle.decode_tiered(w.q, w.k_pool, w.v_pool, w.sel, w.cu, w.softmax_scale,
+                                    w.k_scale, w.v_scale, t["k_ring"], t["v_ring"],
+                                    t["k_ring_scale"], t["v_ring_scale"], t["owner"],
+                                    threads=threads)
+    return oracle.decode(w.q, w.k_pool, w.v_pool, w.fmt, w.sel, w.cu, w.softmax_scale,
+                         w.k_scale, w.v_scale, threads=threads)
+
+
+def make_workloads(fmt: str, seed: int, index_seeds, device, bs: int = BS, num_slots: int = SLOTS):
+    """The saturated config's workloads (one pool, several index sets) for a format."""
+    if fmt == I.TIERED:
+        ring = min(I.RING_SLOTS, num_slots)
+        pools = I.make_tiered_pools(num_slots, HKV, ring, seed, device=device)
+        return [I.tiered(seed=s, device=device, bs=bs, num_slots=num_slots, ring_slots=ring,
+                         lengths=[L] * bs, hot_share=TIER_HOT_SHARE, pools=pools)
+                for s in index_seeds]
+    pools = I.make_pools(num_slots, HKV, fmt, seed=seed, device=device)
+    return [I.tp1_saturated(seed=seed, device=device, fmt=fmt, bs=bs, index_seed=s, pools=pools)
+            for s in index_seeds]
 
 
 def dist_env():
@@ -143,16 +186,15 @@ class ClockSampler:
                 "samples": len(self.samples)}
 
 
-def cpu_baseline(fmt: str, sample_rows: int, work, threads: int = 0):
+def cpu_baseline(fmt: str, sample_rows: int, work, threads: int = 0, call_bytes: int = 0):
     """Time the FP64 oracle on `sample_rows` sequences of the workload; returns a dict."""
     import oracle
 
     sub = I.host_subset(work, list(range(sample_rows)))
     t0 = time.perf_counter()
-    oracle.decode(sub.q, sub.k_pool, sub.v_pool, fmt, sub.sel, sub.cu, sub.softmax_scale,
-                  sub.k_scale, sub.v_scale, threads=threads)
+    oracle_decode(sub, threads=threads)
     dt = time.perf_counter() - t0
-    b = algorithmic_bytes(fmt, bs=sample_rows)
+    b = (call_bytes or algorithmic_bytes(fmt)) * sample_rows // BS
     return {"value": b / dt / 1e9, "unit": "GB/s", "cores": oracle.max_threads(),
             "kind": "oracle", "calls_per_s": (sample_rows / BS) / dt,
             "sample": f"{sample_rows} of {BS} sequences (L={L}, 24Q/2KV), {dt:.2f} s, "
@@ -169,16 +211,16 @@ def run_reference(args):
     gen_dev = "cpu"
     rows = args.ref_rows
     # host-only generation of exactly the sampled sequences' data
-    w = I.tp1_saturated(seed=2, device=gen_dev, fmt=args.fmt, bs=rows, num_slots=SLOTS // 8)
+    w = make_workloads(args.fmt, 2, [2], gen_dev, bs=rows, num_slots=SLOTS // 8)[0]
     times = []
     for i in range(args.warmup + args.steps):
         t0 = time.perf_counter()
-        oracle.decode(w.q, w.k_pool, w.v_pool, args.fmt, w.sel, w.cu, w.softmax_scale,
-                      w.k_scale, w.v_scale)
+        oracle_decode(w)
         if i >= args.warmup:
             times.append(time.perf_counter() - t0)
     dt = sum(times) / len(times)
-    gbs = algorithmic_bytes(args.fmt, bs=rows) / dt / 1e9
+    b = tiered_bytes(w) if args.fmt == I.TIERED else algorithmic_bytes(args.fmt, bs=rows)
+    gbs = b / dt / 1e9
     calls = (rows / BS) / dt
     line = {
         "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": ws,
@@ -206,13 +248,12 @@ def run_native(args):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     fmt = args.fmt
-    pools = I.make_pools(SLOTS, HKV, fmt, seed=2 + rank, device=dev)
-    works = [I.tp1_saturated(seed=2 + rank, device=dev, fmt=fmt, index_seed=100 + 7 * rank + k,
-                             pools=pools) for k in range(args.index_sets)]
+    works = make_workloads(fmt, 2 + rank, [100 + 7 * rank + k for k in range(args.index_sets)], dev)
     w0 = works[0]
     out = torch.empty_like(w0.q)
     scratch = qsa.alloc_scratch(BS, HQ, L, dev)
-    meta = qsa.KVQuantMeta(fmt, L, w0.k_scale, w0.v_scale, w0.softmax_scale)
+    tier = {k: w0.extra[k] for k in I.TIER_KEYS} if fmt == I.TIERED else None
+    meta = qsa.KVQuantMeta(fmt, L, w0.k_scale, w0.v_scale, w0.softmax_scale, 0, tier)
     stream = torch.cuda.current_stream()
     grid = qsa.qsa_decode_grid(BS, HQ, L)
 
@@ -274,7 +315,10 @@ def run_native(args):
 
     step_ms = total_ms / args.steps
     step_ms, e2e_ms = reduce_max([step_ms, e2e_ms if e2e_steps else 0.0], dev)
-    abytes = algorithmic_bytes(fmt)
+    if fmt == I.TIERED:  # the bytes depend on which rows are hot: the mean over the index sets
+        abytes = sum(tiered_bytes(w) for w in works) // len(works)
+    else:
+        abytes = algorithmic_bytes(fmt)
     value = whole_job_gbs(ws, abytes, step_ms)
     e2e_val = whole_job_gbs(ws, abytes, e2e_ms) if e2e_steps else None
     kernel_ms = sum(per) / len(per)
@@ -287,7 +331,7 @@ def run_native(args):
         import oracle
 
         oracle.build()
-        cpu = cpu_baseline(fmt, args.cpu_rows, works[0])
+        cpu = cpu_baseline(fmt, args.cpu_rows, works[0], call_bytes=abytes)
 
     if rank == 0:
         traffic = measured_traffic(fmt)
@@ -297,7 +341,9 @@ def run_native(args):
             "scaling": "weak", "vs_baseline": None, "dtype": fmt, "data": "synthetic",
             "calls_per_s": calls, "tokens_per_s": calls * BS * L,
             "pct_of_hbm_peak": 100.0 * achieved / peak,
-            "config": {"workload": f"packed QSA decode bs={BS} L={L} 24Q/2KV D=256 {fmt} pool",
+            "config": {"workload": f"packed QSA decode bs={BS} L={L} 24Q/2KV D=256 {fmt} pool"
+                                   + (f" (ring {I.RING_SLOTS}, {TIER_HOT_SHARE:.0%} of ids hot)"
+                                      if fmt == I.TIERED else ""),
                        "pool_slots": SLOTS, "index_sets": args.index_sets, "grid_ctas": grid,
                        "l2": "inputs larger than L2: 538 MB of K/V rows per call from a 2 GiB "
                              "pool, rotating index sets",
@@ -320,10 +366,14 @@ def run_native(args):
 KVW_TOKENS = 131072  # one prefill chunk: 128 sequences x 1024 new tokens
 
 
-def kv_write_bytes(fmt: str, n: int = KVW_TOKENS, hkv: int = HKV) -> int:
+def kv_write_bytes(fmt: str, n: int = KVW_TOKENS, hkv: int = HKV, ring_rows: int = 0) -> int:
     """Bytes one qsa_kv_write call must move: the new bf16 K and V rows, the slot
-    ids, the written codes and (int8/int4) the written per-row scales."""
+    ids, the written codes and (int8/int4) the written per-row scales. Tiered: the
+    int4_g32 rows of every token, plus for each ring position the write claims
+    (`ring_rows` of them) its int8_g64 rows with scales and its owner entry."""
     read = 2 * n * hkv * 512 + n * 4 + (8 if fmt == "fp8_e4m3" else 0)
+    if fmt == I.TIERED:
+        return read + 2 * n * hkv * (128 + 16) + ring_rows * (2 * hkv * (256 + 8) + 4)
     write = 2 * n * hkv * (ROW_BYTES[fmt] + SCALE_BYTES[fmt])
     return read + write
 
@@ -335,7 +385,11 @@ def run_kv_write(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     fmt = args.fmt
-    kc, vc, ks, vs = I.make_pools(SLOTS, HKV, fmt, seed=2, device=dev)
+    tier = None
+    if fmt == I.TIERED:
+        kc, vc, ks, vs, tier = I.make_tiered_pools(SLOTS, HKV, I.RING_SLOTS, 2, device=dev)
+    else:
+        kc, vc, ks, vs = I.make_pools(SLOTS, HKV, fmt, seed=2, device=dev)
     g = torch.Generator(device=dev).manual_seed(7)
     xs = [torch.randn(KVW_TOKENS, HKV, 256, generator=g, device=dev).to(torch.bfloat16)
           for _ in range(4)]
@@ -345,7 +399,12 @@ def run_kv_write(args):
     stream = torch.cuda.current_stream()
 
     def step(k):
-        qsa.qsa_kv_write(fmt, xs[k % 4], xs[(k + 1) % 4], slots[k % 2], kc, vc, ks, vs, err, stream)
+        if tier is not None:
+            qsa.qsa_kv_write_tiered(xs[k % 4], xs[(k + 1) % 4], slots[k % 2], kc, vc, ks, vs, tier,
+                                    err, stream)
+        else:
+            qsa.qsa_kv_write(fmt, xs[k % 4], xs[(k + 1) % 4], slots[k % 2], kc, vc, ks, vs, err,
+                             stream)
 
     for k in range(args.warmup):
         step(k)
@@ -360,7 +419,10 @@ def run_kv_write(args):
     if int(err.item()):
         raise RuntimeError("device error flag set")
     ms = e0.elapsed_time(e1) / args.steps
-    b = kv_write_bytes(fmt)
+    ring_rows = 0
+    if tier is not None:  # ring positions each write claims (the same two slot sets alternate)
+        ring_rows = sum(int(torch.unique(sl.long() & (I.RING_SLOTS - 1)).numel()) for sl in slots) // 2
+    b = kv_write_bytes(fmt, ring_rows=ring_rows)
     gbs = b / (ms * 1e-3) / 1e9
     peak, kind = measured_peaks()
     print(json.dumps({
@@ -369,7 +431,8 @@ def run_kv_write(args):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "dtype": fmt,
         "data": "synthetic", "tokens_per_s": KVW_TOKENS / (ms * 1e-3),
         "config": {"workload": f"kv write of {KVW_TOKENS} tokens x 2 KV heads into a "
-                               f"{SLOTS}-slot {fmt} pool, random distinct slots"},
+                               f"{SLOTS}-slot {fmt} pool, random distinct slots"
+                               + (f", {I.RING_SLOTS}-row ring" if tier is not None else "")},
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
                      "frac": gbs / peak, "peak_source": f"{kind} hbm_gbs", "bytes_per_launch": b},
         "gpu_launches": args.steps, "clocks": clk.summary()}), flush=True)
@@ -380,7 +443,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--fmt", default="bf16", choices=list(I.FORMATS))
+    ap.add_argument("--fmt", default="bf16", choices=list(I.FORMATS) + [I.TIERED])
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--op", default="decode", choices=["decode", "kv_write"],
                     help="decode (the headline) or the quantising KV write")

@@ -61,9 +61,11 @@ enum {
                             in the low nibble, fp32 scale per (slot, KV head) */
     QSA_KV_INT8_G64 = 4, /* [slots, Hkv, 256] int8, binary16 scale per (slot, KV head,
                             64-channel group): [slots, Hkv, 4]; group 0 = the rotary dims */
-    QSA_KV_INT4_G32 = 5  /* [slots, Hkv, 128] uint8: offset-binary nibbles (code + 8,
+    QSA_KV_INT4_G32 = 5, /* [slots, Hkv, 128] uint8: offset-binary nibbles (code + 8,
                             code in [-7, 7]), channel 2i in the low nibble, binary16 scale
                             per (slot, KV head, 32-channel group): [slots, Hkv, 8] */
+    QSA_KV_INT8RING_INT4 = 6 /* tiered: the pools and scales are the int4_g32 rows of every
+                                slot; qsa_kv_quant_meta.tier holds the int8_g64 ring */
 };
 
 /* Return codes. Nothing is enqueued when a call returns an error. */
@@ -97,6 +99,20 @@ typedef struct {
     int64_t stride[4];
 } qsa_tensor;
 
+/* The hot tier of a QSA_KV_INT8RING_INT4 pool (sglang PR #37798, "Modifications",
+ * the tiered KV pool module): a ring of R int8_g64 rows with an owner table. Row
+ * (slot, g) is read from ring row (slot & (R - 1), g) when owner[slot & (R - 1)]
+ * == slot (hot), else from the int4_g32 pool (cold). Every token is written to
+ * both (qsa_kv_write_tiered). The caller owns all of it; sizes are not checked. */
+typedef struct {
+    void* k_ring;       /* int8 [R, Hkv, 256] contiguous, 16-byte aligned */
+    void* v_ring;
+    void* k_ring_scale; /* binary16 [R, Hkv, 4] (per 64-channel group), 8-byte aligned */
+    void* v_ring_scale;
+    int32_t* owner;     /* int32 [R]: the slot whose row a ring position holds; -1: none */
+    int32_t ring_slots; /* R: a power of two, 1 .. 2^30 */
+} qsa_kv_tier;
+
 /* Pool format and softmax parameters of one call. */
 typedef struct {
     int32_t format;       /* QSA_KV_* */
@@ -108,6 +124,8 @@ typedef struct {
     float softmax_scale;  /* finite; 1/16 = 1/sqrt(256) for the pages' model */
     int32_t max_ctas;     /* 0: library chooses the grid; > 0: cap on CTAs (e.g. 1 forces
                              one CTA to do all the work, which tests the no-split path) */
+    const qsa_kv_tier* tier; /* QSA_KV_INT8RING_INT4: the hot ring (host struct, read at
+                                the call); other formats: ignored, may be NULL */
 } qsa_kv_quant_meta;
 
 /*
@@ -169,6 +187,23 @@ int qsa_decode(const qsa_tensor* q, const qsa_tensor* k_pool, const qsa_tensor* 
 int qsa_kv_write(int32_t format, const qsa_tensor* k_new, const qsa_tensor* v_new,
                  const qsa_tensor* slots, const qsa_tensor* k_pool, const qsa_tensor* v_pool,
                  void* k_scale, void* v_scale, int32_t* device_error, void* stream);
+
+/*
+ * qsa_kv_write_tiered -- the write of a QSA_KV_INT8RING_INT4 pool: every token i is
+ * written twice, as the int4_g32 row of slot[i] (k_pool / v_pool, binary16 scales
+ * k_scale / v_scale [num_slots * Hkv * 8], 16-byte aligned) and as the int8_g64 row
+ * of ring position p = slot[i] & (R - 1), whose owner entry becomes slot[i]. When
+ * several tokens of one call share a ring position, the last of them (largest i)
+ * owns it, as if the tokens were written in order; owner and ring row always agree.
+ * Arguments otherwise as for qsa_kv_write. Enqueues two kernels on `stream` (claim
+ * the ring positions, then write); allocates nothing. Between the two, the owner
+ * entries of the positions being written hold claim marks (negative values); a
+ * decode ordered after the call sees the final owners.
+ */
+int qsa_kv_write_tiered(const qsa_tensor* k_new, const qsa_tensor* v_new, const qsa_tensor* slots,
+                        const qsa_tensor* k_pool, const qsa_tensor* v_pool, void* k_scale,
+                        void* v_scale, const qsa_kv_tier* tier, int32_t* device_error,
+                        void* stream);
 
 /* Scratch bytes a qsa_decode call with these sizes needs on the current
  * device (0 when the sizes are outside the contract). Split-KV partials take

@@ -13,6 +13,7 @@ from .binding import (  # noqa: F401
     qsa_decode_scratch_bytes,
     qsa_decode_scratch_layout,
     qsa_kv_write,
+    qsa_kv_write_tiered,
     qsa_scratch_error,
     qsa_scratch_init,
     version,
@@ -20,6 +21,6 @@ from .binding import (  # noqa: F401
 
 __all__ = [
     "KVQuantMeta", "QsaError", "alloc_scratch", "qsa_decode", "qsa_decode_grid",
-    "qsa_decode_scratch_bytes", "qsa_decode_scratch_layout", "qsa_kv_write", "qsa_scratch_error",
+    "qsa_decode_scratch_bytes", "qsa_decode_scratch_layout", "qsa_kv_write", "qsa_kv_write_tiered", "qsa_scratch_error",
     "qsa_scratch_init", "version",
 ]

@@ -19,7 +19,8 @@ LIB_PATH = os.path.join(_PKG, "libqsa.so")
 
 # include/qsa.h enums
 DTYPE_BF16, DTYPE_UINT8, DTYPE_INT8, DTYPE_INT32, DTYPE_FLOAT32 = 1, 2, 3, 4, 5
-KV_FORMATS = {"bf16": 0, "fp8_e4m3": 1, "int8": 2, "int4": 3, "int8_g64": 4, "int4_g32": 5}
+KV_FORMATS = {"bf16": 0, "fp8_e4m3": 1, "int8": 2, "int4": 3, "int8_g64": 4, "int4_g32": 5,
+              "int8ring_int4": 6}
 OK, ERR_INVALID_ARGUMENT, ERR_UNSUPPORTED, ERR_SCRATCH_TOO_SMALL, ERR_MISALIGNED, ERR_CUDA = (
     0, -1, -2, -3, -4, -5)
 DEVERR_SLOT_RANGE, DEVERR_CU_SEQLENS, DEVERR_TIMEOUT = 1, 2, 4
@@ -35,7 +36,7 @@ _TORCH_DTYPES = {
 EXPORTED = (
     "qsa_decode", "qsa_decode_scratch_bytes", "qsa_decode_grid", "qsa_decode_scratch_layout",
     "qsa_scratch_init", "qsa_scratch_error", "qsa_strerror", "qsa_last_error_message",
-    "qsa_version", "qsa_decode_static_scratch", "qsa_kv_write",
+    "qsa_version", "qsa_decode_static_scratch", "qsa_kv_write", "qsa_kv_write_tiered",
 )
 
 
@@ -44,10 +45,27 @@ class QsaTensor(ctypes.Structure):
                 ("shape", ctypes.c_int64 * 4), ("stride", ctypes.c_int64 * 4)]
 
 
+class QsaKvTier(ctypes.Structure):
+    _fields_ = [("k_ring", ctypes.c_void_p), ("v_ring", ctypes.c_void_p),
+                ("k_ring_scale", ctypes.c_void_p), ("v_ring_scale", ctypes.c_void_p),
+                ("owner", ctypes.c_void_p), ("ring_slots", ctypes.c_int32)]
+
+
 class QsaKvQuantMeta(ctypes.Structure):
     _fields_ = [("format", ctypes.c_int32), ("capacity", ctypes.c_int32),
                 ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
-                ("softmax_scale", ctypes.c_float), ("max_ctas", ctypes.c_int32)]
+                ("softmax_scale", ctypes.c_float), ("max_ctas", ctypes.c_int32),
+                ("tier", ctypes.POINTER(QsaKvTier))]
+
+
+def tier_struct(tier: dict) -> QsaKvTier:
+    """qsa_kv_tier from a dict of device tensors (k_ring, v_ring, k_ring_scale,
+    v_ring_scale, owner); the ring size is owner's length."""
+    t = QsaKvTier()
+    for key in ("k_ring", "v_ring", "k_ring_scale", "v_ring_scale", "owner"):
+        setattr(t, key, tier[key].data_ptr())
+    t.ring_slots = int(tier["owner"].numel())
+    return t
 
 
 class QsaScratchLayout(ctypes.Structure):
@@ -87,6 +105,10 @@ def load() -> ctypes.CDLL:
     lib.qsa_kv_write.argtypes = [ctypes.c_int32, P(QsaTensor), P(QsaTensor), P(QsaTensor),
                                  P(QsaTensor), P(QsaTensor), ctypes.c_void_p, ctypes.c_void_p,
                                  ctypes.c_void_p, ctypes.c_void_p]
+    lib.qsa_kv_write_tiered.restype = ctypes.c_int
+    lib.qsa_kv_write_tiered.argtypes = [P(QsaTensor), P(QsaTensor), P(QsaTensor), P(QsaTensor),
+                                        P(QsaTensor), ctypes.c_void_p, ctypes.c_void_p, P(QsaKvTier),
+                                        ctypes.c_void_p, ctypes.c_void_p]
     lib.qsa_decode_scratch_bytes.restype = ctypes.c_size_t
     lib.qsa_decode_scratch_bytes.argtypes = [ctypes.c_int32] * 3
     lib.qsa_decode_grid.restype = ctypes.c_int32
@@ -140,9 +162,13 @@ class KVQuantMeta:
     v_scale: Optional[torch.Tensor] = None
     softmax_scale: float = 1.0 / 16.0
     max_ctas: int = 0
+    tier: Optional[dict] = None   # int8ring_int4: k_ring, v_ring, k_ring_scale, v_ring_scale, owner
 
     def to_c(self) -> QsaKvQuantMeta:
         m = QsaKvQuantMeta()
+        if self.tier is not None:
+            m._tier = tier_struct(self.tier)      # kept alive with the struct
+            m.tier = ctypes.pointer(m._tier)
         m.format = KV_FORMATS[self.format]
         m.capacity = int(self.capacity)
         m.k_scale = self.k_scale.data_ptr() if self.k_scale is not None else None
@@ -183,6 +209,18 @@ def qsa_kv_write(fmt: str, k_new, v_new, slots, k_pool, v_pool, k_scale=None, v_
     ptr = lambda t: t.data_ptr() if t is not None else None
     rc = lib.qsa_kv_write(KV_FORMATS[fmt], *(ctypes.byref(x) for x in d), ptr(k_scale),
                           ptr(v_scale), ptr(error_word), _stream_handle(stream))
+    _check(rc)
+
+
+def qsa_kv_write_tiered(k_new, v_new, slots, k_pool, v_pool, k_scale, v_scale, tier: dict,
+                        error_word=None, stream=None) -> None:
+    """Enqueue the two-kernel write of a tiered int8ring_int4 pool (see include/qsa.h)."""
+    lib = load()
+    d = [describe(t) for t in (k_new, v_new, slots, k_pool, v_pool)]
+    ts = tier_struct(tier)
+    ptr = lambda t: t.data_ptr() if t is not None else None
+    rc = lib.qsa_kv_write_tiered(*(ctypes.byref(x) for x in d), ptr(k_scale), ptr(v_scale),
+                                 ctypes.byref(ts), ptr(error_word), _stream_handle(stream))
     _check(rc)
 
 

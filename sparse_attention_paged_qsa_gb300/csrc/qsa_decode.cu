@@ -88,37 +88,51 @@ static_assert(PART_BYTES >= (GROUP * D + 2 * GROUP) * 4, "partial slot size");
 // channel group) when GROUPS > 0); QK_F16: QK runs on f16 operands (exact
 // integer / e4m3 codes, Q rescaled per head by a power of two); PV_F16: PV runs
 // on f16 operands (only when no per-slot scale enters P); NIB4: 4-bit codes,
-// NIB_OFFSET: stored as code + 8 (else two's complement).
+// NIB_OFFSET: stored as code + 8 (else two's complement); TIER: each row is an
+// int8_g64 ring row or an int4_g32 pool row, by the owner table (scales held at
+// the 32-channel granularity, a ring row's 64-channel scales expanded).
 template <int FMT> struct Traits;
 template <> struct Traits<QSA_KV_BF16> {
     static constexpr int ROWB = 512, STAGES = 3, GROUPS = 0;
     static constexpr bool DEQ = false, SCALES = false, QK_F16 = false, PV_F16 = false;
     static constexpr bool NIB4 = false, NIB_OFFSET = false;
+    static constexpr bool TIER = false;
 };
 template <> struct Traits<QSA_KV_FP8_E4M3> {
     static constexpr int ROWB = 256, STAGES = 4, GROUPS = 0;
     static constexpr bool DEQ = true, SCALES = false, QK_F16 = true, PV_F16 = true;
     static constexpr bool NIB4 = false, NIB_OFFSET = false;
+    static constexpr bool TIER = false;
 };
 template <> struct Traits<QSA_KV_INT8> {
     static constexpr int ROWB = 256, STAGES = 4, GROUPS = 0;
     static constexpr bool DEQ = true, SCALES = true, QK_F16 = true, PV_F16 = false;
     static constexpr bool NIB4 = false, NIB_OFFSET = false;
+    static constexpr bool TIER = false;
 };
 template <> struct Traits<QSA_KV_INT4> {
     static constexpr int ROWB = 128, STAGES = 6, GROUPS = 0;
     static constexpr bool DEQ = true, SCALES = true, QK_F16 = true, PV_F16 = false;
     static constexpr bool NIB4 = true, NIB_OFFSET = false;
+    static constexpr bool TIER = false;
 };
 template <> struct Traits<QSA_KV_INT8_G64> {
     static constexpr int ROWB = 256, STAGES = 3, GROUPS = 4;
     static constexpr bool DEQ = true, SCALES = true, QK_F16 = true, PV_F16 = false;
     static constexpr bool NIB4 = false, NIB_OFFSET = false;
+    static constexpr bool TIER = false;
 };
 template <> struct Traits<QSA_KV_INT4_G32> {
     static constexpr int ROWB = 128, STAGES = 6, GROUPS = 8;
     static constexpr bool DEQ = true, SCALES = true, QK_F16 = true, PV_F16 = false;
     static constexpr bool NIB4 = true, NIB_OFFSET = true;
+    static constexpr bool TIER = false;
+};
+template <> struct Traits<QSA_KV_INT8RING_INT4> {
+    static constexpr int ROWB = 256, STAGES = 3, GROUPS = 8;
+    static constexpr bool DEQ = true, SCALES = true, QK_F16 = true, PV_F16 = false;
+    static constexpr bool NIB4 = false, NIB_OFFSET = true;
+    static constexpr bool TIER = true;
 };
 
 template <int FMT> struct Layout {
@@ -126,7 +140,8 @@ template <int FMT> struct Layout {
     static constexpr int STAGE_KV = T * Tr::ROWB;
     static constexpr int SC_TOK = Tr::GROUPS ? Tr::GROUPS * 2 : 4; // scale bytes per token
     static constexpr int STAGE_SC = Tr::SCALES ? 2 * T * SC_TOK : 0;
-    static constexpr int STAGE_BYTES = 2 * STAGE_KV + STAGE_SC;
+    static constexpr int STAGE_FLAGS = Tr::TIER ? T * 4 : 0;    // per token: 1 = ring row
+    static constexpr int STAGE_BYTES = 2 * STAGE_KV + STAGE_SC + STAGE_FLAGS;
     static constexpr int PF = Tr::STAGES;       // slot-id prefetch distance (stages)
     static constexpr int R = PF + 1;            // slot-id ring entries
     static constexpr int off_stage = 0;
@@ -172,6 +187,13 @@ struct Params {
     uint8_t* part;
     int bs, Hkv, capacity;
     float scale_log2; // softmax_scale * log2(e)
+    // tiered pools: int8_g64 ring rows [R, Hkv, 256], binary16 scales [R, Hkv, 4], owner [R]
+    const uint8_t* kring;
+    const uint8_t* vring;
+    const void* kring_scale;
+    const void* vring_scale;
+    const int* owner;
+    int ring_mask; // R - 1
 };
 
 // Byte offset of 16-byte chunk `chunk` of row `row` in a swizzled row buffer.
@@ -693,7 +715,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
             if (!mbar_wait(empty_bar(s), ((i / Tr::STAGES) & 1) ^ 1, p.err, abort_flag)) break;
             uint8_t* const Ks = stage0 + s * Ly::STAGE_BYTES;
             uint8_t* const Vs = Ks + Ly::STAGE_KV;
-            long long myrow = 0;
+            long long myrow = 0, myring = 0;
+            bool myhot = false;
             const bool valid = lane < TPP && mytok < n;
             if (valid) {
                 int slot = ring[(i % Ly::R) * T + mytok];
@@ -702,12 +725,33 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
                     slot = 0;
                 }
                 myrow = (long long)slot * Hkv + g;
+                if constexpr (Tr::TIER) { // hot: the ring position holds this slot's row
+                    const int pos = slot & p.ring_mask;
+                    myhot = __ldg(p.owner + pos) == slot;
+                    myring = (long long)pos * Hkv + g;
+                }
             }
 #pragma unroll
             for (int t0 = 0; t0 < TPP; t0 += RPI) {
                 const int tl = t0 + toff;
                 const long long row = __shfl_sync(0xFFFFFFFFu, myrow, tl);
                 const int t = pw * TPP + tl;
+                if constexpr (Tr::TIER) {
+                    const long long rrow = __shfl_sync(0xFFFFFFFFu, myring, tl);
+                    const bool hot = __shfl_sync(0xFFFFFFFFu, myhot, tl);
+                    if (t < n) {
+                        if (hot) { // 256-byte int8 ring row
+                            cp_async16(smem_u32(Ks + swz<Tr::ROWB>(t, chunk)), p.kring + rrow * 256 + chunk * 16);
+                            cp_async16(smem_u32(Vs + swz<Tr::ROWB>(t, chunk)), p.vring + rrow * 256 + chunk * 16);
+                        } else if (chunk < 8) { // 128-byte int4 pool row
+                            cp_async16(smem_u32(Ks + swz<Tr::ROWB>(t, chunk)), p.kpool + row * 128 + chunk * 16);
+                            cp_async16(smem_u32(Vs + swz<Tr::ROWB>(t, chunk)), p.vpool + row * 128 + chunk * 16);
+                        }
+                    } else {
+                        *reinterpret_cast<uint4*>(Vs + swz<Tr::ROWB>(t, chunk)) = make_uint4(0, 0, 0, 0);
+                    }
+                    continue;
+                }
                 if (t < n) {
                     cp_async16(smem_u32(Ks + swz<Tr::ROWB>(t, chunk)),
                                p.kpool + row * Tr::ROWB + chunk * 16);
@@ -724,7 +768,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
                 const uint32_t vs = ks + T * Ly::SC_TOK;
                 const uint8_t* kg = static_cast<const uint8_t*>(p.k_scale) + myrow * Ly::SC_TOK;
                 const uint8_t* vg = static_cast<const uint8_t*>(p.v_scale) + myrow * Ly::SC_TOK;
-                if (valid) {
+                if constexpr (Tr::TIER) {
+                    if (lane < TPP)
+                        reinterpret_cast<int*>(Vs + Ly::STAGE_KV + Ly::STAGE_SC)[mytok] = valid && myhot;
+                }
+                if (Tr::TIER && valid && myhot) { // 4 binary16 scales of the ring row
+                    cp_async8(ks, static_cast<const uint8_t*>(p.kring_scale) + myring * 8);
+                    cp_async8(vs, static_cast<const uint8_t*>(p.vring_scale) + myring * 8);
+                } else if (valid) {
                     if constexpr (Ly::SC_TOK == 4) {
                         cp_async4(ks, kg);
                         cp_async4(vs, vg);
@@ -858,7 +909,50 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
             uint8_t* const vbf = kbf + T * BF_ROW;
             const int tt = lane & 7, ch = lane >> 3;
             const int t = tok_base + tt;
-            if constexpr (Tr::NIB4) {
+            if constexpr (Tr::TIER) {
+                const int* flag = reinterpret_cast<const int*>(Vs + Ly::STAGE_KV + Ly::STAGE_SC);
+                // K: this warp's 8 tokens, each by its tier
+                if (flag[t]) {
+#pragma unroll
+                    for (int it = 0; it < 4; ++it) {
+                        const int rc = ch + 4 * it;
+                        const uint4 raw = *reinterpret_cast<const uint4*>(Ks + swz<Tr::ROWB>(t, rc));
+                        uint4 o0, o1;
+                        convert16<QSA_KV_INT8, Tr::QK_F16>(raw, o0, o1);
+                        *reinterpret_cast<uint4*>(kbf + swz<BF_ROW>(t, 2 * rc)) = o0;
+                        *reinterpret_cast<uint4*>(kbf + swz<BF_ROW>(t, 2 * rc + 1)) = o1;
+                    }
+                } else {
+#pragma unroll
+                    for (int it = 0; it < 2; ++it) {
+                        const int rc = ch + 4 * it;
+                        const uint4 raw = *reinterpret_cast<const uint4*>(Ks + swz<Tr::ROWB>(t, rc));
+                        uint4 ov[4];
+                        convert32_int4<Tr::QK_F16, true>(raw, ov);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            *reinterpret_cast<uint4*>(kbf + swz<BF_ROW>(t, 4 * rc + k)) = ov[k];
+                    }
+                }
+                // V: this warp's 32 dims of every token: two int8 chunks or one int4 chunk
+#pragma unroll
+                for (int it = 0; it < 2; ++it) {
+                    const int tv = lane + 32 * it;
+                    uint4 ov[4];
+                    if (flag[tv]) {
+                        convert16<QSA_KV_INT8, Tr::PV_F16>(
+                            *reinterpret_cast<const uint4*>(Vs + swz<Tr::ROWB>(tv, 2 * warp)), ov[0], ov[1]);
+                        convert16<QSA_KV_INT8, Tr::PV_F16>(
+                            *reinterpret_cast<const uint4*>(Vs + swz<Tr::ROWB>(tv, 2 * warp + 1)), ov[2], ov[3]);
+                    } else {
+                        convert32_int4<Tr::PV_F16, true>(
+                            *reinterpret_cast<const uint4*>(Vs + swz<Tr::ROWB>(tv, warp)), ov);
+                    }
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        *reinterpret_cast<uint4*>(vbf + swz<BF_ROW>(tv, 4 * warp + k)) = ov[k];
+                }
+            } else if constexpr (Tr::NIB4) {
                 // K: this warp's 8 tokens; 8 raw chunks per row, 32 values each
 #pragma unroll
                 for (int it = 0; it < 2; ++it) {
@@ -921,8 +1015,24 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
                 }
                 const __half* sv = reinterpret_cast<const __half*>(Vs + Ly::STAGE_KV + T * Ly::SC_TOK);
                 const int gv = warp * G / NW;
-                svw[0] = __half2float(sv[(2 * lane) * G + gv]);
-                svw[1] = __half2float(sv[(2 * lane + 1) * G + gv]);
+                if constexpr (Tr::TIER) {
+                    // a ring row holds 4 scales of 64 channels: 32-channel group k reads k / 2
+                    const int* flag = reinterpret_cast<const int*>(Vs + Ly::STAGE_KV + Ly::STAGE_SC);
+#pragma unroll
+                    for (int u = 0; u < 2; ++u)
+                        if (flag[tk0 + u]) {
+                            const uint32_t e0 = ksw[u][0], e1 = ksw[u][1];
+                            ksw[u][0] = __byte_perm(e0, 0, 0x1010);
+                            ksw[u][1] = __byte_perm(e0, 0, 0x3232);
+                            ksw[u][2] = __byte_perm(e1, 0, 0x1010);
+                            ksw[u][3] = __byte_perm(e1, 0, 0x3232);
+                        }
+                    svw[0] = __half2float(sv[(2 * lane) * G + (flag[2 * lane] ? gv >> 1 : gv)]);
+                    svw[1] = __half2float(sv[(2 * lane + 1) * G + (flag[2 * lane + 1] ? gv >> 1 : gv)]);
+                } else {
+                    svw[0] = __half2float(sv[(2 * lane) * G + gv]);
+                    svw[1] = __half2float(sv[(2 * lane + 1) * G + gv]);
+                }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(empty_bar(s));
@@ -1317,7 +1427,7 @@ int fail(int code, const char* fmt, ...) {
 
 struct DeviceState {
     int sms = 0;
-    bool smem_set[QSA_KV_INT4_G32 + 1] = {};
+    bool smem_set[QSA_KV_INT8RING_INT4 + 1] = {};
 };
 
 std::mutex g_mu;
@@ -1484,7 +1594,7 @@ int qsa_decode(const qsa_tensor* q, const qsa_tensor* k_pool, const qsa_tensor* 
     if (!q || !k_pool || !v_pool || !meta || !sel || !cu || !out)
         return fail(QSA_ERR_INVALID_ARGUMENT, "a descriptor pointer is NULL");
     const int fmt = meta->format;
-    if (fmt < QSA_KV_BF16 || fmt > QSA_KV_INT4_G32)
+    if (fmt < QSA_KV_BF16 || fmt > QSA_KV_INT8RING_INT4)
         return fail(QSA_ERR_UNSUPPORTED, "unknown K/V pool format %d", fmt);
     if (q->ndim != 3) return fail(QSA_ERR_INVALID_ARGUMENT, "q must be [bs, Hq, 256]");
     const int64_t bs64 = q->shape[0], hq64 = q->shape[1];
@@ -1507,7 +1617,8 @@ int qsa_decode(const qsa_tensor* q, const qsa_tensor* k_pool, const qsa_tensor* 
     const int want_dtype = fmt == QSA_KV_BF16                              ? QSA_DTYPE_BF16
                            : (fmt == QSA_KV_INT8 || fmt == QSA_KV_INT8_G64) ? QSA_DTYPE_INT8
                                                                             : QSA_DTYPE_UINT8;
-    const int64_t row_elems = (fmt == QSA_KV_INT4 || fmt == QSA_KV_INT4_G32) ? D / 2 : D;
+    const int64_t row_elems =
+        (fmt == QSA_KV_INT4 || fmt == QSA_KV_INT4_G32 || fmt == QSA_KV_INT8RING_INT4) ? D / 2 : D;
     for (const qsa_tensor* pool : {k_pool, v_pool}) {
         const char* nm = pool == k_pool ? "k_pool" : "v_pool";
         if (pool->dtype != want_dtype)
@@ -1541,10 +1652,27 @@ int qsa_decode(const qsa_tensor* q, const qsa_tensor* k_pool, const qsa_tensor* 
         if (meta->k_scale == nullptr || meta->v_scale == nullptr)
             return fail(QSA_ERR_INVALID_ARGUMENT, "quantised pools need k_scale and v_scale");
         // grouped pools read a token's binary16 scales with one 8- or 16-byte copy
-        const uintptr_t al = fmt == QSA_KV_INT8_G64 ? 8 : fmt == QSA_KV_INT4_G32 ? 16 : 4;
+        const uintptr_t al = fmt == QSA_KV_INT8_G64                                  ? 8
+                             : (fmt == QSA_KV_INT4_G32 || fmt == QSA_KV_INT8RING_INT4) ? 16
+                                                                                       : 4;
         if ((reinterpret_cast<uintptr_t>(meta->k_scale) & (al - 1)) ||
             (reinterpret_cast<uintptr_t>(meta->v_scale) & (al - 1)))
             return fail(QSA_ERR_MISALIGNED, "scales must be %d-byte aligned for this format", (int)al);
+    }
+    const qsa_kv_tier* tier = meta->tier;
+    if (fmt == QSA_KV_INT8RING_INT4) {
+        if (tier == nullptr) return fail(QSA_ERR_INVALID_ARGUMENT, "the tiered format needs kv_quant_meta->tier");
+        const int R = tier->ring_slots;
+        if (R < 1 || R > (1 << 30) || (R & (R - 1)))
+            return fail(QSA_ERR_INVALID_ARGUMENT, "ring_slots %d is not a power of two in 1..2^30", R);
+        if (!tier->k_ring || !tier->v_ring || !tier->k_ring_scale || !tier->v_ring_scale || !tier->owner)
+            return fail(QSA_ERR_INVALID_ARGUMENT, "a tier pointer is NULL");
+        if (!aligned16(tier->k_ring) || !aligned16(tier->v_ring) ||
+            (reinterpret_cast<uintptr_t>(tier->k_ring_scale) & 7u) ||
+            (reinterpret_cast<uintptr_t>(tier->v_ring_scale) & 7u) ||
+            (reinterpret_cast<uintptr_t>(tier->owner) & 3u))
+            return fail(QSA_ERR_MISALIGNED,
+                        "ring rows must be 16-byte, ring scales 8-byte and owner 4-byte aligned");
     }
     if (scratch == nullptr) return fail(QSA_ERR_INVALID_ARGUMENT, "scratch is NULL");
     if (reinterpret_cast<uintptr_t>(scratch) & 255u)
@@ -1582,6 +1710,18 @@ int qsa_decode(const qsa_tensor* q, const qsa_tensor* k_pool, const qsa_tensor* 
     prm.Hkv = hkv;
     prm.capacity = meta->capacity;
     prm.scale_log2 = meta->softmax_scale * 1.4426950408889634f;
+    prm.kring = prm.vring = nullptr;
+    prm.kring_scale = prm.vring_scale = nullptr;
+    prm.owner = nullptr;
+    prm.ring_mask = 0;
+    if (fmt == QSA_KV_INT8RING_INT4) {
+        prm.kring = static_cast<const uint8_t*>(tier->k_ring);
+        prm.vring = static_cast<const uint8_t*>(tier->v_ring);
+        prm.kring_scale = tier->k_ring_scale;
+        prm.vring_scale = tier->v_ring_scale;
+        prm.owner = tier->owner;
+        prm.ring_mask = tier->ring_slots - 1;
+    }
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     switch (fmt) {
@@ -1590,7 +1730,8 @@ int qsa_decode(const qsa_tensor* q, const qsa_tensor* k_pool, const qsa_tensor* 
     case QSA_KV_INT8: rc = launch<QSA_KV_INT8>(prm, (int)grid, dev, st); break;
     case QSA_KV_INT4: rc = launch<QSA_KV_INT4>(prm, (int)grid, dev, st); break;
     case QSA_KV_INT8_G64: rc = launch<QSA_KV_INT8_G64>(prm, (int)grid, dev, st); break;
-    default: rc = launch<QSA_KV_INT4_G32>(prm, (int)grid, dev, st); break;
+    case QSA_KV_INT4_G32: rc = launch<QSA_KV_INT4_G32>(prm, (int)grid, dev, st); break;
+    default: rc = launch<QSA_KV_INT8RING_INT4>(prm, (int)grid, dev, st); break;
     }
     if (rc == QSA_OK) g_last_error.clear();
     return rc;

@@ -14,6 +14,10 @@
 //          per 64 / 32-channel group s16 = binary16(min(absmax / q, 65504)),
 //          q = 127 / 7, -> scale[row][group]; codes clamp(rint(x / s16), -q, q);
 //          int4_g32 stores offset-binary nibbles code + 8
+//   int8ring_int4 (the tiered KV pool module): the int4_g32 row of the slot, and
+//          the int8_g64 row of ring position slot & (R - 1) with owner = slot when
+//          the token owns that position (the last token of the write that maps
+//          there, claimed by a first kernel)
 // all in binary32 with IEEE division; an all-zero row gets s = 0 and zero codes.
 //
 // One warp per (token, head, K-or-V) row: a 16-byte load per lane covers the
@@ -52,6 +56,13 @@ struct Params {
     void* kscale; // fp32 (fp8: [1]; int8/int4: [slots * Hkv]) or binary16 [slots * Hkv * groups]
     void* vscale;
     int* err;
+    // tiered: int8_g64 ring rows [R, Hkv, 256], binary16 scales [R, Hkv, 4], owner [R]
+    uint8_t* kring;
+    uint8_t* vring;
+    __half* kring_scale;
+    __half* vring_scale;
+    int* owner;
+    int ring_mask;
 };
 
 // Two binary32 values -> two e4m3fn codes (lo in the low byte), nearest-even,
@@ -146,6 +157,48 @@ __device__ __forceinline__ void store_fp8(const Params& p, const uint4 raw, long
         make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
 }
 
+template <int FMT> __device__ __forceinline__ void codes_divide(const float x[8], float s, uint32_t z[8]);
+template <int FMT>
+__device__ __forceinline__ void codes_markstein(const float x[8], float s, float r, uint32_t z[8]);
+
+// One lane's 8 values of a grouped row (GFMT int8_g64 or int4_g32): the group's
+// absmax over its lanes, the binary16 scale, the codes; the group leaders store
+// the scales (one 8- / 16-byte block per row). tab: (s, s16) pairs per mantissa
+// then fl(1 / s16) per mantissa.
+template <int GFMT>
+__device__ __forceinline__ void store_grouped(const float x[8], const uint32_t* tab, uint8_t* codes,
+                                              __half* scales, int lane) {
+    constexpr int GS = GFMT == QSA_KV_INT8_G64 ? 64 : 32; // channels per scale
+    constexpr int LPG = GS / 8;                            // lanes per group
+    constexpr float qmax = GFMT == QSA_KV_INT8_G64 ? 127.0f : 7.0f;
+    float a = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) a = fmaxf(a, fabsf(x[k]));
+#pragma unroll
+    for (int off = 1; off < LPG; off <<= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, off));
+    // a = (1 + t / 128) * 2^E: fl(a / qmax) from the table, exponent moved by E
+    const uint32_t ab = __float_as_uint(a);
+    const int t = (ab >> 16) & 0x7F;
+    const uint32_t e = (ab & 0x7F800000u) - (127u << 23);
+    const float s32 = __uint_as_float(tab[2 * t] + e);
+    uint32_t z[8];
+    float sc;
+    if (a >= FAST_MIN_ABSMAX && s32 >= 0x1p-14f && s32 <= 65504.0f) { // uniform per group
+        sc = __uint_as_float(tab[2 * t + 1] + e);
+        codes_markstein<GFMT>(x, sc, __uint_as_float(tab[256 + t] - e), z);
+    } else {
+        sc = __half2float(__float2half_rn(fminf(__fdiv_rn(a, qmax), 65504.0f)));
+        codes_divide<GFMT>(x, sc, z);
+    }
+    const uint32_t b0 = low_bytes(z[0], z[1], z[2], z[3]);
+    const uint32_t b1 = low_bytes(z[4], z[5], z[6], z[7]);
+    if constexpr (GFMT == QSA_KV_INT8_G64)
+        reinterpret_cast<uint2*>(codes)[lane] = make_uint2(b0, b1);
+    else // offset binary: code + 8 is code ^ 8 on a two's-complement nibble
+        reinterpret_cast<uint32_t*>(codes)[lane] = (low_nibbles(b0) | (low_nibbles(b1) << 16)) ^ 0x88888888u;
+    if (lane % LPG == 0) scales[lane / LPG] = __float2half_rn(sc);
+}
+
 // Codes of one lane's 8 values, as low bytes of z (int8: -127..127, int4: -8..7).
 template <int FMT>
 __device__ __forceinline__ void codes_markstein(const float x[8], float s, float r, uint32_t z[8]) {
@@ -184,10 +237,12 @@ __device__ __forceinline__ void store_codes(const Params& p, long long row, bool
 template <int FMT> struct Converter {
     float k_lo, k_hi, v_lo, v_hi;     // fp8: 1 / pool scale times 1 -+ 2^-20 (or 1)
     const uint32_t* s_tab;            // int8/int4: s and 1 / s for a = 1 + t / 128;
-    const uint32_t* r_tab;            // grouped: s16 and 1 / s16
+    const uint32_t* r_tab;            // grouped: the store_grouped table (s_tab), tiered: the
+                                      // int4_g32 one (s_tab) and the int8_g64 one (r_tab)
 
+    // row = slot * Hkv + g of token `tok`
     __device__ __forceinline__ void operator()(const Params& p, const uint4 raw, long long row, bool isv,
-                                               int lane) const {
+                                               int lane, int tok, int slot) const {
         if constexpr (FMT == QSA_KV_BF16) {
             reinterpret_cast<uint4*>(row_ptr(p, isv, row, 2 * D))[lane] = raw;
         } else if constexpr (FMT == QSA_KV_FP8_E4M3) {
@@ -197,41 +252,28 @@ template <int FMT> struct Converter {
             else
                 store_fp8<false>(p, raw, row, isv, lane, lo, hi);
         } else if constexpr (FMT == QSA_KV_INT8_G64 || FMT == QSA_KV_INT4_G32) {
-            constexpr int GS = FMT == QSA_KV_INT8_G64 ? 64 : 32; // channels per scale
-            constexpr int LPG = GS / 8;                           // lanes per group
-            constexpr float qmax = FMT == QSA_KV_INT8_G64 ? 127.0f : 7.0f;
+            constexpr int G = FMT == QSA_KV_INT8_G64 ? 4 : 8; // scales per row
             float x[8];
             unpack(raw, x);
-            float a = 0.0f;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) a = fmaxf(a, fabsf(x[k]));
-#pragma unroll
-            for (int off = 1; off < LPG; off <<= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, off));
-            // a = (1 + t / 128) * 2^E: fl(a / qmax) from the table, exponent moved by E
-            const uint32_t ab = __float_as_uint(a);
-            const int t = (ab >> 16) & 0x7F;
-            const uint32_t e = (ab & 0x7F800000u) - (127u << 23);
-            const float s32 = __uint_as_float(s_tab[2 * t] + e);
-            uint32_t z[8];
-            float sc;
-            if (a >= FAST_MIN_ABSMAX && s32 >= 0x1p-14f && s32 <= 65504.0f) { // uniform per group
-                sc = __uint_as_float(s_tab[2 * t + 1] + e);
-                codes_markstein<FMT>(x, sc, __uint_as_float(r_tab[t] - e), z);
-            } else {
-                sc = __half2float(__float2half_rn(fminf(__fdiv_rn(a, qmax), 65504.0f)));
-                codes_divide<FMT>(x, sc, z);
+            store_grouped<FMT>(x, s_tab, row_ptr(p, isv, row, FMT == QSA_KV_INT8_G64 ? D : D / 2),
+                               static_cast<__half*>(isv ? p.vscale : p.kscale) + row * G, lane);
+        } else if constexpr (FMT == QSA_KV_INT8RING_INT4) {
+            float x[8];
+            unpack(raw, x);
+            store_grouped<QSA_KV_INT4_G32>(x, s_tab, row_ptr(p, isv, row, D / 2),
+                                           static_cast<__half*>(isv ? p.vscale : p.kscale) + row * 8, lane);
+            // the ring row: only the token that owns the position (its claim mark, or
+            // its slot once one of its rows has stamped it) writes it; with distinct
+            // slots no other token can match either value
+            const int pos = slot & p.ring_mask;
+            const int own = *reinterpret_cast<volatile const int*>(p.owner + pos);
+            if (own == -2 - tok || own == slot) {
+                const long long rrow = (long long)pos * p.Hkv + (row - (long long)slot * p.Hkv);
+                store_grouped<QSA_KV_INT8_G64>(x, r_tab, (isv ? p.vring : p.kring) + rrow * D,
+                                               (isv ? p.vring_scale : p.kring_scale) + rrow * 4, lane);
+                __syncwarp();
+                if (lane == 0) p.owner[pos] = slot;
             }
-            const uint32_t b0 = low_bytes(z[0], z[1], z[2], z[3]);
-            const uint32_t b1 = low_bytes(z[4], z[5], z[6], z[7]);
-            if constexpr (FMT == QSA_KV_INT8_G64)
-                reinterpret_cast<uint2*>(row_ptr(p, isv, row, D))[lane] = make_uint2(b0, b1);
-            else // offset binary: code + 8 is code ^ 8 on a two's-complement nibble
-                reinterpret_cast<uint32_t*>(row_ptr(p, isv, row, D / 2))[lane] =
-                    (low_nibbles(b0) | (low_nibbles(b1) << 16)) ^ 0x88888888u;
-            // the group leaders' 2-byte stores fill one 8- / 16-byte block per row
-            if (lane % LPG == 0)
-                static_cast<__half*>(isv ? p.vscale : p.kscale)[row * (D / GS) + lane / LPG] =
-                    __float2half_rn(sc);
         } else {
             constexpr float qmax = FMT == QSA_KV_INT8 ? 127.0f : 7.0f;
             float x[8];
@@ -262,13 +304,15 @@ template <int FMT> struct Converter {
 // Task t -> source row and destination pool row; false for t past the end or a
 // slot outside the pool (then *bad).
 __device__ __forceinline__ bool resolve(const Params& p, int rows, int t, const __nv_bfloat16** src,
-                                        long long* dst, bool* isv, bool* bad) {
+                                        long long* dst, bool* isv, bool* bad, int* tok, int* slot_out) {
     *bad = false;
     if (t >= 2 * rows) return false;
     *isv = t >= rows;
     const int r = *isv ? t - rows : t;
     const int i = p.Hkv == 2 ? r >> 1 : r, g = p.Hkv == 2 ? r & 1 : 0;
     const int slot = __ldg(p.slots + i);
+    *tok = i;
+    *slot_out = slot;
     if (slot < 0 || (long long)slot >= p.num_slots) {
         *bad = true;
         return false;
@@ -287,28 +331,42 @@ __device__ __forceinline__ void fp8_factors(float s, float* lo, float* hi) {
     *hi = pow2 ? r : r * (1.0f + 0x1p-20f);
 }
 
+// The grouped-format table of store_grouped for one qmax: per bf16 mantissa t,
+// (fl((1 + t / 128) / qmax), its binary16 rounding) pairs, then fl(1 / s16).
+__device__ __forceinline__ void fill_grouped_table(uint32_t* tab, float qmax) {
+    if (threadIdx.x < 128) {
+        const float s0 = __fdiv_rn(1.0f + threadIdx.x * 0x1p-7f, qmax);
+        const float s16 = __half2float(__float2half_rn(s0));
+        tab[2 * threadIdx.x] = __float_as_uint(s0);
+        tab[2 * threadIdx.x + 1] = __float_as_uint(s16);
+        tab[256 + threadIdx.x] = __float_as_uint(__frcp_rn(s16));
+    }
+}
+
 template <int FMT>
 __global__ void __launch_bounds__(WARPS * 32, 5) kv_write_kernel(const Params p) {
     constexpr bool GROUPED = FMT == QSA_KV_INT8_G64 || FMT == QSA_KV_INT4_G32;
-    constexpr bool INTQ = FMT == QSA_KV_INT8 || FMT == QSA_KV_INT4 || GROUPED;
+    constexpr bool TIERED = FMT == QSA_KV_INT8RING_INT4;
+    constexpr bool INTQ = FMT == QSA_KV_INT8 || FMT == QSA_KV_INT4;
     constexpr float qmax = (FMT == QSA_KV_INT8 || FMT == QSA_KV_INT8_G64) ? 127.0f : 7.0f;
-    // per bf16 mantissa t: s = fl((1 + t / 128) / qmax) and fl(1 / s); grouped:
-    // (s, s16 = fl16(s)) pairs and fl(1 / s16)
-    __shared__ uint32_t s_tab[INTQ ? (GROUPED ? 256 : 128) : 1], r_tab[INTQ ? 128 : 1];
+    // int8/int4: per bf16 mantissa t, s = fl((1 + t / 128) / qmax) and fl(1 / s);
+    // grouped: one store_grouped table; tiered: the int4_g32 and int8_g64 tables
+    constexpr int TAB = INTQ ? 128 : (GROUPED || TIERED) ? 384 : 1;
+    __shared__ uint32_t s_tab[TAB], r_tab[INTQ ? 128 : TIERED ? 384 : 1];
     Converter<FMT> conv{0.0f, 0.0f, 0.0f, 0.0f, s_tab, r_tab};
     if constexpr (INTQ) {
         if (threadIdx.x < 128) {
             const float s0 = __fdiv_rn(1.0f + threadIdx.x * 0x1p-7f, qmax);
-            if constexpr (GROUPED) {
-                const float s16 = __half2float(__float2half_rn(s0));
-                s_tab[2 * threadIdx.x] = __float_as_uint(s0);
-                s_tab[2 * threadIdx.x + 1] = __float_as_uint(s16);
-                r_tab[threadIdx.x] = __float_as_uint(__frcp_rn(s16));
-            } else {
-                s_tab[threadIdx.x] = __float_as_uint(s0);
-                r_tab[threadIdx.x] = __float_as_uint(__frcp_rn(s0));
-            }
+            s_tab[threadIdx.x] = __float_as_uint(s0);
+            r_tab[threadIdx.x] = __float_as_uint(__frcp_rn(s0));
         }
+        __syncthreads();
+    } else if constexpr (GROUPED) {
+        fill_grouped_table(s_tab, qmax);
+        __syncthreads();
+    } else if constexpr (TIERED) {
+        fill_grouped_table(s_tab, 7.0f);
+        fill_grouped_table(r_tab, 127.0f);
         __syncthreads();
     }
     if constexpr (FMT == QSA_KV_FP8_E4M3) {
@@ -321,20 +379,31 @@ __global__ void __launch_bounds__(WARPS * 32, 5) kv_write_kernel(const Params p)
     uint4 raw[RPW];
     long long dst[RPW];
     bool isv[RPW];
+    int tok[RPW], slot[RPW];
 #pragma unroll
     for (int u = 0; u < RPW; ++u) {
         const __nv_bfloat16* src;
         bool bad;
         dst[u] = -1;
         raw[u] = make_uint4(0u, 0u, 0u, 0u);
-        if (resolve(p, rows, first + u, &src, &dst[u], &isv[u], &bad))
+        if (resolve(p, rows, first + u, &src, &dst[u], &isv[u], &bad, &tok[u], &slot[u]))
             raw[u] = __ldg(reinterpret_cast<const uint4*>(src) + lane); // dims 8 lane .. 8 lane + 7
         else if (bad && lane == 0 && p.err)
             atomicOr(p.err, QSA_DEVERR_SLOT_RANGE);
     }
 #pragma unroll
     for (int u = 0; u < RPW; ++u)
-        if (dst[u] >= 0) conv(p, raw[u], dst[u], isv[u], lane);
+        if (dst[u] >= 0) conv(p, raw[u], dst[u], isv[u], lane, tok[u], slot[u]);
+}
+
+// Tiered write, first kernel: every token marks its ring position with -2 - i;
+// the minimum, i.e. the last token of the write mapping there, remains.
+__global__ void ring_claim_kernel(const int* slots, int n, long long num_slots, int* owner, int mask) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+        const int slot = __ldg(slots + i);
+        if (slot < 0 || (long long)slot >= num_slots) continue;
+        atomicMin(owner + (slot & mask), -2 - i);
+    }
 }
 
 namespace {
@@ -363,11 +432,13 @@ template <int FMT> int launch(const Params& prm, cudaStream_t st) {
 } // namespace
 } // namespace qsakv
 
-extern "C" int qsa_kv_write(int32_t format, const qsa_tensor* k_new, const qsa_tensor* v_new,
-                            const qsa_tensor* slots, const qsa_tensor* k_pool,
-                            const qsa_tensor* v_pool, void* k_scale, void* v_scale,
-                            int32_t* device_error, void* stream) {
-    using namespace qsakv;
+namespace qsakv {
+namespace {
+
+// Validate a write of `format` rows and fill the parameters (nothing enqueued).
+int prepare(int32_t format, const qsa_tensor* k_new, const qsa_tensor* v_new, const qsa_tensor* slots,
+            const qsa_tensor* k_pool, const qsa_tensor* v_pool, void* k_scale, void* v_scale,
+            int32_t* device_error, Params* prm) {
     if (!k_new || !v_new || !slots || !k_pool || !v_pool)
         return fail(QSA_ERR_INVALID_ARGUMENT, "a descriptor pointer is NULL");
     if (format < QSA_KV_BF16 || format > QSA_KV_INT4_G32)
@@ -423,25 +494,42 @@ extern "C" int qsa_kv_write(int32_t format, const qsa_tensor* k_new, const qsa_t
             return fail(QSA_ERR_MISALIGNED, "scales must be %d-byte aligned for this format", (int)al);
     }
     if (n > (1LL << 28)) return fail(QSA_ERR_UNSUPPORTED, "more than 2^28 new tokens in one call");
-    qsa_detail_set_error("");
-    if (n == 0) return QSA_OK;
+    prm->kx = static_cast<const __nv_bfloat16*>(k_new->data);
+    prm->vx = static_cast<const __nv_bfloat16*>(v_new->data);
+    prm->k_st = k_new->stride[0];
+    prm->k_sh = k_new->stride[1];
+    prm->v_st = v_new->stride[0];
+    prm->v_sh = v_new->stride[1];
+    prm->slots = static_cast<const int*>(slots->data);
+    prm->n = static_cast<int>(n);
+    prm->Hkv = static_cast<int>(hkv);
+    prm->kpool = static_cast<uint8_t*>(k_pool->data);
+    prm->vpool = static_cast<uint8_t*>(v_pool->data);
+    prm->num_slots = k_pool->shape[0];
+    prm->kscale = k_scale;
+    prm->vscale = v_scale;
+    prm->err = device_error;
+    prm->kring = prm->vring = nullptr;
+    prm->kring_scale = prm->vring_scale = nullptr;
+    prm->owner = nullptr;
+    prm->ring_mask = 0;
+    return QSA_OK;
+}
 
+} // namespace
+} // namespace qsakv
+
+extern "C" int qsa_kv_write(int32_t format, const qsa_tensor* k_new, const qsa_tensor* v_new,
+                            const qsa_tensor* slots, const qsa_tensor* k_pool,
+                            const qsa_tensor* v_pool, void* k_scale, void* v_scale,
+                            int32_t* device_error, void* stream) {
+    using namespace qsakv;
     Params prm;
-    prm.kx = static_cast<const __nv_bfloat16*>(k_new->data);
-    prm.vx = static_cast<const __nv_bfloat16*>(v_new->data);
-    prm.k_st = k_new->stride[0];
-    prm.k_sh = k_new->stride[1];
-    prm.v_st = v_new->stride[0];
-    prm.v_sh = v_new->stride[1];
-    prm.slots = static_cast<const int*>(slots->data);
-    prm.n = static_cast<int>(n);
-    prm.Hkv = static_cast<int>(hkv);
-    prm.kpool = static_cast<uint8_t*>(k_pool->data);
-    prm.vpool = static_cast<uint8_t*>(v_pool->data);
-    prm.num_slots = k_pool->shape[0];
-    prm.kscale = k_scale;
-    prm.vscale = v_scale;
-    prm.err = device_error;
+    const int rc = prepare(format, k_new, v_new, slots, k_pool, v_pool, k_scale, v_scale,
+                           device_error, &prm);
+    if (rc != QSA_OK) return rc;
+    qsa_detail_set_error("");
+    if (prm.n == 0) return QSA_OK;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     switch (format) {
     case QSA_KV_BF16: return launch<QSA_KV_BF16>(prm, st);
@@ -451,4 +539,43 @@ extern "C" int qsa_kv_write(int32_t format, const qsa_tensor* k_new, const qsa_t
     case QSA_KV_INT8_G64: return launch<QSA_KV_INT8_G64>(prm, st);
     default: return launch<QSA_KV_INT4_G32>(prm, st);
     }
+}
+
+extern "C" int qsa_kv_write_tiered(const qsa_tensor* k_new, const qsa_tensor* v_new,
+                                   const qsa_tensor* slots, const qsa_tensor* k_pool,
+                                   const qsa_tensor* v_pool, void* k_scale, void* v_scale,
+                                   const qsa_kv_tier* tier, int32_t* device_error, void* stream) {
+    using namespace qsakv;
+    Params prm;
+    const int rc = prepare(QSA_KV_INT4_G32, k_new, v_new, slots, k_pool, v_pool, k_scale, v_scale,
+                           device_error, &prm);
+    if (rc != QSA_OK) return rc;
+    if (tier == nullptr) return fail(QSA_ERR_INVALID_ARGUMENT, "tier is NULL");
+    const int R = tier->ring_slots;
+    if (R < 1 || R > (1 << 30) || (R & (R - 1)))
+        return fail(QSA_ERR_INVALID_ARGUMENT, "ring_slots %d is not a power of two in 1..2^30", R);
+    if (!tier->k_ring || !tier->v_ring || !tier->k_ring_scale || !tier->v_ring_scale || !tier->owner)
+        return fail(QSA_ERR_INVALID_ARGUMENT, "a tier pointer is NULL");
+    if (!aligned16(tier->k_ring) || !aligned16(tier->v_ring) ||
+        (reinterpret_cast<uintptr_t>(tier->k_ring_scale) & 7u) ||
+        (reinterpret_cast<uintptr_t>(tier->v_ring_scale) & 7u) ||
+        (reinterpret_cast<uintptr_t>(tier->owner) & 3u))
+        return fail(QSA_ERR_MISALIGNED,
+                    "ring rows must be 16-byte, ring scales 8-byte and owner 4-byte aligned");
+    prm.kring = static_cast<uint8_t*>(tier->k_ring);
+    prm.vring = static_cast<uint8_t*>(tier->v_ring);
+    prm.kring_scale = static_cast<__half*>(tier->k_ring_scale);
+    prm.vring_scale = static_cast<__half*>(tier->v_ring_scale);
+    prm.owner = tier->owner;
+    prm.ring_mask = R - 1;
+    qsa_detail_set_error("");
+    if (prm.n == 0) return QSA_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int threads = 256;
+    const long long want = (prm.n + threads - 1) / threads;
+    ring_claim_kernel<<<static_cast<unsigned>(want < 4096 ? want : 4096), threads, 0, st>>>(
+        prm.slots, prm.n, prm.num_slots, prm.owner, prm.ring_mask);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(QSA_ERR_CUDA, "ring claim launch: %s", cudaGetErrorString(e));
+    return launch<QSA_KV_INT8RING_INT4>(prm, st);
 }

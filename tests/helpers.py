@@ -16,8 +16,9 @@ REL_L2_TOL = 2e-3
 
 
 def meta_for(w: I.Workload, max_ctas: int = 0, capacity=None) -> qsa.KVQuantMeta:
+    tier = {k: w.extra[k] for k in I.TIER_KEYS} if w.fmt == I.TIERED else None
     return qsa.KVQuantMeta(w.fmt, capacity or w.capacity, w.k_scale, w.v_scale, w.softmax_scale,
-                           max_ctas)
+                           max_ctas, tier)
 
 
 def run_cuda(wd: I.Workload, max_ctas: int = 0, out=None, scratch=None, stream=None):
@@ -33,6 +34,11 @@ def run_cuda(wd: I.Workload, max_ctas: int = 0, out=None, scratch=None, stream=N
 
 def run_oracle(w: I.Workload, rows=None) -> np.ndarray:
     """FP64 oracle output [n, Hq, 256] on a host workload."""
+    if w.fmt == I.TIERED:
+        t = w.extra
+        return oracle.decode_tiered(w.q, w.k_pool, w.v_pool, w.sel, w.cu, w.softmax_scale,
+                                    w.k_scale, w.v_scale, t["k_ring"], t["v_ring"],
+                                    t["k_ring_scale"], t["v_ring_scale"], t["owner"], rows=rows)
     return oracle.decode(w.q, w.k_pool, w.v_pool, w.fmt, w.sel, w.cu, w.softmax_scale,
                          w.k_scale, w.v_scale, rows=rows)
 
