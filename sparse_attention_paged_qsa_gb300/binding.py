@@ -186,9 +186,19 @@ def _stream_handle(stream) -> Optional[int]:
     return int(stream)
 
 
+def _require_device(*tensors) -> None:
+    """The library takes device pointers; a host tensor here is a caller error."""
+    for t in tensors:
+        if t is not None and not t.is_cuda:
+            raise QsaError(ERR_INVALID_ARGUMENT, "every tensor must be on the GPU (got a host tensor)")
+
+
 def qsa_decode(q, k_pool, v_pool, kv_quant_meta: KVQuantMeta, sel_indices, cu_seqlens, out,
                scratch, stream=None) -> None:
     """Enqueue one packed QSA decode (see include/qsa.h). Raises QsaError on a contract error."""
+    _require_device(q, k_pool, v_pool, sel_indices, cu_seqlens, out, scratch,
+                    kv_quant_meta.k_scale, kv_quant_meta.v_scale,
+                    *((kv_quant_meta.tier or {}).values()))
     lib = load()
     meta = kv_quant_meta.to_c()
     args = [describe(t) for t in (q, k_pool, v_pool)]
@@ -204,6 +214,7 @@ def qsa_decode(q, k_pool, v_pool, kv_quant_meta: KVQuantMeta, sel_indices, cu_se
 def qsa_kv_write(fmt: str, k_new, v_new, slots, k_pool, v_pool, k_scale=None, v_scale=None,
                  error_word=None, stream=None) -> None:
     """Enqueue one quantise + scatter write of new K/V rows (see include/qsa.h)."""
+    _require_device(k_new, v_new, slots, k_pool, v_pool, k_scale, v_scale, error_word)
     lib = load()
     d = [describe(t) for t in (k_new, v_new, slots, k_pool, v_pool)]
     ptr = lambda t: t.data_ptr() if t is not None else None
@@ -215,6 +226,8 @@ def qsa_kv_write(fmt: str, k_new, v_new, slots, k_pool, v_pool, k_scale=None, v_
 def qsa_kv_write_tiered(k_new, v_new, slots, k_pool, v_pool, k_scale, v_scale, tier: dict,
                         error_word=None, stream=None) -> None:
     """Enqueue the two-kernel write of a tiered int8ring_int4 pool (see include/qsa.h)."""
+    _require_device(k_new, v_new, slots, k_pool, v_pool, k_scale, v_scale, error_word,
+                    *tier.values())
     lib = load()
     d = [describe(t) for t in (k_new, v_new, slots, k_pool, v_pool)]
     ts = tier_struct(tier)

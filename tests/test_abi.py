@@ -170,3 +170,15 @@ def test_kv_write_rejections_on_host():
     rc = lib.qsa_kv_write(2, d(empty), d(empty), d(torch.zeros(0, dtype=torch.int32)), d(pool),
                           d(pool), sc.data_ptr(), sc.data_ptr(), None, None)
     assert rc == B.OK  # nothing to write, nothing enqueued
+
+
+def test_binding_rejects_host_tensors():
+    """The C ABI takes device pointers; the binding refuses host tensors before the call."""
+    q = torch.zeros(2, 24, 256, dtype=torch.bfloat16)
+    pool = torch.zeros(8, 2, 256, dtype=torch.bfloat16)
+    meta = B.KVQuantMeta("bf16", 4)
+    with pytest.raises(B.QsaError, match="on the GPU"):
+        B.qsa_decode(q, pool, pool, meta, torch.zeros(4, dtype=torch.int32),
+                     torch.zeros(3, dtype=torch.int32), q, torch.zeros(1024, dtype=torch.uint8))
+    with pytest.raises(B.QsaError, match="on the GPU"):
+        B.qsa_kv_write("bf16", pool, pool, torch.zeros(8, dtype=torch.int32), pool, pool)

@@ -72,8 +72,9 @@ def test_tiered_headline_sampled(cuda_device):
     """bs=128, L=2055, 24Q/2KV over a 1M-slot pool with the pages' 8192-row ring,
     a quarter of each selection hot: sampled sequences against the oracle."""
     pools = I.make_tiered_pools(1048576, 2, I.RING_SLOTS, 55, device=cuda_device)
-    w = I.tiered(seed=55, bs=128, num_slots=1048576, ring_slots=I.RING_SLOTS,
+    w = I.tiered(seed=55, device=cuda_device, bs=128, num_slots=1048576, ring_slots=I.RING_SLOTS,
                  lengths=[2055] * 128, hot_share=0.25, pools=pools)
+    assert w.q.is_cuda and w.sel.is_cuda and w.cu.is_cuda
     out, scratch = run_cuda(w)
     torch.cuda.synchronize()
     rows = [0, 1, 63, 127]
