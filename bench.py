@@ -441,7 +441,7 @@ def run_kv_write(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=3000)  # ~0.3 s timed: several clock samples
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--fmt", default="bf16", choices=list(I.FORMATS) + [I.TIERED])
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
