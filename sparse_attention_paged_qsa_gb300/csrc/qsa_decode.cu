@@ -986,11 +986,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
                     *reinterpret_cast<uint4*>(kbf + swz<BF_ROW>(t, 2 * rc)) = o0;
                     *reinterpret_cast<uint4*>(kbf + swz<BF_ROW>(t, 2 * rc + 1)) = o1;
                 }
-                // V: this warp's 32 dims = raw chunks 2*warp, 2*warp+1 of every token
+                // V: this warp's 32 dims = raw chunks 2*warp, 2*warp+1 of every token;
+                // eight consecutive lanes take eight consecutive tokens of one chunk,
+                // so their swizzled chunks fall in eight different bank groups
 #pragma unroll
                 for (int it = 0; it < 4; ++it) {
-                    const int task = it * 32 + lane;
-                    const int tv = task >> 1, rc = 2 * warp + (task & 1);
+                    const int tv = lane + 32 * (it >> 1), rc = 2 * warp + (it & 1);
                     const uint4 raw = *reinterpret_cast<const uint4*>(Vs + swz<Tr::ROWB>(tv, rc));
                     uint4 o0, o1;
                     convert16<FMT == QSA_KV_FP8_E4M3 ? FMT : QSA_KV_INT8, Tr::PV_F16>(raw, o0, o1);
