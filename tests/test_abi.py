@@ -182,3 +182,49 @@ def test_binding_rejects_host_tensors():
                      torch.zeros(3, dtype=torch.int32), q, torch.zeros(1024, dtype=torch.uint8))
     with pytest.raises(B.QsaError, match="on the GPU"):
         B.qsa_kv_write("bf16", pool, pool, torch.zeros(8, dtype=torch.int32), pool, pool)
+
+
+def _tier_call(ring_slots=64, drop=None, misalign=None, with_tier=True):
+    """qsa_decode on a tiered pool with host tensors (never dereferenced)."""
+    lib = B.load()
+    q = torch.zeros(2, 24, 256, dtype=torch.bfloat16)
+    pool = torch.zeros(64, 2, 128, dtype=torch.uint8)
+    sc = torch.ones(64 * 2 * 8 + 64, dtype=torch.float16)
+    sc = sc[(-sc.data_ptr() // 2) % 8:]
+    ring = torch.zeros(ring_slots * 2 * 256 + 64, dtype=torch.int8)
+    ring = ring[(-ring.data_ptr()) % 16:]
+    rsc = torch.ones(ring_slots * 2 * 4 + 8, dtype=torch.float16)
+    rsc = rsc[(-rsc.data_ptr() // 2) % 4:]
+    owner = torch.full((max(ring_slots, 1),), -1, dtype=torch.int32)
+    tier = {"k_ring": ring, "v_ring": ring, "k_ring_scale": rsc, "v_ring_scale": rsc, "owner": owner}
+    t = B.tier_struct(tier)
+    t.ring_slots = ring_slots
+    if drop:
+        setattr(t, drop, None)
+    if misalign:
+        setattr(t, misalign, getattr(t, misalign) + 2)
+    m = B.KVQuantMeta("int8ring_int4", 100, sc, sc, 1 / 16).to_c()
+    if with_tier:
+        m.tier = ctypes.pointer(t)
+    d = [B.describe(x) for x in (q, pool, pool)]
+    sel, cu, out = torch.zeros(10, dtype=torch.int32), torch.zeros(3, dtype=torch.int32), q.clone()
+    scr = torch.zeros(1 << 16, dtype=torch.uint8)
+    aligned = (scr.data_ptr() + 255) // 256 * 256
+    rc = lib.qsa_decode(ctypes.byref(d[0]), ctypes.byref(d[1]), ctypes.byref(d[2]), ctypes.byref(m),
+                        ctypes.byref(B.describe(sel)), ctypes.byref(B.describe(cu)),
+                        ctypes.byref(B.describe(out)), aligned, 1 << 15, None)
+    return rc, lib.qsa_last_error_message().decode()
+
+
+@pytest.mark.parametrize("kw, code, text", [
+    (dict(with_tier=False), B.ERR_INVALID_ARGUMENT, "tier"),
+    (dict(ring_slots=48), B.ERR_INVALID_ARGUMENT, "power of two"),
+    (dict(ring_slots=0), B.ERR_INVALID_ARGUMENT, "power of two"),
+    (dict(drop="owner"), B.ERR_INVALID_ARGUMENT, "NULL"),
+    (dict(misalign="k_ring"), B.ERR_MISALIGNED, "16-byte"),
+    (dict(misalign="v_ring_scale"), B.ERR_MISALIGNED, "8-byte"),
+])
+def test_tiered_decode_rejections_on_host(kw, code, text):
+    rc, msg = _tier_call(**kw)
+    assert rc == code, msg
+    assert text in msg
