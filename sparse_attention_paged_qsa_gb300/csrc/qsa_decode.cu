@@ -79,7 +79,7 @@ constexpr int MAX_CAPACITY = 2055;
 constexpr int MIN_TOKENS_PER_CTA = 64;
 constexpr int PART_BYTES = 12416;           // fp32 O[12][256] + m[12] + l[12], 128-byte multiple
 constexpr long long WAIT_NS = 2000000000LL; // bounded-wait limit (2 s)
-constexpr int BAR_CONSUMERS = 1;            // named barrier id
+constexpr int BAR_CONSUMERS = 1;            // named barrier id (2..5: consumer warp pairs)
 static_assert(TPW == 8 && MT >= 1 && TPP <= 32, "tile shape");
 static_assert(PART_BYTES >= (GROUP * D + 2 * GROUP) * 4, "partial slot size");
 
@@ -1188,7 +1188,27 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
 
         // ---------------------------------------------------------------- PV
         const uint8_t* Pt = Pb;
-        if constexpr (Tr::GROUPS) {
+        if constexpr (Tr::GROUPS == 4) {
+            // 64-channel groups: warps 2k and 2k + 1 share group k, so the pair builds
+            // one copy (six heads each, double-buffered by stage) and meets at a named
+            // barrier; scaling and split as below
+            const int pair = warp >> 1, h0 = 6 * (warp & 1);
+            uint8_t* const Pw = smem + Ly::off_pw + (pair * 2 + buf) * 24 * PRS;
+            const int t = 2 * lane;
+            const float sv0 = svw[0], sv1 = svw[1];
+#pragma unroll
+            for (int hh = 0; hh < 6; ++hh) {
+                const int h = h0 + hh;
+                const float2 pp = *reinterpret_cast<const float2*>(Pf + h * T + t);
+                uint32_t hi, lo;
+                split_pair<false>(pp.x * sv0, pp.y * sv1, hi, lo);
+                const int rh = h < 8 ? h : 8 + h, rl = h < 8 ? 8 + h : 12 + h;
+                *reinterpret_cast<uint32_t*>(Pw + rh * PRS + t * 2) = hi;
+                *reinterpret_cast<uint32_t*>(Pw + rl * PRS + t * 2) = lo;
+            }
+            asm volatile("bar.sync %0, 64;" ::"r"(BAR_CONSUMERS + 1 + pair) : "memory");
+            Pt = Pw;
+        } else if constexpr (Tr::GROUPS) {
             // this warp's dims lie in one channel group: P^T columns scaled per token
             // by that group's V scale (read into svw above), split into bf16 hi + lo
             uint8_t* const Pw = smem + Ly::off_pw + warp * 24 * PRS;
