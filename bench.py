@@ -186,7 +186,8 @@ class ClockSampler:
                 "samples": len(self.samples)}
 
 
-def cpu_baseline(fmt: str, sample_rows: int, work, threads: int = 0, call_bytes: int = 0):
+def cpu_baseline(fmt: str, sample_rows: int, work, threads: int = 0, call_bytes: int = 0,
+                 bs: int = BS):
     """Time the FP64 oracle on `sample_rows` sequences of the workload; returns a dict."""
     import oracle
 
@@ -194,10 +195,10 @@ def cpu_baseline(fmt: str, sample_rows: int, work, threads: int = 0, call_bytes:
     t0 = time.perf_counter()
     oracle_decode(sub, threads=threads)
     dt = time.perf_counter() - t0
-    b = (call_bytes or algorithmic_bytes(fmt)) * sample_rows // BS
+    b = (call_bytes or algorithmic_bytes(fmt, bs=bs)) * sample_rows // bs
     return {"value": b / dt / 1e9, "unit": "GB/s", "cores": oracle.max_threads(),
-            "kind": "oracle", "calls_per_s": (sample_rows / BS) / dt,
-            "sample": f"{sample_rows} of {BS} sequences (L={L}, 24Q/2KV), {dt:.2f} s, "
+            "kind": "oracle", "calls_per_s": (sample_rows / bs) / dt,
+            "sample": f"{sample_rows} of {bs} sequences (L={L}, 24Q/2KV), {dt:.2f} s, "
                       "scaled to bytes of the full call"}
 
 
@@ -248,14 +249,16 @@ def run_native(args):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     fmt = args.fmt
-    works = make_workloads(fmt, 2 + rank, [100 + 7 * rank + k for k in range(args.index_sets)], dev)
+    bs = args.bs
+    works = make_workloads(fmt, 2 + rank, [100 + 7 * rank + k for k in range(args.index_sets)], dev,
+                           bs=bs)
     w0 = works[0]
     out = torch.empty_like(w0.q)
-    scratch = qsa.alloc_scratch(BS, HQ, L, dev)
+    scratch = qsa.alloc_scratch(bs, HQ, L, dev)
     tier = {k: w0.extra[k] for k in I.TIER_KEYS} if fmt == I.TIERED else None
     meta = qsa.KVQuantMeta(fmt, L, w0.k_scale, w0.v_scale, w0.softmax_scale, 0, tier)
     stream = torch.cuda.current_stream()
-    grid = qsa.qsa_decode_grid(BS, HQ, L)
+    grid = qsa.qsa_decode_grid(bs, HQ, L)
 
     def step(k):
         w = works[k % len(works)]
@@ -267,17 +270,32 @@ def run_native(args):
     if ws > 1:
         torch.distributed.barrier()
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    graph = None
+    if args.graph:  # the timed calls as one CUDA graph: no host time between launches
+        gs = torch.cuda.Stream()
+        gs.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=gs):
+            for k in range(args.steps):
+                qsa.qsa_decode(works[k % len(works)].q, w0.k_pool, w0.v_pool, meta,
+                               works[k % len(works)].sel, works[k % len(works)].cu, out, scratch, gs)
+        torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         torch.cuda.synchronize()
         ev[0].record(stream)
-        for k in range(args.steps):
-            step(k)
-            ev[k + 1].record(stream)
+        if graph is not None:
+            graph.replay()
+            ev[-1].record(stream)
+        else:
+            for k in range(args.steps):
+                step(k)
+                ev[k + 1].record(stream)
         torch.cuda.synchronize()
     if ws > 1:
         torch.distributed.barrier()
-    per = [ev[k].elapsed_time(ev[k + 1]) for k in range(args.steps)]
     total_ms = ev[0].elapsed_time(ev[-1])
+    per = ([total_ms / args.steps] if graph is not None else
+           [ev[k].elapsed_time(ev[k + 1]) for k in range(args.steps)])
     err = qsa.qsa_scratch_error(scratch)
     if err:
         raise RuntimeError(f"device error flags {err}")
@@ -318,20 +336,21 @@ def run_native(args):
     if fmt == I.TIERED:  # the bytes depend on which rows are hot: the mean over the index sets
         abytes = sum(tiered_bytes(w) for w in works) // len(works)
     else:
-        abytes = algorithmic_bytes(fmt)
+        abytes = algorithmic_bytes(fmt, bs=bs)
     value = whole_job_gbs(ws, abytes, step_ms)
     e2e_val = whole_job_gbs(ws, abytes, e2e_ms) if e2e_steps else None
     kernel_ms = sum(per) / len(per)
     achieved = abytes / (kernel_ms * 1e-3) / 1e9
     peak, peak_kind = measured_peaks()
     calls = ws / (step_ms * 1e-3)
+    rows_bytes = bs * HKV * L * 2 * (ROW_BYTES.get(fmt, 0) + SCALE_BYTES.get(fmt, 0))
 
     cpu = None
     if rank == 0 and args.cpu_rows > 0:
         import oracle
 
         oracle.build()
-        cpu = cpu_baseline(fmt, args.cpu_rows, works[0], call_bytes=abytes)
+        cpu = cpu_baseline(fmt, min(args.cpu_rows, bs), works[0], call_bytes=abytes, bs=bs)
 
     if rank == 0:
         traffic = measured_traffic(fmt)
@@ -339,15 +358,20 @@ def run_native(args):
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": fmt, "data": "synthetic",
-            "calls_per_s": calls, "tokens_per_s": calls * BS * L,
+            "calls_per_s": calls, "tokens_per_s": calls * bs * L,
             "pct_of_hbm_peak": 100.0 * achieved / peak,
-            "config": {"workload": f"packed QSA decode bs={BS} L={L} 24Q/2KV D=256 {fmt} pool"
+            "config": {"workload": f"packed QSA decode bs={bs} L={L} 24Q/2KV D=256 {fmt} pool"
                                    + (f" (ring {I.RING_SLOTS}, {TIER_HOT_SHARE:.0%} of ids hot)"
                                       if fmt == I.TIERED else ""),
                        "pool_slots": SLOTS, "index_sets": args.index_sets, "grid_ctas": grid,
-                       "l2": "inputs larger than L2: 538 MB of K/V rows per call from a 2 GiB "
-                             "pool, rotating index sets",
-                       "parallelism": f"replicas x{ws}"},
+                       "l2": ("inputs larger than L2: 538 MB of K/V rows per call from a 2 GiB "
+                              "pool, rotating index sets" if bs == BS else
+                              f"{rows_bytes / 1e6:.0f} MB of K/V rows per index set x "
+                              f"{args.index_sets} sets: " + ("larger than L2" if rows_bytes *
+                              args.index_sets > 129e6 else "L2-warm (fits in the 129 MB L2)")),
+                       "parallelism": f"replicas x{ws}",
+                       "launch": ("the timed calls replayed as one CUDA graph" if args.graph
+                                  else "one stream launch per call")},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
                          "peak_source": f"{peak_kind} hbm_gbs",
@@ -448,6 +472,10 @@ def main():
     ap.add_argument("--op", default="decode", choices=["decode", "kv_write"],
                     help="decode (the headline) or the quantising KV write")
     ap.add_argument("--index-sets", type=int, default=3)
+    ap.add_argument("--bs", type=int, default=BS,
+                    help="sequences per call (the headline is 128; smaller for latency)")
+    ap.add_argument("--graph", action="store_true",
+                    help="time the calls captured in one CUDA graph (no host gaps between them)")
     ap.add_argument("--cpu-rows", type=int, default=128,
                     help="sequences of the oracle CPU-baseline sample (0 disables)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
