@@ -78,10 +78,12 @@ constexpr int MAX_BS = 128;
 constexpr int MAX_CAPACITY = 2055;
 constexpr int MIN_TOKENS_PER_CTA = 64;
 constexpr int PART_BYTES = 12416;           // fp32 O[12][256] + m[12] + l[12], 128-byte multiple
+constexpr int MERGE_BATCH = 6;             // partials per bulk-copy batch of the split merge
 constexpr long long WAIT_NS = 2000000000LL; // bounded-wait limit (2 s)
 constexpr int BAR_CONSUMERS = 1;            // named barrier id (2..5: consumer warp pairs)
 static_assert(TPW == 8 && MT >= 1 && TPP <= 32, "tile shape");
 static_assert(PART_BYTES >= (GROUP * D + 2 * GROUP) * 4, "partial slot size");
+static_assert(PART_BYTES % 16 == 0, "bulk copies move 16-byte multiples");
 
 // ROWB: pool row bytes; DEQ: rows are converted in shared memory; SCALES:
 // per-slot scales (fp32 per (slot, KV head), or binary16 per (slot, KV head,
@@ -161,9 +163,15 @@ template <int FMT> struct Layout {
     static constexpr int off_segP = off_segSrc + (MAX_BS + 4) * 4;
     static constexpr int off_misc = off_segP + (MAX_BS + 4) * 4;
     static constexpr int off_bar = off_misc + 64 * 4;
-    static constexpr int n_bars = 2 * Tr::STAGES + 4;
+    static constexpr int n_bars = 2 * Tr::STAGES + 6; // stages full/empty, Q full/empty, merge
     static constexpr int TOTAL = off_bar + n_bars * 8;
     static_assert(TOTAL <= 227 * 1024, "shared memory budget");
+    // the split merge stages two batches of partials over the (then idle) stage
+    // ring and dequantised tiles, below the Q tiles
+    static_assert(2 * MERGE_BATCH * PART_BYTES <= off_q, "merge buffers");
+    // then this CTA's own partial of a directly merged segment head
+    static constexpr int off_stash = 2 * MERGE_BATCH * PART_BYTES;
+    static_assert(off_stash + PART_BYTES <= off_q, "direct-merge stash");
     static_assert(STAGE_BYTES % 128 == 0 && off_kbf % 128 == 0 && off_q % 16 == 0, "alignment");
     static_assert(off_p % 16 == 0 && off_pw % 16 == 0 && off_red % 16 == 0 && off_bar % 8 == 0,
                   "alignment");
@@ -267,6 +275,28 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* err,
     }
 }
 
+// Wait for bulk copies this CTA issued: bounded like mbar_wait, but blind to the
+// abort flag (the copies must land before the CTA may exit).
+__device__ __noinline__ bool mbar_wait_copies(uint32_t bar, uint32_t parity, int* err) {
+    const unsigned long long t0 = globaltimer();
+    for (uint32_t it = 0;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63) == 63 && globaltimer() - t0 > (unsigned long long)WAIT_NS) {
+            atomicOr(err, QSA_DEVERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ int ld_relaxed(const int* ptr) {
+    int v;
+    asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+    return v;
+}
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
                                          uint32_t bar) {
     asm volatile(
@@ -297,6 +327,9 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
 
 __device__ __forceinline__ void fence_proxy_async() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_all() {
+    asm volatile("fence.proxy.async;" ::: "memory");
 }
 __device__ __forceinline__ void fence_mbarrier_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -572,6 +605,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
     auto empty_bar = [&](int s) { return bar0 + 8u * (Tr::STAGES + s); };
     auto qfull_bar = [&](int i) { return bar0 + 8u * (2 * Tr::STAGES + i); };
     auto qempty_bar = [&](int i) { return bar0 + 8u * (2 * Tr::STAGES + 2 + i); };
+    auto merge_bar = [&](int i) { return bar0 + 8u * (2 * Tr::STAGES + 4 + i); };
 
     // ---------------------------------------------------------------- setup
     if (tid == 0) {
@@ -584,6 +618,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
         for (int i = 0; i < 2; ++i) {
             mbar_init(qfull_bar(i), 1);
             mbar_init(qempty_bar(i), NW);
+            mbar_init(merge_bar(i), 1);
         }
         misc[0] = 0;
         fence_mbarrier_init();
@@ -820,6 +855,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
     float l0 = 0.f, l1 = 0.f;
     int v = 0, buf = 0, seg_j0 = 0;
     int pend0 = -1, pend1 = -1;     // split segments whose partial this CTA wrote
+    int ticket0 = -1;               // thread 0: the arrival ticket taken for pend0
+    int dsid = -1, dn = 0;          // directly merged segment head, its other contributors
+    int arrived = -1;               // thread 0: that segment's counter, read a stage early
+    // contributors of a split segment: CTAs c_first..c_last; c_first's partial
+    // sits in its slot 1 when its range began before the segment
+    auto seg_range = [&](int sid, unsigned& Fs, unsigned& c_first, unsigned& c_last) {
+        const int b = sid / Hkv, g = sid - (sid / Hkv) * Hkv, L = segL[b];
+        Fs = static_cast<unsigned>(Hkv * segP[b] + g * L);
+        c_first = cta_of(Fs, N, G);
+        c_last = cta_of(Fs + static_cast<unsigned>(L) - 1u, N, G);
+    };
     const int tok_base = warp * TPW;
     const int tk0 = tok_base + 2 * c;
     const int xs = lane & 7;                 // row % 8 of every row this lane addresses
@@ -836,6 +882,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
         const bool first = cc.segfirst;
         const bool last = cc.j + n >= cc.j1;
         const int b = cc.b, g = cc.g;
+        // the head of a segment this range ends in: read its arrival counter now,
+        // a stage before the epilogue needs it
+        if (tid == 0 && last && cc.kseg != 0 && cc.j1 < segL[b]) arrived = ld_relaxed(p.cnt + b * Hkv + g);
         if (first) {
             seg_j0 = cc.j;
             const int qb = cc.kseg & 1;
@@ -1258,6 +1307,23 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
             const int L = segL[b];
             const bool complete = (seg_j0 == 0) && (cc.j1 == L);
             const int sid = b * Hkv + g;
+            // The head of a segment that this CTA's range ends in. Every other
+            // contributor starts its range inside the segment, so it has usually
+            // finished its piece and taken its ticket long before: then (at most
+            // two of them) this CTA merges their partials with its own right after
+            // the loop, and neither writes its own partial nor takes a ticket.
+            const bool head_split = !complete && cc.kseg != 0;
+            int n_other = 0;
+            if (head_split) {
+                unsigned Fs, c_first, c_last;
+                seg_range(sid, Fs, c_first, c_last);
+                n_other = static_cast<int>(c_last - c_first); // c_first is this CTA
+                if (tid == 0) {
+                    const bool all_in = n_other <= 2 && arrived == n_other;
+                    if (all_in) fence_acq_rel_gpu(); // acquire: their partials precede
+                    misc[4] = all_in ? 1 : 0;
+                }
+            }
             float la = l0, lb = l1;
             la += __shfl_xor_sync(0xFFFFFFFFu, la, 1);
             la += __shfl_xor_sync(0xFFFFFFFFu, la, 2);
@@ -1288,34 +1354,75 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
                 else
                     part[h * D + d] = val;
             };
+            // this thread's values: [mt][A dA, B dA, A dB, B dB, C dA, D dA, C dB, D dB]
+            float val[MT][8];
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt) {
-                const int dA = warp * DPW + mt * 16 + r, dB = dA + 8;
-                put(hA, dA, (o[mt][0][0] + o[mt][1][0]) * fA);
-                put(hB, dA, (o[mt][0][1] + o[mt][1][1]) * fB);
-                put(hA, dB, (o[mt][0][2] + o[mt][1][2]) * fA);
-                put(hB, dB, (o[mt][0][3] + o[mt][1][3]) * fB);
-                float u[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) u[e] = __shfl_xor_sync(0xFFFFFFFFu, o[mt][2][e], 2);
-                if (c < 2) {
-                    put(hC, dA, (o[mt][2][0] + u[0]) * fC);
-                    put(hD, dA, (o[mt][2][1] + u[1]) * fD);
-                    put(hC, dB, (o[mt][2][2] + u[2]) * fC);
-                    put(hD, dB, (o[mt][2][3] + u[3]) * fD);
+                for (int e = 0; e < 4; ++e) {
+                    val[mt][e] = o[mt][0][e] + o[mt][1][e];
+                    val[mt][4 + e] = o[mt][2][e] + __shfl_xor_sync(0xFFFFFFFFu, o[mt][2][e], 2);
                 }
             }
-            if (!complete) {
-                // split segment: leave the partial (m, l next to O) for the merge; the
-                // arrival ticket is taken after this CTA's whole range is streamed
-                if (tid < GROUP) {
-                    part[GROUP * D + tid] = mref[v * 16 + tid];
-                    part[GROUP * D + GROUP + tid] = ltot(tid);
+            if (head_split && misc[4] != 0) {
+                // keep the unnormalised own partial in shared memory; it is merged
+                // with the other contributors' after the loop (this is the range's
+                // last piece)
+                float* const st = reinterpret_cast<float*>(smem + Ly::off_stash);
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt) {
+                    const int dA = warp * DPW + mt * 16 + r, dB = dA + 8;
+                    st[hA * D + dA] = val[mt][0];
+                    st[hB * D + dA] = val[mt][1];
+                    st[hA * D + dB] = val[mt][2];
+                    st[hB * D + dB] = val[mt][3];
+                    if (c < 2) {
+                        st[hC * D + dA] = val[mt][4];
+                        st[hD * D + dA] = val[mt][5];
+                        st[hC * D + dB] = val[mt][6];
+                        st[hD * D + dB] = val[mt][7];
+                    }
                 }
-                if (cc.kseg == 0)
-                    pend0 = sid;
-                else
-                    pend1 = sid;
+                if (tid < GROUP) {
+                    st[GROUP * D + tid] = mref[v * 16 + tid];
+                    st[GROUP * D + GROUP + tid] = ltot(tid);
+                }
+                dsid = sid;
+                dn = n_other;
+            } else {
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt) {
+                    const int dA = warp * DPW + mt * 16 + r, dB = dA + 8;
+                    put(hA, dA, val[mt][0] * fA);
+                    put(hB, dA, val[mt][1] * fB);
+                    put(hA, dB, val[mt][2] * fA);
+                    put(hB, dB, val[mt][3] * fB);
+                    if (c < 2) {
+                        put(hC, dA, val[mt][4] * fC);
+                        put(hD, dA, val[mt][5] * fD);
+                        put(hC, dB, val[mt][6] * fC);
+                        put(hD, dB, val[mt][7] * fD);
+                    }
+                }
+                if (!complete) {
+                    // split segment: leave the partial (m, l next to O) for the merge
+                    if (tid < GROUP) {
+                        part[GROUP * D + tid] = mref[v * 16 + tid];
+                        part[GROUP * D + GROUP + tid] = ltot(tid);
+                    }
+                    if (cc.kseg == 0) {
+                        // the range's first piece: take its arrival ticket now, so the
+                        // CTA holding the segment's head can merge it directly
+                        pend0 = sid;
+                        consumer_sync();
+                        if (tid == 0) {
+                            __threadfence(); // release: the partial precedes the ticket
+                            ticket0 = atomicAdd(p.cnt + sid, 1);
+                        }
+                    } else {
+                        pend1 = sid; // ticket taken after the whole range is streamed
+                    }
+                }
             }
             // no trailing barrier: lred is next written in a later epilogue, and
             // every stage in between passes the per-stage consumer barrier
@@ -1324,20 +1431,65 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
         buf ^= 1;
     }
 
+    // ------------------------------------------------ direct merge of the last head
+    // Other contributors (CTAs blockIdx+1 .. blockIdx+dn, slot 0: the segment is the
+    // first piece of their ranges) had all arrived when the epilogue checked.
+    if (dsid >= 0) {
+        consumer_sync(); // the stash is complete
+        constexpr int CH = GROUP * (D / 4) / NCT;
+        const float* const st = reinterpret_cast<const float*>(smem + Ly::off_stash);
+        const int b = dsid / Hkv, g = dsid - b * Hkv;
+        __nv_bfloat16* const outb = p.out + b * p.o_sb + (long long)(g * GROUP) * p.o_sh;
+        const float ninf = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < CH; ++e) {
+            const int ch = tid + e * NCT, h = ch / (D / 4), d0 = (ch % (D / 4)) * 4;
+            float mk[2], lk[2];
+            float4 ok[2];
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                if (k >= dn) continue;
+                const float* const pk = reinterpret_cast<const float*>(
+                    p.part + static_cast<size_t>((blockIdx.x + 1u + k) * 2u) * PART_BYTES);
+                mk[k] = __ldcg(pk + GROUP * D + h);
+                lk[k] = __ldcg(pk + GROUP * D + GROUP + h);
+                ok[k] = __ldcg(reinterpret_cast<const float4*>(pk + h * D + d0));
+            }
+            const float mo = st[GROUP * D + h];
+            float M = mo;
+#pragma unroll
+            for (int k = 0; k < 2; ++k)
+                if (k < dn) M = fmaxf(M, mk[k]);
+            const float wo = ex2(mo - M);
+            float den = wo * st[GROUP * D + GROUP + h];
+            float4 acc = *reinterpret_cast<const float4*>(st + h * D + d0);
+            acc.x *= wo;
+            acc.y *= wo;
+            acc.z *= wo;
+            acc.w *= wo;
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                if (k >= dn) continue;
+                const float w = mk[k] == ninf ? 0.f : ex2(mk[k] - M);
+                den = fmaf(w, lk[k], den);
+                acc.x = fmaf(w, ok[k].x, acc.x);
+                acc.y = fmaf(w, ok[k].y, acc.y);
+                acc.z = fmaf(w, ok[k].z, acc.z);
+                acc.w = fmaf(w, ok[k].w, acc.w);
+            }
+            const float f = __fdividef(out_scale, den);
+            *reinterpret_cast<uint2*>(outb + h * p.o_sh + d0) =
+                make_uint2(pack_bf16x2(acc.x * f, acc.y * f), pack_bf16x2(acc.z * f, acc.w * f));
+        }
+        if (tid == 0) atomicExch(p.cnt + dsid, 0);
+    }
+
     // ------------------------------------------------ deferred split merges
     // Each split segment's partials are merged by the CTA that arrives last on
     // its counter; the merger resets the counter to zero. The partial stores of
     // all consumer threads precede thread 0's acq_rel ticket through the
     // barrier (release), and the merger's reads follow its ticket (acquire).
     if (pend0 >= 0 || pend1 >= 0) {
-        // contributors of a split segment: CTAs c_first..c_last; c_first's partial
-        // sits in its slot 1 when its range began before the segment
-        auto seg_range = [&](int sid, unsigned& Fs, unsigned& c_first, unsigned& c_last) {
-            const int b = sid / Hkv, g = sid - (sid / Hkv) * Hkv, L = segL[b];
-            Fs = static_cast<unsigned>(Hkv * segP[b] + g * L);
-            c_first = cta_of(Fs, N, G);
-            c_last = cta_of(Fs + static_cast<unsigned>(L) - 1u, N, G);
-        };
         if (tid == 0) {
             int last[2] = {0, 0};
             __threadfence(); // release: every consumer's partial stores precede the tickets
@@ -1347,69 +1499,148 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
                 if (sid < 0) continue;
                 unsigned Fs, cf, cl;
                 seg_range(sid, Fs, cf, cl);
-                last[q] = atomicAdd(p.cnt + sid, 1) == static_cast<int>(cl - cf) ? 1 : 0;
+                const int ticket = q == 0 ? ticket0 : atomicAdd(p.cnt + sid, 1);
+                last[q] = ticket == static_cast<int>(cl - cf) ? 1 : 0;
             }
             __threadfence(); // acquire: the merge reads below follow the tickets
             misc[2] = last[0];
             misc[3] = last[1];
         }
-        consumer_sync();
-        const float ninf = -INFINITY;
-#pragma unroll 1
-        for (int q = 0; q < 2; ++q) {
-            const int sid = q == 0 ? pend0 : pend1;
-            if (sid < 0 || !misc[2 + q]) continue;
+        // The merges this CTA owns (at most two segments) are cut into batches of
+        // up to MERGE_BATCH contributors. Whole partials come by bulk copy (TMA
+        // engine) into two alternating shared-memory buffers over the idle stage
+        // ring, so one batch lands while the previous one is combined; a
+        // segment's running (M, den, acc) is rescaled once per batch.
+        if (consumer_sync_or(*abort_flag != 0)) return; // a wait ran out: partials untrustworthy
+        int nq0 = 0, nq1 = 0;
+        unsigned cf0 = 0, cf1 = 0, fs0 = 0, fs1 = 0;
+        {
             unsigned Fs, c_first, c_last;
-            seg_range(sid, Fs, c_first, c_last);
-            const int b = sid / Hkv, g = sid - b * Hkv;
-            __nv_bfloat16* const outb = p.out + b * p.o_sb + (long long)(g * GROUP) * p.o_sh;
-            constexpr int CH = GROUP * (D / 4) / NCT; // float4 chunks per thread (3)
-            static_assert(GROUP * (D / 4) % NCT == 0, "merge chunking");
-            float M[CH], den[CH];
-            float4 acc[CH];
-#pragma unroll
-            for (int e = 0; e < CH; ++e) {
-                M[e] = ninf;
-                den[e] = 0.f;
-                acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (pend0 >= 0 && misc[2]) {
+                seg_range(pend0, Fs, c_first, c_last);
+                nq0 = static_cast<int>(c_last - c_first) + 1;
+                cf0 = c_first;
+                fs0 = cta_begin(c_first, N, G) < Fs ? 1u : 0u;
             }
+            if (pend1 >= 0 && misc[3]) {
+                seg_range(pend1, Fs, c_first, c_last);
+                nq1 = static_cast<int>(c_last - c_first) + 1;
+                cf1 = c_first;
+                fs1 = cta_begin(c_first, N, G) < Fs ? 1u : 0u;
+            }
+        }
+        const int nb0 = (nq0 + MERGE_BATCH - 1) / MERGE_BATCH;
+        const int nbatch = nb0 + (nq1 + MERGE_BATCH - 1) / MERGE_BATCH;
+        if (nbatch == 0) return;
+        uint8_t* const mbuf = smem + Ly::off_stage;
+        // batch k -> (segment q, first contributor, count)
+        auto batch = [&](int k, int& q, int& k0, int& n) {
+            q = k < nb0 ? 0 : 1;
+            k0 = (q == 0 ? k : k - nb0) * MERGE_BATCH;
+            n = min(MERGE_BATCH, (q == 0 ? nq0 : nq1) - k0);
+        };
+        auto issue = [&](int k) { // thread 0 only
+            int q, k0, n;
+            batch(k, q, k0, n);
+            const uint32_t bar = merge_bar(k & 1);
+            mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n * PART_BYTES));
+            for (int j = 0; j < n; ++j) {
+                const unsigned cta = (q == 0 ? cf0 : cf1) + static_cast<unsigned>(k0 + j);
+                const unsigned slot = j + k0 == 0 ? (q == 0 ? fs0 : fs1) : 0u;
+                bulk_g2s(smem_u32(mbuf + ((k & 1) * MERGE_BATCH + j) * PART_BYTES),
+                         p.part + static_cast<size_t>(cta * 2u + slot) * PART_BYTES, PART_BYTES,
+                         bar);
+            }
+        };
+        // earlier generic accesses of the stage ring (this CTA) and the other
+        // CTAs' partial stores (acquired through the tickets) before the async proxy
+        fence_proxy_async_all();
+        consumer_sync();
+        if (tid == 0) {
+            issue(0);
+            if (nbatch > 1) issue(1);
+        }
+        constexpr int CH = GROUP * (D / 4) / NCT; // float4 chunks per thread (3)
+        static_assert(GROUP * (D / 4) % NCT == 0, "merge chunking");
+        const float ninf = -INFINITY;
+        int hh[CH], dd[CH];
+        float M[CH], den[CH];
+        float4 acc[CH];
+#pragma unroll
+        for (int e = 0; e < CH; ++e) {
+            const int ch = tid + e * NCT;
+            hh[e] = ch / (D / 4);
+            dd[e] = (ch % (D / 4)) * 4;
+            M[e] = ninf;
+            den[e] = 0.f;
+            acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
 #pragma unroll 1
-            for (unsigned cta = c_first; cta <= c_last; ++cta) {
-                const unsigned slot = (cta == c_first && cta_begin(cta, N, G) < Fs) ? 1u : 0u;
-                const float* pk = reinterpret_cast<const float*>(
-                    p.part + static_cast<size_t>(cta * 2u + slot) * PART_BYTES);
-                float mv[CH], lv[CH];
-                float4 ov[CH];
+        for (int k = 0; k < nbatch; ++k) {
+            int q, k0, n;
+            batch(k, q, k0, n);
+            const bool landed = mbar_wait_copies(merge_bar(k & 1), (k >> 1) & 1, p.err);
+            const float* const pb =
+                reinterpret_cast<const float*>(mbuf + (k & 1) * MERGE_BATCH * PART_BYTES);
+            constexpr int PF = PART_BYTES / 4;
+            float Mb[CH];
 #pragma unroll
-                for (int e = 0; e < CH; ++e) {
-                    const int ch = tid + e * NCT, h = ch / (D / 4), d0 = (ch % (D / 4)) * 4;
-                    mv[e] = __ldcg(pk + GROUP * D + h);
-                    lv[e] = __ldcg(pk + GROUP * D + GROUP + h);
-                    ov[e] = __ldcg(reinterpret_cast<const float4*>(pk + h * D + d0));
-                }
+            for (int e = 0; e < CH; ++e) Mb[e] = M[e];
+            for (int j = 0; j < n; ++j) {
 #pragma unroll
-                for (int e = 0; e < CH; ++e) {
-                    if (mv[e] == ninf) continue;
-                    const float Mn = fmaxf(M[e], mv[e]);
-                    const float r0 = M[e] == ninf ? 0.f : ex2(M[e] - Mn);
-                    const float w = ex2(mv[e] - Mn);
-                    den[e] = den[e] * r0 + w * lv[e];
-                    acc[e].x = acc[e].x * r0 + w * ov[e].x;
-                    acc[e].y = acc[e].y * r0 + w * ov[e].y;
-                    acc[e].z = acc[e].z * r0 + w * ov[e].z;
-                    acc[e].w = acc[e].w * r0 + w * ov[e].w;
-                    M[e] = Mn;
-                }
+                for (int e = 0; e < CH; ++e) Mb[e] = fmaxf(Mb[e], pb[j * PF + GROUP * D + hh[e]]);
             }
 #pragma unroll
             for (int e = 0; e < CH; ++e) {
-                const int ch = tid + e * NCT, h = ch / (D / 4), d0 = (ch % (D / 4)) * 4;
-                const float f = __fdividef(out_scale, den[e]);
-                *reinterpret_cast<uint2*>(outb + h * p.o_sh + d0) =
-                    make_uint2(pack_bf16x2(acc[e].x * f, acc[e].y * f),
-                               pack_bf16x2(acc[e].z * f, acc[e].w * f));
+                // a contributor's m never exceeds Mb; an empty one (m = -inf) weighs 0
+                const float r = M[e] == ninf ? 0.f : ex2(M[e] - Mb[e]);
+                den[e] *= r;
+                acc[e].x *= r;
+                acc[e].y *= r;
+                acc[e].z *= r;
+                acc[e].w *= r;
+                M[e] = Mb[e];
             }
-            if (tid == 0) atomicExch(p.cnt + sid, 0);
+            for (int j = 0; j < n; ++j) {
+                const float* const pk = pb + j * PF;
+#pragma unroll
+                for (int e = 0; e < CH; ++e) {
+                    const float mv = pk[GROUP * D + hh[e]];
+                    const float w = mv == ninf ? 0.f : ex2(mv - M[e]);
+                    const float4 ov = *reinterpret_cast<const float4*>(pk + hh[e] * D + dd[e]);
+                    den[e] = fmaf(w, pk[GROUP * D + GROUP + hh[e]], den[e]);
+                    acc[e].x = fmaf(w, ov.x, acc[e].x);
+                    acc[e].y = fmaf(w, ov.y, acc[e].y);
+                    acc[e].z = fmaf(w, ov.z, acc[e].z);
+                    acc[e].w = fmaf(w, ov.w, acc[e].w);
+                }
+            }
+            // this buffer's reads precede the bulk copy that refills it; a batch
+            // that did not land in time ends the merge for every consumer thread
+            // (after one more bounded wait for copies still in flight)
+            fence_proxy_async();
+            if (consumer_sync_or(!landed)) {
+                mbar_wait_copies(merge_bar(k & 1), (k >> 1) & 1, p.err);
+                if (nbatch > k + 1) mbar_wait_copies(merge_bar((k + 1) & 1), ((k + 1) >> 1) & 1, p.err);
+                return;
+            }
+            if (tid == 0 && k + 2 < nbatch) issue(k + 2);
+            if (k0 + n == (q == 0 ? nq0 : nq1)) { // the segment's last batch: normalise and store
+                const int sid = q == 0 ? pend0 : pend1;
+                const int b = sid / Hkv, g = sid - b * Hkv;
+                __nv_bfloat16* const outb = p.out + b * p.o_sb + (long long)(g * GROUP) * p.o_sh;
+#pragma unroll
+                for (int e = 0; e < CH; ++e) {
+                    const float f = __fdividef(out_scale, den[e]);
+                    *reinterpret_cast<uint2*>(outb + hh[e] * p.o_sh + dd[e]) =
+                        make_uint2(pack_bf16x2(acc[e].x * f, acc[e].y * f),
+                                   pack_bf16x2(acc[e].z * f, acc[e].w * f));
+                    M[e] = ninf;
+                    den[e] = 0.f;
+                    acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+                if (tid == 0) atomicExch(p.cnt + sid, 0);
+            }
         }
     }
 }
