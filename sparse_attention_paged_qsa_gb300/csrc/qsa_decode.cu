@@ -288,6 +288,16 @@ __device__ __noinline__ bool mbar_wait_copies(uint32_t bar, uint32_t parity, int
     }
 }
 
+// Programmatic dependent launch: wait until the grids this launch depends on
+// have completed and their memory is visible (a no-op for an ordinary launch);
+// let the next dependent launch be scheduled.
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ int ld_relaxed(const int* ptr) {
     int v;
     asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
@@ -632,6 +642,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
                      rem % (Q_RS / 16);
         *dst = make_uint4(0, 0, 0, 0);
     }
+    // Everything above touched shared memory only; global memory is read and
+    // written from here on, after the previous grid in the stream has finished.
+    griddep_wait();
+    griddep_launch_dependents();
     // sanitised lengths, index offsets and prefix sums (warp 0; bs <= 128)
     if (warp == 0) {
         int bad = 0, Ls[4], run = 0;
@@ -1492,7 +1506,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
     if (pend0 >= 0 || pend1 >= 0) {
         if (tid == 0) {
             int last[2] = {0, 0};
-            __threadfence(); // release: every consumer's partial stores precede the tickets
+            // pend0's ticket was taken when its partial was stored; pend1's is now
+            if (pend1 >= 0) __threadfence(); // release: the partial stores precede it
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
                 const int sid = q == 0 ? pend0 : pend1;
@@ -1502,7 +1517,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
                 const int ticket = q == 0 ? ticket0 : atomicAdd(p.cnt + sid, 1);
                 last[q] = ticket == static_cast<int>(cl - cf) ? 1 : 0;
             }
-            __threadfence(); // acquire: the merge reads below follow the tickets
+            if (last[0] || last[1]) __threadfence(); // acquire: the merge reads follow
             misc[2] = last[0];
             misc[3] = last[1];
         }
@@ -1766,8 +1781,20 @@ int launch(const Params& prm, int grid, int dev, cudaStream_t stream) {
             g_dev[dev].smem_set[FMT] = true;
         }
     }
-    qsa_decode_kernel<FMT><<<grid, NTHREADS, smem, stream>>>(prm);
-    cudaError_t e = cudaGetLastError();
+    // programmatic dependent launch: the kernel waits for the previous grid
+    // itself (griddepcontrol.wait) before it touches global memory
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(NTHREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, qsa_decode_kernel<FMT>, prm);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return fail(QSA_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
     return QSA_OK;
 }

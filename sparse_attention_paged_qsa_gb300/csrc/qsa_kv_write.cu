@@ -343,6 +343,16 @@ __device__ __forceinline__ void fill_grouped_table(uint32_t* tab, float qmax) {
     }
 }
 
+// Programmatic dependent launch: wait until the grids this launch depends on
+// have completed and their memory is visible (a no-op for an ordinary launch);
+// let the next dependent launch be scheduled.
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 template <int FMT>
 __global__ void __launch_bounds__(WARPS * 32, 5) kv_write_kernel(const Params p) {
     constexpr bool GROUPED = FMT == QSA_KV_INT8_G64 || FMT == QSA_KV_INT4_G32;
@@ -369,6 +379,9 @@ __global__ void __launch_bounds__(WARPS * 32, 5) kv_write_kernel(const Params p)
         fill_grouped_table(r_tab, 127.0f);
         __syncthreads();
     }
+    // the tables above are shared memory only; global memory from here on
+    griddep_wait();
+    griddep_launch_dependents();
     if constexpr (FMT == QSA_KV_FP8_E4M3) {
         fp8_factors(__ldg(static_cast<const float*>(p.kscale)), &conv.k_lo, &conv.k_hi);
         fp8_factors(__ldg(static_cast<const float*>(p.vscale)), &conv.v_lo, &conv.v_hi);
@@ -399,6 +412,8 @@ __global__ void __launch_bounds__(WARPS * 32, 5) kv_write_kernel(const Params p)
 // Tiered write, first kernel: every token marks its ring position with -2 - i;
 // the minimum, i.e. the last token of the write mapping there, remains.
 __global__ void ring_claim_kernel(const int* slots, int n, long long num_slots, int* owner, int mask) {
+    griddep_wait();
+    griddep_launch_dependents();
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
         const int slot = __ldg(slots + i);
         if (slot < 0 || (long long)slot >= num_slots) continue;
@@ -420,11 +435,28 @@ int fail(int code, const char* fmt, ...) {
 
 bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
+// Launch with programmatic stream serialization: the kernels wait for the
+// previous grid themselves (griddepcontrol.wait) before touching global memory.
+template <typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Args...), unsigned grid, unsigned block, cudaStream_t st,
+                       Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+    return e == cudaSuccess ? cudaGetLastError() : e;
+}
+
 template <int FMT> int launch(const Params& prm, cudaStream_t st) {
     const long long tasks = 2LL * prm.n * prm.Hkv;
     const long long blocks = (tasks + WARPS * RPW - 1) / (WARPS * RPW);
-    kv_write_kernel<FMT><<<static_cast<unsigned>(blocks), WARPS * 32, 0, st>>>(prm);
-    const cudaError_t e = cudaGetLastError();
+    const cudaError_t e = launch_pdl(kv_write_kernel<FMT>, static_cast<unsigned>(blocks), WARPS * 32, st, prm);
     if (e != cudaSuccess) return fail(QSA_ERR_CUDA, "kv write launch: %s", cudaGetErrorString(e));
     return QSA_OK;
 }
@@ -573,9 +605,9 @@ extern "C" int qsa_kv_write_tiered(const qsa_tensor* k_new, const qsa_tensor* v_
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int threads = 256;
     const long long want = (prm.n + threads - 1) / threads;
-    ring_claim_kernel<<<static_cast<unsigned>(want < 4096 ? want : 4096), threads, 0, st>>>(
-        prm.slots, prm.n, prm.num_slots, prm.owner, prm.ring_mask);
-    const cudaError_t e = cudaGetLastError();
+    const cudaError_t e = launch_pdl(ring_claim_kernel, static_cast<unsigned>(want < 4096 ? want : 4096),
+                                     threads, st, prm.slots, prm.n, prm.num_slots, prm.owner,
+                                     prm.ring_mask);
     if (e != cudaSuccess) return fail(QSA_ERR_CUDA, "ring claim launch: %s", cudaGetErrorString(e));
     return launch<QSA_KV_INT8RING_INT4>(prm, st);
 }
