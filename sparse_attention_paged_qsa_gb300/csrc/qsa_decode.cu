@@ -631,6 +631,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
             mbar_init(merge_bar(i), 1);
         }
         misc[0] = 0;
+        // merge bookkeeping of the consumer loop (see mstate below)
+        misc[8] = -1;  // pend0
+        misc[9] = -1;  // pend1
+        misc[10] = -1; // dsid
+        misc[11] = 0;  // dn
+        misc[12] = -1; // ticket0 (thread 0)
         fence_mbarrier_init();
     }
     // zero the padding rows 12..15 of both Q tiles (rows of the 16-row MMA tile)
@@ -868,10 +874,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
     float o[MT][3][4];
     float l0 = 0.f, l1 = 0.f;
     int v = 0, buf = 0, seg_j0 = 0;
-    int pend0 = -1, pend1 = -1;     // split segments whose partial this CTA wrote
-    int ticket0 = -1;               // thread 0: the arrival ticket taken for pend0
-    int dsid = -1, dn = 0;          // directly merged segment head, its other contributors
-    int arrived = -1;               // thread 0: that segment's counter, read a stage early
+    // Merge bookkeeping, kept in shared memory rather than in registers carried
+    // through the main loop: [0] pend0 / [1] pend1, the split segments whose
+    // partial this CTA wrote (first / last piece of its range); [2] the segment
+    // head merged directly after the loop and [3] its other contributors; [4]
+    // thread 0's arrival ticket for pend0. Every consumer thread writes the same
+    // values, so each reads back what it wrote.
+    volatile int* const mstate = misc + 8;
     // contributors of a split segment: CTAs c_first..c_last; c_first's partial
     // sits in its slot 1 when its range began before the segment
     auto seg_range = [&](int sid, unsigned& Fs, unsigned& c_first, unsigned& c_last) {
@@ -896,9 +905,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
         const bool first = cc.segfirst;
         const bool last = cc.j + n >= cc.j1;
         const int b = cc.b, g = cc.g;
-        // the head of a segment this range ends in: read its arrival counter now,
-        // a stage before the epilogue needs it
-        if (tid == 0 && last && cc.kseg != 0 && cc.j1 < segL[b]) arrived = ld_relaxed(p.cnt + b * Hkv + g);
         if (first) {
             seg_j0 = cc.j;
             const int qb = cc.kseg & 1;
@@ -1333,7 +1339,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
                 seg_range(sid, Fs, c_first, c_last);
                 n_other = static_cast<int>(c_last - c_first); // c_first is this CTA
                 if (tid == 0) {
-                    const bool all_in = n_other <= 2 && arrived == n_other;
+                    const bool all_in = n_other <= 2 && ld_relaxed(p.cnt + sid) == n_other;
                     if (all_in) fence_acq_rel_gpu(); // acquire: their partials precede
                     misc[4] = all_in ? 1 : 0;
                 }
@@ -1401,8 +1407,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
                     st[GROUP * D + tid] = mref[v * 16 + tid];
                     st[GROUP * D + GROUP + tid] = ltot(tid);
                 }
-                dsid = sid;
-                dn = n_other;
+                mstate[2] = sid;
+                mstate[3] = n_other;
             } else {
 #pragma unroll
                 for (int mt = 0; mt < MT; ++mt) {
@@ -1427,14 +1433,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
                     if (cc.kseg == 0) {
                         // the range's first piece: take its arrival ticket now, so the
                         // CTA holding the segment's head can merge it directly
-                        pend0 = sid;
+                        mstate[0] = sid;
                         consumer_sync();
                         if (tid == 0) {
                             __threadfence(); // release: the partial precedes the ticket
-                            ticket0 = atomicAdd(p.cnt + sid, 1);
+                            mstate[4] = atomicAdd(p.cnt + sid, 1);
                         }
                     } else {
-                        pend1 = sid; // ticket taken after the whole range is streamed
+                        mstate[1] = sid; // ticket taken after the whole range is streamed
                     }
                 }
             }
@@ -1446,6 +1452,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
     }
 
     // ------------------------------------------------ direct merge of the last head
+    const int pend0 = mstate[0], pend1 = mstate[1], dsid = mstate[2], dn = mstate[3];
     // Other contributors (CTAs blockIdx+1 .. blockIdx+dn, slot 0: the segment is the
     // first piece of their ranges) had all arrived when the epilogue checked.
     if (dsid >= 0) {
@@ -1514,7 +1521,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
                 if (sid < 0) continue;
                 unsigned Fs, cf, cl;
                 seg_range(sid, Fs, cf, cl);
-                const int ticket = q == 0 ? ticket0 : atomicAdd(p.cnt + sid, 1);
+                const int ticket = q == 0 ? mstate[4] : atomicAdd(p.cnt + sid, 1);
                 last[q] = ticket == static_cast<int>(cl - cf) ? 1 : 0;
             }
             if (last[0] || last[1]) __threadfence(); // acquire: the merge reads follow
