@@ -77,6 +77,8 @@ constexpr float TAU = 8.0f;                 // lazy-rescale threshold (log2 unit
 constexpr int MAX_BS = 128;
 constexpr int MAX_CAPACITY = 2055;
 constexpr int MIN_TOKENS_PER_CTA = 64;
+constexpr unsigned FEW_SEGMENTS = 4;        // up to this many (sequence, KV head) segments ...
+constexpr unsigned MAX_FANIN = 16;          // ... each gets a whole number (<= this) of CTAs
 constexpr int PART_BYTES = 12416;           // fp32 O[12][256] + m[12] + l[12], 128-byte multiple
 constexpr int MERGE_BATCH = 6;             // partials per bulk-copy batch of the split merge
 constexpr long long WAIT_NS = 2000000000LL; // bounded-wait limit (2 s)
@@ -716,6 +718,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
     if (N == 0) return;
     unsigned G = (N + MIN_TOKENS_PER_CTA - 1) / MIN_TOKENS_PER_CTA;
     G = G < gridDim.x ? G : gridDim.x;
+    // Few segments (bs * Hkv <= FEW_SEGMENTS): a whole number of CTAs per segment,
+    // at most MAX_FANIN. With equal lengths no CTA then holds pieces of two
+    // segments, so their merges run on different CTAs, and each merge reads at
+    // most MAX_FANIN partials.
+    {
+        const unsigned S = static_cast<unsigned>(p.bs * Hkv);
+        if (S <= FEW_SEGMENTS && 2 * S <= G) {
+            const unsigned per = G / S < MAX_FANIN ? G / S : MAX_FANIN;
+            G = per * S;
+        }
+    }
     if (blockIdx.x >= G) return;
     const long long t_begin = cta_begin(blockIdx.x, N, G);
     const long long t_end = cta_begin(blockIdx.x + 1, N, G);
