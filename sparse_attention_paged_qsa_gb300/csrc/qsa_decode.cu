@@ -50,6 +50,7 @@
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
+#include <cstdlib>
 #include <initializer_list>
 #include <mutex>
 #include <string>
@@ -204,6 +205,7 @@ struct Params {
     const void* vring_scale;
     const int* owner;
     int ring_mask; // R - 1
+    int stall_stage; // test hook: CTA 0's producers leave this stage incomplete (-1: off)
 };
 
 // Byte offset of 16-byte chunk `chunk` of row `row` in a swizzled row buffer.
@@ -862,8 +864,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
                         *reinterpret_cast<uint4*>(sc + T * Ly::SC_TOK + mytok * 16) = make_uint4(0, 0, 0, 0);
                 }
             }
-            cp_async_arrive_noinc(full_bar(s));
-            mbar_arrive(full_bar(s));
+            if (blockIdx.x != 0 || i != p.stall_stage) {
+                cp_async_arrive_noinc(full_bar(s));
+                mbar_arrive(full_bar(s));
+            }
             cursor_advance(ic, t_end, segL, Hkv);
         }
         cp_async_wait<0>();
@@ -1771,6 +1775,15 @@ void layout_for(int32_t bs, int32_t num_q_heads, long long grid, qsa_scratch_lay
 
 bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
+// Test hook for the bounded pipeline waits: with QSA_TEST_STALL_STAGE=k in the
+// environment, CTA 0's producers never complete their k-th stage. Its consumers'
+// wait then runs out (WAIT_NS), the launch records QSA_DEVERR_TIMEOUT and ends;
+// nothing faults and nothing spins without a limit.
+int test_stall_stage() {
+    const char* e = std::getenv("QSA_TEST_STALL_STAGE");
+    return e ? std::atoi(e) : -1;
+}
+
 int check_row_tensor(const qsa_tensor* t, const char* name, int bs, int hq) {
     if (t->dtype != QSA_DTYPE_BF16)
         return fail(QSA_ERR_UNSUPPORTED, "%s must be bf16 (dtype %d given)", name, t->dtype);
@@ -2013,6 +2026,7 @@ int qsa_decode(const qsa_tensor* q, const qsa_tensor* k_pool, const qsa_tensor* 
     prm.kring_scale = prm.vring_scale = nullptr;
     prm.owner = nullptr;
     prm.ring_mask = 0;
+    prm.stall_stage = test_stall_stage();
     if (fmt == QSA_KV_INT8RING_INT4) {
         prm.kring = static_cast<const uint8_t*>(tier->k_ring);
         prm.vring = static_cast<const uint8_t*>(tier->v_ring);
