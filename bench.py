@@ -298,21 +298,41 @@ def run_native(args):
     if err:
         raise RuntimeError(f"device error flags {err}")
 
-    # e2e: host (pinned) q / slot ids / cu_seqlens -> device, decode, output -> host
+    # e2e: host (pinned) q / slot ids / cu_seqlens -> device, decode, output -> host,
+    # every step. Device inputs and outputs are double-buffered over three streams
+    # (copy in, compute, copy out), as a serving loop would run them: step k+1's
+    # inputs land while step k computes, and step k's output returns meanwhile.
     e2e_steps = args.steps if not args.no_e2e else 0
     hq_ = [w.q.cpu().pin_memory() for w in works]
     hsel = [w.sel.cpu().pin_memory() for w in works]
     hcu = [w.cu.cpu().pin_memory() for w in works]
-    hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-    dq, dsel, dcu = torch.empty_like(w0.q), torch.empty_like(w0.sel), torch.empty_like(w0.cu)
+    hout = [torch.empty(out.shape, dtype=out.dtype, pin_memory=True) for _ in range(2)]
+    dq = [torch.empty_like(w0.q) for _ in range(2)]
+    dsel = [torch.empty_like(w0.sel) for _ in range(2)]
+    dcu = [torch.empty_like(w0.cu) for _ in range(2)]
+    dout = [torch.empty_like(out) for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    in_ready = [torch.cuda.Event() for _ in range(2)]   # inputs of buffer j copied in
+    computed = [torch.cuda.Event() for _ in range(2)]   # decode of buffer j done
+    drained = [torch.cuda.Event() for _ in range(2)]    # output of buffer j copied out
+    for j in range(2):
+        drained[j].record(stream)
 
     def e2e_step(k):
-        j = k % len(works)
-        dq.copy_(hq_[j], non_blocking=True)
-        dsel.copy_(hsel[j], non_blocking=True)
-        dcu.copy_(hcu[j], non_blocking=True)
-        qsa.qsa_decode(dq, w0.k_pool, w0.v_pool, meta, dsel, dcu, out, scratch, stream)
-        hout.copy_(out, non_blocking=True)
+        j, b = k % len(works), k % 2
+        s_in.wait_event(drained[b])        # the buffer's previous decode and copy-out are done
+        with torch.cuda.stream(s_in):
+            dq[b].copy_(hq_[j], non_blocking=True)
+            dsel[b].copy_(hsel[j], non_blocking=True)
+            dcu[b].copy_(hcu[j], non_blocking=True)
+        in_ready[b].record(s_in)
+        stream.wait_event(in_ready[b])
+        qsa.qsa_decode(dq[b], w0.k_pool, w0.v_pool, meta, dsel[b], dcu[b], dout[b], scratch, stream)
+        computed[b].record(stream)
+        s_out.wait_event(computed[b])
+        with torch.cuda.stream(s_out):
+            hout[b].copy_(dout[b], non_blocking=True)
+        drained[b].record(s_out)
 
     e2e_ms = float("nan")
     if e2e_steps:
@@ -321,13 +341,15 @@ def run_native(args):
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
+        s_in.wait_stream(stream)  # nothing of the timed steps starts before e0
         for k in range(e2e_steps):
             e2e_step(k)
+        stream.wait_stream(s_out)  # ... and e1 follows the last copy out
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = e0.elapsed_time(e1) / e2e_steps
     h2d = hq_[0].numel() * 2 + hsel[0].numel() * 4 + hcu[0].numel() * 4
-    d2h = hout.numel() * 2
+    d2h = hout[0].numel() * 2
 
     step_ms = total_ms / args.steps
     step_ms, e2e_ms = reduce_max([step_ms, e2e_ms if e2e_steps else 0.0], dev)
