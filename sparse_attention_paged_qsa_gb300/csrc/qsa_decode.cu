@@ -92,7 +92,8 @@ static_assert(PART_BYTES % 16 == 0, "bulk copies move 16-byte multiples");
 // per-slot scales (fp32 per (slot, KV head), or binary16 per (slot, KV head,
 // channel group) when GROUPS > 0); QK_F16: QK runs on f16 operands (exact
 // integer / e4m3 codes, Q rescaled per head by a power of two); PV_F16: PV runs
-// on f16 operands (only when no per-slot scale enters P); NIB4: 4-bit codes,
+// on f16 operands (for int8, with a per-head power-of-two offset that keeps
+// P * s_v in range); NIB4: 4-bit codes,
 // NIB_OFFSET: stored as code + 8 (else two's complement); TIER: each row is an
 // int8_g64 ring row or an int4_g32 pool row, by the owner table (scales held at
 // the 32-channel granularity, a ring row's 64-channel scales expanded).
@@ -111,7 +112,7 @@ template <> struct Traits<QSA_KV_FP8_E4M3> {
 };
 template <> struct Traits<QSA_KV_INT8> {
     static constexpr int ROWB = 256, STAGES = 4, GROUPS = 0;
-    static constexpr bool DEQ = true, SCALES = true, QK_F16 = true, PV_F16 = false;
+    static constexpr bool DEQ = true, SCALES = true, QK_F16 = true, PV_F16 = true;
     static constexpr bool NIB4 = false, NIB_OFFSET = false;
     static constexpr bool TIER = false;
 };
@@ -160,7 +161,12 @@ template <int FMT> struct Layout {
     static constexpr int off_red = off_p + p_bytes;
     static constexpr int off_mref = off_red + 2 * NW * 16 * 4;
     static constexpr int off_lred = off_mref + 2 * 16 * 4;
-    static constexpr int off_ring = off_lred + NW * 16 * 4;
+    // per-slot V scales (f16 PV): per-warp maxima of the scale offsets t, and
+    // the per-head offsets E (double-buffered like mref)
+    static constexpr bool NUM_REF = Tr::SCALES && Tr::GROUPS == 0 && Tr::PV_F16;
+    static constexpr int off_nred = off_lred + NW * 16 * 4;
+    static constexpr int off_eref = off_nred + (NUM_REF ? NW * 16 * 4 : 0);
+    static constexpr int off_ring = off_eref + (NUM_REF ? 2 * 16 * 4 : 0);
     static constexpr int off_segL = off_ring + R * T * 4;
     static constexpr int off_segSrc = off_segL + (MAX_BS + 4) * 4;
     static constexpr int off_segP = off_segSrc + (MAX_BS + 4) * 4;
@@ -885,6 +891,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
     float* const red = reinterpret_cast<float*>(smem + Ly::off_red);    // [2][NW][16]
     float* const mref = reinterpret_cast<float*>(smem + Ly::off_mref);  // [2][16]
     float* const lred = reinterpret_cast<float*>(smem + Ly::off_lred);  // [NW][16]
+    float* const nred = reinterpret_cast<float*>(smem + Ly::off_nred);  // [NW][16]
+    float* const eref = reinterpret_cast<float*>(smem + Ly::off_eref);  // [2][16]
+    constexpr bool VSH = Ly::NUM_REF;
 
     uint32_t qa[16][4];
     float qmul_a = 1.f, qmul_b = 1.f; // undo the per-head Q scaling of f16 QK
@@ -1192,6 +1201,33 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
         const float* const mrefv = mref + v * 16;
         const float mo_a = first ? ninf : mrefv[r];
         const float mo_b = first ? ninf : mrefv[r + 8];
+        // Per-slot V scales in f16 PV (int8): PV runs on pn = p * s_v * 2^-E_h,
+        // p = 2^(x - m_h). The per-head offset E_h is kept at or above every
+        // t = (x - m_h) + floor(log2 |s_v|) - 14 of the piece, so pn < 2^15 (when
+        // a t exceeds it, it rises to that t + TAU, so it seldom rises again); it
+        // is held relative to the reference m_h, so that a huge score cannot
+        // absorb the scale's exponent. O is accumulated against m_h + E_h,
+        // rescaled when that rises and multiplied by 2^E_h in the epilogue.
+        // E_h >= -119 keeps 2^-E_h and p * 2^-E_h finite.
+        float fa = 1.f, fb = 1.f, eo_a = 0.f, eo_b = 0.f, g0 = 0.f, g1 = 0.f;
+        const float* const erefv = eref + v * 16;
+        bool vraise = false;
+        if constexpr (VSH) {
+            auto lgs = [](float sv) {
+                return static_cast<float>(static_cast<int>((__float_as_uint(sv) >> 23) & 0xFFu) - 141);
+            };
+            g0 = lgs(svr[0]);
+            g1 = lgs(svr[1]);
+            if (!first) {
+                eo_a = erefv[r];
+                eo_b = erefv[r + 8];
+                fa = ex2(-eo_a);
+                fb = row8 ? ex2(-eo_b) : 0.f;
+                const float ta = fmaxf((x[0] - mo_a) + g0, (x[1] - mo_a) + g1);
+                const float tb = fmaxf((x[2] - mo_b) + g0, (x[3] - mo_b) + g1);
+                vraise = ta > eo_a || (row8 && tb > eo_b);
+            }
+        }
 
         uint8_t* const Pb = smem + Ly::off_p + buf * 24 * PRS;
         float pr[4];
@@ -1203,7 +1239,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
         };
         float* const Pf = reinterpret_cast<float*>(smem + Ly::off_p) + buf * GROUP * T;
         auto write_p = [&]() {
-            float pv[4] = {pr[0] * svr[0], pr[1] * svr[1], pr[2] * svr[0], pr[3] * svr[1]};
+            // p * s_v * f in an order whose partial product stays finite: with f <= 1,
+            // s_v * f <= s_v; with f > 1, p * f <= 2^TAU * 2^119 (masked tokens have p = 0)
+            auto pnum = [](float pp, float sv, float f) { return f <= 1.f ? pp * (sv * f) : (pp * f) * sv; };
+            float pv[4] = {pnum(pr[0], svr[0], fa), pnum(pr[1], svr[1], fa), pnum(pr[2], svr[0], fb),
+                           pnum(pr[3], svr[1], fb)};
             pv[0] = v0 ? pv[0] : 0.f;
             pv[1] = v1 ? pv[1] : 0.f;
             pv[2] = v0 ? pv[2] : 0.f;
@@ -1228,7 +1268,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
         write_p();
         // One barrier publishes P and the per-warp maxima and ORs "some score of
         // this stage exceeds its head's reference by more than TAU" over all warps.
-        const bool nd_local = first || ma > mo_a + TAU || (row8 && mb > mo_b + TAU);
+        const bool nd_local = first || ma > mo_a + TAU || (row8 && mb > mo_b + TAU) || vraise;
         if (consumer_sync_or(nd_local)) {
             // stage maximum per head vs the running reference
             auto stage_max = [&](int h) {
@@ -1247,10 +1287,45 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
             const float na = new_ref(r), nb = row8 ? new_ref(r + 8) : 0.f;
             l0 *= alpha(r);
             l1 *= row8 ? alpha(r + 8) : 0.f;
+            // per-slot V scales: the stage's largest offset t per head against the
+            // new references (one more exchange), then the new E_h
+            if constexpr (VSH) {
+                float ta = fmaxf((x[0] - na) + g0, (x[1] - na) + g1);
+                float tb = fmaxf((x[2] - nb) + g0, (x[3] - nb) + g1);
+                ta = fmaxf(ta, __shfl_xor_sync(0xFFFFFFFFu, ta, 1));
+                ta = fmaxf(ta, __shfl_xor_sync(0xFFFFFFFFu, ta, 2));
+                tb = fmaxf(tb, __shfl_xor_sync(0xFFFFFFFFu, tb, 1));
+                tb = fmaxf(tb, __shfl_xor_sync(0xFFFFFFFFu, tb, 2));
+                if (c == 0) {
+                    nred[warp * 16 + r] = ta;
+                    nred[warp * 16 + r + 8] = row8 ? tb : ninf;
+                }
+                consumer_sync();
+            }
+            // E_h after this stage: the old offset carried to the new reference or,
+            // when the stage's largest t exceeds it, that t plus TAU of slack (as the
+            // lazy maximum has), so that E_h rarely needs to rise again; at least
+            // -119 (fmaxf drops the NaN of -inf - -inf)
+            auto new_e = [&](int h) {
+                float t = nred[h];
+#pragma unroll
+                for (int w = 1; w < NW; ++w) t = fmaxf(t, nred[w * 16 + h]);
+                const float carried = first ? ninf : erefv[h] + (old_ref(h) - new_ref(h));
+                return fmaxf(t > carried ? t + TAU : carried, -119.f);
+            };
+            auto o_scale = [&](int h) {
+                if constexpr (!VSH) return alpha(h);
+                if (first || old_ref(h) == ninf) return 0.f; // O is still zero then
+                return ex2((old_ref(h) - new_ref(h)) + (erefv[h] - new_e(h)));
+            };
+            if constexpr (VSH) {
+                fa = ex2(-new_e(r));
+                fb = row8 ? ex2(-new_e(r + 8)) : 0.f;
+            }
             compute_p(na, nb);
             write_p();
-            const float a0 = alpha(2 * c), a1 = alpha(2 * c + 1);
-            const float a2 = alpha(8 + ((2 * c) & 3)), a3 = alpha(8 + ((2 * c + 1) & 3));
+            const float a0 = o_scale(2 * c), a1 = o_scale(2 * c + 1);
+            const float a2 = o_scale(8 + ((2 * c) & 3)), a3 = o_scale(8 + ((2 * c + 1) & 3));
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
@@ -1266,6 +1341,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
                 o[mt][2][3] *= a3;
             }
             if (warp == 0 && lane < GROUP) mref[(v ^ 1) * 16 + lane] = new_ref(lane);
+            if (VSH && warp == 1 && lane < GROUP) eref[(v ^ 1) * 16 + lane] = new_e(lane);
             v ^= 1;
             consumer_sync();
         }
@@ -1378,10 +1454,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
                 return t;
             };
             const int hA = 2 * c, hB = 2 * c + 1, hC = 8 + 2 * c, hD = 9 + 2 * c;
-            const float fA = complete ? __fdividef(out_scale, ltot(hA)) : 1.f;
-            const float fB = complete ? __fdividef(out_scale, ltot(hB)) : 1.f;
-            const float fC = (complete && c < 2) ? __fdividef(out_scale, ltot(hC)) : 1.f;
-            const float fD = (complete && c < 2) ? __fdividef(out_scale, ltot(hD)) : 1.f;
+            // per-slot V scales: O was accumulated against m_h + E_h; back to m_h
+            auto esc = [&](int h) { return VSH ? ex2(eref[v * 16 + h]) : 1.f; };
+            const float eA = esc(hA), eB = esc(hB);
+            const float eC = c < 2 ? esc(hC) : 1.f, eD = c < 2 ? esc(hD) : 1.f;
+            const float fA = complete ? __fdividef(out_scale, ltot(hA)) * eA : eA;
+            const float fB = complete ? __fdividef(out_scale, ltot(hB)) * eB : eB;
+            const float fC = (complete && c < 2) ? __fdividef(out_scale, ltot(hC)) * eC : eC;
+            const float fD = (complete && c < 2) ? __fdividef(out_scale, ltot(hD)) * eD : eD;
             __nv_bfloat16* const outb = p.out + b * p.o_sb + (long long)(g * GROUP) * p.o_sh;
             float* const part = reinterpret_cast<float*>(
                 p.part + ((long long)blockIdx.x * 2 + (cc.kseg == 0 ? 0 : 1)) * PART_BYTES);
@@ -1409,15 +1489,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
 #pragma unroll
                 for (int mt = 0; mt < MT; ++mt) {
                     const int dA = warp * DPW + mt * 16 + r, dB = dA + 8;
-                    st[hA * D + dA] = val[mt][0];
-                    st[hB * D + dA] = val[mt][1];
-                    st[hA * D + dB] = val[mt][2];
-                    st[hB * D + dB] = val[mt][3];
+                    st[hA * D + dA] = val[mt][0] * eA;
+                    st[hB * D + dA] = val[mt][1] * eB;
+                    st[hA * D + dB] = val[mt][2] * eA;
+                    st[hB * D + dB] = val[mt][3] * eB;
                     if (c < 2) {
-                        st[hC * D + dA] = val[mt][4];
-                        st[hD * D + dA] = val[mt][5];
-                        st[hC * D + dB] = val[mt][6];
-                        st[hD * D + dB] = val[mt][7];
+                        st[hC * D + dA] = val[mt][4] * eC;
+                        st[hD * D + dA] = val[mt][5] * eD;
+                        st[hC * D + dB] = val[mt][6] * eC;
+                        st[hD * D + dB] = val[mt][7] * eD;
                     }
                 }
                 if (tid < GROUP) {
