@@ -219,3 +219,21 @@ def test_group_scales_reach_their_channels(cuda_device, fmt):
     ref = torch.tensor([2.0 ** (d // I.GROUPED[fmt]) for d in range(256)])
     for h in range(12):
         assert torch.equal(out[0, h].float().cpu(), ref)
+
+
+@pytest.mark.parametrize("max_ctas", [0, 1])
+def test_int8_wide_v_scales(cuda_device, max_ctas):
+    """int8 PV runs in f16 on P * s_v * 2^-E_h with a per-head offset E_h that must
+    follow the largest products: per-slot V scales spread over 2^-40 .. 2^40, and
+    along one selection rising from 2^-30 to 2^30 (the offset rises stage after
+    stage), against the oracle, with the split merge (all CTAs) and without (one)."""
+    lengths = [2055, 700, 64, 1, 1500, 300]
+    w = I.tp1_mixed(seed=71, bs=len(lengths), num_slots=8192, fmt="int8", lengths=lengths)
+    g = torch.Generator().manual_seed(71)
+    vs = w.v_scale.double().clone()
+    vs *= torch.pow(2.0, torch.randint(-40, 41, vs.shape, generator=g).double())
+    lo, hi = int(w.cu[4]), int(w.cu[5])
+    ramp = torch.pow(2.0, torch.linspace(-30.0, 30.0, hi - lo, dtype=torch.float64))
+    vs[w.sel[lo:hi].long()] = w.v_scale.double()[w.sel[lo:hi].long()] * ramp[:, None]
+    w.v_scale = vs.float()
+    _parity(w, cuda_device, max_ctas)
