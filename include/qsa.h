@@ -24,7 +24,10 @@
  * descriptors on the host (reading no device memory) and enqueues exactly one
  * kernel on `stream`. Live lengths are read from cu_seqlens on the device,
  * so a captured CUDA graph stays valid when cu_seqlens and sel_indices
- * change between replays.
+ * change between replays. Kernels are launched with programmatic stream
+ * serialization: a launch may become resident while the previous grid in the
+ * stream drains, but it waits for that grid (griddepcontrol.wait) before it
+ * reads or writes any global memory, so stream order holds as usual.
  *
  * Scratch. A caller-owned device buffer of qsa_decode_scratch_bytes() bytes,
  * zeroed once with qsa_scratch_init(). It holds a sticky device error word,
