@@ -122,18 +122,29 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-def measured_traffic(fmt: str):
-    """DRAM bytes per launch from profiles/traffic.txt, if taken on the current kernel source."""
+def kernel_source_key(path: str) -> str:
+    """sha256 of a CUDA source with its comments and whitespace removed: a key that
+    changes when the code does, not when a comment does (no string literal in the
+    kernel sources contains a comment marker)."""
     import hashlib
+    import re
 
+    text = open(path, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return hashlib.sha256(" ".join(text.split()).encode()).hexdigest()
+
+
+def measured_traffic(fmt: str):
+    """DRAM bytes per launch from profiles/traffic.txt, if taken on the current kernel code."""
     src = os.path.join(ROOT, "sparse_attention_paged_qsa_gb300", "csrc", "qsa_decode.cu")
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    key = kernel_source_key(src)
     for line in open(path):
         parts = line.split()
-        if len(parts) == 3 and not line.startswith("#") and parts[0] == fmt and parts[2] == sha:
+        if len(parts) == 3 and not line.startswith("#") and parts[0] == fmt and parts[2] == key:
             return int(parts[1])
     return None
 

@@ -14,9 +14,15 @@
 // GB300 design:
 //  * Persistent, balanced grid: the (sequence, KV head, token) space of the
 //    live lengths is cut into gridDim.x equal token ranges on the device, so
-//    a fixed (graph-captured) grid balances any length mix. A CTA whose range
-//    covers a whole (sequence, KV head) segment writes the output directly;
-//    segments cut between CTAs are merged by the last arriving CTA.
+//    a fixed (graph-captured) grid balances any length mix (with at most four
+//    segments, a whole number of CTAs per segment). A CTA whose range covers a
+//    whole (sequence, KV head) segment writes the output directly. A segment
+//    cut between CTAs is merged in the same launch: the CTA that holds its head
+//    at the end of its range merges directly when the other contributors have
+//    already arrived (they take their tickets as soon as their piece is done);
+//    otherwise the last CTA to arrive merges partials it bulk-copies into
+//    shared memory. Launches are programmatic dependent launches that wait for
+//    the previous grid before touching global memory.
 //  * Warp-specialised CTA (one per SM): four producer warps, one per SM
 //    sub-partition, gather whole K/V rows with 16-byte cp.async into a
 //    multi-stage shared-memory ring of 64-token stages, completing each stage
@@ -27,14 +33,17 @@
 //    the 12 heads padded to 16 rows, 8 tokens per warp; a per-stage max
 //    exchange with lazy rescaling (the reference max only moves when a score
 //    exceeds it by 2^8); PV computed transposed, O^T = V^T P^T, with P split
-//    into bf16 hi + lo columns (24 columns: 12 heads x {hi, lo}) so P keeps
-//    ~16 significant bits; each warp owns 32 of the 256 output dims.
+//    into hi + lo columns of the PV operand type (24 columns: 12 heads x {hi,
+//    lo}), so P keeps ~16 (bf16) or ~22 (f16) significant bits; each warp owns
+//    32 of the 256 output dims.
 //  * Quantised pools are converted exactly, in shared memory, by the warp
 //    that consumes them: codes become f16 for QK (Q is rescaled per head by a
-//    power of two so it converts to f16 exactly) and f16 (fp8) or bf16
-//    (int8/int4) for PV, with magic-number integer conversions and the
-//    hardware e4m3 conversion. Per-slot scales scale the scores (K) and the
-//    probabilities (V) in FP32; per-pool fp8 scales fold into constants.
+//    power of two so it converts to f16 exactly) and f16 (fp8, int8) or bf16
+//    (int4, grouped, tiered) for PV, with magic-number integer conversions and
+//    the hardware e4m3 conversion. Per-slot scales scale the scores (K) and the
+//    probabilities (V) in FP32 (int8 keeps a per-head power-of-two offset so
+//    that P times its V scale fits f16); per-pool fp8 scales fold into
+//    constants.
 //    Grouped pools (binary16 scale per 64 / 32 channels): QK accumulates each
 //    channel group's k-steps apart and adds them with the token's group scale;
 //    each consumer warp's 32 PV dims lie in one group, so the warp rebuilds its

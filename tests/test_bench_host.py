@@ -1,7 +1,6 @@
 """Host logic of the measurement (no GPU): the algorithmic bytes every bench line
 divides by, the DRAM-traffic lookup keyed to the kernel source, and the JSON
 contract of the reference arm."""
-import hashlib
 import json
 import os
 
@@ -38,15 +37,17 @@ def test_traffic_lookup_is_keyed_to_the_kernel_source(tmp_path, monkeypatch):
     src_dir.mkdir(parents=True)
     (tmp_path / "profiles").mkdir()
     src = src_dir / "qsa_decode.cu"
-    src.write_bytes(b"kernel v1\n")
-    sha = hashlib.sha256(b"kernel v1\n").hexdigest()
+    src.write_text("int f() { return 1; } // v1\n")
+    key = bench.kernel_source_key(str(src))
     (tmp_path / "profiles" / "traffic.txt").write_text(
-        f"# comment\nbf16 123 {sha}\nint8 456 {'0' * 64}\n")
+        f"# comment\nbf16 123 {key}\nint8 456 {'0' * 64}\n")
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     assert bench.measured_traffic("bf16") == 123
-    assert bench.measured_traffic("int8") is None      # taken on another source
+    assert bench.measured_traffic("int8") is None      # taken on other code
     assert bench.measured_traffic("fp8_e4m3") is None  # never taken
-    src.write_bytes(b"kernel v2\n")                      # the kernel changed since
+    src.write_text("/* a new comment */\nint f()  {\n  return 1;\n}  // v2\n")
+    assert bench.measured_traffic("bf16") == 123       # comments and layout only
+    src.write_text("int f() { return 2; } // v1\n")   # the code changed since
     assert bench.measured_traffic("bf16") is None
 
 
