@@ -8,6 +8,7 @@ the first call raises.
 from __future__ import annotations
 
 import ctypes
+import struct
 import os
 from dataclasses import dataclass
 from typing import Optional
@@ -136,20 +137,24 @@ def _check(rc: int) -> None:
         raise QsaError(rc, msg)
 
 
+# qsa_tensor as packed bytes: void* data, int32 dtype, int32 ndim, int64 shape[4],
+# int64 stride[4] (one pack is faster than filling the ctypes arrays field by field)
+_TENSOR_PACK = struct.Struct("<qii4q4q")
+_PAD = ((), (0,), (0, 0), (0, 0, 0), (0, 0, 0, 0))
+assert _TENSOR_PACK.size == ctypes.sizeof(QsaTensor)
+
+
 def describe(t: Optional[torch.Tensor]) -> QsaTensor:
     """qsa_tensor view of a torch tensor (no copy)."""
-    d = QsaTensor()
     if t is None:
-        return d
-    if t.dim() > 4:
+        return QsaTensor()
+    nd = t.dim()
+    if nd > 4:
         raise ValueError("at most 4 dimensions")
-    d.data = t.data_ptr() if t.numel() else None
-    d.dtype = _TORCH_DTYPES.get(t.dtype, 0)
-    d.ndim = t.dim()
-    for i in range(t.dim()):
-        d.shape[i] = t.shape[i]
-        d.stride[i] = t.stride(i)
-    return d
+    pad = _PAD[4 - nd]
+    return QsaTensor.from_buffer_copy(_TENSOR_PACK.pack(
+        t.data_ptr() if t.numel() else 0, _TORCH_DTYPES.get(t.dtype, 0), nd,
+        *t.shape, *pad, *t.stride(), *pad))
 
 
 @dataclass
