@@ -253,12 +253,12 @@ def run_native(args):
     import sparse_attention_paged_qsa_gb300 as qsa
 
     ws, rank, local = dist_env()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)  # before the process group, so NCCL binds this rank's GPU
     if ws > 1:
         import torch.distributed as dist
 
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
     fmt = args.fmt
     bs = args.bs
     works = make_workloads(fmt, 2 + rank, [100 + 7 * rank + k for k in range(args.index_sets)], dev,
