@@ -165,8 +165,10 @@ int qsa_decode(const qsa_tensor* q, const qsa_tensor* k_pool, const qsa_tensor* 
  *  format      QSA_KV_* of the pools.
  *  k_new,      bf16 [n, Hkv, 256] (Hkv 1 or 2); stride[2] == 1, other strides
  *  v_new       non-negative multiples of 8; base 16-byte aligned. n may be 0.
- *  slots       int32 [n], contiguous: destination slot of token i. Slots should be
- *              distinct within a call; for a repeated slot one of the writes wins.
+ *  slots       int32 [n], contiguous: destination slot of token i. Slots must be
+ *              distinct within a call: each (token, head, K or V) row is written by
+ *              its own warp, so a repeated slot leaves that row's codes and scale
+ *              unspecified (they may mix the repeated tokens' writes).
  *  k_pool,     pools as for qsa_decode; row slot[i] * Hkv + g receives token i, head g.
  *  v_pool
  *  k_scale,    fp8: the pool's fp32 scale [1] (read; must be finite and > 0);
@@ -196,8 +198,10 @@ int qsa_kv_write(int32_t format, const qsa_tensor* k_new, const qsa_tensor* v_ne
  * written twice, as the int4_g32 row of slot[i] (k_pool / v_pool, binary16 scales
  * k_scale / v_scale [num_slots * Hkv * 8], 16-byte aligned) and as the int8_g64 row
  * of ring position p = slot[i] & (R - 1), whose owner entry becomes slot[i]. When
- * several tokens of one call share a ring position, the last of them (largest i)
- * owns it, as if the tokens were written in order; owner and ring row always agree.
+ * several tokens of one call (with distinct slots) share a ring position, the last
+ * of them (largest i) owns it, as if the tokens were written in order; owner and
+ * ring row then agree. Slots must be distinct within a call, as for qsa_kv_write: a
+ * repeated slot leaves its rows, its ring row and the owner entry unspecified.
  * Arguments otherwise as for qsa_kv_write. Enqueues two kernels on `stream` (claim
  * the ring positions, then write); allocates nothing. Between the two, the owner
  * entries of the positions being written hold claim marks (negative values); a
@@ -210,15 +214,25 @@ int qsa_kv_write_tiered(const qsa_tensor* k_new, const qsa_tensor* v_new, const 
 
 /* Scratch bytes a qsa_decode call with these sizes needs on the current
  * device (0 when the sizes are outside the contract). Split-KV partials take
- * two 12 KiB slots per CTA of the grid the library would choose. */
+ * two 12 KiB slots per CTA of the grid the library would choose.
+ * Source: sglang PR #36845, "Optimized kernel" (long KV rows split across CTAs,
+ * whose partial results the final split merges; its device counter lives here)
+ * and "Changes" (the contract that bounds the size: 1 <= bs <= 128, TP1 24Q or TP2
+ * 12Q, selected capacity <= 2055; the pages give 32.3 MiB as their worst case at
+ * TP1 bs=128, this layout needs under 4 MB). */
 size_t qsa_decode_scratch_bytes(int32_t bs, int32_t num_q_heads, int32_t capacity);
 
 /* Number of CTAs qsa_decode launches for these sizes on the current device
- * (after applying max_ctas when > 0); negative QSA_ERR_* on bad sizes. */
+ * (after applying max_ctas when > 0); negative QSA_ERR_* on bad sizes.
+ * Source: sglang PR #36845, "Optimized kernel" (the split of long KV rows across
+ * CTAs); the grid is fixed by the sizes, so a captured graph keeps it. */
 int32_t qsa_decode_grid(int32_t bs, int32_t num_q_heads, int32_t capacity, int32_t max_ctas);
 
 /* Offsets of the scratch regions, for callers that inspect them (tests):
- * the error word (int32), the counters (int32 [bs * Hkv]) and the partials. */
+ * the error word (int32), the counters (int32 [bs * Hkv]) and the partials.
+ * Source: sglang PR #36845, "Optimized kernel" (the per-split device counters that
+ * the final split resets in the same launch; the pages check them zero after
+ * 150,000 consecutive launches). */
 typedef struct {
     size_t error_word_offset;
     size_t counters_offset;
@@ -232,18 +246,30 @@ int qsa_decode_scratch_layout(int32_t bs, int32_t num_q_heads, int32_t capacity,
                               qsa_scratch_layout* layout);
 
 /* Zero a scratch buffer (cudaMemsetAsync on `stream`). Call once after
- * allocating it; counters then stay zero across launches by themselves. */
+ * allocating it; counters then stay zero across launches by themselves.
+ * Source: sglang PR #36845, "Optimized kernel": the final split resets its device
+ * counter in the same launch, and every counter is back at zero after 150,000
+ * consecutive launches, so one zeroing at allocation is all the state needs. */
 int qsa_scratch_init(void* scratch, size_t scratch_bytes, void* stream);
 
 /* Read the sticky device error word into *flags (QSA_DEVERR_* bits). This
  * is the library's only device readback: it copies 4 bytes on `stream` and
- * synchronises that stream. With clear != 0 the word is reset to zero. */
+ * synchronises that stream. With clear != 0 the word is reset to zero.
+ * Source: sglang PR #36845, "Changes" (lengths are read on the device, so the
+ * decode itself never reads back to the host) and "Motivation" (the failure the
+ * pages fight is silent: wrong outputs while the server stays healthy; bad device
+ * data is therefore recorded here instead of being passed over). */
 int qsa_scratch_error(const void* scratch, int32_t* flags, int32_t clear, void* stream);
 
-/* Static description of a return code. */
+/* Static description of a return code.
+ * Source: sglang PR #36845, "Changes": unsupported calls fail with a descriptive
+ * contract error. */
 const char* qsa_strerror(int code);
 
-/* Descriptive message of the last failing call on this host thread ("" if none). */
+/* Descriptive message of the last failing call on this host thread ("" if none):
+ * which argument broke which rule of the contract.
+ * Source: sglang PR #36845, "Changes": unsupported calls fail with a descriptive
+ * contract error. */
 const char* qsa_last_error_message(void);
 
 /*
@@ -279,7 +305,8 @@ int qsa_decode_static_scratch(const qsa_tensor* q, const qsa_tensor* k_pool,
                               const qsa_tensor* sel_indices, const qsa_tensor* cu_seqlens,
                               const qsa_tensor* out, void* stream);
 
-/* Library version, major * 10000 + minor * 100 + patch. */
+/* Library version, major * 10000 + minor * 100 + patch. The pages have no
+ * counterpart; a caller checks it against the header it was built with. */
 int qsa_version(void);
 
 #ifdef __cplusplus

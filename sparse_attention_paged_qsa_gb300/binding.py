@@ -87,46 +87,42 @@ _lib = None
 def load() -> ctypes.CDLL:
     """Load libqsa.so from the package directory (raises if it was not built)."""
     global _lib
-    if _lib is not None:
-        return _lib
-    if not os.path.exists(LIB_PATH):
-        raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+    if _lib is None:
+        _lib = open_library(LIB_PATH)
+    return _lib
+
+
+def _signatures():
+    """(restype, argtypes) of every export of qsa.h."""
+    P, T, M = ctypes.POINTER, ctypes.POINTER(QsaTensor), ctypes.POINTER(QsaKvQuantMeta)
+    vp, i32 = ctypes.c_void_p, ctypes.c_int32
+    return {
+        "qsa_decode": (ctypes.c_int, [T, T, T, M, T, T, T, vp, ctypes.c_size_t, vp]),
+        "qsa_decode_static_scratch": (ctypes.c_int, [T, T, T, M, T, T, T, vp]),
+        "qsa_kv_write": (ctypes.c_int, [i32, T, T, T, T, T, vp, vp, vp, vp]),
+        "qsa_kv_write_tiered": (ctypes.c_int, [T, T, T, T, T, vp, vp, P(QsaKvTier), vp, vp]),
+        "qsa_decode_scratch_bytes": (ctypes.c_size_t, [i32] * 3),
+        "qsa_decode_grid": (i32, [i32] * 4),
+        "qsa_decode_scratch_layout": (ctypes.c_int, [i32] * 3 + [P(QsaScratchLayout)]),
+        "qsa_scratch_init": (ctypes.c_int, [vp, ctypes.c_size_t, vp]),
+        "qsa_scratch_error": (ctypes.c_int, [vp, P(i32), i32, vp]),
+        "qsa_strerror": (ctypes.c_char_p, [ctypes.c_int]),
+        "qsa_last_error_message": (ctypes.c_char_p, []),
+        "qsa_version": (ctypes.c_int, []),
+    }
+
+
+def open_library(path: str) -> ctypes.CDLL:
+    """Open a build of the C ABI at `path` and declare the signatures of the
+    qsa.h exports it has (a test build carries the decode only)."""
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with __graft_entry__.build() "
                            "(nvcc, sm_103a); there is no CPU fallback")
-    lib = ctypes.CDLL(LIB_PATH)
-    P = ctypes.POINTER
-    lib.qsa_decode.restype = ctypes.c_int
-    lib.qsa_decode.argtypes = [P(QsaTensor), P(QsaTensor), P(QsaTensor), P(QsaKvQuantMeta),
-                               P(QsaTensor), P(QsaTensor), P(QsaTensor), ctypes.c_void_p,
-                               ctypes.c_size_t, ctypes.c_void_p]
-    lib.qsa_decode_static_scratch.restype = ctypes.c_int
-    lib.qsa_decode_static_scratch.argtypes = [P(QsaTensor), P(QsaTensor), P(QsaTensor),
-                                              P(QsaKvQuantMeta), P(QsaTensor), P(QsaTensor),
-                                              P(QsaTensor), ctypes.c_void_p]
-    lib.qsa_kv_write.restype = ctypes.c_int
-    lib.qsa_kv_write.argtypes = [ctypes.c_int32, P(QsaTensor), P(QsaTensor), P(QsaTensor),
-                                 P(QsaTensor), P(QsaTensor), ctypes.c_void_p, ctypes.c_void_p,
-                                 ctypes.c_void_p, ctypes.c_void_p]
-    lib.qsa_kv_write_tiered.restype = ctypes.c_int
-    lib.qsa_kv_write_tiered.argtypes = [P(QsaTensor), P(QsaTensor), P(QsaTensor), P(QsaTensor),
-                                        P(QsaTensor), ctypes.c_void_p, ctypes.c_void_p, P(QsaKvTier),
-                                        ctypes.c_void_p, ctypes.c_void_p]
-    lib.qsa_decode_scratch_bytes.restype = ctypes.c_size_t
-    lib.qsa_decode_scratch_bytes.argtypes = [ctypes.c_int32] * 3
-    lib.qsa_decode_grid.restype = ctypes.c_int32
-    lib.qsa_decode_grid.argtypes = [ctypes.c_int32] * 4
-    lib.qsa_decode_scratch_layout.restype = ctypes.c_int
-    lib.qsa_decode_scratch_layout.argtypes = [ctypes.c_int32] * 3 + [P(QsaScratchLayout)]
-    lib.qsa_scratch_init.restype = ctypes.c_int
-    lib.qsa_scratch_init.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
-    lib.qsa_scratch_error.restype = ctypes.c_int
-    lib.qsa_scratch_error.argtypes = [ctypes.c_void_p, P(ctypes.c_int32), ctypes.c_int32,
-                                      ctypes.c_void_p]
-    lib.qsa_strerror.restype = ctypes.c_char_p
-    lib.qsa_strerror.argtypes = [ctypes.c_int]
-    lib.qsa_last_error_message.restype = ctypes.c_char_p
-    lib.qsa_last_error_message.argtypes = []
-    lib.qsa_version.restype = ctypes.c_int
-    _lib = lib
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _signatures().items():
+        if hasattr(lib, name):
+            fn = getattr(lib, name)
+            fn.restype, fn.argtypes = res, args
     return lib
 
 

@@ -51,6 +51,7 @@
 //  * Every wait is bounded; bad slot ids / cu_seqlens set a sticky error
 //    word and are clamped, never trapped.
 
+#include <cuda.h> // driver types only (CUcontext, CUresult); nothing links libcuda
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -59,7 +60,6 @@
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
-#include <cstdlib>
 #include <initializer_list>
 #include <mutex>
 #include <string>
@@ -220,7 +220,9 @@ struct Params {
     const void* vring_scale;
     const int* owner;
     int ring_mask; // R - 1
-    int stall_stage; // test hook: CTA 0's producers leave this stage incomplete (-1: off)
+#ifdef QSA_TEST_HOOKS
+    int stall_stage; // CTA 0's producers leave this stage incomplete (-1: off)
+#endif
 };
 
 // Byte offset of 16-byte chunk `chunk` of row `row` in a swizzled row buffer.
@@ -879,10 +881,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
                         *reinterpret_cast<uint4*>(sc + T * Ly::SC_TOK + mytok * 16) = make_uint4(0, 0, 0, 0);
                 }
             }
-            if (blockIdx.x != 0 || i != p.stall_stage) {
-                cp_async_arrive_noinc(full_bar(s));
-                mbar_arrive(full_bar(s));
+#ifdef QSA_TEST_HOOKS
+            if (blockIdx.x == 0 && i == p.stall_stage) { // test build only: never complete it
+                cursor_advance(ic, t_end, segL, Hkv);
+                continue;
             }
+#endif
+            cp_async_arrive_noinc(full_bar(s));
+            mbar_arrive(full_bar(s));
             cursor_advance(ic, t_end, segL, Hkv);
         }
         cp_async_wait<0>();
@@ -1864,14 +1870,14 @@ void layout_for(int32_t bs, int32_t num_q_heads, long long grid, qsa_scratch_lay
 
 bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
-// Test hook for the bounded pipeline waits: with QSA_TEST_STALL_STAGE=k in the
-// environment, CTA 0's producers never complete their k-th stage. Its consumers'
-// wait then runs out (WAIT_NS), the launch records QSA_DEVERR_TIMEOUT and ends;
-// nothing faults and nothing spins without a limit.
-int test_stall_stage() {
-    const char* e = std::getenv("QSA_TEST_STALL_STAGE");
-    return e ? std::atoi(e) : -1;
-}
+#ifdef QSA_TEST_HOOKS
+// Test build only (libqsa_testhooks.so, compiled with -DQSA_TEST_HOOKS; the shipped
+// libqsa.so has none of this): qsa_test_set_stall_stage(k) makes CTA 0's producers
+// of the following launches never complete their k-th stage. Its consumers' wait
+// then runs out (WAIT_NS), the launch records QSA_DEVERR_TIMEOUT and ends; nothing
+// faults and nothing spins without a limit. k < 0 turns it off.
+int g_test_stall_stage = -1;
+#endif
 
 int check_row_tensor(const qsa_tensor* t, const char* name, int bs, int hq) {
     if (t->dtype != QSA_DTYPE_BF16)
@@ -2115,7 +2121,9 @@ int qsa_decode(const qsa_tensor* q, const qsa_tensor* k_pool, const qsa_tensor* 
     prm.kring_scale = prm.vring_scale = nullptr;
     prm.owner = nullptr;
     prm.ring_mask = 0;
-    prm.stall_stage = test_stall_stage();
+#ifdef QSA_TEST_HOOKS
+    prm.stall_stage = g_test_stall_stage;
+#endif
     if (fmt == QSA_KV_INT8RING_INT4) {
         prm.kring = static_cast<const uint8_t*>(tier->k_ring);
         prm.vring = static_cast<const uint8_t*>(tier->v_ring);
@@ -2139,6 +2147,10 @@ int qsa_decode(const qsa_tensor* q, const qsa_tensor* k_pool, const qsa_tensor* 
     return rc;
 }
 
+#ifdef QSA_TEST_HOOKS
+void qsa_test_set_stall_stage(int stage) { g_test_stall_stage = stage; }
+#endif
+
 } // extern "C"
 
 // ============================================ decode without caller-provided scratch
@@ -2155,7 +2167,43 @@ constexpr size_t STATIC_HEADER_BYTES = 256 + 1024;   // error word + 256 counter
 constexpr size_t STATIC_SCRATCH_BYTES =
     STATIC_HEADER_BYTES + (size_t)STATIC_MAX_CTAS * 2 * PART_BYTES; // 3,974,400 bytes
 
-void* g_static_ptr[64] = {nullptr};                  // per-device address, under g_mu
+// Per device: the array's device address and the id of the context it was looked
+// up in (under g_mu). A device reset (cudaDeviceReset) ends the primary context and
+// unloads the module; the next context gets a new id and the address is looked up
+// again instead of reusing the stale one.
+struct StaticScratch {
+    void* ptr = nullptr;
+    unsigned long long ctx_id = 0;
+};
+StaticScratch g_static[64];
+
+// Id of the calling thread's current CUDA context, unique for the life of the
+// process (the driver's cuCtxGetId, reached through the runtime's entry-point
+// query); 0 when there is no current context or the query is unavailable.
+unsigned long long current_context_id() {
+    using GetCurrent = CUresult (*)(CUcontext*);
+    using GetId = CUresult (*)(CUcontext, unsigned long long*);
+    static GetCurrent get_current = nullptr;
+    static GetId get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<GetCurrent>(fn);
+        fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<GetId>(fn);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current == nullptr || get_id == nullptr || get_current(&ctx) != CUDA_SUCCESS ||
+        ctx == nullptr || get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
 
 } // namespace
 
@@ -2174,18 +2222,22 @@ extern "C" int qsa_decode_static_scratch(const qsa_tensor* q, const qsa_tensor* 
     if (dev < 0 || dev >= 64) return fail(QSA_ERR_CUDA, "device ordinal %d out of range", dev);
     void* ptr = nullptr;
     {
-        // Set-up, once per device, with that device current: the array's name is
-        // only a host-side stand-in, so look up its device address.
+        // Set-up, once per device (and again after a reset of its context), with that
+        // device current: the array's name is only a host-side stand-in, so look up
+        // its device address.
         std::lock_guard<std::mutex> lk(g_mu);
-        if (g_static_ptr[dev] == nullptr) {
+        StaticScratch& st = g_static[dev];
+        const unsigned long long id = st.ptr ? current_context_id() : 0;
+        if (st.ptr == nullptr || id == 0 || id != st.ctx_id) {
             void* addr = nullptr;
             e = cudaGetSymbolAddress(&addr, g_static_scratch);
             if (e != cudaSuccess)
                 return fail(QSA_ERR_CUDA, "cudaGetSymbolAddress(static scratch): %s",
                             cudaGetErrorString(e));
-            g_static_ptr[dev] = addr;
+            st.ptr = addr;
+            st.ctx_id = current_context_id(); // the lookup made the primary context current
         }
-        ptr = g_static_ptr[dev];
+        ptr = st.ptr;
     }
     // Cap the grid so the partial results fit the fixed array; any size the
     // decode contract admits then fits, and qsa_decode rejects the rest.

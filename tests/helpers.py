@@ -2,6 +2,8 @@
 compare per (sequence, head)."""
 from __future__ import annotations
 
+import os
+
 import numpy as np
 import torch
 
@@ -72,8 +74,16 @@ def compare(got_bf16: torch.Tensor, ref64: np.ndarray, lengths, rows=None, tol=R
     ref_b = oracle.round_bf16(ref64)
     e_b = rel_l2(got, ref_b)
     e_u = rel_l2(got, ref64)
+    finite_u = e_u[np.isfinite(e_u)]
+    REPORT.append((os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0], float(e_b.max()),
+                   float(finite_u.max()) if finite_u.size else 0.0))
     assert e_b.max() <= tol, f"rel-L2 {e_b.max():.3e} > {tol} (worst at {np.unravel_index(e_b.argmax(), e_b.shape)})"
     return float(e_b.max()), float(e_u.max())
+
+
+# (test, max rel-L2 vs bf16(oracle), max rel-L2 vs the unrounded oracle) of every
+# compare() in this session; the terminal summary prints them (tests/conftest.py)
+REPORT = []
 
 
 def counters(scratch: torch.Tensor, bs: int, hq: int, capacity: int) -> torch.Tensor:

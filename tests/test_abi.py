@@ -34,6 +34,17 @@ def test_library_exports_every_declared_symbol():
         assert re.search(rf"\bT {name}$", out, flags=re.M), name
 
 
+def test_shipped_library_reads_no_environment_and_has_no_test_hook():
+    lib = B.load()
+    assert not hasattr(lib, "qsa_test_set_stall_stage")
+    out = subprocess.run(["nm", "-D", "--undefined-only", B.LIB_PATH], capture_output=True,
+                         text=True).stdout
+    assert not re.search(r"\bgetenv\b", out), "libqsa.so imports getenv"
+    # the test build carries the hook (and only the decode)
+    test_lib = B.open_library(os.path.join(os.path.dirname(B.LIB_PATH), "libqsa_testhooks.so"))
+    assert hasattr(test_lib, "qsa_test_set_stall_stage") and hasattr(test_lib, "qsa_decode")
+
+
 def test_struct_layouts_match_header(tmp_path):
     src = tmp_path / "sizes.c"
     src.write_text(

@@ -65,3 +65,26 @@ def test_algorithmic_bytes_of_the_headline():
     assert bench.algorithmic_bytes("fp8_e4m3") == 273551364 + 8  # + the two per-pool fp32 scales
     assert bench.algorithmic_bytes("int8") == 277760004
     assert bench.algorithmic_bytes("int4") == 143083524
+
+
+def test_gpus_flag_launches_that_many_ranks():
+    """--gpus 2 without a launcher re-runs the script under torch.distributed.run
+    with two ranks (gloo on CPU here); the line reports n_gpus 2 and the slower
+    rank's step time."""
+    import json
+    import subprocess
+    import sys
+
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT")}
+    stub = os.path.join(os.path.dirname(os.path.abspath(__file__)), "rank_stub.py")
+    r = subprocess.run([sys.executable, stub, "--gpus", "2", "--steps", "3"], capture_output=True,
+                       text=True, timeout=300, env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout            # rank 0 alone prints
+    line = json.loads(lines[0])
+    assert line["n_gpus"] == 2
+    assert line["ms_per_step"] >= 40.0          # rank 1's stand-in step: 40 ms
+    assert line["ms_per_step"] > line["rank0_ms"] + 10.0
+    assert line["value"] == pytest.approx(2 * 542904324 / (line["ms_per_step"] * 1e-3) / 1e9)

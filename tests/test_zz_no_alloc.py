@@ -4,8 +4,10 @@ This entry point serves callers that cannot allocate device memory when they
 call (fixed-budget plugins, allocator-less bindings, loops where an
 allocation would synchronise the device): its scratch is a fixed device array
 inside libqsa. Here it is called through the C ABI, twice in a row on
-different workloads, and each result must match qsa_decode (which uses a
-caller-allocated scratch buffer) within the parity tolerance.
+different workloads; each result must match qsa_decode (which uses a
+caller-allocated scratch buffer) within the parity tolerance, and each is also
+checked against the FP64 oracle with the suite's degenerate-output rejections,
+so a fault shared by both entry points cannot pass unnoticed.
 """
 import ctypes
 
@@ -15,7 +17,7 @@ import torch
 
 from sparse_attention_paged_qsa_gb300 import binding as B
 from sparse_attention_paged_qsa_gb300 import inputs as I
-from tests.helpers import REL_L2_TOL, rel_l2, run_cuda
+from tests.helpers import REL_L2_TOL, compare, rel_l2, run_cuda, run_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -41,15 +43,17 @@ def _matches(a: torch.Tensor, b: torch.Tensor) -> float:
 
 
 def test_static_scratch_matches_qsa_decode_on_two_calls(cuda_device):
-    w1 = I.tp1_mixed(seed=31, bs=16, num_slots=65536).to(cuda_device)
-    w2 = I.tiny_tp2(seed=32, length=2055, fmt="int8").to(cuda_device)
-    for w in (w1, w2):
-        ref, _ = run_cuda(w)
-        out = torch.full_like(w.q, float("nan"))
-        rc, msg = _call_static(w, out)
+    hosts = (I.tp1_mixed(seed=31, bs=16, num_slots=65536),
+             I.tiny_tp2(seed=32, length=2055, fmt="int8"))
+    for w in hosts:
+        wd = w.to(cuda_device)
+        ref, _ = run_cuda(wd)
+        out = torch.full_like(wd.q, float("nan"))
+        rc, msg = _call_static(wd, out)
         assert rc == B.OK, msg
         torch.cuda.synchronize()
         assert _matches(out, ref) <= REL_L2_TOL
+        compare(out, run_oracle(w), w.lengths().numpy())
 
 
 def test_static_scratch_rejects_sizes_beyond_its_limit(cuda_device):
