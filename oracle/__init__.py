@@ -357,3 +357,8 @@ def quantize_rows(x, fmt: str, fp8_scale: float = 1.0):
 
 def max_threads() -> int:
     return _load().orc_max_threads()
+
+
+# The step that produces the selected slots (exact top-k over compressed-block
+# scores and index expansion) lives in topk.py: index work, plain numpy.
+from .topk import TopkRefused, row_width, topk_blocks, topk_expand  # noqa: E402,F401
