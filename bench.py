@@ -7,8 +7,9 @@ gathered, QK, softmax, PV, split merge). Prints one JSON line.
                   [--impl native|reference] [--op decode|kv_write|topk]
 
 The default bf16 line also carries `formats` (every quantised pool at the
-headline shape) and `small_batch` (batch sizes 1..64 of both topologies in
-the short and saturated length bands, each call replayed from a CUDA graph).
+headline shape), `small_batch` (batch sizes 1..64 of both topologies in the
+short and saturated length bands, each call replayed from a CUDA graph) and
+`topk` (the exact top-k + index expansion that produces the selected slots).
 
 Timing: every timed region starts behind a few milliseconds of a clock-spin
 kernel (torch.cuda._sleep), so all of its calls are queued before the GPU
@@ -559,6 +560,88 @@ def measure_small_batches(args, dev, peak):
     return out_rows
 
 
+# ------------------------------------------------------------ top-k + index expansion
+
+TOPK_PAGE = 64
+
+
+def topk_bytes(bs: int, cap: int, ratio: int, topk: int) -> int:
+    """Bytes one qsa_topk_expand call must move with full contexts of `cap` tokens:
+    every block score once, the context lengths, one page-table entry per kept block
+    or tail page, the packed slot ids written and cu_seqlens."""
+    nb = cap // ratio
+    kb = min(nb, topk // ratio)
+    row = ratio * kb + cap % ratio
+    pages = kb + (1 if cap % ratio else 0)
+    return bs * (nb * 4 + 4 + pages * 4 + row * 4) + (bs + 1) * 4
+
+
+def measure_topk(args, dev, peak):
+    """qsa_topk_expand at the pages' sizes (token_topk 2048 -- 2032 at ratio 16, whose rows
+    must fit the decode's 2055 --, compress ratios 4 / 8 / 16,
+    8K and 256K-token contexts, bs 1 and 128, through a 64-token page table): two
+    sets of N(0,1) block scores in turn, back-to-back stream launches behind the gate."""
+    import sparse_attention_paged_qsa_gb300 as qsa
+
+    n = max(min(args.steps, 200), 1)
+    stream = torch.cuda.current_stream()
+    rows = []
+    for cap in (8192, I.TOPK_CAPACITY):
+        for bs in (1, BS):
+            for ratio in (4, 8, 16):
+                topk = I.topk_budget(ratio)
+                sets = [I.block_scores(bs, cap // ratio, 100 + k, dev, specials=False)
+                        for k in range(2)]
+                lens = torch.full((bs,), cap, dtype=torch.int32, device=dev)
+                pt = I.page_table(bs, cap, TOPK_PAGE, 7, dev)
+                sel = torch.empty(bs * (topk + ratio - 1), dtype=torch.int32, device=dev)
+                cu = torch.empty(bs + 1, dtype=torch.int32, device=dev)
+
+                def launch(k, sets=sets, lens=lens, pt=pt, sel=sel, cu=cu, ratio=ratio, cap=cap):
+                    qsa.qsa_topk_expand(sets[k % 2], lens, sel, cu, topk, ratio, cap,
+                                        page_table=pt, page_size=TOPK_PAGE, stream=stream)
+
+                for k in range(args.warmup):
+                    launch(k)
+                ms = time_calls(launch, n, stream)
+                b = topk_bytes(bs, cap, ratio, topk)
+                rows.append({"context": cap, "bs": bs, "compress_ratio": ratio, "token_topk": topk,
+                             "us_per_call": ms * 1e3, "calls_per_s": 1e3 / ms,
+                             "gb_s": b / (ms * 1e-3) / 1e9,
+                             "pct_of_hbm_peak": 100.0 * b / (ms * 1e-3) / 1e9 / peak,
+                             "bytes_per_call": b})
+                del sets, lens, pt, sel, cu
+    torch.cuda.empty_cache()
+    return rows
+
+
+def run_topk(args):
+    """The top-k + index expansion alone: one JSON line (bs=128, 256K contexts, ratio 4
+    as the value; every measured point under `points`)."""
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peak, kind = measured_peaks()
+    clk = Clocks(dev).__enter__()
+    t0 = time.perf_counter()
+    pts = measure_topk(args, dev, peak)
+    clocks = clk.summary(t0, time.perf_counter())
+    clk.__exit__()
+    head = next(p for p in pts if p["context"] == I.TOPK_CAPACITY and p["bs"] == BS
+                and p["compress_ratio"] == 4)
+    print(json.dumps({
+        "metric": "qsa_topk_expand calls/s (exact top-k 2048 tokens + index expansion, 256K contexts)",
+        "op": "topk", "value": head["calls_per_s"], "unit": "calls/s", "n_gpus": 1,
+        "steps": max(min(args.steps, 200), 1), "warmup": args.warmup,
+        "ms_per_step": head["us_per_call"] * 1e-3, "higher_is_better": True, "dtype": "int32",
+        "data": "synthetic",
+        "config": {"workload": "bs=128, 262144-token contexts, compress ratio 4, token_topk 2048, "
+                               "64-token page table"},
+        "roofline": {"bound": "hbm", "achieved": head["gb_s"], "peak": peak, "unit": "GB/s",
+                     "frac": head["gb_s"] / peak, "peak_source": f"{kind} hbm_gbs",
+                     "bytes_per_launch": head["bytes_per_call"]},
+        "points": pts, "clocks": clocks}), flush=True)
+
+
 # ------------------------------------------------------------ the headline
 
 def run_native(args):
@@ -676,10 +759,11 @@ def run_native(args):
     rows_bytes = bs * HKV * L * 2 * (ROW_BYTES.get(fmt, 0) + SCALE_BYTES.get(fmt, 0))
 
     extras = not args.no_extras and ws == 1 and fmt == "bf16" and bs == BS
-    formats = small = None
+    formats = small = topk = None
     if extras:
         formats = measure_formats(args, dev, stream, scratch, peak)
         small = measure_small_batches(args, dev, peak)
+        topk = measure_topk(args, dev, peak)
 
     cpu = None
     if rank == 0 and args.cpu_rows > 0:
@@ -725,6 +809,8 @@ def run_native(args):
             line["formats"] = formats
         if small is not None:
             line["small_batch"] = small
+        if topk is not None:
+            line["topk"] = topk
         print(json.dumps(line), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
@@ -811,8 +897,9 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--fmt", default="bf16", choices=list(I.FORMATS) + [I.TIERED])
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--op", default="decode", choices=["decode", "kv_write"],
-                    help="decode (the headline) or the quantising KV write")
+    ap.add_argument("--op", default="decode", choices=["decode", "kv_write", "topk"],
+                    help="decode (the headline), the quantising KV write, or the top-k + "
+                         "index expansion")
     ap.add_argument("--index-sets", type=int, default=3)
     ap.add_argument("--bs", type=int, default=BS,
                     help="sequences per call (the headline is 128; smaller for latency)")
@@ -841,6 +928,8 @@ def main():
         run_reference(args)
     elif args.op == "kv_write":
         run_kv_write(args)
+    elif args.op == "topk":
+        run_topk(args)
     else:
         run_native(args)
 

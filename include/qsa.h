@@ -88,8 +88,10 @@ enum {
     QSA_DEVERR_SLOT_RANGE = 1, /* a selected slot id outside [0, num_slots); slot 0 read instead */
     QSA_DEVERR_CU_SEQLENS = 2, /* cu_seqlens decreasing, negative, past the index buffer,
                                   or a length above capacity; the length is clamped */
-    QSA_DEVERR_TIMEOUT = 4     /* an internal pipeline wait exceeded its limit (a library
+    QSA_DEVERR_TIMEOUT = 4,    /* an internal pipeline wait exceeded its limit (a library
                                   fault, not a data fault); the launch gave up early */
+    QSA_DEVERR_CTX_LEN = 8     /* qsa_topk_expand: a context length outside [0, capacity];
+                                  it is clamped into that range */
 };
 
 /* A strided view of caller memory. `data` is a device pointer for
@@ -304,6 +306,63 @@ int qsa_decode_static_scratch(const qsa_tensor* q, const qsa_tensor* k_pool,
                               const qsa_tensor* v_pool, const qsa_kv_quant_meta* kv_quant_meta,
                               const qsa_tensor* sel_indices, const qsa_tensor* cu_seqlens,
                               const qsa_tensor* out, void* stream);
+
+/* Sizes of one qsa_topk_expand call. */
+typedef struct {
+    int32_t token_topk;     /* tokens kept from whole blocks per sequence: a positive multiple
+                               of compress_ratio; token_topk + compress_ratio - 1 <= 2055 */
+    int32_t compress_ratio; /* tokens per compressed block, 1..64 (the pages use 4, 8, 16) */
+    int32_t capacity;       /* largest context length, 1..262144 (the pages' 256K) */
+    int32_t page_size;      /* page_table's page size, a power of two (the pages use 64);
+                               0: no page table, the ids are logical token positions */
+} qsa_topk_params;
+
+/*
+ * qsa_topk_expand -- the step that produces qsa_decode's sel_indices and
+ * cu_seqlens: exact top-k over compressed-block scores, then index expansion
+ * (1Cat-vLLM PR #523, "Follow-up: device-planned MQA and QSA quality
+ * attribution": exact top-k + index expansion at a fixed 256K capacity; sglang
+ * PR #37798, "Decode routing": index-row width token_topk + compress_ratio - 1 =
+ * 2048 + 4 - 1 = 2051, 64-token pages). The scores themselves come from the
+ * caller; the pages give no formula for them.
+ *
+ * For sequence b with context length T = ctx_lens[b] and r = compress_ratio,
+ * block i covers tokens [i r, (i + 1) r); the floor(T / r) complete blocks carry
+ * scores[b][i]; the last T mod r tokens are in no block yet. k = token_topk / r
+ * blocks are kept: all of them when there are at most k, else the k ranked first
+ * -- higher score first, equal scores by lower block index, NaN below every
+ * number, -0.0 equal to +0.0. Row b lists the kept blocks' tokens in ascending
+ * position, then the tail tokens: r * min(floor(T / r), k) + T mod r <=
+ * token_topk + r - 1 ids. With a page table, position p becomes slot
+ * page_table[b][p / page_size] * page_size + p % page_size. Rows are packed in
+ * sequence order from sel_indices[0]; cu_seqlens[0] = 0 and cu_seqlens[b + 1] is
+ * the end of row b, as qsa_decode reads them.
+ *
+ *  scores       float32 [bs, >= capacity / compress_ratio], unit stride along the
+ *               blocks; row stride >= the row length. Entries past a row's
+ *               floor(T / r) blocks are not read.
+ *  ctx_lens     int32 [bs], contiguous, 1 <= bs <= 128, read on the device only.
+ *               A length outside [0, capacity] is clamped into it and sets
+ *               QSA_DEVERR_CTX_LEN.
+ *  page_table   int32 [bs, >= ceil(capacity / page_size)], unit stride along the
+ *               pages, when page_size > 0 (else ignored, may be NULL). A page id
+ *               that puts a slot outside [0, 2^31) writes -1 there and sets
+ *               QSA_DEVERR_SLOT_RANGE.
+ *  params       the sizes above (host struct, read at the call).
+ *  sel_indices  int32, contiguous, at least bs * (token_topk + compress_ratio - 1)
+ *               entries; entries past cu_seqlens[bs] are left as they were.
+ *  cu_seqlens   int32 [bs + 1], contiguous.
+ *  device_error optional int32 device word the QSA_DEVERR_* bits are OR-ed into.
+ *  stream       cudaStream_t.
+ *
+ * Validates on the host, enqueues one kernel (one CTA per sequence), allocates
+ * nothing and needs no scratch; a captured graph stays valid when ctx_lens and
+ * scores change between replays. Returns QSA_OK or a negative QSA_ERR_*.
+ */
+int qsa_topk_expand(const qsa_tensor* scores, const qsa_tensor* ctx_lens,
+                    const qsa_tensor* page_table, const qsa_topk_params* params,
+                    const qsa_tensor* sel_indices, const qsa_tensor* cu_seqlens,
+                    int32_t* device_error, void* stream);
 
 /* Library version, major * 10000 + minor * 100 + patch. The pages have no
  * counterpart; a caller checks it against the header it was built with. */

@@ -24,7 +24,7 @@ KV_FORMATS = {"bf16": 0, "fp8_e4m3": 1, "int8": 2, "int4": 3, "int8_g64": 4, "in
               "int8ring_int4": 6}
 OK, ERR_INVALID_ARGUMENT, ERR_UNSUPPORTED, ERR_SCRATCH_TOO_SMALL, ERR_MISALIGNED, ERR_CUDA = (
     0, -1, -2, -3, -4, -5)
-DEVERR_SLOT_RANGE, DEVERR_CU_SEQLENS, DEVERR_TIMEOUT = 1, 2, 4
+DEVERR_SLOT_RANGE, DEVERR_CU_SEQLENS, DEVERR_TIMEOUT, DEVERR_CTX_LEN = 1, 2, 4, 8
 
 _TORCH_DTYPES = {
     torch.bfloat16: DTYPE_BF16,
@@ -38,6 +38,7 @@ EXPORTED = (
     "qsa_decode", "qsa_decode_scratch_bytes", "qsa_decode_grid", "qsa_decode_scratch_layout",
     "qsa_scratch_init", "qsa_scratch_error", "qsa_strerror", "qsa_last_error_message",
     "qsa_version", "qsa_decode_static_scratch", "qsa_kv_write", "qsa_kv_write_tiered",
+    "qsa_topk_expand",
 )
 
 
@@ -67,6 +68,11 @@ def tier_struct(tier: dict) -> QsaKvTier:
         setattr(t, key, tier[key].data_ptr())
     t.ring_slots = int(tier["owner"].numel())
     return t
+
+
+class QsaTopkParams(ctypes.Structure):
+    _fields_ = [("token_topk", ctypes.c_int32), ("compress_ratio", ctypes.c_int32),
+                ("capacity", ctypes.c_int32), ("page_size", ctypes.c_int32)]
 
 
 class QsaScratchLayout(ctypes.Structure):
@@ -109,6 +115,7 @@ def _signatures():
         "qsa_strerror": (ctypes.c_char_p, [ctypes.c_int]),
         "qsa_last_error_message": (ctypes.c_char_p, []),
         "qsa_version": (ctypes.c_int, []),
+        "qsa_topk_expand": (ctypes.c_int, [T, T, T, P(QsaTopkParams), T, T, vp, vp]),
     }
 
 
@@ -235,6 +242,22 @@ def qsa_kv_write_tiered(k_new, v_new, slots, k_pool, v_pool, k_scale, v_scale, t
     ptr = lambda t: t.data_ptr() if t is not None else None
     rc = lib.qsa_kv_write_tiered(*(ctypes.byref(x) for x in d), ptr(k_scale), ptr(v_scale),
                                  ctypes.byref(ts), ptr(error_word), _stream_handle(stream))
+    _check(rc)
+
+
+def qsa_topk_expand(scores, ctx_lens, sel_indices, cu_seqlens, token_topk: int = 2048,
+                    compress_ratio: int = 4, capacity: int = 262144, page_table=None,
+                    page_size: int = 0, error_word=None, stream=None) -> None:
+    """Enqueue the exact top-k + index expansion that fills sel_indices and
+    cu_seqlens for qsa_decode (see include/qsa.h). page_size > 0 needs page_table."""
+    _require_device(scores, ctx_lens, sel_indices, cu_seqlens, page_table, error_word)
+    lib = load()
+    prm = QsaTopkParams(int(token_topk), int(compress_ratio), int(capacity), int(page_size))
+    d = [describe(t) for t in (scores, ctx_lens, page_table, sel_indices, cu_seqlens)]
+    rc = lib.qsa_topk_expand(*(ctypes.byref(x) for x in d[:3]), ctypes.byref(prm),
+                             ctypes.byref(d[3]), ctypes.byref(d[4]),
+                             error_word.data_ptr() if error_word is not None else None,
+                             _stream_handle(stream))
     _check(rc)
 
 

@@ -15,7 +15,7 @@ from concurrent.futures import ThreadPoolExecutor
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
-SOURCES = [os.path.join(CSRC, f) for f in ("qsa_decode.cu", "qsa_kv_write.cu")]
+SOURCES = [os.path.join(CSRC, f) for f in ("qsa_decode.cu", "qsa_kv_write.cu", "qsa_topk.cu")]
 HEADERS = [os.path.join(ROOT, "include", "qsa.h")]
 LIB = os.path.join(PKG, "libqsa.so")
 TEST_LIB = os.path.join(PKG, "libqsa_testhooks.so")

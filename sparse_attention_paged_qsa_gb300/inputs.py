@@ -426,3 +426,86 @@ def _tiered_subset(w: Workload, rows, cu, sel, uniq, inv) -> Workload:
                     cu_from_lengths(lens), w.fmt, w.k_scale.index_select(0, dev_idx).cpu(),
                     w.v_scale.index_select(0, dev_idx).cpu(), w.softmax_scale, w.capacity,
                     w.name + "_subset", new_tier)
+
+
+# ------------------------------------------- compressed-block scores (top-k input)
+#
+# The top-k step takes one float32 score per compressed block of `ratio` tokens,
+# produced upstream by a scoring step the pages do not define. These generators
+# draw such scores: N(0,1) values with planted ties, -0.0 / +0.0, -inf and NaN, so
+# the exact ranking rules are exercised; and context lengths that include the
+# edge cases of the expansion (no block, whole blocks only, the longest tail).
+
+TOPK_CAPACITY = 262144   # the pages' fixed 256K context capacity
+TOPK_BUDGET = 2048       # token_topk (indexer budget)
+TOPK_RATIO = 4           # compress ratio; row width 2048 + 4 - 1 = 2051
+
+
+def topk_budget(ratio: int) -> int:
+    """token_topk for a compress ratio: the pages' 2048, or the largest multiple of the
+    ratio whose rows (token_topk + ratio - 1) still fit the decode's 2055 (2032 at 16)."""
+    return min(TOPK_BUDGET, (MAX_CAPACITY - ratio + 1) // ratio * ratio)
+
+
+def block_scores(bs: int, nblocks: int, seed: int, device="cpu", specials: bool = True) -> torch.Tensor:
+    """float32 [bs, nblocks] N(0,1) block scores; with `specials`, about 1 % of the
+    entries are replaced by repeats of a few shared values (ties), and a few by
+    -0.0, +0.0, -inf and NaN."""
+    g = _gen(seed, "cpu")
+    s = torch.randn(bs, nblocks, generator=g, dtype=torch.float32)
+    if specials:
+        u = torch.rand(bs, nblocks, generator=g)
+        shared = torch.tensor([0.5, 1.25, -0.75, 2.0], dtype=torch.float32)
+        pick = torch.randint(0, 4, (bs, nblocks), generator=g)
+        s = torch.where(u < 0.010, shared[pick], s)
+        s = torch.where((u >= 0.010) & (u < 0.012), torch.full_like(s, -0.0), s)
+        s = torch.where((u >= 0.012) & (u < 0.014), torch.zeros_like(s), s)
+        s = torch.where((u >= 0.014) & (u < 0.016), torch.full_like(s, -float("inf")), s)
+        s = torch.where((u >= 0.016) & (u < 0.018), torch.full_like(s, float("nan")), s)
+    return s.to(device)
+
+
+def context_lengths(bs: int, capacity: int, ratio: int, token_topk: int, seed: int) -> torch.Tensor:
+    """int32 [bs] context lengths: uniform in [0, capacity], with the edge cases of
+    the expansion placed first (empty, shorter than a block, exactly the kept
+    blocks, the kept blocks plus the longest tail, one block more, the capacity)."""
+    g = _gen(seed, "cpu")
+    edge = [0, ratio - 1, ratio, token_topk, token_topk + ratio - 1, token_topk + ratio, capacity,
+            capacity - 1]
+    edge = [min(max(e, 0), capacity) for e in edge]
+    lens = torch.randint(0, capacity + 1, (bs,), generator=g, dtype=torch.int64)
+    for i, e in enumerate(edge[:bs]):
+        lens[i] = e
+    return lens.to(torch.int32)
+
+
+def page_table(bs: int, capacity: int, page: int, seed: int, device="cpu") -> torch.Tensor:
+    """int32 [bs, ceil(capacity / page)]: every sequence's pages are distinct
+    physical pages of one shared pool, in a seeded random order."""
+    g = _gen(seed, "cpu")
+    npg = -(-capacity // page)
+    perm = torch.randperm(bs * npg, generator=g, dtype=torch.int64)
+    return perm.view(bs, npg).to(torch.int32).to(device)
+
+
+def replay_block_scores(seed: int, replay: torch.Tensor, out: torch.Tensor) -> None:
+    """Regenerate [bs, nblocks] block scores in place from the counter-based hash
+    of (seed, replay, b, i), on the tensor's device (graph-capturable). The scores
+    take 2^20 distinct values, so equal scores occur; hash values 0 and 1 mod 509
+    give -0.0 and NaN."""
+    bs, nb = out.shape
+    dev = out.device
+    b = torch.arange(bs, dtype=torch.int64, device=dev).view(-1, 1)
+    i = torch.arange(nb, dtype=torch.int64, device=dev).view(1, -1)
+    h = hash_key(seed, replay, b, i)
+    v = ((h >> 12).to(torch.float32) - 524288.0) * (1.0 / 65536.0)
+    v = torch.where(h % 509 == 0, torch.full_like(v, -0.0), v)
+    v = torch.where(h % 509 == 1, torch.full_like(v, float("nan")), v)
+    out.copy_(v)
+
+
+def replay_context_lengths(seed: int, replay: torch.Tensor, capacity: int, out: torch.Tensor) -> None:
+    """Regenerate int32 [bs] context lengths in [0, capacity] in place (graph-capturable)."""
+    bs = out.shape[0]
+    b = torch.arange(bs, dtype=torch.int64, device=out.device)
+    out.copy_((hash_key(seed, replay, b, -7) % (capacity + 1)).to(torch.int32))

@@ -239,3 +239,50 @@ def test_tiered_decode_rejections_on_host(kw, code, text):
     rc, msg = _tier_call(**kw)
     assert rc == code, msg
     assert text in msg
+
+
+def _topk_host_call(bs=2, cap=4096, ratio=4, topk=2048, page=0, pt_cols=None, score_cols=None,
+                    sel_len=None, cu_len=None, score_dtype=torch.float32, ctx_len=None):
+    """Describe host tensors (never dereferenced) and call qsa_topk_expand."""
+    scores = torch.zeros(bs, score_cols or cap // max(ratio, 1), dtype=score_dtype)
+    ctx = torch.zeros(ctx_len or bs, dtype=torch.int32)
+    pt = torch.zeros(bs, pt_cols or max(1, -(-cap // max(page, 1))), dtype=torch.int32)
+    sel = torch.zeros(sel_len or bs * (topk + ratio - 1), dtype=torch.int32)
+    cu = torch.zeros(cu_len or bs + 1, dtype=torch.int32)
+    lib = B.load()
+    prm = B.QsaTopkParams(topk, ratio, cap, page)
+    d = [B.describe(t) for t in (scores, ctx, pt if page else None, sel, cu)]
+    rc = lib.qsa_topk_expand(ctypes.byref(d[0]), ctypes.byref(d[1]), ctypes.byref(d[2]),
+                             ctypes.byref(prm), ctypes.byref(d[3]), ctypes.byref(d[4]), None, None)
+    return rc, lib.qsa_last_error_message().decode()
+
+
+@pytest.mark.parametrize("kw, code, text", [
+    (dict(ratio=0), B.ERR_UNSUPPORTED, "compress ratio"),
+    (dict(ratio=65, topk=65 * 4), B.ERR_UNSUPPORTED, "compress ratio"),
+    (dict(topk=2046), B.ERR_UNSUPPORTED, "multiple"),
+    (dict(topk=2056, ratio=8), B.ERR_UNSUPPORTED, "2055"),
+    (dict(cap=262145), B.ERR_UNSUPPORTED, "capacity"),
+    (dict(bs=129), B.ERR_UNSUPPORTED, "bs"),
+    (dict(score_cols=1000), B.ERR_INVALID_ARGUMENT, "scores"),
+    (dict(score_dtype=torch.bfloat16), B.ERR_INVALID_ARGUMENT, "scores"),
+    (dict(page=48), B.ERR_UNSUPPORTED, "page size"),
+    (dict(page=64, pt_cols=63), B.ERR_INVALID_ARGUMENT, "page_table"),
+    (dict(sel_len=2 * 2051 - 1), B.ERR_INVALID_ARGUMENT, "sel_indices"),
+    (dict(cu_len=2), B.ERR_INVALID_ARGUMENT, "cu_seqlens"),
+])
+def test_topk_rejections_on_host(kw, code, text):
+    rc, msg = _topk_host_call(**kw)
+    assert rc == code, msg
+    assert text in msg
+
+
+def test_topk_struct_layout_matches_header(tmp_path):
+    src = tmp_path / "tk.c"
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "qsa.h"\n'
+                   'int main(void){printf("%zu %zu\\n", sizeof(qsa_topk_params),'
+                   ' offsetof(qsa_topk_params, page_size));return 0;}\n')
+    exe = tmp_path / "tk"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = list(map(int, subprocess.run([str(exe)], capture_output=True, text=True).stdout.split()))
+    assert got == [ctypes.sizeof(B.QsaTopkParams), B.QsaTopkParams.page_size.offset]
