@@ -16,19 +16,27 @@
 //     tokens; a page table maps position p to slot pt[p / page] * page + p % page;
 //   * rows are packed in sequence order; cu_seqlens[b] is where row b starts.
 //
-// GB300 design: one CTA of 1024 threads per sequence, no scratch memory.
+// GB300 design: one CTA of 512 threads per sequence, no global scratch.
 //  * Scores become order-preserving 32-bit keys (sign-flipped IEEE bits, NaN ->
 //    0, -0.0 -> +0.0), so ranking is unsigned integer comparison.
-//  * Radix select, four 8-bit digits from the top: each pass histograms the
-//    digit of the keys that still match the chosen prefix (warp-aggregated
-//    shared-memory atomics: __match_any_sync groups equal digits), and a
-//    256-thread descending scan picks the digit holding the k-th key. After
-//    four passes the k-th key (the threshold) and the number of blocks equal to
-//    it that are kept (the lowest-indexed ones) are exact.
-//  * Compaction in index order: chunks of 4096 blocks, each warp 4 rounds of 32;
-//    ballots give every block its rank among the threshold ties and among the
-//    kept blocks, warp totals a block-wide prefix. A kept block's r token slots
-//    go straight to its place in the packed row.
+//  * The score row streams into shared memory in 16 KB pieces by bulk copies
+//    (cp.async.bulk, the TMA engine) into a two-slot ring completed on
+//    mbarriers, so a whole piece is in flight per slot instead of one load per
+//    thread. Every wait is bounded.
+//  * Radix select with digits of 11, 11 and 10 bits from the top: a histogram
+//    of the digit (shared-memory atomics) and a descending scan over its bins
+//    give the digit that holds the k-th key. A row of at most KEYS_CAP blocks is
+//    kept as keys in shared memory after the first streaming pass, and the
+//    other passes and the compaction run there. A longer row (the 256K context
+//    at ratio 4: 65,536 blocks) streams once for the top digit's histogram,
+//    once to gather the keys of the bin that holds the k-th key (in index
+//    order) into shared memory -- the rest of the selection runs on those --
+//    and once more for the compaction; rows whose bin is too large fall back to
+//    streaming every pass.
+//  * Compaction in index order: per 4096-block piece each warp takes 8 rounds of
+//    32; ballots give every block its rank among the threshold ties (or the
+//    gathered bin) and among the kept blocks, warp totals a block-wide prefix. A
+//    kept block's r token slots go straight to its place in the packed row.
 //  * Each CTA computes its row's offset from the context lengths of the rows
 //    before it, so the whole step is one launch with no host readback, and a
 //    captured graph stays valid when the lengths and scores change.
@@ -38,6 +46,7 @@
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
+#include <mutex>
 
 #include "qsa.h"
 
@@ -45,14 +54,25 @@ void qsa_detail_set_error(const char* msg);
 
 namespace qsatk {
 
-constexpr int THREADS = 1024;
+constexpr int THREADS = 512;
 constexpr int WARPS = THREADS / 32;
-constexpr int ROUNDS = 4;                      // 32-block rounds per warp per chunk
-constexpr int CHUNK = THREADS * ROUNDS;        // blocks per compaction chunk
+constexpr int ROUNDS = 8;                      // 32-block rounds per warp per piece
+constexpr int PIECE = THREADS * ROUNDS;        // blocks per piece (4096 = 16 KB of scores)
+constexpr int KEYS_CAP = 44 * 1024;            // keys kept in shared memory (176 KB)
 constexpr int MAX_BS = 128;
 constexpr int MAX_CAPACITY = 262144;           // the pages' fixed 256K context capacity
 constexpr int MAX_ROW = 2055;                  // the decode's selected-KV capacity
 constexpr unsigned FULL = 0xFFFFFFFFu;
+constexpr int NBINS = 2048;                    // bins of an 11-bit digit
+constexpr long long WAIT_NS = 2000000000LL;    // bounded-wait limit (2 s)
+constexpr uint32_t KEPT = 0xFFFFFFFFu;         // not a key: order_key maps every NaN to 0
+// dynamic shared memory: the two ring slots, the keys, the histogram
+constexpr int OFF_RING = 0;
+constexpr int OFF_KEYS = OFF_RING + 2 * PIECE * 4;
+constexpr int OFF_HIST = OFF_KEYS + KEYS_CAP * 4;
+constexpr int SMEM_BYTES = OFF_HIST + NBINS * 4;
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+static_assert(NBINS % THREADS == 0 && NBINS / THREADS <= 4, "digit scan");
 
 struct Params {
     const float* scores;
@@ -70,6 +90,52 @@ struct Params {
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t smem_u32(const void* ptr) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(ptr));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ unsigned long long globaltimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Wait for the phase with `parity` of an mbarrier for at most WAIT_NS.
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    const unsigned long long t0 = globaltimer();
+    for (uint32_t it = 0;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63) == 63 && globaltimer() - t0 > (unsigned long long)WAIT_NS) return false;
+    }
+}
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void fence_mbarrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
 // Unsigned key with the order of the ranking: +x above -x, larger above smaller,
@@ -107,32 +173,179 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
     return m;
 }
 
+// Exclusive prefix over the warps of one value per warp; returns (before, total).
+// Bracketed by barriers, so `wsum` may be reused right after.
+__device__ __forceinline__ int2 block_prefix(int v, int* wsum) {
+    const int warp = threadIdx.x >> 5;
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) wsum[warp] = v;
+    __syncthreads();
+    int before = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w < WARPS; ++w) {
+        const int x = wsum[w];
+        before += w < warp ? x : 0;
+        total += x;
+    }
+    return make_int2(before, total);
+}
+
+// The digit (of a `bins`-bin histogram, taken from the top) whose bin holds the
+// need-th key, and the number of keys in the bins above it.
+__device__ __forceinline__ int2 find_digit(const uint32_t* hist, int bins, int need, int* wsum, int* sh) {
+    const int tid = threadIdx.x, lane = tid & 31, per = bins / THREADS;
+    int c[4] = {0, 0, 0, 0}, s = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        if (q < per) {
+            c[q] = static_cast<int>(hist[bins - 1 - (tid * per + q)]);
+            s += c[q];
+        }
+    int incl = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(FULL, incl, o);
+        if (lane >= o) incl += v;
+    }
+    const int2 pw = block_prefix(__shfl_sync(FULL, incl, 31), wsum);
+    int excl = pw.x + incl - s;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        if (q < per) {
+            if (excl < need && need <= excl + c[q]) {
+                sh[0] = bins - 1 - (tid * per + q);
+                sh[1] = excl;
+            }
+            excl += c[q];
+        }
+    __syncthreads();
+    return make_int2(sh[0], sh[1]);
+}
+
+// One piece of an index-ordered scan: n <= PIECE keys key_at(0 .. n-1), global
+// positions base + j. Each key gets its rank among the keys with is_a() (counted
+// from `carry_a`), decide(key, is_a, rank_a) says whether it is kept, and
+// emit(j, rank) receives every kept key with its rank among the kept ones
+// (counted from `carry_s`). The carries advance by the piece's totals.
+template <class KeyAt, class IsA, class Decide, class Emit>
+__device__ __forceinline__ void scan_piece(int n, KeyAt key_at, IsA is_a, Decide decide, Emit emit,
+                                           int& carry_a, int& carry_s, int* wsum) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t lt = lanemask_lt();
+    const int wbase = warp * 32 * ROUNDS;
+    uint32_t am[ROUNDS];
+    int wa = 0;
+#pragma unroll
+    for (int e = 0; e < ROUNDS; ++e) {
+        const int j = wbase + e * 32 + lane;
+        am[e] = __ballot_sync(FULL, j < n && is_a(key_at(j)));
+        wa += __popc(am[e]);
+    }
+    const int2 pa = block_prefix(wa, wsum);
+    int ra = carry_a + pa.x;
+    uint32_t sm[ROUNDS];
+    int ws = 0;
+#pragma unroll
+    for (int e = 0; e < ROUNDS; ++e) {
+        const int j = wbase + e * 32 + lane;
+        const bool isa = (am[e] >> lane) & 1u;
+        const bool sel = j < n && decide(key_at(j), isa, ra + __popc(am[e] & lt));
+        ra += __popc(am[e]);
+        sm[e] = __ballot_sync(FULL, sel);
+        ws += __popc(sm[e]);
+    }
+    const int2 ps = block_prefix(ws, wsum);
+    int rs = carry_s + ps.x;
+#pragma unroll
+    for (int e = 0; e < ROUNDS; ++e) {
+        if ((sm[e] >> lane) & 1u) emit(wbase + e * 32 + lane, rs + __popc(sm[e] & lt));
+        rs += __popc(sm[e]);
+    }
+    carry_a += pa.y;
+    carry_s += ps.y;
+}
+
+// Streams the first nb scores of a row through the two-slot ring, one PIECE at a
+// time, calling fn(piece, base, n) with the piece in shared memory (n floats at
+// row positions base .. base + n - 1). Thread 0 keeps the next piece in flight.
+// `seq` counts pieces across passes (ring slot and mbarrier parity). Returns
+// false (uniformly) when a wait ran out; copies in flight have then landed or
+// been waited for, with a limit.
+template <class Fn>
+__device__ bool stream_row(const float* srow, int nb, float* ring, uint32_t bar0, uint32_t& seq, Fn fn) {
+    const int tid = threadIdx.x;
+    const int pieces = (nb + PIECE - 1) / PIECE;
+    auto issue = [&](int c) { // thread 0: piece c into slot (seq + c) & 1
+        const int n = min(PIECE, nb - c * PIECE), al = n & ~3;
+        const uint32_t slot = (seq + c) & 1u, bar = bar0 + 8u * slot;
+        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(al * 4));
+        if (al > 0) bulk_g2s(smem_u32(ring + slot * PIECE), srow + (long long)c * PIECE, al * 4, bar);
+    };
+    if (tid == 0) {
+        fence_proxy_async(); // earlier generic accesses of the ring before the copies
+        issue(0);
+        if (pieces > 1) issue(1);
+    }
+    bool ok = true;
+    int c = 0;
+    for (; c < pieces; ++c) {
+        const uint32_t slot = (seq + c) & 1u;
+        const bool landed = mbar_wait(bar0 + 8u * slot, ((seq + c) >> 1) & 1u);
+        if (__syncthreads_or(!landed)) {
+            ok = false;
+            break;
+        }
+        float* const piece = ring + slot * PIECE;
+        const int n = min(PIECE, nb - c * PIECE), al = n & ~3;
+        if (tid < n - al) piece[al + tid] = srow[(long long)c * PIECE + al + tid]; // unaligned end
+        __syncthreads();
+        fn(piece, c * PIECE, n);
+        __syncthreads(); // the slot's readers are done
+        if (tid == 0 && c + 2 < pieces) {
+            fence_proxy_async();
+            issue(c + 2);
+        }
+    }
+    if (!ok && tid == 0) { // let the copies still in flight land before the CTA leaves
+        for (int k = c; k < pieces && k < c + 2; ++k)
+            mbar_wait(bar0 + 8u * ((seq + k) & 1u), ((seq + k) >> 1) & 1u);
+    }
+    seq += static_cast<uint32_t>(pieces);
+    return ok;
+}
+
 __global__ void __launch_bounds__(THREADS, 1) topk_expand_kernel(const Params p) {
-    __shared__ uint32_t hist[256];
+    extern __shared__ __align__(128) uint8_t smem[];
+    float* const ring = reinterpret_cast<float*>(smem + OFF_RING);
+    uint32_t* const keys = reinterpret_cast<uint32_t*>(smem + OFF_KEYS);
+    uint32_t* const hist = reinterpret_cast<uint32_t*>(smem + OFF_HIST);
+    __shared__ __align__(8) uint64_t bars[2];
     __shared__ int wsum[WARPS];
-    __shared__ int sh_digit, sh_before, sh_off;
+    __shared__ int sh[4];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int b = blockIdx.x;
+    const uint32_t bar0 = smem_u32(bars);
+    if (tid == 0) {
+        mbar_init(bar0, 1);
+        mbar_init(bar0 + 8, 1);
+        fence_mbarrier_init();
+        sh[0] = sh[1] = 0;
+    }
     griddep_wait();
     griddep_launch_dependents();
 
     // ---------------------------------------------------------------- the row's place
     const int r = p.ratio, kb = p.kb;
-    {
-        int before = tid < b ? row_len(clamp_len(p.ctx[tid], p.capacity), r, kb) : 0;
+    int before = 0;
+    for (int j = tid; j < b; j += THREADS) before += row_len(clamp_len(p.ctx[j], p.capacity), r, kb);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) before += __shfl_xor_sync(FULL, before, o);
-        if (lane == 0 && warp < MAX_BS / 32) wsum[warp] = before;
-        __syncthreads();
-        if (tid == 0) sh_off = wsum[0] + wsum[1] + wsum[2] + wsum[3];
-    }
+    for (int o = 16; o > 0; o >>= 1) before += __shfl_xor_sync(FULL, before, o);
+    const int off = block_prefix(before, wsum).y;
     const int Traw = p.ctx[b];
     if (tid == 0 && p.err != nullptr && (Traw < 0 || Traw > p.capacity))
         atomicOr(p.err, QSA_DEVERR_CTX_LEN);
     const int T = clamp_len(Traw, p.capacity);
     const int nb = T / r, tail = T - nb * r;
-    __syncthreads();
-    const int off = sh_off;
     if (tid == 0) {
         p.cu[b + 1] = off + row_len(T, r, kb);
         if (b == 0) p.cu[0] = 0;
@@ -147,115 +360,151 @@ __global__ void __launch_bounds__(THREADS, 1) topk_expand_kernel(const Params p)
         return;
     }
     const float* const srow = p.scores + (long long)b * p.s_stride;
+    uint32_t seq = 0;
+    auto timed_out = [&]() {
+        if (tid == 0 && p.err != nullptr) atomicOr(p.err, QSA_DEVERR_TIMEOUT);
+    };
+    auto clear_hist = [&]() {
+        for (int i = tid; i < NBINS; i += THREADS) hist[i] = 0u;
+        __syncthreads();
+    };
+    // writes a kept block's r token slots at its rank
+    auto put_block = [&](int i, int j) {
+        if (j < kb) { // exactly kb are kept; the bound guards the row
+            int* const dst = out + j * r;
+            for (int t = 0; t < r; ++t) dst[t] = slot_of(p, ptrow, i * r + t, bad);
+        }
+    };
+    // radix passes 1 and 2 (digits of 11 and 10 bits) over keys in shared memory
+    auto select_in_smem = [&](int n, uint32_t& prefix, uint32_t& mask, int& need) {
+        for (int pass = 1; pass < 3; ++pass) {
+            const int shift = pass == 1 ? 10 : 0, bins = pass == 1 ? 2048 : 1024;
+            clear_hist();
+            for (int i = tid; i < n; i += THREADS) {
+                const uint32_t k = keys[i];
+                if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & (bins - 1)], 1u);
+            }
+            __syncthreads();
+            const int2 d = find_digit(hist, bins, need, wsum, sh);
+            prefix |= static_cast<uint32_t>(d.x) << shift;
+            mask |= static_cast<uint32_t>(bins - 1) << shift;
+            need -= d.y;
+        }
+    };
 
-    // ---------------------------------------------------------------- radix select
     uint32_t prefix = 0u, mask = 0u;
-    int need = kb; // rank of the wanted key among the keys matching the prefix
-#pragma unroll 1
-    for (int shift = 24; shift >= 0; shift -= 8) {
-        if (tid < 256) hist[tid] = 0u;
-        __syncthreads();
-#pragma unroll 1
-        for (int base = 0; base < nb; base += THREADS) {
-            const int i = base + tid;
-            const uint32_t key = i < nb ? order_key(srow[i]) : 0u;
-            const bool cand = i < nb && (key & mask) == prefix;
-            const unsigned act = __ballot_sync(FULL, cand);
-            if (cand) {
-                const uint32_t dig = (key >> shift) & 255u;
-                const unsigned peers = __match_any_sync(act, dig);
-                if (lane == __ffs(peers) - 1) atomicAdd(&hist[dig], static_cast<uint32_t>(__popc(peers)));
+    int need = kb; // rank of the wanted key among the keys that match the prefix
+    if (nb <= KEYS_CAP) {
+        // ------------------------------------------------ the row fits: keys in shared memory
+        clear_hist();
+        const bool ok = stream_row(srow, nb, ring, bar0, seq, [&](const float* piece, int base, int n) {
+            for (int j = tid; j < n; j += THREADS) {
+                const uint32_t k = order_key(piece[j]);
+                keys[base + j] = k;
+                atomicAdd(&hist[k >> 21], 1u);
             }
-        }
+        });
+        if (!ok) return timed_out();
         __syncthreads();
-        // digits from the top: the one whose bin holds the need-th key
-        int incl = 0, c = 0;
-        if (tid < 256) {
-            c = static_cast<int>(hist[255 - tid]);
-            incl = c;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int v = __shfl_up_sync(FULL, incl, o);
-                if (lane >= o) incl += v;
+        const int2 d = find_digit(hist, NBINS, need, wsum, sh);
+        prefix = static_cast<uint32_t>(d.x) << 21;
+        mask = 0x7FFu << 21;
+        need -= d.y;
+        select_in_smem(nb, prefix, mask, need);
+        const uint32_t thr = prefix;
+        int ca = 0, cs = 0;
+        for (int base = 0; base < nb; base += PIECE)
+            scan_piece(min(PIECE, nb - base), [&](int j) { return keys[base + j]; },
+                       [&](uint32_t k) { return k == thr; },
+                       [&](uint32_t k, bool eq, int rank) { return k > thr || (eq && rank < need); },
+                       [&](int j, int rank) { put_block(base + j, rank); }, ca, cs, wsum);
+    } else {
+        // ------------------------------------------------ a long row: stream the passes
+        clear_hist();
+        bool ok = stream_row(srow, nb, ring, bar0, seq, [&](const float* piece, int base, int n) {
+            for (int j = tid; j < n; j += THREADS) atomicAdd(&hist[order_key(piece[j]) >> 21], 1u);
+        });
+        if (!ok) return timed_out();
+        __syncthreads();
+        const int2 d = find_digit(hist, NBINS, need, wsum, sh);
+        const uint32_t d1 = static_cast<uint32_t>(d.x) & (NBINS - 1);
+        const int cand = static_cast<int>(hist[d1]); // keys in the bin of the k-th key
+        need -= d.y;
+        __syncthreads();
+        if (cand <= KEYS_CAP) {
+            // gather that bin's keys, in index order, into shared memory
+            int ca = 0, cs = 0;
+            ok = stream_row(srow, nb, ring, bar0, seq, [&](const float* piece, int base, int n) {
+                scan_piece(n, [&](int j) { return order_key(piece[j]); },
+                           [&](uint32_t) { return false; },
+                           [&](uint32_t k, bool, int) { return (k >> 21) == d1; },
+                           [&](int j, int rank) {
+                               if (rank < KEYS_CAP) keys[rank] = order_key(piece[j]);
+                           }, ca, cs, wsum);
+            });
+            if (!ok) return timed_out();
+            __syncthreads();
+            prefix = d1 << 21;
+            mask = 0x7FFu << 21;
+            select_in_smem(cand, prefix, mask, need);
+            const uint32_t thr = prefix;
+            // mark the kept keys of the bin (ties: the first `need` in index order) with
+            // 0xFFFFFFFF, a value order_key never returns; a piece's keys are all read
+            // before its emits run
+            ca = cs = 0;
+            for (int base = 0; base < cand; base += PIECE)
+                scan_piece(min(PIECE, cand - base), [&](int j) { return keys[base + j]; },
+                           [&](uint32_t k) { return k == thr; },
+                           [&](uint32_t k, bool eq, int rank) { return k > thr || (eq && rank < need); },
+                           [&](int j, int) { keys[base + j] = KEPT; }, ca, cs, wsum);
+            __syncthreads();
+            // the compaction: bins above d1 are kept, bin d1's keys by their flag
+            ca = cs = 0;
+            ok = stream_row(srow, nb, ring, bar0, seq, [&](const float* piece, int base, int n) {
+                scan_piece(n, [&](int j) { return order_key(piece[j]); },
+                           [&](uint32_t k) { return (k >> 21) == d1; },
+                           [&](uint32_t k, bool inbin, int rank) {
+                               return (k >> 21) > d1 || (inbin && keys[rank] == KEPT);
+                           },
+                           [&](int j, int rank) { put_block(base + j, rank); }, ca, cs, wsum);
+            });
+            if (!ok) return timed_out();
+        } else {
+            // the bin is too large to gather: stream the remaining passes too
+            prefix = d1 << 21;
+            mask = 0x7FFu << 21;
+            for (int pass = 1; pass < 3; ++pass) {
+                const int shift = pass == 1 ? 10 : 0, bins = pass == 1 ? 2048 : 1024;
+                clear_hist();
+                ok = stream_row(srow, nb, ring, bar0, seq, [&](const float* piece, int, int n) {
+                    for (int j = tid; j < n; j += THREADS) {
+                        const uint32_t k = order_key(piece[j]);
+                        if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & (bins - 1)], 1u);
+                    }
+                });
+                if (!ok) return timed_out();
+                __syncthreads();
+                const int2 dd = find_digit(hist, bins, need, wsum, sh);
+                prefix |= static_cast<uint32_t>(dd.x) << shift;
+                mask |= static_cast<uint32_t>(bins - 1) << shift;
+                need -= dd.y;
             }
-            if (lane == 31) wsum[warp] = incl;
+            const uint32_t thr = prefix;
+            int ca = 0, cs = 0;
+            ok = stream_row(srow, nb, ring, bar0, seq, [&](const float* piece, int base, int n) {
+                scan_piece(n, [&](int j) { return order_key(piece[j]); },
+                           [&](uint32_t k) { return k == thr; },
+                           [&](uint32_t k, bool eq, int rank) { return k > thr || (eq && rank < need); },
+                           [&](int j, int rank) { put_block(base + j, rank); }, ca, cs, wsum);
+            });
+            if (!ok) return timed_out();
         }
-        __syncthreads();
-        if (tid < 256) {
-            for (int w = 0; w < warp; ++w) incl += wsum[w];
-            const int excl = incl - c;
-            if (excl < need && need <= incl) {
-                sh_digit = 255 - tid;
-                sh_before = excl;
-            }
-        }
-        __syncthreads();
-        prefix |= static_cast<uint32_t>(sh_digit) << shift;
-        mask |= 255u << shift;
-        need -= sh_before;
-    }
-    const uint32_t thr = prefix; // the k-th key; `need` blocks equal to it are kept
-
-    // ---------------------------------------------------------------- compaction
-    int eq_carry = 0, sel_carry = 0;
-    const uint32_t lt = lanemask_lt();
-#pragma unroll 1
-    for (int base = 0; base < nb; base += CHUNK) {
-        const int wbase = base + warp * 32 * ROUNDS;
-        uint32_t eqm[ROUNDS], gtm[ROUNDS];
-        int weq = 0;
-#pragma unroll
-        for (int e = 0; e < ROUNDS; ++e) {
-            const int i = wbase + e * 32 + lane;
-            const uint32_t key = i < nb ? order_key(srow[i]) : 0u;
-            eqm[e] = __ballot_sync(FULL, i < nb && key == thr);
-            gtm[e] = __ballot_sync(FULL, i < nb && key > thr);
-            weq += __popc(eqm[e]);
-        }
-        __syncthreads(); // wsum free (previous chunk's readers are done)
-        if (lane == 0) wsum[warp] = weq;
-        __syncthreads();
-        int eq_before = eq_carry, eq_total = 0;
-        for (int w = 0; w < WARPS; ++w) {
-            const int v = wsum[w];
-            if (w < warp) eq_before += v;
-            eq_total += v;
-        }
-        uint32_t selm[ROUNDS];
-        int wsel = 0;
-#pragma unroll
-        for (int e = 0; e < ROUNDS; ++e) {
-            const bool eq = (eqm[e] >> lane) & 1u;
-            const bool sel = ((gtm[e] >> lane) & 1u) || (eq && eq_before + __popc(eqm[e] & lt) < need);
-            eq_before += __popc(eqm[e]);
-            selm[e] = __ballot_sync(FULL, sel);
-            wsel += __popc(selm[e]);
-        }
-        __syncthreads();
-        if (lane == 0) wsum[warp] = wsel;
-        __syncthreads();
-        int rank = sel_carry, sel_total = 0;
-        for (int w = 0; w < WARPS; ++w) {
-            const int v = wsum[w];
-            if (w < warp) rank += v;
-            sel_total += v;
-        }
-#pragma unroll
-        for (int e = 0; e < ROUNDS; ++e) {
-            const int j = rank + __popc(selm[e] & lt);
-            if (((selm[e] >> lane) & 1u) && j < kb) { // exactly kb are kept; the bound guards the row
-                const int i = wbase + e * 32 + lane;
-                int* const dst = out + j * r;
-                for (int t = 0; t < r; ++t) dst[t] = slot_of(p, ptrow, i * r + t, bad);
-            }
-            rank += __popc(selm[e]);
-        }
-        eq_carry += eq_total;
-        sel_carry += sel_total;
     }
     // the tail tokens, after the k kept blocks
     for (int t = tid; t < tail; t += THREADS) out[kb * r + t] = slot_of(p, ptrow, nb * r + t, bad);
     if (bad && p.err != nullptr) atomicOr(p.err, QSA_DEVERR_SLOT_RANGE);
+    (void)lane;
+    (void)warp;
 }
 
 namespace {
@@ -310,6 +559,10 @@ extern "C" int qsa_topk_expand(const qsa_tensor* scores, const qsa_tensor* ctx_l
         return fail(QSA_ERR_INVALID_ARGUMENT,
                     "scores must be float32 [bs, >= capacity / compress_ratio = %lld], unit stride "
                     "along the blocks", nbmax);
+    if ((reinterpret_cast<uintptr_t>(scores->data) & 15u) || scores->stride[0] % 4 != 0)
+        return fail(QSA_ERR_MISALIGNED,
+                    "scores rows must start on 16-byte boundaries (base 16-byte aligned, row "
+                    "stride a multiple of 4)");
     const int ps = params->page_size;
     int shift = 0;
     const int* pt = nullptr;
@@ -350,16 +603,33 @@ extern "C" int qsa_topk_expand(const qsa_tensor* scores, const qsa_tensor* ctx_l
     p.kb = K / r;
     p.capacity = cap;
 
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(QSA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= 64) return fail(QSA_ERR_CUDA, "device ordinal %d out of range", dev);
+    {
+        static std::mutex mu;
+        static bool smem_set[64] = {};
+        std::lock_guard<std::mutex> lk(mu);
+        if (!smem_set[dev]) {
+            e = cudaFuncSetAttribute(topk_expand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     SMEM_BYTES);
+            if (e != cudaSuccess)
+                return fail(QSA_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+            smem_set[dev] = true;
+        }
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(bs));
     cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
     cfg.stream = static_cast<cudaStream_t>(stream);
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, topk_expand_kernel, p);
+    e = cudaLaunchKernelEx(&cfg, topk_expand_kernel, p);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return fail(QSA_ERR_CUDA, "top-k launch: %s", cudaGetErrorString(e));
     qsa_detail_set_error("");

@@ -200,3 +200,23 @@ def test_topk_feeds_the_decode_in_one_graph(cuda_device):
                                             capacity=width), list(range(bs)))
             compare(out, run_oracle(host), host.lengths().numpy())
     assert qsa.qsa_scratch_error(scratch) == 0
+
+
+def test_long_rows_through_every_path(cuda_device):
+    """256K contexts (65,536 blocks at ratio 4, 262,144 at ratio 1), longer than the
+    kernel keeps in shared memory: N(0,1) scores take the gathered-bin path; scores
+    in [1, 1.25) share their top 11 bits, so the bin of the k-th key holds every
+    block and the kernel streams every pass instead."""
+    cap = I.TOPK_CAPACITY
+    g = torch.Generator(device=cuda_device).manual_seed(3)
+    for ratio, topk, crowded in ((4, 2048, False), (4, 2048, True), (1, 2048, False)):
+        bs = 2
+        if crowded:
+            scores = 1.0 + 0.25 * torch.rand(bs, cap // ratio, generator=g, device=cuda_device)
+            scores[:, ::1000] = 1.125     # and ties inside the crowded bin
+        else:
+            scores = I.block_scores(bs, cap // ratio, 31 + ratio, cuda_device)
+        lens = torch.tensor([cap, cap - 2], dtype=torch.int32, device=cuda_device)
+        sel, cu = _run(scores, lens, topk, ratio, cap)
+        torch.cuda.synchronize()
+        _check(sel, cu, scores, lens, topk, ratio, cap)
