@@ -36,14 +36,19 @@
 //    into hi + lo columns of the PV operand type (24 columns: 12 heads x {hi,
 //    lo}), so P keeps ~16 (bf16) or ~22 (f16) significant bits; each warp owns
 //    32 of the 256 output dims.
-//  * Quantised pools are converted exactly, in shared memory, by the warp
-//    that consumes them: codes become f16 for QK (Q is rescaled per head by a
-//    power of two so it converts to f16 exactly) and f16 (fp8, int8) or bf16
-//    (int4, grouped, tiered) for PV, with magic-number integer conversions and
-//    the hardware e4m3 conversion. Per-slot scales scale the scores (K) and the
-//    probabilities (V) in FP32 (int8 keeps a per-head power-of-two offset so
-//    that P times its V scale fits f16); per-pool fp8 scales fold into
-//    constants.
+//  * Quantised pools are converted exactly, in registers, from the raw stage:
+//    a K row's ldmatrix word (4 codes of 8 bits, or 8 of 4 bits) becomes the f16
+//    pairs of an MMA B fragment (the k-slots follow the word's codes and Q is
+//    loaded in that order; Q is rescaled per head by a power of two so it
+//    converts to f16 exactly), and ldmatrix.trans of the raw V rows gives each
+//    lane one code of two consecutive tokens, the f16 (fp8, int8) or bf16 (int4,
+//    grouped) pairs of the PV A fragment (the warp's 32 output dims are spread
+//    over its two m-tiles accordingly). Integers use magic-number conversions,
+//    e4m3 the hardware conversion; no converted tile and no shared-memory round
+//    trip. Per-slot scales scale the scores (K) and the probabilities (V) in
+//    FP32 (int8 keeps a per-head power-of-two offset so that P times its V scale
+//    fits f16); per-pool fp8 scales fold into constants. The tiered pool, whose
+//    rows mix two formats, is converted in shared memory by the consuming warp.
 //    Grouped pools (binary16 scale per 64 / 32 channels): QK accumulates each
 //    channel group's k-steps apart and adds them with the token's group scale;
 //    each consumer warp's 32 PV dims lie in one group, so the warp rebuilds its
@@ -97,57 +102,52 @@ static_assert(TPW == 8 && MT >= 1 && TPP <= 32, "tile shape");
 static_assert(PART_BYTES >= (GROUP * D + 2 * GROUP) * 4, "partial slot size");
 static_assert(PART_BYTES % 16 == 0, "bulk copies move 16-byte multiples");
 
-// ROWB: pool row bytes; DEQ: rows are converted in shared memory; SCALES:
-// per-slot scales (fp32 per (slot, KV head), or binary16 per (slot, KV head,
-// channel group) when GROUPS > 0); QK_F16: QK runs on f16 operands (exact
-// integer / e4m3 codes, Q rescaled per head by a power of two); PV_F16: PV runs
-// on f16 operands (for int8, with a per-head power-of-two offset that keeps
-// P * s_v in range); NIB4: 4-bit codes,
-// NIB_OFFSET: stored as code + 8 (else two's complement); TIER: each row is an
-// int8_g64 ring row or an int4_g32 pool row, by the owner table (scales held at
-// the 32-channel granularity, a ring row's 64-channel scales expanded).
+// ROWB: pool row bytes; STAGES: ring depth; DEQ: rows are converted in shared
+// memory by the consuming warp (tiered pools); RQ: codes are converted in
+// registers from the raw stage (K as MMA B fragments, V as PV A fragments), no
+// converted tiles; QK_F16: QK runs on f16 operands (exact integer / e4m3 codes,
+// Q rescaled per head by a power of two); PV_F16: PV runs on f16
+// operands (for int8, with a per-head power-of-two offset that keeps P * s_v in
+// range), else bf16; SCALES: per-slot scales (fp32 per (slot, KV head), or
+// binary16 per (slot, KV head, channel group) when GROUPS > 0); NIB4: 4-bit
+// codes, NIB_OFFSET: stored as code + 8 (else two's complement); TIER: each row
+// is an int8_g64 ring row or an int4_g32 pool row, by the owner table (scales
+// held at the 32-channel granularity, a ring row's 64-channel scales expanded).
 template <int FMT> struct Traits;
 template <> struct Traits<QSA_KV_BF16> {
     static constexpr int ROWB = 512, STAGES = 3, GROUPS = 0;
-    static constexpr bool DEQ = false, SCALES = false, QK_F16 = false, PV_F16 = false;
-    static constexpr bool NIB4 = false, NIB_OFFSET = false;
-    static constexpr bool TIER = false;
+    static constexpr bool DEQ = false, RQ = false, SCALES = false, QK_F16 = false;
+    static constexpr bool PV_F16 = false, NIB4 = false, NIB_OFFSET = false, TIER = false;
 };
 template <> struct Traits<QSA_KV_FP8_E4M3> {
-    static constexpr int ROWB = 256, STAGES = 4, GROUPS = 0;
-    static constexpr bool DEQ = true, SCALES = false, QK_F16 = true, PV_F16 = true;
-    static constexpr bool NIB4 = false, NIB_OFFSET = false;
-    static constexpr bool TIER = false;
+    static constexpr int ROWB = 256, STAGES = 6, GROUPS = 0;
+    static constexpr bool DEQ = false, RQ = true, SCALES = false, QK_F16 = true;
+    static constexpr bool PV_F16 = true, NIB4 = false, NIB_OFFSET = false, TIER = false;
 };
 template <> struct Traits<QSA_KV_INT8> {
-    static constexpr int ROWB = 256, STAGES = 4, GROUPS = 0;
-    static constexpr bool DEQ = true, SCALES = true, QK_F16 = true, PV_F16 = true;
-    static constexpr bool NIB4 = false, NIB_OFFSET = false;
-    static constexpr bool TIER = false;
+    static constexpr int ROWB = 256, STAGES = 6, GROUPS = 0;
+    static constexpr bool DEQ = false, RQ = true, SCALES = true, QK_F16 = true;
+    static constexpr bool PV_F16 = true, NIB4 = false, NIB_OFFSET = false, TIER = false;
 };
 template <> struct Traits<QSA_KV_INT4> {
-    static constexpr int ROWB = 128, STAGES = 6, GROUPS = 0;
-    static constexpr bool DEQ = true, SCALES = true, QK_F16 = true, PV_F16 = false;
-    static constexpr bool NIB4 = true, NIB_OFFSET = false;
-    static constexpr bool TIER = false;
+    static constexpr int ROWB = 128, STAGES = 11, GROUPS = 0;
+    static constexpr bool DEQ = false, RQ = true, SCALES = true, QK_F16 = true;
+    static constexpr bool PV_F16 = false, NIB4 = true, NIB_OFFSET = false, TIER = false;
 };
 template <> struct Traits<QSA_KV_INT8_G64> {
-    static constexpr int ROWB = 256, STAGES = 3, GROUPS = 4;
-    static constexpr bool DEQ = true, SCALES = true, QK_F16 = true, PV_F16 = false;
-    static constexpr bool NIB4 = false, NIB_OFFSET = false;
-    static constexpr bool TIER = false;
+    static constexpr int ROWB = 256, STAGES = 5, GROUPS = 4;
+    static constexpr bool DEQ = false, RQ = true, SCALES = true, QK_F16 = true;
+    static constexpr bool PV_F16 = false, NIB4 = false, NIB_OFFSET = false, TIER = false;
 };
 template <> struct Traits<QSA_KV_INT4_G32> {
-    static constexpr int ROWB = 128, STAGES = 6, GROUPS = 8;
-    static constexpr bool DEQ = true, SCALES = true, QK_F16 = true, PV_F16 = false;
-    static constexpr bool NIB4 = true, NIB_OFFSET = true;
-    static constexpr bool TIER = false;
+    static constexpr int ROWB = 128, STAGES = 9, GROUPS = 8;
+    static constexpr bool DEQ = false, RQ = true, SCALES = true, QK_F16 = true;
+    static constexpr bool PV_F16 = false, NIB4 = true, NIB_OFFSET = true, TIER = false;
 };
 template <> struct Traits<QSA_KV_INT8RING_INT4> {
     static constexpr int ROWB = 256, STAGES = 3, GROUPS = 8;
-    static constexpr bool DEQ = true, SCALES = true, QK_F16 = true, PV_F16 = false;
-    static constexpr bool NIB4 = false, NIB_OFFSET = true;
-    static constexpr bool TIER = true;
+    static constexpr bool DEQ = true, RQ = false, SCALES = true, QK_F16 = true;
+    static constexpr bool PV_F16 = false, NIB4 = false, NIB_OFFSET = true, TIER = true;
 };
 
 template <int FMT> struct Layout {
@@ -426,6 +426,12 @@ __device__ __forceinline__ void mma16816(float* d, const uint32_t* a, uint32_t b
         mma_bf16(d, a, b0, b1);
 }
 
+__device__ __forceinline__ void ldsm_x2_t(uint32_t& r0, uint32_t& r1, uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];"
+                 : "=r"(r0), "=r"(r1)
+                 : "r"(addr));
+}
+
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -521,6 +527,39 @@ __device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t& lo, uint32_t
         : "r"(w));
 }
 
+// ---------------------------------------------- register-level dequant (RQ pools)
+//
+// ldmatrix.trans of raw 8-bit rows (8 tokens x 16 codes as 8 x 8 pairs) gives a
+// lane the codes [v(2t, 2g), v(2t, 2g+1), v(2t+1, 2g), v(2t+1, 2g+1)] (tokens 2t,
+// 2t+1 of the 8, codes 2g, 2g+1 of the 16). Bytes 0, 2 are one code of two
+// consecutive tokens: a PV A-fragment pair for code 2g; bytes 1, 3 for code 2g+1.
+// `odd` picks which. Exact, as in the shared-memory conversions above.
+template <int FMT, bool F16>
+__device__ __forceinline__ uint32_t pair8(uint32_t w, bool odd) {
+    if constexpr (FMT == QSA_KV_FP8_E4M3) {
+        uint32_t lo, hi;
+        e4m3x4_to_f16(__byte_perm(w, 0u, 0x3120), lo, hi);
+        return odd ? hi : lo;
+    } else if constexpr (F16) {
+        return sub_f16x2(__byte_perm(w ^ 0x80808080u, 0x64646464u, odd ? 0x4341 : 0x4240), 0x64806480u);
+    } else {
+        const uint32_t t = __byte_perm(w, 0u, odd ? 0x4341 : 0x4240);
+        return sub_bf16x2((t & 0x007F007Fu) | 0x43004300u, (t & 0x00800080u) | 0x43004300u);
+    }
+}
+
+// ldmatrix.trans of raw 4-bit rows: bytes 0, 2 hold codes 4g, 4g+1 (low, high
+// nibble) of tokens 2t, 2t+1 and bytes 1, 3 codes 4g+2, 4g+3. Code 4g + j as a
+// pair of the two tokens (f16 or bf16); w already xor-ed with 0x88888888 for
+// two's-complement codes, so every nibble reads as code + 8.
+template <bool F16>
+__device__ __forceinline__ uint32_t pair4(uint32_t w, int j) {
+    constexpr uint32_t MAGIC = F16 ? 0x64006400u : 0x43004300u;
+    constexpr uint32_t BIAS = F16 ? 0x64086408u : 0x43084308u; // 1032 / 136
+    const uint32_t v = ((w >> (4 * j)) & 0x000F000Fu) | MAGIC;
+    return F16 ? sub_f16x2(v, BIAS) : sub_bf16x2(v, BIAS);
+}
+
 // 16 raw bytes of an 8-bit row -> 16 values as two 16-byte chunks (f16 or bf16).
 template <int FMT, bool F16>
 __device__ __forceinline__ void convert16(const uint4 raw, uint4& o0, uint4& o1) {
@@ -549,6 +588,80 @@ __device__ __forceinline__ void convert32_int4(const uint4 raw, uint4* o) {
         i4x8_to<F16, OFFSET>(w[k], r);
         o[k] = make_uint4(r[0], r[1], r[2], r[3]);
     }
+}
+
+// Q fragments of the register-dequant pools (f16, k16 steps), built from the bf16
+// Q tile (rows = heads, 12 real and 4 zero rows, row stride Q_RS). Lane (g, t)
+// holds rows g and g + 8. A K B fragment comes from one ldmatrix word of the raw
+// rows, so the k-slots follow the codes of that word:
+//  * 8-bit codes: a word holds codes 4t .. 4t+3 of a 16-code chunk (the chunk of
+//    step c); k-slots {2t, 2t+1, 8+2t, 9+2t} take codes {4t .. 4t+3}: qa[c] = (row g:
+//    16c+4t,+1; row g+8: same; row g: 16c+4t+2,+3; row g+8: same).
+//  * 4-bit codes: a word holds codes 8t .. 8t+7 of a 32-code chunk c, the pairs
+//    (8t, 8t+1), (8t+2, 8t+3) feed step 2c and (8t+4, 8t+5), (8t+6, 8t+7) step 2c+1.
+// Each row is scaled by a power of two that brings its largest |q| into
+// [2^14, 2^15), so the bf16 values are exact in f16; mul = the inverse factor.
+template <int FMT>
+__device__ __forceinline__ void build_q_rq(const uint8_t* qt, int lane, uint32_t (&qa)[16][4],
+                                           float& mul_a, float& mul_b) {
+    using Tr = Traits<FMT>;
+    const int g = lane >> 2, t = lane & 3;
+    const uint8_t* const ra = qt + g * Q_RS;
+    const uint8_t* const rb = qt + (g + 8) * Q_RS;
+    if constexpr (!Tr::NIB4) {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+            const uint2 a = *reinterpret_cast<const uint2*>(ra + (16 * c + 4 * t) * 2);
+            const uint2 b = *reinterpret_cast<const uint2*>(rb + (16 * c + 4 * t) * 2);
+            qa[c][0] = a.x;
+            qa[c][1] = b.x;
+            qa[c][2] = a.y;
+            qa[c][3] = b.y;
+        }
+    } else {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const uint4 a = *reinterpret_cast<const uint4*>(ra + (32 * c + 8 * t) * 2);
+            const uint4 b = *reinterpret_cast<const uint4*>(rb + (32 * c + 8 * t) * 2);
+            qa[2 * c][0] = a.x;
+            qa[2 * c][1] = b.x;
+            qa[2 * c][2] = a.y;
+            qa[2 * c][3] = b.y;
+            qa[2 * c + 1][0] = a.z;
+            qa[2 * c + 1][1] = b.z;
+            qa[2 * c + 1][2] = a.w;
+            qa[2 * c + 1][3] = b.w;
+        }
+    }
+    float ma = 0.f, mb = 0.f; // row maxima: rows g (registers 0, 2) and g + 8 (1, 3)
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+        ma = fmaxf(ma, fmaxf(fmaxf(fabsf(bf16_lo(qa[c][0])), fabsf(bf16_hi(qa[c][0]))),
+                             fmaxf(fabsf(bf16_lo(qa[c][2])), fabsf(bf16_hi(qa[c][2])))));
+        mb = fmaxf(mb, fmaxf(fmaxf(fabsf(bf16_lo(qa[c][1])), fabsf(bf16_hi(qa[c][1]))),
+                             fmaxf(fabsf(bf16_lo(qa[c][3])), fabsf(bf16_hi(qa[c][3])))));
+    }
+    ma = fmaxf(ma, __shfl_xor_sync(0xFFFFFFFFu, ma, 1));
+    ma = fmaxf(ma, __shfl_xor_sync(0xFFFFFFFFu, ma, 2));
+    mb = fmaxf(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 1));
+    mb = fmaxf(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 2));
+    auto shift_of = [](float m) {
+        const int e = static_cast<int>((__float_as_uint(m) >> 23) & 0xFFu) - 127;
+        const int sh = m > 0.f ? e - 14 : 0;
+        return sh < -100 ? -100 : (sh > 100 ? 100 : sh);
+    };
+    auto pow2 = [](int e) { return __uint_as_float(static_cast<uint32_t>(127 + e) << 23); };
+    const int sa = shift_of(ma), sb = shift_of(mb);
+    const float da = pow2(-sa), db = pow2(-sb);
+    mul_a = pow2(sa);
+    mul_b = pow2(sb);
+#pragma unroll
+    for (int c = 0; c < 16; ++c)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float d = (j & 1) ? db : da;
+            qa[c][j] = pack_f16x2(bf16_lo(qa[c][j]) * d, bf16_hi(qa[c][j]) * d);
+        }
 }
 
 // ------------------------------------------------------------ work cursor
@@ -951,16 +1064,20 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
             const int qb = cc.kseg & 1;
             if (!mbar_wait(qfull_bar(qb), (cc.kseg >> 1) & 1, p.err, abort_flag)) break;
             const uint32_t qbase = smem_u32(smem + Ly::off_q + qb * 16 * Q_RS);
+            if constexpr (Tr::RQ) {
+                build_q_rq<FMT>(smem + Ly::off_q + qb * 16 * Q_RS, lane, qa, qmul_a, qmul_b);
+            } else {
 #pragma unroll
-            for (int ks = 0; ks < 16; ++ks) {
-                const int mi = lane >> 3;
-                const uint32_t addr =
-                    qbase + ((mi & 1) * 8 + (lane & 7)) * Q_RS + (ks * 16 + (mi >> 1) * 8) * 2;
-                ldsm_x4(qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], addr);
+                for (int ks = 0; ks < 16; ++ks) {
+                    const int mi = lane >> 3;
+                    const uint32_t addr =
+                        qbase + ((mi & 1) * 8 + (lane & 7)) * Q_RS + (ks * 16 + (mi >> 1) * 8) * 2;
+                    ldsm_x4(qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], addr);
+                }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(qempty_bar(qb));
-            if constexpr (Tr::QK_F16) {
+            if constexpr (Tr::QK_F16 && !Tr::RQ) {
                 // Q to f16, exactly: scale each head (row) by a power of two that
                 // brings its largest |q| into [2^14, 2^15); undo it on the scores.
                 float mr = 0.f, mr8 = 0.f;
@@ -1014,12 +1131,51 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
         uint32_t ksw[2][GP];
         float svw[2] = {0.f, 0.f};
 
-        if constexpr (Tr::DEQ) {
+        // per-slot scales, into registers while the stage is held
+        if constexpr (Tr::SCALES && !Tr::GROUPS) {
+            const float* sc = reinterpret_cast<const float*>(Vs + Ly::STAGE_KV);
+            skr[0] = sc[tk0];
+            skr[1] = sc[tk0 + 1];
+            svr[0] = sc[T + tk0];
+            svr[1] = sc[T + tk0 + 1];
+        }
+        if constexpr (Tr::GROUPS) { // read before the stage is released
+            constexpr int G = Tr::GROUPS;
+            const uint32_t* sk = reinterpret_cast<const uint32_t*>(Vs + Ly::STAGE_KV);
+#pragma unroll
+            for (int k = 0; k < GP; ++k) {
+                ksw[0][k] = sk[tk0 * GP + k];
+                ksw[1][k] = sk[(tk0 + 1) * GP + k];
+            }
+            const __half* sv = reinterpret_cast<const __half*>(Vs + Ly::STAGE_KV + T * Ly::SC_TOK);
+            const int gv = warp * G / NW;
+            if constexpr (Tr::TIER) {
+                // a ring row holds 4 scales of 64 channels: 32-channel group k reads k / 2
+                const int* flag = reinterpret_cast<const int*>(Vs + Ly::STAGE_KV + Ly::STAGE_SC);
+#pragma unroll
+                for (int u = 0; u < 2; ++u)
+                    if (flag[tk0 + u]) {
+                        const uint32_t e0 = ksw[u][0], e1 = ksw[u][1];
+                        ksw[u][0] = __byte_perm(e0, 0, 0x1010);
+                        ksw[u][1] = __byte_perm(e0, 0, 0x3232);
+                        ksw[u][2] = __byte_perm(e1, 0, 0x1010);
+                        ksw[u][3] = __byte_perm(e1, 0, 0x3232);
+                    }
+                svw[0] = __half2float(sv[(2 * lane) * G + (flag[2 * lane] ? gv >> 1 : gv)]);
+                svw[1] = __half2float(sv[(2 * lane + 1) * G + (flag[2 * lane + 1] ? gv >> 1 : gv)]);
+            } else {
+                svw[0] = __half2float(sv[(2 * lane) * G + gv]);
+                svw[1] = __half2float(sv[(2 * lane + 1) * G + gv]);
+            }
+        }
+
+        if constexpr (Tr::DEQ) { // tiered pools: each token converted by its tier, in shared memory
+            static_assert(Tr::TIER, "shared-memory conversion serves the tiered pools");
             uint8_t* const kbf = smem + Ly::off_kbf;
             uint8_t* const vbf = kbf + T * BF_ROW;
             const int tt = lane & 7, ch = lane >> 3;
             const int t = tok_base + tt;
-            if constexpr (Tr::TIER) {
+            {
                 const int* flag = reinterpret_cast<const int*>(Vs + Ly::STAGE_KV + Ly::STAGE_SC);
                 // K: this warp's 8 tokens, each by its tier
                 if (flag[t]) {
@@ -1062,88 +1218,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
                     for (int k = 0; k < 4; ++k)
                         *reinterpret_cast<uint4*>(vbf + swz<BF_ROW>(tv, 4 * warp + k)) = ov[k];
                 }
-            } else if constexpr (Tr::NIB4) {
-                // K: this warp's 8 tokens; 8 raw chunks per row, 32 values each
-#pragma unroll
-                for (int it = 0; it < 2; ++it) {
-                    const int rc = ch + 4 * it;
-                    const uint4 raw = *reinterpret_cast<const uint4*>(Ks + swz<Tr::ROWB>(t, rc));
-                    uint4 ov[4];
-                    convert32_int4<Tr::QK_F16, Tr::NIB_OFFSET>(raw, ov);
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        *reinterpret_cast<uint4*>(kbf + swz<BF_ROW>(t, 4 * rc + k)) = ov[k];
-                }
-                // V: this warp's 32 dims = raw chunk `warp` of every token
-#pragma unroll
-                for (int it = 0; it < 2; ++it) {
-                    const int tv = lane + 32 * it;
-                    const uint4 raw = *reinterpret_cast<const uint4*>(Vs + swz<Tr::ROWB>(tv, warp));
-                    uint4 ov[4];
-                    convert32_int4<Tr::PV_F16, Tr::NIB_OFFSET>(raw, ov);
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        *reinterpret_cast<uint4*>(vbf + swz<BF_ROW>(tv, 4 * warp + k)) = ov[k];
-                }
-            } else {
-                // K: this warp's 8 tokens; 16 raw chunks per row, 16 values each
-#pragma unroll
-                for (int it = 0; it < 4; ++it) {
-                    const int rc = ch + 4 * it;
-                    const uint4 raw = *reinterpret_cast<const uint4*>(Ks + swz<Tr::ROWB>(t, rc));
-                    uint4 o0, o1;
-                    convert16<FMT == QSA_KV_FP8_E4M3 ? FMT : QSA_KV_INT8, Tr::QK_F16>(raw, o0, o1);
-                    *reinterpret_cast<uint4*>(kbf + swz<BF_ROW>(t, 2 * rc)) = o0;
-                    *reinterpret_cast<uint4*>(kbf + swz<BF_ROW>(t, 2 * rc + 1)) = o1;
-                }
-                // V: this warp's 32 dims = raw chunks 2*warp, 2*warp+1 of every token;
-                // eight consecutive lanes take eight consecutive tokens of one chunk,
-                // so their swizzled chunks fall in eight different bank groups
-#pragma unroll
-                for (int it = 0; it < 4; ++it) {
-                    const int tv = lane + 32 * (it >> 1), rc = 2 * warp + (it & 1);
-                    const uint4 raw = *reinterpret_cast<const uint4*>(Vs + swz<Tr::ROWB>(tv, rc));
-                    uint4 o0, o1;
-                    convert16<FMT == QSA_KV_FP8_E4M3 ? FMT : QSA_KV_INT8, Tr::PV_F16>(raw, o0, o1);
-                    *reinterpret_cast<uint4*>(vbf + swz<BF_ROW>(tv, 2 * rc)) = o0;
-                    *reinterpret_cast<uint4*>(vbf + swz<BF_ROW>(tv, 2 * rc + 1)) = o1;
-                }
-            }
-            if constexpr (Tr::SCALES && !Tr::GROUPS) {
-                const float* sc = reinterpret_cast<const float*>(Vs + Ly::STAGE_KV);
-                skr[0] = sc[tk0];
-                skr[1] = sc[tk0 + 1];
-                svr[0] = sc[T + tk0];
-                svr[1] = sc[T + tk0 + 1];
-            }
-            if constexpr (Tr::GROUPS) { // read before the stage is released below
-                constexpr int G = Tr::GROUPS;
-                const uint32_t* sk = reinterpret_cast<const uint32_t*>(Vs + Ly::STAGE_KV);
-#pragma unroll
-                for (int k = 0; k < GP; ++k) {
-                    ksw[0][k] = sk[tk0 * GP + k];
-                    ksw[1][k] = sk[(tk0 + 1) * GP + k];
-                }
-                const __half* sv = reinterpret_cast<const __half*>(Vs + Ly::STAGE_KV + T * Ly::SC_TOK);
-                const int gv = warp * G / NW;
-                if constexpr (Tr::TIER) {
-                    // a ring row holds 4 scales of 64 channels: 32-channel group k reads k / 2
-                    const int* flag = reinterpret_cast<const int*>(Vs + Ly::STAGE_KV + Ly::STAGE_SC);
-#pragma unroll
-                    for (int u = 0; u < 2; ++u)
-                        if (flag[tk0 + u]) {
-                            const uint32_t e0 = ksw[u][0], e1 = ksw[u][1];
-                            ksw[u][0] = __byte_perm(e0, 0, 0x1010);
-                            ksw[u][1] = __byte_perm(e0, 0, 0x3232);
-                            ksw[u][2] = __byte_perm(e1, 0, 0x1010);
-                            ksw[u][3] = __byte_perm(e1, 0, 0x3232);
-                        }
-                    svw[0] = __half2float(sv[(2 * lane) * G + (flag[2 * lane] ? gv >> 1 : gv)]);
-                    svw[1] = __half2float(sv[(2 * lane + 1) * G + (flag[2 * lane + 1] ? gv >> 1 : gv)]);
-                } else {
-                    svw[0] = __half2float(sv[(2 * lane) * G + gv]);
-                    svw[1] = __half2float(sv[(2 * lane + 1) * G + gv]);
-                }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(empty_bar(s));
@@ -1153,7 +1227,56 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
 
         // ---------------------------------------------------------------- QK
         float sacc[4][4] = {};
-        if constexpr (Tr::GROUPS == 0) {
+        if constexpr (Tr::RQ) {
+            // this warp's 8 tokens from the raw stage: ldmatrix matrix (lane >> 3) of
+            // word set j reads 16-byte chunk 4j + (lane >> 3) of its token's row; each
+            // word becomes f16 B fragments in registers (k16 step ks: chunk ks for
+            // 8-bit codes, half of chunk ks / 2 for 4-bit codes)
+            const uint32_t krow = smem_u32(Ks) + (tok_base + (lane & 7)) * Tr::ROWB;
+            constexpr int G = Tr::GROUPS ? Tr::GROUPS : 1, KPG = 16 / G; // k16 steps per group
+            float acc[2][4] = {};
+            uint32_t w[4], nb[4];
+#pragma unroll
+            for (int ks = 0; ks < 16; ++ks) {
+                uint32_t b0, b1;
+                if constexpr (Tr::NIB4) {
+                    if ((ks & 7) == 0)
+                        ldsm_x4(w[0], w[1], w[2], w[3], krow + ((((ks >> 1) + (lane >> 3)) ^ xs) << 4));
+                    if ((ks & 1) == 0) i4x8_to<true, Tr::NIB_OFFSET>(w[(ks >> 1) & 3], nb);
+                    b0 = nb[2 * (ks & 1)];
+                    b1 = nb[2 * (ks & 1) + 1];
+                } else {
+                    if ((ks & 3) == 0) ldsm_x4(w[0], w[1], w[2], w[3], krow + (((ks + (lane >> 3)) ^ xs) << 4));
+                    if constexpr (FMT == QSA_KV_FP8_E4M3)
+                        e4m3x4_to_f16(w[ks & 3], b0, b1);
+                    else
+                        i8x4_to_f16(w[ks & 3], b0, b1);
+                }
+                mma_f16(acc[ks & 1], qa[ks], b0, b1);
+                if constexpr (Tr::GROUPS) {
+                    if ((ks + 1) % KPG == 0) { // a group's end: fold with the token's group scale
+                        const int gi = ks / KPG;
+                        float t4[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            t4[e] = acc[0][e] + acc[1][e];
+                            acc[0][e] = acc[1][e] = 0.f;
+                        }
+                        const uint32_t w0 = ksw[0][gi >> 1], w1 = ksw[1][gi >> 1];
+                        const float s0 = __half2float(__ushort_as_half(static_cast<unsigned short>(gi & 1 ? w0 >> 16 : w0)));
+                        const float s1 = __half2float(__ushort_as_half(static_cast<unsigned short>(gi & 1 ? w1 >> 16 : w1)));
+                        sacc[0][0] += t4[0] * s0;
+                        sacc[0][1] += t4[1] * s1;
+                        sacc[0][2] += t4[2] * s0;
+                        sacc[0][3] += t4[3] * s1;
+                    }
+                }
+            }
+            if constexpr (!Tr::GROUPS) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) sacc[0][e] = acc[0][e] + acc[1][e];
+            }
+        } else if constexpr (Tr::GROUPS == 0) {
             const uint32_t krow = smem_u32(Kb) + (tok_base + (lane & 7)) * BF_ROW;
 #pragma unroll
             for (int ks = 0; ks < 16; ks += 2) {
@@ -1415,13 +1538,52 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
                             (kk * 16 + ((lane >> 3) & 1) * 8) * 2);
                 ldsm_x2(pb[2][0], pb[2][1],
                         pbase + (16 + (lane & 7)) * PRS + (kk * 16 + ((lane >> 3) & 1) * 8) * 2);
+                if constexpr (Tr::RQ) {
+                    // V^T fragments straight from the raw stage (ldmatrix.trans of the
+                    // codes, converted in registers); the warp's 32 dims are spread
+                    // over its two m-tiles as the epilogue's dim map says
+                    uint32_t a[MT][4];
+                    const uint32_t vst = smem_u32(Vs);
+                    if constexpr (Tr::NIB4) { // chunk `warp` (32 codes) of tokens 0-7 / 8-15
+                        const int tv = kk * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+                        uint32_t r0, r1;
+                        ldsm_x2_t(r0, r1, vst + tv * Tr::ROWB + ((warp ^ xs) << 4));
+                        if constexpr (!Tr::NIB_OFFSET) {
+                            r0 ^= 0x88888888u;
+                            r1 ^= 0x88888888u;
+                        }
 #pragma unroll
-                for (int mt = 0; mt < MT; ++mt) {
-                    uint32_t a[4];
-                    ldsm_x4_t(a[0], a[1], a[2], a[3],
-                              vrow + kk * 16 * BF_ROW + (((4 * warp + 2 * mt) << 4) ^ vx));
+                        for (int mt = 0; mt < MT; ++mt) {
+                            a[mt][0] = pair4<Tr::PV_F16>(r0, 2 * mt);
+                            a[mt][1] = pair4<Tr::PV_F16>(r0, 2 * mt + 1);
+                            a[mt][2] = pair4<Tr::PV_F16>(r1, 2 * mt);
+                            a[mt][3] = pair4<Tr::PV_F16>(r1, 2 * mt + 1);
+                        }
+                    } else { // chunks 2 warp, 2 warp + 1 (16 codes each) of tokens 0-7 / 8-15
+                        const int mi = lane >> 3;
+                        const int tv = kk * 16 + (mi >> 1) * 8 + (lane & 7);
+                        uint32_t r[4];
+                        ldsm_x4_t(r[0], r[1], r[2], r[3],
+                                  vst + tv * Tr::ROWB + (((2 * warp + (mi & 1)) ^ xs) << 4));
 #pragma unroll
-                    for (int j = 0; j < 3; ++j) mma16816<Tr::PV_F16>(o[mt][j], a, pb[j][0], pb[j][1]);
+                        for (int q = 0; q < 4; ++q) {
+                            a[0][q] = pair8<FMT, Tr::PV_F16>(r[q], false);
+                            a[1][q] = pair8<FMT, Tr::PV_F16>(r[q], true);
+                        }
+                    }
+#pragma unroll
+                    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                        for (int j = 0; j < 3; ++j) mma16816<Tr::PV_F16>(o[mt][j], a[mt], pb[j][0], pb[j][1]);
+                } else {
+#pragma unroll
+                    for (int mt = 0; mt < MT; ++mt) {
+                        uint32_t a[4];
+                        ldsm_x4_t(a[0], a[1], a[2], a[3],
+                                  vrow + kk * 16 * BF_ROW + (((4 * warp + 2 * mt) << 4) ^ vx));
+#pragma unroll
+                        for (int j = 0; j < 3; ++j) mma16816<Tr::PV_F16>(o[mt][j], a, pb[j][0], pb[j][1]);
+                    }
                 }
             }
         }
@@ -1469,6 +1631,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
                 return t;
             };
             const int hA = 2 * c, hB = 2 * c + 1, hC = 8 + 2 * c, hD = 9 + 2 * c;
+            // output dims of accumulator rows r and r + 8 of m-tile mt: 16-dim blocks,
+            // or (register-dequant pools) the warp's 32 dims spread over its two
+            // m-tiles -- 8-bit codes: tile mt holds dims 2i + mt of both 16-dim chunks;
+            // 4-bit codes: tile mt holds dims 4i + 2 mt and 4i + 2 mt + 1
+            auto dim_a = [&](int mt) {
+                return Tr::RQ ? (Tr::NIB4 ? warp * DPW + 4 * r + 2 * mt : warp * DPW + 2 * r + mt)
+                              : warp * DPW + mt * 16 + r;
+            };
+            auto dim_b = [&](int mt) { return dim_a(mt) + (Tr::RQ ? (Tr::NIB4 ? 1 : 16) : 8); };
             // per-slot V scales: O was accumulated against m_h + E_h; back to m_h
             auto esc = [&](int h) { return VSH ? ex2(eref[v * 16 + h]) : 1.f; };
             const float eA = esc(hA), eB = esc(hB);
@@ -1503,7 +1674,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
                 float* const st = reinterpret_cast<float*>(smem + Ly::off_stash);
 #pragma unroll
                 for (int mt = 0; mt < MT; ++mt) {
-                    const int dA = warp * DPW + mt * 16 + r, dB = dA + 8;
+                    const int dA = dim_a(mt), dB = dim_b(mt);
                     st[hA * D + dA] = val[mt][0] * eA;
                     st[hB * D + dA] = val[mt][1] * eB;
                     st[hA * D + dB] = val[mt][2] * eA;
@@ -1524,7 +1695,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
             } else {
 #pragma unroll
                 for (int mt = 0; mt < MT; ++mt) {
-                    const int dA = warp * DPW + mt * 16 + r, dB = dA + 8;
+                    const int dA = dim_a(mt), dB = dim_b(mt);
                     put(hA, dA, val[mt][0] * fA);
                     put(hB, dA, val[mt][1] * fB);
                     put(hA, dB, val[mt][2] * fA);
