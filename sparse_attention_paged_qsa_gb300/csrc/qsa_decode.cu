@@ -98,6 +98,15 @@ constexpr int PART_BYTES = 12416;           // fp32 O[12][256] + m[12] + l[12], 
 constexpr int MERGE_BATCH = 6;             // partials per bulk-copy batch of the split merge
 constexpr long long WAIT_NS = 2000000000LL; // bounded-wait limit (2 s)
 constexpr int BAR_CONSUMERS = 1;            // named barrier id (2..5: consumer warp pairs)
+// Register split between the warp roles (setmaxnreg) of the pools whose consumer
+// warps set the pace (the dequantising ones): the block is launched with
+// LAUNCH_REGS per thread; the producer warpgroup gives registers back and the two
+// consumer warpgroups take them, the shares adding up to the launch's total. The
+// bf16 pool, bound by its producers' gather, keeps the even split.
+constexpr int LAUNCH_REGS = 65536 / NTHREADS / 8 * 8;   // 168
+constexpr int PRODUCER_REGS = 56, CONSUMER_REGS = 224;
+static_assert(NP * PRODUCER_REGS + NW * CONSUMER_REGS <= (NP + NW) * LAUNCH_REGS, "register split");
+static_assert(NP == 4 && NW == 8, "the split works on whole warpgroups");
 static_assert(TPW == 8 && MT >= 1 && TPP <= 32, "tile shape");
 static_assert(PART_BYTES >= (GROUP * D + 2 * GROUP) * 4, "partial slot size");
 static_assert(PART_BYTES % 16 == 0, "bulk copies move 16-byte multiples");
@@ -279,8 +288,14 @@ __device__ __forceinline__ unsigned long long globaltimer() {
 
 // Wait for the phase with `parity` of an mbarrier, for at most WAIT_NS. On
 // timeout, record QSA_DEVERR_TIMEOUT, raise the CTA abort flag and return false.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* err,
-                                       volatile int* abort_flag) {
+// Inline (a call would make the caller save its live registers around it in the
+// hot loop); the error path alone is out of line.
+__device__ __noinline__ void wait_timed_out(int* err, volatile int* abort_flag) {
+    atomicOr(err, QSA_DEVERR_TIMEOUT);
+    *abort_flag = 1;
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* err,
+                                          volatile int* abort_flag) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();
     for (uint32_t it = 1;; ++it) {
@@ -288,8 +303,7 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* err,
         if ((it & 63) == 0) {
             if (*abort_flag) return false;
             if (globaltimer() - t0 > (unsigned long long)WAIT_NS) {
-                atomicOr(err, QSA_DEVERR_TIMEOUT);
-                *abort_flag = 1;
+                wait_timed_out(err, abort_flag);
                 return false;
             }
         }
@@ -317,6 +331,13 @@ __device__ __forceinline__ void griddep_wait() {
 }
 __device__ __forceinline__ void griddep_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void regs_producer() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(PRODUCER_REGS));
+}
+__device__ __forceinline__ void regs_consumer() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(CONSUMER_REGS));
 }
 
 __device__ __forceinline__ int ld_relaxed(const int* ptr) {
@@ -871,6 +892,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
     if (warp >= NW) {
         // ============================================================ producers
         // Producer warp pw gathers tokens [pw*TPP, (pw+1)*TPP) of every stage.
+        if constexpr (Tr::RQ || Tr::DEQ) regs_producer(); // consumer-bound pools only
         const int pw = warp - NW;
         const int mytok = pw * TPP + lane;
         Cursor pc, ic;
@@ -1009,6 +1031,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
     }
 
     // ================================================================ consumers
+    if constexpr (Tr::RQ || Tr::DEQ) regs_consumer();
     const int r = lane >> 2, c = lane & 3;
     float kscale_g = 1.0f, out_scale = 1.0f;
     if constexpr (FMT == QSA_KV_FP8_E4M3) {
@@ -1234,7 +1257,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
             // 8-bit codes, half of chunk ks / 2 for 4-bit codes)
             const uint32_t krow = smem_u32(Ks) + (tok_base + (lane & 7)) * Tr::ROWB;
             constexpr int G = Tr::GROUPS ? Tr::GROUPS : 1, KPG = 16 / G; // k16 steps per group
-            float acc[2][4] = {};
+            float acc[4][4] = {};
             uint32_t w[4], nb[4];
 #pragma unroll
             for (int ks = 0; ks < 16; ++ks) {
@@ -1252,15 +1275,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
                     else
                         i8x4_to_f16(w[ks & 3], b0, b1);
                 }
-                mma_f16(acc[ks & 1], qa[ks], b0, b1);
+                mma_f16(acc[ks & 3], qa[ks], b0, b1);
                 if constexpr (Tr::GROUPS) {
                     if ((ks + 1) % KPG == 0) { // a group's end: fold with the token's group scale
                         const int gi = ks / KPG;
                         float t4[4];
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            t4[e] = acc[0][e] + acc[1][e];
-                            acc[0][e] = acc[1][e] = 0.f;
+                            t4[e] = (acc[0][e] + acc[1][e]) + (acc[2][e] + acc[3][e]);
+                            acc[0][e] = acc[1][e] = acc[2][e] = acc[3][e] = 0.f;
                         }
                         const uint32_t w0 = ksw[0][gi >> 1], w1 = ksw[1][gi >> 1];
                         const float s0 = __half2float(__ushort_as_half(static_cast<unsigned short>(gi & 1 ? w0 >> 16 : w0)));
@@ -1274,7 +1297,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
             }
             if constexpr (!Tr::GROUPS) {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) sacc[0][e] = acc[0][e] + acc[1][e];
+                for (int e = 0; e < 4; ++e) sacc[0][e] = (acc[0][e] + acc[1][e]) + (acc[2][e] + acc[3][e]);
             }
         } else if constexpr (Tr::GROUPS == 0) {
             const uint32_t krow = smem_u32(Kb) + (tok_base + (lane & 7)) * BF_ROW;
