@@ -367,6 +367,32 @@ __device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
+// L2 eviction priorities. The pools with per-slot scales read each K/V row once
+// per call but each 32-byte scale sector twice (the sequence's two KV heads sit
+// side by side in it, read by different stages or CTAs): rows go first, scales
+// last, so the second read of a sector finds it in L2.
+__device__ __forceinline__ uint64_t l2_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ uint64_t l2_evict_last() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ void cp_async4_l2(uint32_t dst, const void* src, uint64_t pol) {
+    asm volatile("cp.async.ca.shared.global.L2::cache_hint [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "l"(pol)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async8_l2(uint32_t dst, const void* src, uint64_t pol) {
+    asm volatile("cp.async.ca.shared.global.L2::cache_hint [%0], [%1], 8, %2;" ::"r"(dst), "l"(src), "l"(pol)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async16_l2(uint32_t dst, const void* src, uint64_t pol) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "l"(pol)
+                 : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() {
     asm volatile("cp.async.commit_group;" ::: "memory");
 }
@@ -912,6 +938,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
         }
         constexpr int CPR = Tr::ROWB / 16; // 16-byte chunks per row
         constexpr int RPI = 32 / CPR;      // rows per warp-wide copy instruction
+        const uint64_t pol_row = l2_evict_first(), pol_sc = l2_evict_last();
         const int toff = lane / CPR, chunk = lane % CPR;
 #pragma unroll 1
         for (int i = 0; ic.t < t_end; ++i) {
@@ -966,8 +993,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
                             cp_async16(smem_u32(Ks + swz<Tr::ROWB>(t, chunk)), p.kring + rrow * 256 + chunk * 16);
                             cp_async16(smem_u32(Vs + swz<Tr::ROWB>(t, chunk)), p.vring + rrow * 256 + chunk * 16);
                         } else if (chunk < 8) { // 128-byte int4 pool row
-                            cp_async16(smem_u32(Ks + swz<Tr::ROWB>(t, chunk)), p.kpool + row * 128 + chunk * 16);
-                            cp_async16(smem_u32(Vs + swz<Tr::ROWB>(t, chunk)), p.vpool + row * 128 + chunk * 16);
+                            cp_async16_l2(smem_u32(Ks + swz<Tr::ROWB>(t, chunk)), p.kpool + row * 128 + chunk * 16,
+                                          pol_row);
+                            cp_async16_l2(smem_u32(Vs + swz<Tr::ROWB>(t, chunk)), p.vpool + row * 128 + chunk * 16,
+                                          pol_row);
                         }
                     } else {
                         *reinterpret_cast<uint4*>(Vs + swz<Tr::ROWB>(t, chunk)) = make_uint4(0, 0, 0, 0);
@@ -975,10 +1004,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
                     continue;
                 }
                 if (t < n) {
-                    cp_async16(smem_u32(Ks + swz<Tr::ROWB>(t, chunk)),
-                               p.kpool + row * Tr::ROWB + chunk * 16);
-                    cp_async16(smem_u32(Vs + swz<Tr::ROWB>(t, chunk)),
-                               p.vpool + row * Tr::ROWB + chunk * 16);
+                    if constexpr (Tr::SCALES) {
+                        cp_async16_l2(smem_u32(Ks + swz<Tr::ROWB>(t, chunk)),
+                                      p.kpool + row * Tr::ROWB + chunk * 16, pol_row);
+                        cp_async16_l2(smem_u32(Vs + swz<Tr::ROWB>(t, chunk)),
+                                      p.vpool + row * Tr::ROWB + chunk * 16, pol_row);
+                    } else {
+                        cp_async16(smem_u32(Ks + swz<Tr::ROWB>(t, chunk)),
+                                   p.kpool + row * Tr::ROWB + chunk * 16);
+                        cp_async16(smem_u32(Vs + swz<Tr::ROWB>(t, chunk)),
+                                   p.vpool + row * Tr::ROWB + chunk * 16);
+                    }
                 } else {
                     // rows past the live length hold zeros (P is 0 there, V must be finite)
                     *reinterpret_cast<uint4*>(Vs + swz<Tr::ROWB>(t, chunk)) = make_uint4(0, 0, 0, 0);
@@ -999,14 +1035,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
                     cp_async8(vs, static_cast<const uint8_t*>(p.vring_scale) + myring * 8);
                 } else if (valid) {
                     if constexpr (Ly::SC_TOK == 4) {
-                        cp_async4(ks, kg);
-                        cp_async4(vs, vg);
+                        cp_async4_l2(ks, kg, pol_sc);
+                        cp_async4_l2(vs, vg, pol_sc);
                     } else if constexpr (Ly::SC_TOK == 8) {
-                        cp_async8(ks, kg);
-                        cp_async8(vs, vg);
+                        cp_async8_l2(ks, kg, pol_sc);
+                        cp_async8_l2(vs, vg, pol_sc);
                     } else {
-                        cp_async16(ks, kg);
-                        cp_async16(vs, vg);
+                        cp_async16_l2(ks, kg, pol_sc);
+                        cp_async16_l2(vs, vg, pol_sc);
                     }
                 } else if (Tr::GROUPS && lane < TPP) {
                     // past the live length: zero V scales keep 0 * scale finite in P
@@ -1048,7 +1084,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
 
     uint32_t qa[16][4];
     float qmul_a = 1.f, qmul_b = 1.f; // undo the per-head Q scaling of f16 QK
-    float o[MT][3][4];
+    // PV n-tiles: f16 P without per-slot V scales (fp8: P <= 2^TAU, 11 significand
+    // bits) is used as is, heads 0-7 and 8-11 (+4 zero rows); otherwise P (or
+    // P * s_v) is split into hi + lo columns of the PV type, 24 rows in 3 tiles
+    constexpr bool P_HI = Tr::PV_F16 && !Tr::SCALES;
+    constexpr int NJ = P_HI ? 2 : 3;
+    float o[MT][NJ][4];
     float l0 = 0.f, l1 = 0.f;
     int v = 0, buf = 0, seg_j0 = 0;
     // Merge bookkeeping, kept in shared memory rather than in registers carried
@@ -1074,6 +1115,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
     // PV A-fragment chunk pattern: chunk 4*warp + 2*mt + ((lane >> 3) & 1)
     const int vx = ((((lane >> 3) & 1)) ^ xs) << 4;
 
+    if constexpr (P_HI) { // the padding rows 12-15 of both P^T buffers, read as zeros
+        for (int k = tid; k < 2 * 4 * PRS / 4; k += NCT) {
+            const int bsel = k / (4 * PRS / 4), w = k - bsel * (4 * PRS / 4);
+            reinterpret_cast<int*>(smem + Ly::off_p + bsel * 24 * PRS + 12 * PRS)[w] = 0;
+        }
+    }
     Cursor cc;
     cursor_init(cc, t_begin, t_end, segL, segP, p.bs, Hkv);
 #pragma unroll 1
@@ -1136,7 +1183,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-                for (int j = 0; j < 3; ++j)
+                for (int j = 0; j < NJ; ++j)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) o[mt][j][e] = 0.f;
             l0 = l1 = 0.f;
@@ -1414,6 +1461,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
                 if (row8) *reinterpret_cast<float2*>(Pf + (8 + r) * T + tk0) = make_float2(pv[2], pv[3]);
                 return;
             }
+            if constexpr (P_HI) { // P^T rows: heads 0-11; rows 12-15 stay zero
+                *reinterpret_cast<uint32_t*>(Pb + r * PRS + tk0 * 2) = pack_f16x2(pv[0], pv[1]);
+                if (row8) *reinterpret_cast<uint32_t*>(Pb + (8 + r) * PRS + tk0 * 2) = pack_f16x2(pv[2], pv[3]);
+                return;
+            }
             uint32_t hi_a, lo_a;
             split_pair<Tr::PV_F16>(pv[0], pv[1], hi_a, lo_a);
             *reinterpret_cast<uint32_t*>(Pb + r * PRS + tk0 * 2) = hi_a;
@@ -1490,16 +1542,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
+                for (int j = 0; j < NJ - 1; ++j) {
                     o[mt][j][0] *= a0;
                     o[mt][j][1] *= a1;
                     o[mt][j][2] *= a0;
                     o[mt][j][3] *= a1;
                 }
-                o[mt][2][0] *= a2;
-                o[mt][2][1] *= a3;
-                o[mt][2][2] *= a2;
-                o[mt][2][3] *= a3;
+                o[mt][NJ - 1][0] *= a2;
+                o[mt][NJ - 1][1] *= a3;
+                o[mt][NJ - 1][2] *= a2;
+                o[mt][NJ - 1][3] *= a3;
             }
             if (warp == 0 && lane < GROUP) mref[(v ^ 1) * 16 + lane] = new_ref(lane);
             if (VSH && warp == 1 && lane < GROUP) eref[(v ^ 1) * 16 + lane] = new_e(lane);
@@ -1555,12 +1607,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
             const uint32_t vrow = smem_u32(Vb) + ((lane >> 4) * 8 + (lane & 7)) * BF_ROW;
 #pragma unroll
             for (int kk = 0; kk < KK; ++kk) {
-                uint32_t pb[3][2];
+                uint32_t pb[NJ][2];
                 ldsm_x4(pb[0][0], pb[0][1], pb[1][0], pb[1][1],
                         pbase + ((lane >> 4) * 8 + (lane & 7)) * PRS +
                             (kk * 16 + ((lane >> 3) & 1) * 8) * 2);
-                ldsm_x2(pb[2][0], pb[2][1],
-                        pbase + (16 + (lane & 7)) * PRS + (kk * 16 + ((lane >> 3) & 1) * 8) * 2);
+                if constexpr (NJ == 3)
+                    ldsm_x2(pb[NJ - 1][0], pb[NJ - 1][1],
+                            pbase + (16 + (lane & 7)) * PRS + (kk * 16 + ((lane >> 3) & 1) * 8) * 2);
                 if constexpr (Tr::RQ) {
                     // V^T fragments straight from the raw stage (ldmatrix.trans of the
                     // codes, converted in registers); the warp's 32 dims are spread
@@ -1597,7 +1650,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
 #pragma unroll
                     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-                        for (int j = 0; j < 3; ++j) mma16816<Tr::PV_F16>(o[mt][j], a[mt], pb[j][0], pb[j][1]);
+                        for (int j = 0; j < NJ; ++j) mma16816<Tr::PV_F16>(o[mt][j], a[mt], pb[j][0], pb[j][1]);
                 } else {
 #pragma unroll
                     for (int mt = 0; mt < MT; ++mt) {
@@ -1605,7 +1658,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
                         ldsm_x4_t(a[0], a[1], a[2], a[3],
                                   vrow + kk * 16 * BF_ROW + (((4 * warp + 2 * mt) << 4) ^ vx));
 #pragma unroll
-                        for (int j = 0; j < 3; ++j) mma16816<Tr::PV_F16>(o[mt][j], a, pb[j][0], pb[j][1]);
+                        for (int j = 0; j < NJ; ++j) mma16816<Tr::PV_F16>(o[mt][j], a, pb[j][0], pb[j][1]);
                     }
                 }
             }
@@ -1686,8 +1739,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
             for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    val[mt][e] = o[mt][0][e] + o[mt][1][e];
-                    val[mt][4 + e] = o[mt][2][e] + __shfl_xor_sync(0xFFFFFFFFu, o[mt][2][e], 2);
+                    if constexpr (NJ == 3) { // hi + lo columns
+                        val[mt][e] = o[mt][0][e] + o[mt][1][e];
+                        val[mt][4 + e] = o[mt][2][e] + __shfl_xor_sync(0xFFFFFFFFu, o[mt][2][e], 2);
+                    } else {
+                        val[mt][e] = o[mt][0][e];
+                        val[mt][4 + e] = o[mt][1][e];
+                    }
                 }
             }
             if (head_split && misc[4] != 0) {
@@ -1817,6 +1875,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
     // all consumer threads precede thread 0's acq_rel ticket through the
     // barrier (release), and the merger's reads follow its ticket (acquire).
     if (pend0 >= 0 || pend1 >= 0) {
+        consumer_sync(); // every consumer thread's partial stores precede the release below
         if (tid == 0) {
             int last[2] = {0, 0};
             // pend0's ticket was taken when its partial was stored; pend1's is now
