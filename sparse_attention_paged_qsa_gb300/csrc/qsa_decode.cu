@@ -95,7 +95,7 @@ constexpr int MIN_TOKENS_PER_CTA = 64;
 constexpr unsigned FEW_SEGMENTS = 4;        // up to this many (sequence, KV head) segments ...
 constexpr unsigned MAX_FANIN = 16;          // ... each gets a whole number (<= this) of CTAs
 constexpr int PART_BYTES = 12416;           // fp32 O[12][256] + m[12] + l[12], 128-byte multiple
-constexpr int MERGE_BATCH = 6;             // partials per bulk-copy batch of the split merge
+constexpr int MERGE_BATCH = 6;             // partials per bulk-copy batch of the split merge (at most)
 constexpr long long WAIT_NS = 2000000000LL; // bounded-wait limit (2 s)
 constexpr int BAR_CONSUMERS = 1;            // named barrier id (2..5: consumer warp pairs)
 // Register split between the warp roles (setmaxnreg) of the pools whose consumer
@@ -111,8 +111,7 @@ static_assert(TPW == 8 && MT >= 1 && TPP <= 32, "tile shape");
 static_assert(PART_BYTES >= (GROUP * D + 2 * GROUP) * 4, "partial slot size");
 static_assert(PART_BYTES % 16 == 0, "bulk copies move 16-byte multiples");
 
-// ROWB: pool row bytes; STAGES: ring depth; DEQ: rows are converted in shared
-// memory by the consuming warp (tiered pools); RQ: codes are converted in
+// ROWB: pool row bytes; STAGES: ring depth; RQ: codes are converted in
 // registers from the raw stage (K as MMA B fragments, V as PV A fragments), no
 // converted tiles; QK_F16: QK runs on f16 operands (exact integer / e4m3 codes,
 // Q rescaled per head by a power of two); PV_F16: PV runs on f16
@@ -120,42 +119,44 @@ static_assert(PART_BYTES % 16 == 0, "bulk copies move 16-byte multiples");
 // range), else bf16; SCALES: per-slot scales (fp32 per (slot, KV head), or
 // binary16 per (slot, KV head, channel group) when GROUPS > 0); NIB4: 4-bit
 // codes, NIB_OFFSET: stored as code + 8 (else two's complement); TIER: each row
-// is an int8_g64 ring row or an int4_g32 pool row, by the owner table (scales
-// held at the 32-channel granularity, a ring row's 64-channel scales expanded).
+// is an int8_g64 ring row or an int4_g32 pool row, by the owner table; the
+// consuming warps widen the int4 rows to int8 codes in shared memory, so the
+// stage reads as int8 rows with 32-channel scales (a ring row's 64-channel scales
+// serve both of their 32-channel halves).
 template <int FMT> struct Traits;
 template <> struct Traits<QSA_KV_BF16> {
     static constexpr int ROWB = 512, STAGES = 3, GROUPS = 0;
-    static constexpr bool DEQ = false, RQ = false, SCALES = false, QK_F16 = false;
+    static constexpr bool RQ = false, SCALES = false, QK_F16 = false;
     static constexpr bool PV_F16 = false, NIB4 = false, NIB_OFFSET = false, TIER = false;
 };
 template <> struct Traits<QSA_KV_FP8_E4M3> {
     static constexpr int ROWB = 256, STAGES = 6, GROUPS = 0;
-    static constexpr bool DEQ = false, RQ = true, SCALES = false, QK_F16 = true;
+    static constexpr bool RQ = true, SCALES = false, QK_F16 = true;
     static constexpr bool PV_F16 = true, NIB4 = false, NIB_OFFSET = false, TIER = false;
 };
 template <> struct Traits<QSA_KV_INT8> {
     static constexpr int ROWB = 256, STAGES = 6, GROUPS = 0;
-    static constexpr bool DEQ = false, RQ = true, SCALES = true, QK_F16 = true;
+    static constexpr bool RQ = true, SCALES = true, QK_F16 = true;
     static constexpr bool PV_F16 = true, NIB4 = false, NIB_OFFSET = false, TIER = false;
 };
 template <> struct Traits<QSA_KV_INT4> {
     static constexpr int ROWB = 128, STAGES = 11, GROUPS = 0;
-    static constexpr bool DEQ = false, RQ = true, SCALES = true, QK_F16 = true;
+    static constexpr bool RQ = true, SCALES = true, QK_F16 = true;
     static constexpr bool PV_F16 = false, NIB4 = true, NIB_OFFSET = false, TIER = false;
 };
 template <> struct Traits<QSA_KV_INT8_G64> {
     static constexpr int ROWB = 256, STAGES = 5, GROUPS = 4;
-    static constexpr bool DEQ = false, RQ = true, SCALES = true, QK_F16 = true;
+    static constexpr bool RQ = true, SCALES = true, QK_F16 = true;
     static constexpr bool PV_F16 = false, NIB4 = false, NIB_OFFSET = false, TIER = false;
 };
 template <> struct Traits<QSA_KV_INT4_G32> {
     static constexpr int ROWB = 128, STAGES = 9, GROUPS = 8;
-    static constexpr bool DEQ = false, RQ = true, SCALES = true, QK_F16 = true;
+    static constexpr bool RQ = true, SCALES = true, QK_F16 = true;
     static constexpr bool PV_F16 = false, NIB4 = true, NIB_OFFSET = true, TIER = false;
 };
 template <> struct Traits<QSA_KV_INT8RING_INT4> {
-    static constexpr int ROWB = 256, STAGES = 3, GROUPS = 8;
-    static constexpr bool DEQ = true, RQ = false, SCALES = true, QK_F16 = true;
+    static constexpr int ROWB = 256, STAGES = 4, GROUPS = 8;
+    static constexpr bool RQ = true, SCALES = true, QK_F16 = true;
     static constexpr bool PV_F16 = false, NIB4 = false, NIB_OFFSET = true, TIER = true;
 };
 
@@ -169,9 +170,11 @@ template <int FMT> struct Layout {
     static constexpr int PF = Tr::STAGES;       // slot-id prefetch distance (stages)
     static constexpr int R = PF + 1;            // slot-id ring entries
     static constexpr int off_stage = 0;
-    static constexpr int off_kbf = off_stage + Tr::STAGES * STAGE_BYTES;
-    static constexpr int kbf_bytes = Tr::DEQ ? 2 * T * BF_ROW : 0;
-    static constexpr int off_q = off_kbf + kbf_bytes;
+    // tiered pools: the int4 rows' V codes widened to int8 [T][256] (swizzled);
+    // consumer warp w owns 16-byte chunks 2w, 2w + 1 of every row
+    static constexpr int off_vexp = off_stage + Tr::STAGES * STAGE_BYTES;
+    static constexpr int vexp_bytes = Tr::TIER ? T * 256 : 0;
+    static constexpr int off_q = off_vexp + vexp_bytes;
     static constexpr int off_p = off_q + 2 * 16 * Q_RS;
     // P^T hi/lo (two buffers); grouped pools: FP32 P [2][12][T] then one P^T per warp
     static constexpr int off_pw = off_p + 2 * GROUP * T * 4;
@@ -185,7 +188,9 @@ template <int FMT> struct Layout {
     static constexpr int off_nred = off_lred + NW * 16 * 4;
     static constexpr int off_eref = off_nred + (NUM_REF ? NW * 16 * 4 : 0);
     static constexpr int off_ring = off_eref + (NUM_REF ? 2 * 16 * 4 : 0);
-    static constexpr int off_segL = off_ring + R * T * 4;
+    // tiered pools: per producer warp, its tokens listed by tier (16 hot, 16 cold)
+    static constexpr int off_tlist = off_ring + R * T * 4;
+    static constexpr int off_segL = off_tlist + (Tr::TIER ? NP * 32 * 4 : 0);
     static constexpr int off_segSrc = off_segL + (MAX_BS + 4) * 4;
     static constexpr int off_segP = off_segSrc + (MAX_BS + 4) * 4;
     static constexpr int off_misc = off_segP + (MAX_BS + 4) * 4;
@@ -193,13 +198,15 @@ template <int FMT> struct Layout {
     static constexpr int n_bars = 2 * Tr::STAGES + 6; // stages full/empty, Q full/empty, merge
     static constexpr int TOTAL = off_bar + n_bars * 8;
     static_assert(TOTAL <= 227 * 1024, "shared memory budget");
-    // the split merge stages two batches of partials over the (then idle) stage
-    // ring and dequantised tiles, below the Q tiles
-    static_assert(2 * MERGE_BATCH * PART_BYTES <= off_q, "merge buffers");
-    // then this CTA's own partial of a directly merged segment head
-    static constexpr int off_stash = 2 * MERGE_BATCH * PART_BYTES;
+    // the split merge stages two batches of up to MB partials over the (then
+    // idle) stage ring, below the Q tiles, then this CTA's own partial of a
+    // directly merged segment head
+    static constexpr int MB = (off_q / PART_BYTES - 1) / 2 < MERGE_BATCH ? (off_q / PART_BYTES - 1) / 2
+                                                                          : MERGE_BATCH;
+    static_assert(MB >= 2, "merge buffers");
+    static constexpr int off_stash = 2 * MB * PART_BYTES;
     static_assert(off_stash + PART_BYTES <= off_q, "direct-merge stash");
-    static_assert(STAGE_BYTES % 128 == 0 && off_kbf % 128 == 0 && off_q % 16 == 0, "alignment");
+    static_assert(STAGE_BYTES % 128 == 0 && off_vexp % 128 == 0 && off_q % 16 == 0, "alignment");
     static_assert(off_p % 16 == 0 && off_pw % 16 == 0 && off_red % 16 == 0 && off_bar % 8 == 0,
                   "alignment");
 };
@@ -540,15 +547,6 @@ __device__ __forceinline__ void i8x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& 
     hi = sub_f16x2(__byte_perm(x, 0x64646464u, 0x4342), 0x64806480u);
 }
 
-// 4 int8 codes -> 2 bf16x2. bf16 has 7 stored mantissa bits, so the sign bit
-// is handled apart: 0x43 0b0mmmmmmm is 128 + (code & 127) and 0x43 0bs0000000
-// is 128 or 256 by the sign bit; their difference is the two's-complement code.
-__device__ __forceinline__ void i8x4_to_bf16(uint32_t w, uint32_t& lo, uint32_t& hi) {
-    const uint32_t t0 = __byte_perm(w, 0u, 0x4140), t1 = __byte_perm(w, 0u, 0x4342);
-    lo = sub_bf16x2((t0 & 0x007F007Fu) | 0x43004300u, (t0 & 0x00800080u) | 0x43004300u);
-    hi = sub_bf16x2((t1 & 0x007F007Fu) | 0x43004300u, (t1 & 0x00800080u) | 0x43004300u);
-}
-
 // 8 int4 codes (channel 2i in the low nibble) -> 4 packed pairs, f16 or bf16:
 // nibble u = code + 8 (offset-binary storage as it is; two's complement
 // code ^ 8) under the magic 1024 (f16) or 128 (bf16).
@@ -607,34 +605,25 @@ __device__ __forceinline__ uint32_t pair4(uint32_t w, int j) {
     return F16 ? sub_f16x2(v, BIAS) : sub_bf16x2(v, BIAS);
 }
 
-// 16 raw bytes of an 8-bit row -> 16 values as two 16-byte chunks (f16 or bf16).
-template <int FMT, bool F16>
-__device__ __forceinline__ void convert16(const uint4 raw, uint4& o0, uint4& o1) {
+// 16 bytes of an int4 row (32 codes; byte k holds code 2k in its low nibble and
+// 2k + 1 in its high one) -> the same 32 codes as int8 values 16 * code (two
+// 16-byte chunks): a two's-complement nibble in the high half of a byte reads as
+// 16 times its value, so no per-byte carry or sign extension is needed; the
+// caller folds the factor 1/16 into the token's scales. Nibbles stored as code +
+// 8 (OFFSET) become two's complement by flipping bit 3.
+template <bool OFFSET>
+__device__ __forceinline__ void widen16_i4x32(const uint4 raw, uint4& o0, uint4& o1) {
     const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
     uint32_t r[8];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        if constexpr (FMT == QSA_KV_FP8_E4M3)
-            e4m3x4_to_f16(w[k], r[2 * k], r[2 * k + 1]);
-        else if constexpr (F16)
-            i8x4_to_f16(w[k], r[2 * k], r[2 * k + 1]);
-        else
-            i8x4_to_bf16(w[k], r[2 * k], r[2 * k + 1]);
+        const uint32_t v = OFFSET ? w[k] ^ 0x88888888u : w[k];
+        const uint32_t hi = v & 0xF0F0F0F0u, lo = (v << 4) & 0xF0F0F0F0u; // codes 2j+1 / 2j of byte j
+        r[2 * k] = __byte_perm(lo, hi, 0x5140);     // codes 8k .. 8k+3
+        r[2 * k + 1] = __byte_perm(lo, hi, 0x7362); // codes 8k+4 .. 8k+7
     }
     o0 = make_uint4(r[0], r[1], r[2], r[3]);
     o1 = make_uint4(r[4], r[5], r[6], r[7]);
-}
-
-// 16 raw bytes of a 4-bit row (32 codes) -> four 16-byte chunks.
-template <bool F16, bool OFFSET>
-__device__ __forceinline__ void convert32_int4(const uint4 raw, uint4* o) {
-    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        uint32_t r[4];
-        i4x8_to<F16, OFFSET>(w[k], r);
-        o[k] = make_uint4(r[0], r[1], r[2], r[3]);
-    }
 }
 
 // Q fragments of the register-dequant pools (f16, k16 steps), built from the bf16
@@ -918,7 +907,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
     if (warp >= NW) {
         // ============================================================ producers
         // Producer warp pw gathers tokens [pw*TPP, (pw+1)*TPP) of every stage.
-        if constexpr (Tr::RQ || Tr::DEQ) regs_producer(); // consumer-bound pools only
+        if constexpr (Tr::RQ) regs_producer(); // consumer-bound pools only
         const int pw = warp - NW;
         const int mytok = pw * TPP + lane;
         Cursor pc, ic;
@@ -980,44 +969,73 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
                     myring = (long long)pos * Hkv + g;
                 }
             }
+            if constexpr (Tr::TIER) {
+                // Rows of two sizes: list the warp's tokens by tier (ballot ranks), then
+                // copy 256-byte ring rows two per instruction (16 lanes each) and
+                // 128-byte pool rows four per instruction (8 lanes each), so no
+                // instruction mixes the two and no lane idles inside a pass.
+                int* const tlist = reinterpret_cast<int*>(smem + Ly::off_tlist) + pw * 32;
+                const unsigned hm = __ballot_sync(0xFFFFFFFFu, valid && myhot);
+                const unsigned cm = __ballot_sync(0xFFFFFFFFu, valid && !myhot);
+                const unsigned zm = __ballot_sync(0xFFFFFFFFu, lane < TPP && !valid);
+                const unsigned below = (1u << lane) - 1u;
+                __syncwarp(); // the previous stage's reads of the lists are done
+                if (valid) tlist[myhot ? __popc(hm & below) : 16 + __popc(cm & below)] = lane;
+                __syncwarp();
+                const int nh = __popc(hm), nc = __popc(cm);
+#pragma unroll 1
+                for (int r0 = 0; r0 < nh; r0 += 2) {
+                    const int rr = r0 + (lane >> 4), ch = lane & 15;
+                    const int src = tlist[rr < nh ? rr : nh - 1];
+                    const long long rrow = __shfl_sync(0xFFFFFFFFu, myring, src);
+                    if (rr < nh) {
+                        const int t = pw * TPP + src;
+                        cp_async16(smem_u32(Ks + swz<Tr::ROWB>(t, ch)), p.kring + rrow * 256 + ch * 16);
+                        cp_async16(smem_u32(Vs + swz<Tr::ROWB>(t, ch)), p.vring + rrow * 256 + ch * 16);
+                    }
+                }
+#pragma unroll 1
+                for (int r0 = 0; r0 < nc; r0 += 4) {
+                    const int rr = r0 + (lane >> 3), ch = lane & 7;
+                    const int src = tlist[16 + (rr < nc ? rr : nc - 1)];
+                    const long long row = __shfl_sync(0xFFFFFFFFu, myrow, src);
+                    if (rr < nc) {
+                        const int t = pw * TPP + src;
+                        cp_async16_l2(smem_u32(Ks + swz<Tr::ROWB>(t, ch)), p.kpool + row * 128 + ch * 16, pol_row);
+                        cp_async16_l2(smem_u32(Vs + swz<Tr::ROWB>(t, ch)), p.vpool + row * 128 + ch * 16, pol_row);
+                    }
+                }
+                if (zm) { // rows past the live length hold zeros (P is 0 there, V must be finite)
+#pragma unroll 1
+                    for (int t0 = 0; t0 < TPP; t0 += 2) {
+                        const int tl = t0 + (lane >> 4);
+                        if ((zm >> tl) & 1u)
+                            *reinterpret_cast<uint4*>(Vs + swz<Tr::ROWB>(pw * TPP + tl, lane & 15)) =
+                                make_uint4(0, 0, 0, 0);
+                    }
+                }
+            } else {
 #pragma unroll
-            for (int t0 = 0; t0 < TPP; t0 += RPI) {
-                const int tl = t0 + toff;
-                const long long row = __shfl_sync(0xFFFFFFFFu, myrow, tl);
-                const int t = pw * TPP + tl;
-                if constexpr (Tr::TIER) {
-                    const long long rrow = __shfl_sync(0xFFFFFFFFu, myring, tl);
-                    const bool hot = __shfl_sync(0xFFFFFFFFu, myhot, tl);
+                for (int t0 = 0; t0 < TPP; t0 += RPI) {
+                    const int tl = t0 + toff;
+                    const long long row = __shfl_sync(0xFFFFFFFFu, myrow, tl);
+                    const int t = pw * TPP + tl;
                     if (t < n) {
-                        if (hot) { // 256-byte int8 ring row
-                            cp_async16(smem_u32(Ks + swz<Tr::ROWB>(t, chunk)), p.kring + rrow * 256 + chunk * 16);
-                            cp_async16(smem_u32(Vs + swz<Tr::ROWB>(t, chunk)), p.vring + rrow * 256 + chunk * 16);
-                        } else if (chunk < 8) { // 128-byte int4 pool row
-                            cp_async16_l2(smem_u32(Ks + swz<Tr::ROWB>(t, chunk)), p.kpool + row * 128 + chunk * 16,
-                                          pol_row);
-                            cp_async16_l2(smem_u32(Vs + swz<Tr::ROWB>(t, chunk)), p.vpool + row * 128 + chunk * 16,
-                                          pol_row);
+                        if constexpr (Tr::SCALES) {
+                            cp_async16_l2(smem_u32(Ks + swz<Tr::ROWB>(t, chunk)),
+                                          p.kpool + row * Tr::ROWB + chunk * 16, pol_row);
+                            cp_async16_l2(smem_u32(Vs + swz<Tr::ROWB>(t, chunk)),
+                                          p.vpool + row * Tr::ROWB + chunk * 16, pol_row);
+                        } else {
+                            cp_async16(smem_u32(Ks + swz<Tr::ROWB>(t, chunk)),
+                                       p.kpool + row * Tr::ROWB + chunk * 16);
+                            cp_async16(smem_u32(Vs + swz<Tr::ROWB>(t, chunk)),
+                                       p.vpool + row * Tr::ROWB + chunk * 16);
                         }
                     } else {
+                        // rows past the live length hold zeros (P is 0 there, V must be finite)
                         *reinterpret_cast<uint4*>(Vs + swz<Tr::ROWB>(t, chunk)) = make_uint4(0, 0, 0, 0);
                     }
-                    continue;
-                }
-                if (t < n) {
-                    if constexpr (Tr::SCALES) {
-                        cp_async16_l2(smem_u32(Ks + swz<Tr::ROWB>(t, chunk)),
-                                      p.kpool + row * Tr::ROWB + chunk * 16, pol_row);
-                        cp_async16_l2(smem_u32(Vs + swz<Tr::ROWB>(t, chunk)),
-                                      p.vpool + row * Tr::ROWB + chunk * 16, pol_row);
-                    } else {
-                        cp_async16(smem_u32(Ks + swz<Tr::ROWB>(t, chunk)),
-                                   p.kpool + row * Tr::ROWB + chunk * 16);
-                        cp_async16(smem_u32(Vs + swz<Tr::ROWB>(t, chunk)),
-                                   p.vpool + row * Tr::ROWB + chunk * 16);
-                    }
-                } else {
-                    // rows past the live length hold zeros (P is 0 there, V must be finite)
-                    *reinterpret_cast<uint4*>(Vs + swz<Tr::ROWB>(t, chunk)) = make_uint4(0, 0, 0, 0);
                 }
             }
             if constexpr (Tr::SCALES) {
@@ -1067,7 +1085,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
     }
 
     // ================================================================ consumers
-    if constexpr (Tr::RQ || Tr::DEQ) regs_consumer();
+    if constexpr (Tr::RQ) regs_consumer();
     const int r = lane >> 2, c = lane & 3;
     float kscale_g = 1.0f, out_scale = 1.0f;
     if constexpr (FMT == QSA_KV_FP8_E4M3) {
@@ -1192,8 +1210,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
         if (!mbar_wait(full_bar(s), (i / Tr::STAGES) & 1, p.err, abort_flag)) break;
         uint8_t* const Ks = stage0 + s * Ly::STAGE_BYTES;
         uint8_t* const Vs = Ks + Ly::STAGE_KV;
-        const uint8_t* Kb = Ks;   // bf16 rows [T][BF_ROW] (swizzled) used by the MMAs
-        const uint8_t* Vb = Vs;
         float skr[2] = {1.f, 1.f}, svr[2] = {1.f, 1.f};
         // grouped pools: K scales (binary16 pairs) of tokens tk0, tk0 + 1, and V
         // scales of tokens 2 lane, 2 lane + 1 in this warp's channel group
@@ -1223,76 +1239,67 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
                 // a ring row holds 4 scales of 64 channels: 32-channel group k reads k / 2
                 const int* flag = reinterpret_cast<const int*>(Vs + Ly::STAGE_KV + Ly::STAGE_SC);
 #pragma unroll
-                for (int u = 0; u < 2; ++u)
+                for (int u = 0; u < 2; ++u) {
                     if (flag[tk0 + u]) {
                         const uint32_t e0 = ksw[u][0], e1 = ksw[u][1];
                         ksw[u][0] = __byte_perm(e0, 0, 0x1010);
                         ksw[u][1] = __byte_perm(e0, 0, 0x3232);
                         ksw[u][2] = __byte_perm(e1, 0, 0x1010);
                         ksw[u][3] = __byte_perm(e1, 0, 0x3232);
+                    } else {
+                        skr[u] = 0.0625f; // the int4 row's codes are widened as 16 * code
                     }
-                svw[0] = __half2float(sv[(2 * lane) * G + (flag[2 * lane] ? gv >> 1 : gv)]);
-                svw[1] = __half2float(sv[(2 * lane + 1) * G + (flag[2 * lane + 1] ? gv >> 1 : gv)]);
+                }
+                const bool h0 = flag[2 * lane] != 0, h1 = flag[2 * lane + 1] != 0;
+                svw[0] = __half2float(sv[(2 * lane) * G + (h0 ? gv >> 1 : gv)]) * (h0 ? 1.f : 0.0625f);
+                svw[1] = __half2float(sv[(2 * lane + 1) * G + (h1 ? gv >> 1 : gv)]) * (h1 ? 1.f : 0.0625f);
             } else {
                 svw[0] = __half2float(sv[(2 * lane) * G + gv]);
                 svw[1] = __half2float(sv[(2 * lane + 1) * G + gv]);
             }
         }
 
-        if constexpr (Tr::DEQ) { // tiered pools: each token converted by its tier, in shared memory
-            static_assert(Tr::TIER, "shared-memory conversion serves the tiered pools");
-            uint8_t* const kbf = smem + Ly::off_kbf;
-            uint8_t* const vbf = kbf + T * BF_ROW;
-            const int tt = lane & 7, ch = lane >> 3;
-            const int t = tok_base + tt;
-            {
-                const int* flag = reinterpret_cast<const int*>(Vs + Ly::STAGE_KV + Ly::STAGE_SC);
-                // K: this warp's 8 tokens, each by its tier
-                if (flag[t]) {
+        uint32_t hot_lo = 0, hot_hi = 0; // tiered pools: ring-row tokens of the stage (bit t)
+        if constexpr (Tr::TIER) {
+            // Widen the stage's int4 rows to int8 (16 * code): K in place, for this warp's
+            // own 8 tokens (only this warp reads them); V into this warp's chunks
+            // 2w, 2w + 1 of the side buffer, for every token (only this warp reads
+            // them). Everything read comes before everything written (__syncwarp).
+            const int* flag = reinterpret_cast<const int*>(Vs + Ly::STAGE_KV + Ly::STAGE_SC);
+            hot_lo = __ballot_sync(0xFFFFFFFFu, flag[lane] != 0);
+            hot_hi = __ballot_sync(0xFFFFFFFFu, flag[lane + 32] != 0);
+            const int tt = tok_base + (lane & 7), kc = lane >> 3; // K: token, chunks kc, kc + 4
+            const bool kcold = !(((tt < 32 ? hot_lo : hot_hi) >> (tt & 31)) & 1u);
+            uint4 kr[2], vr[2];
+            if (kcold) {
+                kr[0] = *reinterpret_cast<const uint4*>(Ks + swz<Tr::ROWB>(tt, kc));
+                kr[1] = *reinterpret_cast<const uint4*>(Ks + swz<Tr::ROWB>(tt, kc + 4));
+            }
+            const bool vcold0 = !((hot_lo >> lane) & 1u), vcold1 = !((hot_hi >> lane) & 1u);
+            if (vcold0) vr[0] = *reinterpret_cast<const uint4*>(Vs + swz<Tr::ROWB>(lane, warp));
+            if (vcold1) vr[1] = *reinterpret_cast<const uint4*>(Vs + swz<Tr::ROWB>(lane + 32, warp));
+            __syncwarp();
+            if (kcold) {
 #pragma unroll
-                    for (int it = 0; it < 4; ++it) {
-                        const int rc = ch + 4 * it;
-                        const uint4 raw = *reinterpret_cast<const uint4*>(Ks + swz<Tr::ROWB>(t, rc));
-                        uint4 o0, o1;
-                        convert16<QSA_KV_INT8, Tr::QK_F16>(raw, o0, o1);
-                        *reinterpret_cast<uint4*>(kbf + swz<BF_ROW>(t, 2 * rc)) = o0;
-                        *reinterpret_cast<uint4*>(kbf + swz<BF_ROW>(t, 2 * rc + 1)) = o1;
-                    }
-                } else {
-#pragma unroll
-                    for (int it = 0; it < 2; ++it) {
-                        const int rc = ch + 4 * it;
-                        const uint4 raw = *reinterpret_cast<const uint4*>(Ks + swz<Tr::ROWB>(t, rc));
-                        uint4 ov[4];
-                        convert32_int4<Tr::QK_F16, true>(raw, ov);
-#pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            *reinterpret_cast<uint4*>(kbf + swz<BF_ROW>(t, 4 * rc + k)) = ov[k];
-                    }
+                for (int u = 0; u < 2; ++u) {
+                    uint4 o0, o1;
+                    widen16_i4x32<Tr::NIB_OFFSET>(kr[u], o0, o1);
+                    *reinterpret_cast<uint4*>(Ks + swz<Tr::ROWB>(tt, 2 * (kc + 4 * u))) = o0;
+                    *reinterpret_cast<uint4*>(Ks + swz<Tr::ROWB>(tt, 2 * (kc + 4 * u) + 1)) = o1;
                 }
-                // V: this warp's 32 dims of every token: two int8 chunks or one int4 chunk
+            }
+            uint8_t* const vexp = smem + Ly::off_vexp;
 #pragma unroll
-                for (int it = 0; it < 2; ++it) {
-                    const int tv = lane + 32 * it;
-                    uint4 ov[4];
-                    if (flag[tv]) {
-                        convert16<QSA_KV_INT8, Tr::PV_F16>(
-                            *reinterpret_cast<const uint4*>(Vs + swz<Tr::ROWB>(tv, 2 * warp)), ov[0], ov[1]);
-                        convert16<QSA_KV_INT8, Tr::PV_F16>(
-                            *reinterpret_cast<const uint4*>(Vs + swz<Tr::ROWB>(tv, 2 * warp + 1)), ov[2], ov[3]);
-                    } else {
-                        convert32_int4<Tr::PV_F16, true>(
-                            *reinterpret_cast<const uint4*>(Vs + swz<Tr::ROWB>(tv, warp)), ov);
-                    }
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        *reinterpret_cast<uint4*>(vbf + swz<BF_ROW>(tv, 4 * warp + k)) = ov[k];
+            for (int u = 0; u < 2; ++u) {
+                if (u == 0 ? vcold0 : vcold1) {
+                    const int tv = lane + 32 * u;
+                    uint4 o0, o1;
+                    widen16_i4x32<Tr::NIB_OFFSET>(vr[u], o0, o1);
+                    *reinterpret_cast<uint4*>(vexp + swz<Tr::ROWB>(tv, 2 * warp)) = o0;
+                    *reinterpret_cast<uint4*>(vexp + swz<Tr::ROWB>(tv, 2 * warp + 1)) = o1;
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(empty_bar(s));
-            Kb = kbf;
-            Vb = vbf;
         }
 
         // ---------------------------------------------------------------- QK
@@ -1346,8 +1353,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) sacc[0][e] = (acc[0][e] + acc[1][e]) + (acc[2][e] + acc[3][e]);
             }
-        } else if constexpr (Tr::GROUPS == 0) {
-            const uint32_t krow = smem_u32(Kb) + (tok_base + (lane & 7)) * BF_ROW;
+        } else { // bf16 rows
+            const uint32_t krow = smem_u32(Ks) + (tok_base + (lane & 7)) * BF_ROW;
 #pragma unroll
             for (int ks = 0; ks < 16; ks += 2) {
                 uint32_t b0, b1, b2, b3;
@@ -1358,34 +1365,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
             }
 #pragma unroll
             for (int e = 0; e < 4; ++e) sacc[0][e] += sacc[1][e] + sacc[2][e] + sacc[3][e];
-        } else {
-            // score = sum over channel groups of (group dot product) * K scale of
-            // (token, group); each group is KPG k-steps of 16 channels
-            constexpr int G = Tr::GROUPS, KPG = 16 / G;
-            const uint32_t krow = smem_u32(Kb) + (tok_base + (lane & 7)) * BF_ROW;
-#pragma unroll
-            for (int gi = 0; gi < G; ++gi) {
-                float acc[KPG][4] = {};
-#pragma unroll
-                for (int kk = 0; kk < KPG; kk += 2) {
-                    const int ks = gi * KPG + kk;
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4(b0, b1, b2, b3, krow + ((ks * 32) ^ kx));
-                    mma16816<Tr::QK_F16>(acc[kk], qa[ks], b0, b1);
-                    mma16816<Tr::QK_F16>(acc[kk + 1], qa[ks + 1], b2, b3);
-                }
-#pragma unroll
-                for (int kk = 1; kk < KPG; ++kk)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) acc[0][e] += acc[kk][e];
-                const uint32_t w0 = ksw[0][gi >> 1], w1 = ksw[1][gi >> 1];
-                const float s0 = __half2float(__ushort_as_half(static_cast<unsigned short>(gi & 1 ? w0 >> 16 : w0)));
-                const float s1 = __half2float(__ushort_as_half(static_cast<unsigned short>(gi & 1 ? w1 >> 16 : w1)));
-                sacc[0][0] += acc[0][0] * s0;
-                sacc[0][1] += acc[0][1] * s1;
-                sacc[0][2] += acc[0][2] * s0;
-                sacc[0][3] += acc[0][3] * s1;
-            }
         }
         const bool v0 = tk0 < n, v1 = tk0 + 1 < n;
         const bool row8 = r < 4; // head r + 8 is a real head (8..11)
@@ -1604,7 +1583,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
         }
         {
             const uint32_t pbase = smem_u32(Pt);
-            const uint32_t vrow = smem_u32(Vb) + ((lane >> 4) * 8 + (lane & 7)) * BF_ROW;
+            const uint32_t vrow = smem_u32(Vs) + ((lane >> 4) * 8 + (lane & 7)) * BF_ROW;
 #pragma unroll
             for (int kk = 0; kk < KK; ++kk) {
                 uint32_t pb[NJ][2];
@@ -1638,9 +1617,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
                     } else { // chunks 2 warp, 2 warp + 1 (16 codes each) of tokens 0-7 / 8-15
                         const int mi = lane >> 3;
                         const int tv = kk * 16 + (mi >> 1) * 8 + (lane & 7);
+                        uint32_t vrow_base = vst;
+                        if constexpr (Tr::TIER) // int4 rows: their widened codes in the side buffer
+                            if (!((((tv < 32) ? hot_lo : hot_hi) >> (tv & 31)) & 1u))
+                                vrow_base = smem_u32(smem + Ly::off_vexp);
                         uint32_t r[4];
                         ldsm_x4_t(r[0], r[1], r[2], r[3],
-                                  vst + tv * Tr::ROWB + (((2 * warp + (mi & 1)) ^ xs) << 4));
+                                  vrow_base + tv * Tr::ROWB + (((2 * warp + (mi & 1)) ^ xs) << 4));
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
                             a[0][q] = pair8<FMT, Tr::PV_F16>(r[q], false);
@@ -1663,10 +1646,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
                 }
             }
         }
-        if constexpr (!Tr::DEQ) {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(empty_bar(s));
-        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_bar(s));
 
         // ------------------------------------------------------------ epilogue
         if (last) {
@@ -1916,15 +1897,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
                 fs1 = cta_begin(c_first, N, G) < Fs ? 1u : 0u;
             }
         }
-        const int nb0 = (nq0 + MERGE_BATCH - 1) / MERGE_BATCH;
-        const int nbatch = nb0 + (nq1 + MERGE_BATCH - 1) / MERGE_BATCH;
+        constexpr int MB = Ly::MB;
+        const int nb0 = (nq0 + MB - 1) / MB;
+        const int nbatch = nb0 + (nq1 + MB - 1) / MB;
         if (nbatch == 0) return;
         uint8_t* const mbuf = smem + Ly::off_stage;
         // batch k -> (segment q, first contributor, count)
         auto batch = [&](int k, int& q, int& k0, int& n) {
             q = k < nb0 ? 0 : 1;
-            k0 = (q == 0 ? k : k - nb0) * MERGE_BATCH;
-            n = min(MERGE_BATCH, (q == 0 ? nq0 : nq1) - k0);
+            k0 = (q == 0 ? k : k - nb0) * MB;
+            n = min(MB, (q == 0 ? nq0 : nq1) - k0);
         };
         auto issue = [&](int k) { // thread 0 only
             int q, k0, n;
@@ -1934,7 +1916,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
             for (int j = 0; j < n; ++j) {
                 const unsigned cta = (q == 0 ? cf0 : cf1) + static_cast<unsigned>(k0 + j);
                 const unsigned slot = j + k0 == 0 ? (q == 0 ? fs0 : fs1) : 0u;
-                bulk_g2s(smem_u32(mbuf + ((k & 1) * MERGE_BATCH + j) * PART_BYTES),
+                bulk_g2s(smem_u32(mbuf + ((k & 1) * MB + j) * PART_BYTES),
                          p.part + static_cast<size_t>(cta * 2u + slot) * PART_BYTES, PART_BYTES,
                          bar);
             }
@@ -1968,7 +1950,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
             batch(k, q, k0, n);
             const bool landed = mbar_wait_copies(merge_bar(k & 1), (k >> 1) & 1, p.err);
             const float* const pb =
-                reinterpret_cast<const float*>(mbuf + (k & 1) * MERGE_BATCH * PART_BYTES);
+                reinterpret_cast<const float*>(mbuf + (k & 1) * MB * PART_BYTES);
             constexpr int PF = PART_BYTES / 4;
             float Mb[CH];
 #pragma unroll
