@@ -1304,7 +1304,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
 
         // ---------------------------------------------------------------- QK
         float sacc[4][4] = {};
-        if constexpr (Tr::RQ) {
+        // a stage past the live length (a piece's last, partial stage): warps whose
+        // 8 tokens are all masked skip their MMAs and (bf16) PV runs the live k16
+        // steps only; kept to the pools where it measured faster (elsewhere the
+        // extra branches cost more than the skipped work)
+        constexpr bool SKIP_QK = !Tr::SCALES, SKIP_PV = !Tr::RQ;
+        if (SKIP_QK && tok_base >= n) {
+            // nothing: every score of this warp is masked below
+        } else if constexpr (Tr::RQ) {
             // this warp's 8 tokens from the raw stage: ldmatrix matrix (lane >> 3) of
             // word set j reads 16-byte chunk 4j + (lane >> 3) of its token's row; each
             // word becomes f16 B fragments in registers (k16 step ks: chunk ks for
@@ -1586,62 +1593,64 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
             const uint32_t vrow = smem_u32(Vs) + ((lane >> 4) * 8 + (lane & 7)) * BF_ROW;
 #pragma unroll
             for (int kk = 0; kk < KK; ++kk) {
-                uint32_t pb[NJ][2];
-                ldsm_x4(pb[0][0], pb[0][1], pb[1][0], pb[1][1],
-                        pbase + ((lane >> 4) * 8 + (lane & 7)) * PRS +
-                            (kk * 16 + ((lane >> 3) & 1) * 8) * 2);
-                if constexpr (NJ == 3)
-                    ldsm_x2(pb[NJ - 1][0], pb[NJ - 1][1],
-                            pbase + (16 + (lane & 7)) * PRS + (kk * 16 + ((lane >> 3) & 1) * 8) * 2);
-                if constexpr (Tr::RQ) {
-                    // V^T fragments straight from the raw stage (ldmatrix.trans of the
-                    // codes, converted in registers); the warp's 32 dims are spread
-                    // over its two m-tiles as the epilogue's dim map says
-                    uint32_t a[MT][4];
-                    const uint32_t vst = smem_u32(Vs);
-                    if constexpr (Tr::NIB4) { // chunk `warp` (32 codes) of tokens 0-7 / 8-15
-                        const int tv = kk * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
-                        uint32_t r0, r1;
-                        ldsm_x2_t(r0, r1, vst + tv * Tr::ROWB + ((warp ^ xs) << 4));
-                        if constexpr (!Tr::NIB_OFFSET) {
-                            r0 ^= 0x88888888u;
-                            r1 ^= 0x88888888u;
+                if (!SKIP_PV || kk * 16 < n) { // P is 0 past n (V rows past n are zero-filled)
+                    uint32_t pb[NJ][2];
+                    ldsm_x4(pb[0][0], pb[0][1], pb[1][0], pb[1][1],
+                            pbase + ((lane >> 4) * 8 + (lane & 7)) * PRS +
+                                (kk * 16 + ((lane >> 3) & 1) * 8) * 2);
+                    if constexpr (NJ == 3)
+                        ldsm_x2(pb[NJ - 1][0], pb[NJ - 1][1],
+                                pbase + (16 + (lane & 7)) * PRS + (kk * 16 + ((lane >> 3) & 1) * 8) * 2);
+                    if constexpr (Tr::RQ) {
+                        // V^T fragments straight from the raw stage (ldmatrix.trans of the
+                        // codes, converted in registers); the warp's 32 dims are spread
+                        // over its two m-tiles as the epilogue's dim map says
+                        uint32_t a[MT][4];
+                        const uint32_t vst = smem_u32(Vs);
+                        if constexpr (Tr::NIB4) { // chunk `warp` (32 codes) of tokens 0-7 / 8-15
+                            const int tv = kk * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+                            uint32_t r0, r1;
+                            ldsm_x2_t(r0, r1, vst + tv * Tr::ROWB + ((warp ^ xs) << 4));
+                            if constexpr (!Tr::NIB_OFFSET) {
+                                r0 ^= 0x88888888u;
+                                r1 ^= 0x88888888u;
+                            }
+    #pragma unroll
+                            for (int mt = 0; mt < MT; ++mt) {
+                                a[mt][0] = pair4<Tr::PV_F16>(r0, 2 * mt);
+                                a[mt][1] = pair4<Tr::PV_F16>(r0, 2 * mt + 1);
+                                a[mt][2] = pair4<Tr::PV_F16>(r1, 2 * mt);
+                                a[mt][3] = pair4<Tr::PV_F16>(r1, 2 * mt + 1);
+                            }
+                        } else { // chunks 2 warp, 2 warp + 1 (16 codes each) of tokens 0-7 / 8-15
+                            const int mi = lane >> 3;
+                            const int tv = kk * 16 + (mi >> 1) * 8 + (lane & 7);
+                            uint32_t vrow_base = vst;
+                            if constexpr (Tr::TIER) // int4 rows: their widened codes in the side buffer
+                                if (!((((tv < 32) ? hot_lo : hot_hi) >> (tv & 31)) & 1u))
+                                    vrow_base = smem_u32(smem + Ly::off_vexp);
+                            uint32_t r[4];
+                            ldsm_x4_t(r[0], r[1], r[2], r[3],
+                                      vrow_base + tv * Tr::ROWB + (((2 * warp + (mi & 1)) ^ xs) << 4));
+    #pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                a[0][q] = pair8<FMT, Tr::PV_F16>(r[q], false);
+                                a[1][q] = pair8<FMT, Tr::PV_F16>(r[q], true);
+                            }
                         }
-#pragma unroll
+    #pragma unroll
+                        for (int mt = 0; mt < MT; ++mt)
+    #pragma unroll
+                            for (int j = 0; j < NJ; ++j) mma16816<Tr::PV_F16>(o[mt][j], a[mt], pb[j][0], pb[j][1]);
+                    } else {
+    #pragma unroll
                         for (int mt = 0; mt < MT; ++mt) {
-                            a[mt][0] = pair4<Tr::PV_F16>(r0, 2 * mt);
-                            a[mt][1] = pair4<Tr::PV_F16>(r0, 2 * mt + 1);
-                            a[mt][2] = pair4<Tr::PV_F16>(r1, 2 * mt);
-                            a[mt][3] = pair4<Tr::PV_F16>(r1, 2 * mt + 1);
+                            uint32_t a[4];
+                            ldsm_x4_t(a[0], a[1], a[2], a[3],
+                                      vrow + kk * 16 * BF_ROW + (((4 * warp + 2 * mt) << 4) ^ vx));
+    #pragma unroll
+                            for (int j = 0; j < NJ; ++j) mma16816<Tr::PV_F16>(o[mt][j], a, pb[j][0], pb[j][1]);
                         }
-                    } else { // chunks 2 warp, 2 warp + 1 (16 codes each) of tokens 0-7 / 8-15
-                        const int mi = lane >> 3;
-                        const int tv = kk * 16 + (mi >> 1) * 8 + (lane & 7);
-                        uint32_t vrow_base = vst;
-                        if constexpr (Tr::TIER) // int4 rows: their widened codes in the side buffer
-                            if (!((((tv < 32) ? hot_lo : hot_hi) >> (tv & 31)) & 1u))
-                                vrow_base = smem_u32(smem + Ly::off_vexp);
-                        uint32_t r[4];
-                        ldsm_x4_t(r[0], r[1], r[2], r[3],
-                                  vrow_base + tv * Tr::ROWB + (((2 * warp + (mi & 1)) ^ xs) << 4));
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            a[0][q] = pair8<FMT, Tr::PV_F16>(r[q], false);
-                            a[1][q] = pair8<FMT, Tr::PV_F16>(r[q], true);
-                        }
-                    }
-#pragma unroll
-                    for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-                        for (int j = 0; j < NJ; ++j) mma16816<Tr::PV_F16>(o[mt][j], a[mt], pb[j][0], pb[j][1]);
-                } else {
-#pragma unroll
-                    for (int mt = 0; mt < MT; ++mt) {
-                        uint32_t a[4];
-                        ldsm_x4_t(a[0], a[1], a[2], a[3],
-                                  vrow + kk * 16 * BF_ROW + (((4 * warp + 2 * mt) << 4) ^ vx));
-#pragma unroll
-                        for (int j = 0; j < NJ; ++j) mma16816<Tr::PV_F16>(o[mt][j], a, pb[j][0], pb[j][1]);
                     }
                 }
             }
