@@ -710,41 +710,47 @@ struct Cursor {
     bool segfirst;
 };
 
+// The flattened work space is head-major: KV head g's tokens of all sequences,
+// [g NT, (g + 1) NT) with NT = segP[bs] the live tokens per head, sequence b's
+// at offset segP[b] within it. The CTAs working on head 0 and head 1 of the same
+// slots then run at the same time, so the second read of what the heads share
+// (slot ids, the 32-byte scale sector of a slot's two heads) hits L2.
 __device__ __forceinline__ void cursor_init(Cursor& c, long long t, long long t_end,
                                             const int* segL, const int* segP, int bs, int Hkv) {
-    int lo = 0, hi = bs - 1; // largest b with Hkv * segP[b] <= t
+    const long long NT = segP[bs];
+    c.g = static_cast<int>(t / NT);
+    const long long r = t - (long long)c.g * NT;
+    int lo = 0, hi = bs - 1; // largest b with segP[b] <= r (a sequence with tokens left)
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if ((long long)Hkv * segP[mid] <= t)
+        if (segP[mid] <= r)
             lo = mid;
         else
             hi = mid - 1;
     }
     c.b = lo;
-    const long long off = t - (long long)Hkv * segP[lo];
-    const int L = segL[lo];
-    c.g = static_cast<int>(off / L);
-    c.j = static_cast<int>(off - (long long)c.g * L);
+    c.j = static_cast<int>(r - segP[lo]);
     c.t = t;
-    c.j1 = static_cast<int>(min((long long)L, c.j + (t_end - t)));
+    c.j1 = static_cast<int>(min((long long)segL[lo], c.j + (t_end - t)));
     c.kseg = 0;
     c.segfirst = true;
 }
 
 __device__ __forceinline__ int cursor_n(const Cursor& c) { return min(T, c.j1 - c.j); }
 
-__device__ __forceinline__ void cursor_advance(Cursor& c, long long t_end, const int* segL,
-                                               int Hkv) {
+__device__ __forceinline__ void cursor_advance(Cursor& c, long long t_end, const int* segL, int bs) {
     const int n = cursor_n(c);
     c.t += n;
     c.j += n;
     c.segfirst = false;
     if (c.j >= c.j1 && c.t < t_end) {
-        if (++c.g == Hkv) {
-            c.g = 0;
-            do {
-                ++c.b;
-            } while (segL[c.b] == 0);
+        do {
+            ++c.b;
+        } while (c.b < bs && segL[c.b] == 0);
+        if (c.b >= bs) { // the next KV head, from its first sequence with tokens
+            ++c.g;
+            c.b = 0;
+            while (segL[c.b] == 0) ++c.b;
         }
         c.j = 0;
         c.j1 = static_cast<int>(min((long long)segL[c.b], t_end - c.t));
@@ -921,7 +927,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
         for (int i = 0; i < Ly::PF; ++i) {
             if (pc.t < t_end) {
                 prefetch(pc, i % Ly::R);
-                cursor_advance(pc, t_end, segL, Hkv);
+                cursor_advance(pc, t_end, segL, p.bs);
             }
             cp_async_commit();
         }
@@ -933,7 +939,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
         for (int i = 0; ic.t < t_end; ++i) {
             if (pc.t < t_end) {
                 prefetch(pc, (i + Ly::PF) % Ly::R);
-                cursor_advance(pc, t_end, segL, Hkv);
+                cursor_advance(pc, t_end, segL, p.bs);
             }
             cp_async_commit();
             cp_async_wait<Ly::PF>();
@@ -1072,13 +1078,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
             }
 #ifdef QSA_TEST_HOOKS
             if (blockIdx.x == 0 && i == p.stall_stage) { // test build only: never complete it
-                cursor_advance(ic, t_end, segL, Hkv);
+                cursor_advance(ic, t_end, segL, p.bs);
                 continue;
             }
 #endif
             cp_async_arrive_noinc(full_bar(s));
             mbar_arrive(full_bar(s));
-            cursor_advance(ic, t_end, segL, Hkv);
+            cursor_advance(ic, t_end, segL, p.bs);
         }
         cp_async_wait<0>();
         return;
@@ -1121,7 +1127,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
     // sits in its slot 1 when its range began before the segment
     auto seg_range = [&](int sid, unsigned& Fs, unsigned& c_first, unsigned& c_last) {
         const int b = sid / Hkv, g = sid - (sid / Hkv) * Hkv, L = segL[b];
-        Fs = static_cast<unsigned>(Hkv * segP[b] + g * L);
+        Fs = static_cast<unsigned>(g * segP[p.bs] + segP[b]);
         c_first = cta_of(Fs, N, G);
         c_last = cta_of(Fs + static_cast<unsigned>(L) - 1u, N, G);
     };
@@ -1801,7 +1807,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
             // no trailing barrier: lred is next written in a later epilogue, and
             // every stage in between passes the per-stage consumer barrier
         }
-        cursor_advance(cc, t_end, segL, Hkv);
+        cursor_advance(cc, t_end, segL, p.bs);
         buf ^= 1;
     }
 
