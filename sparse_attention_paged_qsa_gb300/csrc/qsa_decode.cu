@@ -1115,6 +1115,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
     constexpr int NJ = P_HI ? 2 : 3;
     float o[MT][NJ][4];
     float l0 = 0.f, l1 = 0.f;
+    // this lane's heads r, r + 8: reference maxima, and (per-slot V scales in f16
+    // PV) offsets E and 2^-E, as published in mref / eref; they change only on the
+    // slow path, so the fast path keeps them in registers
+    float mr_a = 0.f, mr_b = 0.f, er_a = 0.f, er_b = 0.f, fr_a = 1.f, fr_b = 1.f;
     int v = 0, buf = 0, seg_j0 = 0;
     // Merge bookkeeping, kept in shared memory rather than in registers carried
     // through the main loop: [0] pend0 / [1] pend1, the split segments whose
@@ -1399,8 +1403,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
             redb[warp * 16 + r + 8] = mb;
         }
         const float* const mrefv = mref + v * 16;
-        const float mo_a = first ? ninf : mrefv[r];
-        const float mo_b = first ? ninf : mrefv[r + 8];
+        const float mo_a = first ? ninf : mr_a;
+        const float mo_b = first ? ninf : mr_b;
         // Per-slot V scales in f16 PV (int8): PV runs on pn = p * s_v * 2^-E_h,
         // p = 2^(x - m_h). The per-head offset E_h is kept at or above every
         // t = (x - m_h) + floor(log2 |s_v|) - 14 of the piece, so pn < 2^15 (when
@@ -1419,10 +1423,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
             g0 = lgs(svr[0]);
             g1 = lgs(svr[1]);
             if (!first) {
-                eo_a = erefv[r];
-                eo_b = erefv[r + 8];
-                fa = ex2(-eo_a);
-                fb = row8 ? ex2(-eo_b) : 0.f;
+                eo_a = er_a;
+                eo_b = er_b;
+                fa = fr_a;
+                fb = row8 ? fr_b : 0.f;
                 const float ta = fmaxf((x[0] - mo_a) + g0, (x[1] - mo_a) + g1);
                 const float tb = fmaxf((x[2] - mo_b) + g0, (x[3] - mo_b) + g1);
                 vraise = ta > eo_a || (row8 && tb > eo_b);
@@ -1490,6 +1494,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
                 return mo == ninf ? 0.f : ex2(mo - new_ref(h));
             };
             const float na = new_ref(r), nb = row8 ? new_ref(r + 8) : 0.f;
+            mr_a = na;
+            mr_b = nb;
             l0 *= alpha(r);
             l1 *= row8 ? alpha(r + 8) : 0.f;
             // per-slot V scales: the stage's largest offset t per head against the
@@ -1524,8 +1530,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
                 return ex2((old_ref(h) - new_ref(h)) + (erefv[h] - new_e(h)));
             };
             if constexpr (VSH) {
-                fa = ex2(-new_e(r));
-                fb = row8 ? ex2(-new_e(r + 8)) : 0.f;
+                er_a = new_e(r);
+                er_b = row8 ? new_e(r + 8) : 0.f;
+                fr_a = ex2(-er_a);
+                fr_b = row8 ? ex2(-er_b) : 0.f;
+                fa = fr_a;
+                fb = fr_b;
             }
             compute_p(na, nb);
             write_p();
