@@ -88,6 +88,7 @@ constexpr int TPP = T / NP;                 // tokens gathered per producer warp
 constexpr int BF_ROW = D * 2;               // bf16 row bytes (swizzled, unpadded)
 constexpr int Q_RS = 528;                   // Q tile row stride (512 + 16 pad)
 constexpr int PRS = T * 2 + 16;             // P^T row stride (bytes)
+constexpr int PFS = T + 8;                  // FP32 P row stride (floats; 72 = 8 mod 32 banks)
 constexpr float TAU = 8.0f;                 // lazy-rescale threshold (log2 units)
 constexpr int MAX_BS = 128;
 constexpr int MAX_CAPACITY = 2055;
@@ -150,12 +151,12 @@ template <> struct Traits<QSA_KV_INT8_G64> {
     static constexpr bool PV_F16 = false, NIB4 = false, NIB_OFFSET = false, TIER = false;
 };
 template <> struct Traits<QSA_KV_INT4_G32> {
-    static constexpr int ROWB = 128, STAGES = 9, GROUPS = 8;
+    static constexpr int ROWB = 128, STAGES = 10, GROUPS = 8;
     static constexpr bool RQ = true, SCALES = true, QK_F16 = true;
     static constexpr bool PV_F16 = false, NIB4 = true, NIB_OFFSET = true, TIER = false;
 };
 template <> struct Traits<QSA_KV_INT8RING_INT4> {
-    static constexpr int ROWB = 256, STAGES = 4, GROUPS = 8;
+    static constexpr int ROWB = 256, STAGES = 5, GROUPS = 8;
     static constexpr bool RQ = true, SCALES = true, QK_F16 = true;
     static constexpr bool PV_F16 = false, NIB4 = false, NIB_OFFSET = true, TIER = true;
 };
@@ -176,9 +177,13 @@ template <int FMT> struct Layout {
     static constexpr int vexp_bytes = Tr::TIER ? T * 256 : 0;
     static constexpr int off_q = off_vexp + vexp_bytes;
     static constexpr int off_p = off_q + 2 * 16 * Q_RS;
-    // P^T hi/lo (two buffers); grouped pools: FP32 P [2][12][T] then one P^T per warp
-    static constexpr int off_pw = off_p + 2 * GROUP * T * 4;
-    static constexpr int p_bytes = Tr::GROUPS ? 2 * GROUP * T * 4 + NW * 24 * PRS : 2 * 24 * PRS;
+    // P^T hi/lo (two buffers); grouped pools: FP32 P [2][12][PFS], from which each
+    // warp builds its PV B fragments in registers (32-channel groups), or each pair
+    // of warps sharing a 64-channel group one scaled P^T per stage [4][2][24][PRS]
+    static constexpr int off_pw = off_p + 2 * GROUP * PFS * 4;
+    static constexpr int p_bytes = Tr::GROUPS == 4 ? 2 * GROUP * PFS * 4 + 8 * 24 * PRS
+                                   : Tr::GROUPS    ? 2 * GROUP * PFS * 4
+                                                   : 2 * 24 * PRS;
     static constexpr int off_red = off_p + p_bytes;
     static constexpr int off_mref = off_red + 2 * NW * 16 * 4;
     static constexpr int off_lred = off_mref + 2 * 16 * 4;
@@ -1441,7 +1446,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
             pr[2] = x[2] == ninf ? 0.f : ex2(x[2] - rb);
             pr[3] = x[3] == ninf ? 0.f : ex2(x[3] - rb);
         };
-        float* const Pf = reinterpret_cast<float*>(smem + Ly::off_p) + buf * GROUP * T;
+        float* const Pf = reinterpret_cast<float*>(smem + Ly::off_p) + buf * GROUP * PFS;
         auto write_p = [&]() {
             // p * s_v * f in an order whose partial product stays finite: with f <= 1,
             // s_v * f <= s_v; with f > 1, p * f <= 2^TAU * 2^119 (masked tokens have p = 0)
@@ -1452,9 +1457,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
             pv[1] = v1 ? pv[1] : 0.f;
             pv[2] = v0 ? pv[2] : 0.f;
             pv[3] = v1 ? pv[3] : 0.f;
-            if constexpr (Tr::GROUPS) { // FP32 P; each warp scales and splits its own copy
-                *reinterpret_cast<float2*>(Pf + r * T + tk0) = make_float2(pv[0], pv[1]);
-                if (row8) *reinterpret_cast<float2*>(Pf + (8 + r) * T + tk0) = make_float2(pv[2], pv[3]);
+            if constexpr (Tr::GROUPS) { // FP32 P; each warp scales and splits its own fragments
+                *reinterpret_cast<float2*>(Pf + r * PFS + tk0) = make_float2(pv[0], pv[1]);
+                if (row8) *reinterpret_cast<float2*>(Pf + (8 + r) * PFS + tk0) = make_float2(pv[2], pv[3]);
                 return;
             }
             if constexpr (P_HI) { // P^T rows: heads 0-11; rows 12-15 stay zero
@@ -1566,9 +1571,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
         // ---------------------------------------------------------------- PV
         const uint8_t* Pt = Pb;
         if constexpr (Tr::GROUPS == 4) {
-            // 64-channel groups: warps 2k and 2k + 1 share group k, so the pair builds
-            // one copy (six heads each, double-buffered by stage) and meets at a named
-            // barrier; scaling and split as below
+            // 64-channel groups: warps 2k and 2k + 1 share group k and need the same
+            // scaled P^T, so the pair builds one copy (six heads each, double-buffered
+            // by stage) and meets at a named barrier; each P times its token's V
+            // scale, split into bf16 hi + lo
             const int pair = warp >> 1, h0 = 6 * (warp & 1);
             uint8_t* const Pw = smem + Ly::off_pw + (pair * 2 + buf) * 24 * PRS;
             const int t = 2 * lane;
@@ -1576,7 +1582,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
 #pragma unroll
             for (int hh = 0; hh < 6; ++hh) {
                 const int h = h0 + hh;
-                const float2 pp = *reinterpret_cast<const float2*>(Pf + h * T + t);
+                const float2 pp = *reinterpret_cast<const float2*>(Pf + h * PFS + t);
                 uint32_t hi, lo;
                 split_pair<false>(pp.x * sv0, pp.y * sv1, hi, lo);
                 const int rh = h < 8 ? h : 8 + h, rl = h < 8 ? 8 + h : 12 + h;
@@ -1584,24 +1590,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
                 *reinterpret_cast<uint32_t*>(Pw + rl * PRS + t * 2) = lo;
             }
             asm volatile("bar.sync %0, 64;" ::"r"(BAR_CONSUMERS + 1 + pair) : "memory");
-            Pt = Pw;
-        } else if constexpr (Tr::GROUPS) {
-            // this warp's dims lie in one channel group: P^T columns scaled per token
-            // by that group's V scale (read into svw above), split into bf16 hi + lo
-            uint8_t* const Pw = smem + Ly::off_pw + warp * 24 * PRS;
-            const int t = 2 * lane;
-            const float sv0 = svw[0], sv1 = svw[1];
-            __syncwarp(); // the previous stage's reads of Pw are done
-#pragma unroll
-            for (int h = 0; h < GROUP; ++h) {
-                const float2 pp = *reinterpret_cast<const float2*>(Pf + h * T + t);
-                uint32_t hi, lo;
-                split_pair<false>(pp.x * sv0, pp.y * sv1, hi, lo);
-                const int rh = h < 8 ? h : 8 + h, rl = h < 8 ? 8 + h : 12 + h;
-                *reinterpret_cast<uint32_t*>(Pw + rh * PRS + t * 2) = hi;
-                *reinterpret_cast<uint32_t*>(Pw + rl * PRS + t * 2) = lo;
-            }
-            __syncwarp();
             Pt = Pw;
         }
         {
@@ -1611,12 +1599,38 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
             for (int kk = 0; kk < KK; ++kk) {
                 if (!SKIP_PV || kk * 16 < n) { // P is 0 past n (V rows past n are zero-filled)
                     uint32_t pb[NJ][2];
-                    ldsm_x4(pb[0][0], pb[0][1], pb[1][0], pb[1][1],
-                            pbase + ((lane >> 4) * 8 + (lane & 7)) * PRS +
-                                (kk * 16 + ((lane >> 3) & 1) * 8) * 2);
-                    if constexpr (NJ == 3)
-                        ldsm_x2(pb[NJ - 1][0], pb[NJ - 1][1],
-                                pbase + (16 + (lane & 7)) * PRS + (kk * 16 + ((lane >> 3) & 1) * 8) * 2);
+                    if constexpr (Tr::GROUPS == 8) {
+                        // 32-channel groups: the B fragments of P^T scaled per token by this
+                        // warp's group V scale, built in registers. Lane (r, c) takes
+                        // heads r (hi, lo: tiles 0, 1) and 8 + (r & 3) (tile 2: hi for
+                        // r < 4, lo above), tokens 2c, 2c + 1 and 8 + 2c, 9 + 2c of the
+                        // k-step; token 2l + u's scale is lane l's svw[u]
+                        const int ta = kk * 16 + 2 * c, tb = ta + 8;
+                        const float s0 = __shfl_sync(0xFFFFFFFFu, svw[0], ta >> 1);
+                        const float s1 = __shfl_sync(0xFFFFFFFFu, svw[1], ta >> 1);
+                        const float s8 = __shfl_sync(0xFFFFFFFFu, svw[0], tb >> 1);
+                        const float s9 = __shfl_sync(0xFFFFFFFFu, svw[1], tb >> 1);
+                        const float* const Pr = Pf + r * PFS;
+                        const float* const P2 = Pf + (8 + (r & 3)) * PFS;
+                        const float2 p0 = *reinterpret_cast<const float2*>(Pr + ta);
+                        const float2 p1 = *reinterpret_cast<const float2*>(Pr + tb);
+                        const float2 p2 = *reinterpret_cast<const float2*>(P2 + ta);
+                        const float2 p3 = *reinterpret_cast<const float2*>(P2 + tb);
+                        split_pair<false>(p0.x * s0, p0.y * s1, pb[0][0], pb[1][0]);
+                        split_pair<false>(p1.x * s8, p1.y * s9, pb[0][1], pb[1][1]);
+                        uint32_t h2a, l2a, h2b, l2b;
+                        split_pair<false>(p2.x * s0, p2.y * s1, h2a, l2a);
+                        split_pair<false>(p3.x * s8, p3.y * s9, h2b, l2b);
+                        pb[NJ - 1][0] = r < 4 ? h2a : l2a;
+                        pb[NJ - 1][1] = r < 4 ? h2b : l2b;
+                    } else {
+                        ldsm_x4(pb[0][0], pb[0][1], pb[1][0], pb[1][1],
+                                pbase + ((lane >> 4) * 8 + (lane & 7)) * PRS +
+                                    (kk * 16 + ((lane >> 3) & 1) * 8) * 2);
+                        if constexpr (NJ == 3)
+                            ldsm_x2(pb[NJ - 1][0], pb[NJ - 1][1],
+                                    pbase + (16 + (lane & 7)) * PRS + (kk * 16 + ((lane >> 3) & 1) * 8) * 2);
+                    }
                     if constexpr (Tr::RQ) {
                         // V^T fragments straight from the raw stage (ldmatrix.trans of the
                         // codes, converted in registers); the warp's 32 dims are spread
