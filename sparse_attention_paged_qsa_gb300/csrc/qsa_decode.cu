@@ -870,9 +870,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
             excl += Ls[k];
         }
         const int total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+        int lmax = max(max(Ls[0], Ls[1]), max(Ls[2], Ls[3]));
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) lmax = max(lmax, __shfl_xor_sync(0xFFFFFFFFu, lmax, off));
         if (lane == 0) {
             segP[p.bs] = total;
             segL[p.bs] = 1; // sentinel for the segment walk
+            misc[20] = lmax; // the longest selection
         }
         bad = __any_sync(0xFFFFFFFFu, bad);
         if (bad && lane == 0 && blockIdx.x == 0) atomicOr(p.err, QSA_DEVERR_CU_SEQLENS);
@@ -895,22 +899,36 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
         }
     }
     if (N == 0) return;
+    // Short selections (every one fits a 64-token stage): the CTAs split whole
+    // (sequence, KV head) segments, [c S / G, (c + 1) S / G) of the S = bs Hkv in
+    // head-major order, so that no segment is cut and nothing is merged.
+    const unsigned S_all = static_cast<unsigned>(p.bs * Hkv);
+    const bool whole = misc[20] <= T;
     unsigned G = (N + MIN_TOKENS_PER_CTA - 1) / MIN_TOKENS_PER_CTA;
     G = G < gridDim.x ? G : gridDim.x;
+    if (whole) G = S_all < gridDim.x ? S_all : gridDim.x;
     // Few segments (bs * Hkv <= FEW_SEGMENTS): a whole number of CTAs per segment,
     // at most MAX_FANIN. With equal lengths no CTA then holds pieces of two
     // segments, so their merges run on different CTAs, and each merge reads at
     // most MAX_FANIN partials.
     {
         const unsigned S = static_cast<unsigned>(p.bs * Hkv);
-        if (S <= FEW_SEGMENTS && 2 * S <= G) {
+        if (!whole && S <= FEW_SEGMENTS && 2 * S <= G) {
             const unsigned per = G / S < MAX_FANIN ? G / S : MAX_FANIN;
             G = per * S;
         }
     }
     if (blockIdx.x >= G) return;
-    const long long t_begin = cta_begin(blockIdx.x, N, G);
-    const long long t_end = cta_begin(blockIdx.x + 1, N, G);
+    long long t_begin, t_end;
+    if (whole) { // the first token of segment k = g bs + b is g NT + segP[b]
+        const long long NT = segP[p.bs];
+        const unsigned k0 = blockIdx.x * S_all / G, k1 = (blockIdx.x + 1) * S_all / G;
+        t_begin = (long long)(k0 / p.bs) * NT + segP[k0 % p.bs];
+        t_end = k1 >= S_all ? (long long)N : (long long)(k1 / p.bs) * NT + segP[k1 % p.bs];
+    } else {
+        t_begin = cta_begin(blockIdx.x, N, G);
+        t_end = cta_begin(blockIdx.x + 1, N, G);
+    }
 
     uint8_t* const stage0 = smem + Ly::off_stage;
     int* const ring = reinterpret_cast<int*>(smem + Ly::off_ring);
