@@ -131,22 +131,22 @@ template <> struct Traits<QSA_KV_BF16> {
     static constexpr bool PV_F16 = false, NIB4 = false, NIB_OFFSET = false, TIER = false;
 };
 template <> struct Traits<QSA_KV_FP8_E4M3> {
-    static constexpr int ROWB = 256, STAGES = 6, GROUPS = 0;
+    static constexpr int ROWB = 256, STAGES = 4, GROUPS = 0;
     static constexpr bool RQ = true, SCALES = false, QK_F16 = true;
     static constexpr bool PV_F16 = true, NIB4 = false, NIB_OFFSET = false, TIER = false;
 };
 template <> struct Traits<QSA_KV_INT8> {
-    static constexpr int ROWB = 256, STAGES = 6, GROUPS = 0;
+    static constexpr int ROWB = 256, STAGES = 4, GROUPS = 0;
     static constexpr bool RQ = true, SCALES = true, QK_F16 = true;
     static constexpr bool PV_F16 = true, NIB4 = false, NIB_OFFSET = false, TIER = false;
 };
 template <> struct Traits<QSA_KV_INT4> {
-    static constexpr int ROWB = 128, STAGES = 11, GROUPS = 0;
+    static constexpr int ROWB = 128, STAGES = 8, GROUPS = 0;
     static constexpr bool RQ = true, SCALES = true, QK_F16 = true;
     static constexpr bool PV_F16 = false, NIB4 = true, NIB_OFFSET = false, TIER = false;
 };
 template <> struct Traits<QSA_KV_INT8_G64> {
-    static constexpr int ROWB = 256, STAGES = 5, GROUPS = 4;
+    static constexpr int ROWB = 256, STAGES = 4, GROUPS = 4;
     static constexpr bool RQ = true, SCALES = true, QK_F16 = true;
     static constexpr bool PV_F16 = false, NIB4 = false, NIB_OFFSET = false, TIER = false;
 };
@@ -156,7 +156,7 @@ template <> struct Traits<QSA_KV_INT4_G32> {
     static constexpr bool PV_F16 = false, NIB4 = true, NIB_OFFSET = true, TIER = false;
 };
 template <> struct Traits<QSA_KV_INT8RING_INT4> {
-    static constexpr int ROWB = 256, STAGES = 5, GROUPS = 8;
+    static constexpr int ROWB = 256, STAGES = 3, GROUPS = 8;
     static constexpr bool RQ = true, SCALES = true, QK_F16 = true;
     static constexpr bool PV_F16 = false, NIB4 = false, NIB_OFFSET = true, TIER = true;
 };
