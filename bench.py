@@ -496,12 +496,13 @@ def measure_formats(args, dev, stream, scratch, peak):
 # ------------------------------------------------------------ batch / length sweep
 
 SWEEP_BATCHES = (1, 4, 16, 64)
-SWEEP_BANDS = ("short", "saturated")
+SWEEP_BANDS = ("short", "medium", "saturated")
 
 
 def measure_small_batches(args, dev, peak):
     """Batch sizes 1..64 of both topologies (TP1 24Q/2KV, TP2 12Q/1KV) over a bf16 pool
-    of 524,288 slots, in the short (1-64) and saturated (2055) length bands. Each
+    of 524,288 slots, in the short (1-64), medium (512-1024) and saturated (2055)
+    length bands. Each
     point's calls are captured in one CUDA graph (three index sets in turn) and
     replayed behind the gate, as a serving loop replays its decode."""
     import sparse_attention_paged_qsa_gb300 as qsa
@@ -514,7 +515,7 @@ def measure_small_batches(args, dev, peak):
         for band in SWEEP_BANDS:
             lo, hi = I.BANDS[band]
             for bs in SWEEP_BATCHES:
-                g = torch.Generator().manual_seed(1000 * bs + 10 * hkv + (band == "short"))
+                g = torch.Generator().manual_seed(1000 * bs + 10 * hkv + SWEEP_BANDS.index(band) + 1)
                 sets = []
                 for _ in range(args.index_sets):
                     lens = torch.randint(lo, hi + 1, (bs,), generator=g, dtype=torch.int64)
