@@ -372,7 +372,20 @@ __global__ void __launch_bounds__(THREADS, 1) topk_expand_kernel(const Params p)
     auto put_block = [&](int i, int j) {
         if (j < kb) { // exactly kb are kept; the bound guards the row
             int* const dst = out + j * r;
-            for (int t = 0; t < r; ++t) dst[t] = slot_of(p, ptrow, i * r + t, bad);
+            const int pos0 = i * r;
+            if (ptrow != nullptr && (pos0 >> p.page_shift) == ((pos0 + r - 1) >> p.page_shift)) {
+                // the block's r tokens lie in one page: one page-table read for all
+                const long long page = 1LL << p.page_shift;
+                const long long s0 = (long long)__ldg(ptrow + (pos0 >> p.page_shift)) * page + (pos0 & (page - 1));
+                for (int t = 0; t < r; ++t) { // the same range check as slot_of, per token
+                    const long long st = s0 + t;
+                    const bool out_of_range = st < 0 || st > 0x7FFFFFFFLL;
+                    bad |= out_of_range;
+                    dst[t] = out_of_range ? -1 : static_cast<int>(st);
+                }
+            } else {
+                for (int t = 0; t < r; ++t) dst[t] = slot_of(p, ptrow, pos0 + t, bad);
+            }
         }
     };
     // radix passes 1 and 2 (digits of 11 and 10 bits) over keys in shared memory
