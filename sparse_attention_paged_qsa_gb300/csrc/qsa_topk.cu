@@ -70,7 +70,8 @@ constexpr uint32_t KEPT = 0xFFFFFFFFu;         // not a key: order_key maps ever
 constexpr int OFF_RING = 0;
 constexpr int OFF_KEYS = OFF_RING + 2 * PIECE * 4;
 constexpr int OFF_HIST = OFF_KEYS + KEYS_CAP * 4;
-constexpr int SMEM_BYTES = OFF_HIST + NBINS * 4;
+constexpr int OFF_KEPT = OFF_HIST + NBINS * 4;           // kept block index by rank
+constexpr int SMEM_BYTES = OFF_KEPT + (MAX_ROW + 1) * 4;
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 static_assert(NBINS % THREADS == 0 && NBINS / THREADS <= 4, "digit scan");
 
@@ -319,6 +320,7 @@ __global__ void __launch_bounds__(THREADS, 1) topk_expand_kernel(const Params p)
     float* const ring = reinterpret_cast<float*>(smem + OFF_RING);
     uint32_t* const keys = reinterpret_cast<uint32_t*>(smem + OFF_KEYS);
     uint32_t* const hist = reinterpret_cast<uint32_t*>(smem + OFF_HIST);
+    int* const kept = reinterpret_cast<int*>(smem + OFF_KEPT);
     __shared__ __align__(8) uint64_t bars[2];
     __shared__ int wsum[WARPS];
     __shared__ int sh[4];
@@ -368,11 +370,16 @@ __global__ void __launch_bounds__(THREADS, 1) topk_expand_kernel(const Params p)
         for (int i = tid; i < NBINS; i += THREADS) hist[i] = 0u;
         __syncthreads();
     };
-    // writes a kept block's r token slots at its rank
+    // a kept block at its rank; its r token slots are written after the scan by
+    // write_kept, all blocks at once, so the page-table reads overlap
     auto put_block = [&](int i, int j) {
-        if (j < kb) { // exactly kb are kept; the bound guards the row
+        if (j < kb) kept[j] = i; // exactly kb are kept; the bound guards the row
+    };
+    auto write_kept = [&]() {
+        __syncthreads();
+        for (int j = tid; j < kb; j += THREADS) {
             int* const dst = out + j * r;
-            const int pos0 = i * r;
+            const int pos0 = kept[j] * r;
             if (ptrow != nullptr && (pos0 >> p.page_shift) == ((pos0 + r - 1) >> p.page_shift)) {
                 // the block's r tokens lie in one page: one page-table read for all
                 const long long page = 1LL << p.page_shift;
@@ -513,6 +520,7 @@ __global__ void __launch_bounds__(THREADS, 1) topk_expand_kernel(const Params p)
             if (!ok) return timed_out();
         }
     }
+    write_kept(); // the kept blocks' slots, at their ranks
     // the tail tokens, after the k kept blocks
     for (int t = tid; t < tail; t += THREADS) out[kb * r + t] = slot_of(p, ptrow, nb * r + t, bad);
     if (bad && p.err != nullptr) atomicOr(p.err, QSA_DEVERR_SLOT_RANGE);
