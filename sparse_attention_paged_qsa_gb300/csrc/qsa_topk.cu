@@ -64,6 +64,8 @@ constexpr int MAX_CAPACITY = 262144;           // the pages' fixed 256K context 
 constexpr int MAX_ROW = 2055;                  // the decode's selected-KV capacity
 constexpr unsigned FULL = 0xFFFFFFFFu;
 constexpr int NBINS = 2048;                    // bins of an 11-bit digit
+constexpr int P16_CAP = 65536;                 // blocks whose 16-bit key prefixes fit the key area
+constexpr int CAND_CAP = KEYS_CAP - P16_CAP / 2; // candidate keys kept next to those prefixes
 constexpr long long WAIT_NS = 2000000000LL;    // bounded-wait limit (2 s)
 constexpr uint32_t KEPT = 0xFFFFFFFFu;         // not a key: order_key maps every NaN to 0
 // dynamic shared memory: the two ring slots, the keys, the histogram
@@ -74,6 +76,7 @@ constexpr int OFF_KEPT = OFF_HIST + NBINS * 4;           // kept block index by 
 constexpr int SMEM_BYTES = OFF_KEPT + (MAX_ROW + 1) * 4;
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 static_assert(NBINS % THREADS == 0 && NBINS / THREADS <= 4, "digit scan");
+static_assert(CAND_CAP > 0 && P16_CAP % 2 == 0, "prefix and candidate areas");
 
 struct Params {
     const float* scores;
@@ -396,12 +399,12 @@ __global__ void __launch_bounds__(THREADS, 1) topk_expand_kernel(const Params p)
         }
     };
     // radix passes 1 and 2 (digits of 11 and 10 bits) over keys in shared memory
-    auto select_in_smem = [&](int n, uint32_t& prefix, uint32_t& mask, int& need) {
+    auto select_in_smem = [&](const uint32_t* kk, int n, uint32_t& prefix, uint32_t& mask, int& need) {
         for (int pass = 1; pass < 3; ++pass) {
             const int shift = pass == 1 ? 10 : 0, bins = pass == 1 ? 2048 : 1024;
             clear_hist();
             for (int i = tid; i < n; i += THREADS) {
-                const uint32_t k = keys[i];
+                const uint32_t k = kk[i];
                 if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & (bins - 1)], 1u);
             }
             __syncthreads();
@@ -430,7 +433,7 @@ __global__ void __launch_bounds__(THREADS, 1) topk_expand_kernel(const Params p)
         prefix = static_cast<uint32_t>(d.x) << 21;
         mask = 0x7FFu << 21;
         need -= d.y;
-        select_in_smem(nb, prefix, mask, need);
+        select_in_smem(keys, nb, prefix, mask, need);
         const uint32_t thr = prefix;
         int ca = 0, cs = 0;
         for (int base = 0; base < nb; base += PIECE)
@@ -440,9 +443,18 @@ __global__ void __launch_bounds__(THREADS, 1) topk_expand_kernel(const Params p)
                        [&](int j, int rank) { put_block(base + j, rank); }, ca, cs, wsum);
     } else {
         // ------------------------------------------------ a long row: stream the passes
+        // Up to P16_CAP blocks, the first pass also keeps every key's top 16 bits in
+        // shared memory; the rest of the selection then reads only the scores of the
+        // blocks that share the k-th key's 16-bit prefix (unless too many do).
+        const bool pre16 = nb <= P16_CAP;
+        uint16_t* const p16 = reinterpret_cast<uint16_t*>(keys);
         clear_hist();
         bool ok = stream_row(srow, nb, ring, bar0, seq, [&](const float* piece, int base, int n) {
-            for (int j = tid; j < n; j += THREADS) atomicAdd(&hist[order_key(piece[j]) >> 21], 1u);
+            for (int j = tid; j < n; j += THREADS) {
+                const uint32_t k = order_key(piece[j]);
+                if (pre16) p16[base + j] = static_cast<uint16_t>(k >> 16);
+                atomicAdd(&hist[k >> 21], 1u);
+            }
         });
         if (!ok) return timed_out();
         __syncthreads();
@@ -451,7 +463,71 @@ __global__ void __launch_bounds__(THREADS, 1) topk_expand_kernel(const Params p)
         const int cand = static_cast<int>(hist[d1]); // keys in the bin of the k-th key
         need -= d.y;
         __syncthreads();
-        if (cand <= KEYS_CAP) {
+        bool done = false;
+        if (pre16) {
+            // key bits 20..16 of the blocks in bin d1, counted from the prefixes
+            if (tid < 32) hist[tid] = 0u;
+            __syncthreads();
+            for (int i = tid; i < nb; i += THREADS) {
+                const uint32_t v = p16[i];
+                if ((v >> 5) == d1) atomicAdd(&hist[v & 31u], 1u);
+            }
+            __syncthreads();
+            if (warp == 0) { // the 5-bit digit (from the top) that holds the need-th key
+                const int bin = 31 - lane;
+                const int cnt = static_cast<int>(hist[bin]);
+                int incl = cnt;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int v = __shfl_up_sync(FULL, incl, o);
+                    if (lane >= o) incl += v;
+                }
+                if (incl - cnt < need && need <= incl) {
+                    sh[0] = bin;
+                    sh[1] = incl - cnt;
+                    sh[2] = cnt;
+                }
+            }
+            __syncthreads();
+            const uint32_t P = (d1 << 5) | static_cast<uint32_t>(sh[0]);
+            const int nc = sh[2]; // blocks whose key has the prefix P
+            if (nc <= CAND_CAP) {
+                int needc = need - sh[1];
+                uint32_t* const ck = keys + P16_CAP / 2;
+                // the candidates' full keys, in index order (one score read each)
+                int ca = 0, cs = 0;
+                for (int base = 0; base < nb; base += PIECE)
+                    scan_piece(min(PIECE, nb - base), [&](int j) { return static_cast<uint32_t>(p16[base + j]); },
+                               [&](uint32_t) { return false; },
+                               [&](uint32_t v, bool, int) { return v == P; },
+                               [&](int j, int rank) { ck[rank] = order_key(__ldg(srow + base + j)); }, ca, cs,
+                               wsum);
+                __syncthreads();
+                uint32_t pfx = P << 16, msk = 0xFFFF0000u;
+                select_in_smem(ck, nc, pfx, msk, needc);
+                const uint32_t thr = pfx;
+                // mark the kept candidates (ties: the first needc in index order)
+                ca = cs = 0;
+                for (int base = 0; base < nc; base += PIECE)
+                    scan_piece(min(PIECE, nc - base), [&](int j) { return ck[base + j]; },
+                               [&](uint32_t k) { return k == thr; },
+                               [&](uint32_t k, bool eq, int rank) { return k > thr || (eq && rank < needc); },
+                               [&](int j, int) { ck[base + j] = KEPT; }, ca, cs, wsum);
+                __syncthreads();
+                // the compaction over the prefixes: above P kept, at P by the flag
+                ca = cs = 0;
+                for (int base = 0; base < nb; base += PIECE)
+                    scan_piece(min(PIECE, nb - base), [&](int j) { return static_cast<uint32_t>(p16[base + j]); },
+                               [&](uint32_t v) { return v == P; },
+                               [&](uint32_t v, bool isc, int rank) { return v > P || (isc && ck[rank] == KEPT); },
+                               [&](int j, int rank) { put_block(base + j, rank); }, ca, cs, wsum);
+                done = true;
+            }
+            __syncthreads();
+        }
+        if (done) {
+            // selected from the prefixes and candidates
+        } else if (cand <= KEYS_CAP) {
             // gather that bin's keys, in index order, into shared memory
             int ca = 0, cs = 0;
             ok = stream_row(srow, nb, ring, bar0, seq, [&](const float* piece, int base, int n) {
@@ -466,7 +542,7 @@ __global__ void __launch_bounds__(THREADS, 1) topk_expand_kernel(const Params p)
             __syncthreads();
             prefix = d1 << 21;
             mask = 0x7FFu << 21;
-            select_in_smem(cand, prefix, mask, need);
+            select_in_smem(keys, cand, prefix, mask, need);
             const uint32_t thr = prefix;
             // mark the kept keys of the bin (ties: the first `need` in index order) with
             // 0xFFFFFFFF, a value order_key never returns; a piece's keys are all read
