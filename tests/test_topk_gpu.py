@@ -204,18 +204,30 @@ def test_topk_feeds_the_decode_in_one_graph(cuda_device):
 
 def test_long_rows_through_every_path(cuda_device):
     """256K contexts (65,536 blocks at ratio 4, 262,144 at ratio 1), longer than the
-    kernel keeps in shared memory: N(0,1) scores take the gathered-bin path; scores
-    in [1, 1.25) share their top 11 bits, so the bin of the k-th key holds every
-    block and the kernel streams every pass instead."""
+    kernel keeps as keys in shared memory. At ratio 4 the first pass also keeps the
+    keys' top 16 bits: N(0,1) scores, and scores in [1, 1.25) with ties, leave few
+    enough blocks on the k-th key's 16-bit prefix to select from those; 20,000
+    scores within 2^-12 of 2 (one 16-bit prefix, the top of the row) take the
+    gathered-bin path; scores all within 2^-12 of 1 (every block in one 11-bit bin)
+    stream every pass. At ratio 1 (no prefixes) N(0,1) scores take the gathered
+    bin."""
     cap = I.TOPK_CAPACITY
     g = torch.Generator(device=cuda_device).manual_seed(3)
-    for ratio, topk, crowded in ((4, 2048, False), (4, 2048, True), (1, 2048, False)):
+    for ratio, topk, kind in ((4, 2048, "normal"), (4, 2048, "crowded"), (4, 2048, "top_cluster"),
+                              (4, 2048, "one_bin"), (1, 2048, "normal")):
         bs = 2
-        if crowded:
-            scores = 1.0 + 0.25 * torch.rand(bs, cap // ratio, generator=g, device=cuda_device)
+        nbk = cap // ratio
+        if kind == "crowded":
+            scores = 1.0 + 0.25 * torch.rand(bs, nbk, generator=g, device=cuda_device)
             scores[:, ::1000] = 1.125     # and ties inside the crowded bin
+        elif kind == "top_cluster":
+            scores = torch.randn(bs, nbk, generator=g, device=cuda_device).clamp(-4.0, 1.0)
+            idx = torch.randperm(nbk, generator=g, device=cuda_device)[:20000]
+            scores[:, idx] = 2.0 + 2.0 ** -12 * torch.rand(bs, 20000, generator=g, device=cuda_device)
+        elif kind == "one_bin":
+            scores = 1.0 + 2.0 ** -12 * torch.rand(bs, nbk, generator=g, device=cuda_device)
         else:
-            scores = I.block_scores(bs, cap // ratio, 31 + ratio, cuda_device)
+            scores = I.block_scores(bs, nbk, 31 + ratio, cuda_device)
         lens = torch.tensor([cap, cap - 2], dtype=torch.int32, device=cuda_device)
         sel, cu = _run(scores, lens, topk, ratio, cap)
         torch.cuda.synchronize()
