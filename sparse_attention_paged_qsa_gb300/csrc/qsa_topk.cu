@@ -27,16 +27,20 @@
 //    of the digit (shared-memory atomics) and a descending scan over its bins
 //    give the digit that holds the k-th key. A row of at most KEYS_CAP blocks is
 //    kept as keys in shared memory after the first streaming pass, and the
-//    other passes and the compaction run there. A longer row (the 256K context
-//    at ratio 4: 65,536 blocks) streams once for the top digit's histogram,
-//    once to gather the keys of the bin that holds the k-th key (in index
-//    order) into shared memory -- the rest of the selection runs on those --
-//    and once more for the compaction; rows whose bin is too large fall back to
-//    streaming every pass.
-//  * Compaction in index order: per 4096-block piece each warp takes 8 rounds of
-//    32; ballots give every block its rank among the threshold ties (or the
-//    gathered bin) and among the kept blocks, warp totals a block-wide prefix. A
-//    kept block's r token slots go straight to its place in the packed row.
+//    other passes and the compaction run there. A longer row of up to 65,536
+//    blocks (the 256K context at ratio 4) keeps each key's top 16 bits in shared
+//    memory during its one streaming pass; from those, the blocks whose top
+//    digit is the k-th key's or above (about k + one bin) are gathered in index
+//    order and only their scores are read again. Rows where those are too many,
+//    or longer rows, stream again to gather the k-th key's bin, and rows whose
+//    bin is too large stream every pass.
+//  * Compaction in index order. Over keys in shared memory each warp takes one
+//    contiguous run, a lane 4 keys per 16-byte load: one pass counts the keys
+//    above the threshold and the ties, one block-wide prefix, one pass emits.
+//    Over streamed pieces, per 4096-block piece each warp takes 8 rounds of 32;
+//    ballots give every block its rank among the ties (or the gathered bin) and
+//    among the kept blocks, warp totals a block-wide prefix. The kept blocks'
+//    r token slots are written after the selection, all blocks at once.
 //  * Each CTA computes its row's offset from the context lengths of the rows
 //    before it, so the whole step is one launch with no host readback, and a
 //    captured graph stays valid when the lengths and scores change.
@@ -65,7 +69,7 @@ constexpr int MAX_ROW = 2055;                  // the decode's selected-KV capac
 constexpr unsigned FULL = 0xFFFFFFFFu;
 constexpr int NBINS = 2048;                    // bins of an 11-bit digit
 constexpr int P16_CAP = 65536;                 // blocks whose 16-bit key prefixes fit the key area
-constexpr int CAND_CAP = KEYS_CAP - P16_CAP / 2; // candidate keys kept next to those prefixes
+constexpr int CAND_CAP = KEYS_CAP - P16_CAP / 2; // gathered block indices kept next to those prefixes
 constexpr long long WAIT_NS = 2000000000LL;    // bounded-wait limit (2 s)
 constexpr uint32_t KEPT = 0xFFFFFFFFu;         // not a key: order_key maps every NaN to 0
 // dynamic shared memory: the two ring slots, the keys, the histogram
@@ -76,7 +80,9 @@ constexpr int OFF_KEPT = OFF_HIST + NBINS * 4;           // kept block index by 
 constexpr int SMEM_BYTES = OFF_KEPT + (MAX_ROW + 1) * 4;
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 static_assert(NBINS % THREADS == 0 && NBINS / THREADS <= 4, "digit scan");
+static_assert(ROUNDS % 4 == 0 && PIECE % 4096 == 0, "16-byte first-pass accesses stay aligned");
 static_assert(CAND_CAP > 0 && P16_CAP % 2 == 0, "prefix and candidate areas");
+static_assert(P16_CAP / 32 <= MAX_ROW + 1 && P16_CAP <= 128 * THREADS, "prefix bitmap in the kept-list area");
 
 struct Params {
     const float* scores;
@@ -122,12 +128,16 @@ __device__ __forceinline__ unsigned long long globaltimer() {
     return t;
 }
 // Wait for the phase with `parity` of an mbarrier for at most WAIT_NS.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity) {
     const unsigned long long t0 = globaltimer();
     for (uint32_t it = 0;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 63) == 63 && globaltimer() - t0 > (unsigned long long)WAIT_NS) return false;
     }
+}
+// The timer is read only when the first try does not see the phase complete.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    return mbar_try_wait(bar, parity) || mbar_wait_slow(bar, parity);
 }
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
     asm volatile(
@@ -269,6 +279,163 @@ __device__ __forceinline__ void scan_piece(int n, KeyAt key_at, IsA is_a, Decide
     carry_s += ps.y;
 }
 
+// Index-ordered compaction of n keys in shared memory: every key above thr and
+// the first need_t keys equal to thr go to emit(i, rank), rank counted among the
+// emitted keys in index order. Each warp takes one contiguous run of 4-key
+// chunks, a lane one chunk per 16-byte load, so the whole array takes a single
+// block-wide prefix of the warps' counts, packed as (above << 16) | equal: fewer
+// than k <= 2048 keys lie above thr, and n < 65536.
+template <class Emit>
+__device__ __forceinline__ void compact_keys(const uint32_t* kk, int n, uint32_t thr, int need_t, Emit emit,
+                                             int* wsum) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int chunks = (n + 3) >> 2;
+    const int per = (((chunks + WARPS - 1) / WARPS) + 31) & ~31;
+    const int c0 = min(chunks, warp * per), c1 = min(chunks, c0 + per);
+    const uint4* const kv = reinterpret_cast<const uint4*>(kk);
+    auto count = [&](const uint4& v, int i) {
+        const uint32_t k[4] = {v.x, v.y, v.z, v.w};
+        int s = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            if (i + q < n) s += k[q] > thr ? 0x10000 : (k[q] == thr ? 1 : 0);
+        return s;
+    };
+    int cnt = 0;
+#pragma unroll 4
+    for (int c = c0 + lane; c < c1; c += 32) cnt += count(kv[c], 4 * c);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(FULL, cnt, o);
+    int before = block_prefix(cnt, wsum).x;
+    for (int cb = c0; cb < c1; cb += 32) { // warp-uniform bounds
+        const int c = cb + lane;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        int my = 0;
+        if (c < c1) {
+            v = kv[c];
+            my = count(v, 4 * c);
+        }
+        int incl = my;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(FULL, incl, o);
+            if (lane >= o) incl += t;
+        }
+        if (my != 0) {
+            const int at0 = before + incl - my;
+            int above = at0 >> 16, at = at0 & 0xFFFF;
+            const uint32_t k[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int i = 4 * c + q;
+                if (i < n && k[q] > thr) {
+                    emit(i, above + min(at, need_t));
+                    ++above;
+                } else if (i < n && k[q] == thr) {
+                    if (at < need_t) emit(i, above + at);
+                    ++at;
+                }
+            }
+        }
+        before += __shfl_sync(FULL, incl, 31);
+    }
+}
+
+// A bitmap of the n <= 128 * THREADS 16-bit key prefixes in shared memory that
+// are >= t, in index order: bit b of bm[w] for prefix 32w + b. A thread takes
+// 8 adjacent prefixes per 16-byte load (units tid, tid + THREADS, ... , 4 in
+// flight) and stores their 8 bits as one byte (bits past n are zero through the
+// end of the last word). Ends with a barrier.
+__device__ __forceinline__ void bitmap_ge16(const uint16_t* p16, int n, uint32_t t, uint32_t* bm) {
+    const int tid = threadIdx.x;
+    const int units = (n + 7) >> 3, nbytes = ((n + 31) >> 5) * 4; // whole words, zero past n
+    const uint4* const pv = reinterpret_cast<const uint4*>(p16);
+    uint8_t* const bb = reinterpret_cast<uint8_t*>(bm);
+    const uint32_t T = t << 16; // a word is >= T when its upper prefix is >= t
+    auto bits2 = [&](uint32_t w) { // the word's lower prefix in bit 0, upper in bit 1
+        return static_cast<uint32_t>((w << 16) >= T) | (static_cast<uint32_t>(w >= T) << 1);
+    };
+#pragma unroll 4
+    for (int u = tid; u < nbytes; u += THREADS) {
+        uint32_t m = 0u;
+        if (u < units) {
+            const uint4 v = pv[u];
+            m = bits2(v.x) | (bits2(v.y) << 2) | (bits2(v.z) << 4) | (bits2(v.w) << 6);
+            const int left = n - 8 * u; // prefixes of this unit inside the row (>= 1)
+            if (left < 8) m &= (1u << left) - 1u;
+        }
+        bb[u] = static_cast<uint8_t>(m);
+    }
+    __syncthreads();
+}
+
+// The same bitmap of the n <= 128 * THREADS 32-bit keys in shared memory that
+// are >= t, a thread taking 4 adjacent keys per 16-byte load and storing their 4
+// bits in one half of a byte; two threads' halves share a byte, so the pair
+// combine theirs by shuffle and the even one stores it (bits past n are zero
+// through the end of the last word). Ends with a barrier.
+__device__ __forceinline__ void bitmap_ge32(const uint32_t* kk, int n, uint32_t t, uint32_t* bm) {
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int quads = (n + 3) >> 2, nquads = ((n + 31) >> 5) * 8; // whole words, zero past n
+    const int rounds = (nquads + THREADS - 1) / THREADS;
+    const uint4* const kv = reinterpret_cast<const uint4*>(kk);
+    uint8_t* const bb = reinterpret_cast<uint8_t*>(bm);
+#pragma unroll 4
+    for (int r = 0; r < rounds; ++r) { // uniform trip count: the shuffle sees the whole warp
+        const int u = r * THREADS + tid;
+        uint32_t m = 0u;
+        if (u < quads) {
+            const uint4 v = kv[u];
+            m = static_cast<uint32_t>(v.x >= t) | (static_cast<uint32_t>(v.y >= t) << 1) |
+                (static_cast<uint32_t>(v.z >= t) << 2) | (static_cast<uint32_t>(v.w >= t) << 3);
+            const int left = n - 4 * u;
+            if (left < 4) m &= (1u << left) - 1u;
+        }
+        const uint32_t hi = __shfl_down_sync(FULL, m, 1);
+        if ((lane & 1) == 0 && u < nquads) bb[u >> 1] = static_cast<uint8_t>(m | (hi << 4));
+    }
+    __syncthreads();
+}
+
+// The set bits of a bitmap over n <= 128 * THREADS positions, in index order:
+// each thread takes up to 4 consecutive words, their popcounts take one
+// block-wide prefix, and when the total lies in [lo, cap] each set position goes
+// to out[rank]. Returns the total.
+__device__ __forceinline__ int emit_bitmap(const uint32_t* bm, int n, int lo, int cap, uint32_t* out,
+                                           int* wsum) {
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int words = (n + 31) >> 5, per = (words + THREADS - 1) / THREADS;
+    const int w0 = min(words, tid * per), w1 = min(words, w0 + per);
+    int cnt = 0;
+    for (int w = w0; w < w1; ++w) cnt += __popc(bm[w]);
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int x = __shfl_up_sync(FULL, incl, o);
+        if (lane >= o) incl += x;
+    }
+    const int2 pw = block_prefix(__shfl_sync(FULL, incl, 31), wsum);
+    if (pw.y >= lo && pw.y <= cap) {
+        int rank = pw.x + incl - cnt;
+        for (int w = w0; w < w1; ++w) {
+            uint32_t m = bm[w];
+            while (m != 0u) {
+                const int bit = __ffs(m) - 1;
+                m &= m - 1u;
+                out[rank++] = static_cast<uint32_t>(w * 32 + bit);
+            }
+        }
+    }
+    return pw.y;
+}
+
+// Index-ordered gather of the prefixes >= t (see bitmap_ge16 and emit_bitmap).
+__device__ __forceinline__ int gather_ge16(const uint16_t* p16, int n, uint32_t t, uint32_t* bm, uint32_t* out,
+                                           int cap, int* wsum) {
+    bitmap_ge16(p16, n, t, bm);
+    return emit_bitmap(bm, n, 0, cap, out, wsum);
+}
+
 // Streams the first nb scores of a row through the two-slot ring, one PIECE at a
 // time, calling fn(piece, base, n) with the piece in shared memory (n floats at
 // row positions base .. base + n - 1). Thread 0 keeps the next piece in flight.
@@ -301,8 +468,10 @@ __device__ bool stream_row(const float* srow, int nb, float* ring, uint32_t bar0
         }
         float* const piece = ring + slot * PIECE;
         const int n = min(PIECE, nb - c * PIECE), al = n & ~3;
-        if (tid < n - al) piece[al + tid] = srow[(long long)c * PIECE + al + tid]; // unaligned end
-        __syncthreads();
+        if (n != al) { // the unaligned end (uniform)
+            if (tid < n - al) piece[al + tid] = srow[(long long)c * PIECE + al + tid];
+            __syncthreads();
+        }
         fn(piece, c * PIECE, n);
         __syncthreads(); // the slot's readers are done
         if (tid == 0 && c + 2 < pieces) {
@@ -421,10 +590,26 @@ __global__ void __launch_bounds__(THREADS, 1) topk_expand_kernel(const Params p)
         // ------------------------------------------------ the row fits: keys in shared memory
         clear_hist();
         const bool ok = stream_row(srow, nb, ring, bar0, seq, [&](const float* piece, int base, int n) {
-            for (int j = tid; j < n; j += THREADS) {
-                const uint32_t k = order_key(piece[j]);
-                keys[base + j] = k;
-                atomicAdd(&hist[k >> 21], 1u);
+            if (n == PIECE) { // 16-byte loads and stores: a thread takes 4 adjacent blocks
+                float4 x[ROUNDS / 4];
+#pragma unroll
+                for (int e = 0; e < ROUNDS / 4; ++e) x[e] = reinterpret_cast<const float4*>(piece)[tid + e * THREADS];
+#pragma unroll
+                for (int e = 0; e < ROUNDS / 4; ++e) {
+                    const uint4 k = make_uint4(order_key(x[e].x), order_key(x[e].y), order_key(x[e].z),
+                                               order_key(x[e].w));
+                    reinterpret_cast<uint4*>(keys + base)[tid + e * THREADS] = k;
+                    atomicAdd(&hist[k.x >> 21], 1u);
+                    atomicAdd(&hist[k.y >> 21], 1u);
+                    atomicAdd(&hist[k.z >> 21], 1u);
+                    atomicAdd(&hist[k.w >> 21], 1u);
+                }
+            } else {
+                for (int j = tid; j < n; j += THREADS) {
+                    const uint32_t k = order_key(piece[j]);
+                    keys[base + j] = k;
+                    atomicAdd(&hist[k >> 21], 1u);
+                }
             }
         });
         if (!ok) return timed_out();
@@ -433,27 +618,60 @@ __global__ void __launch_bounds__(THREADS, 1) topk_expand_kernel(const Params p)
         prefix = static_cast<uint32_t>(d.x) << 21;
         mask = 0x7FFu << 21;
         need -= d.y;
-        select_in_smem(keys, nb, prefix, mask, need);
-        const uint32_t thr = prefix;
-        int ca = 0, cs = 0;
-        for (int base = 0; base < nb; base += PIECE)
-            scan_piece(min(PIECE, nb - base), [&](int j) { return keys[base + j]; },
-                       [&](uint32_t k) { return k == thr; },
-                       [&](uint32_t k, bool eq, int rank) { return k > thr || (eq && rank < need); },
-                       [&](int j, int rank) { put_block(base + j, rank); }, ca, cs, wsum);
+        // (16-byte aligned areas: compact_keys reads 4 keys at a time)
+        const int nb4 = (nb + 3) & ~3, ng = d.y + static_cast<int>(hist[d.x & (NBINS - 1)]);
+        const int ng4 = (ng + 3) & ~3;
+        __syncthreads();
+        if (nb4 + 2 * ng4 <= KEYS_CAP && 16 * ng <= nb) {
+            // the blocks whose top digit is the k-th key's or above, in index order
+            // (their indices, then their keys, past the row's keys); the rest of the
+            // selection runs on those. Only when they are few: a thread emits a
+            // 128-block group's indices one by one.
+            uint32_t* const gl = keys + nb4;
+            uint32_t* const ck = gl + ng4;
+            bitmap_ge32(keys, nb, prefix, reinterpret_cast<uint32_t*>(kept));
+            emit_bitmap(reinterpret_cast<uint32_t*>(kept), nb, 0, ng, gl, wsum);
+            __syncthreads();
+            for (int g = tid; g < ng; g += THREADS) ck[g] = keys[gl[g]];
+            __syncthreads();
+            select_in_smem(ck, ng, prefix, mask, need);
+            compact_keys(ck, ng, prefix, need, [&](int g, int rank) { put_block(static_cast<int>(gl[g]), rank); },
+                         wsum);
+        } else {
+            select_in_smem(keys, nb, prefix, mask, need);
+            compact_keys(keys, nb, prefix, need, put_block, wsum);
+        }
     } else {
         // ------------------------------------------------ a long row: stream the passes
         // Up to P16_CAP blocks, the first pass also keeps every key's top 16 bits in
         // shared memory; the rest of the selection then reads only the scores of the
-        // blocks that share the k-th key's 16-bit prefix (unless too many do).
+        // blocks whose top digit is the k-th key's or above (unless too many are).
         const bool pre16 = nb <= P16_CAP;
         uint16_t* const p16 = reinterpret_cast<uint16_t*>(keys);
         clear_hist();
         bool ok = stream_row(srow, nb, ring, bar0, seq, [&](const float* piece, int base, int n) {
-            for (int j = tid; j < n; j += THREADS) {
-                const uint32_t k = order_key(piece[j]);
-                if (pre16) p16[base + j] = static_cast<uint16_t>(k >> 16);
-                atomicAdd(&hist[k >> 21], 1u);
+            if (n == PIECE) { // 16-byte loads, 8-byte prefix stores: a thread takes 4 adjacent blocks
+                float4 x[ROUNDS / 4];
+#pragma unroll
+                for (int e = 0; e < ROUNDS / 4; ++e) x[e] = reinterpret_cast<const float4*>(piece)[tid + e * THREADS];
+#pragma unroll
+                for (int e = 0; e < ROUNDS / 4; ++e) {
+                    const uint32_t k0 = order_key(x[e].x), k1 = order_key(x[e].y), k2 = order_key(x[e].z),
+                                   k3 = order_key(x[e].w);
+                    if (pre16) // the lower index in the lower half of each word
+                        reinterpret_cast<uint2*>(p16 + base)[tid + e * THREADS] =
+                            make_uint2((k0 >> 16) | (k1 & 0xFFFF0000u), (k2 >> 16) | (k3 & 0xFFFF0000u));
+                    atomicAdd(&hist[k0 >> 21], 1u);
+                    atomicAdd(&hist[k1 >> 21], 1u);
+                    atomicAdd(&hist[k2 >> 21], 1u);
+                    atomicAdd(&hist[k3 >> 21], 1u);
+                }
+            } else {
+                for (int j = tid; j < n; j += THREADS) {
+                    const uint32_t k = order_key(piece[j]);
+                    if (pre16) p16[base + j] = static_cast<uint16_t>(k >> 16);
+                    atomicAdd(&hist[k >> 21], 1u);
+                }
             }
         });
         if (!ok) return timed_out();
@@ -465,68 +683,60 @@ __global__ void __launch_bounds__(THREADS, 1) topk_expand_kernel(const Params p)
         __syncthreads();
         bool done = false;
         if (pre16) {
-            // key bits 20..16 of the blocks in bin d1, counted from the prefixes
-            if (tid < 32) hist[tid] = 0u;
-            __syncthreads();
-            for (int i = tid; i < nb; i += THREADS) {
-                const uint32_t v = p16[i];
-                if ((v >> 5) == d1) atomicAdd(&hist[v & 31u], 1u);
-            }
-            __syncthreads();
-            if (warp == 0) { // the 5-bit digit (from the top) that holds the need-th key
-                const int bin = 31 - lane;
-                const int cnt = static_cast<int>(hist[bin]);
-                int incl = cnt;
+            // Gather, in index order, every block whose key prefix is at or above
+            // t16: the kept ones and the rest of the k-th key's bin. The bin is the
+            // top 11-bit digit d1, or, when that leaves too many blocks, the 16-bit
+            // prefix below it that holds the k-th key.
+            uint32_t t16 = d1 << 5, pfx = d1 << 21, msk = 0x7FFu << 21;
+            int ng = d.y + cand, needg = need;
+            if (ng > CAND_CAP) {
+                // key bits 20..16 of the blocks in bin d1, counted from the prefixes
+                if (tid < 32) hist[tid] = 0u;
+                __syncthreads();
+                for (int i = tid; i < nb; i += THREADS) {
+                    const uint32_t v = p16[i];
+                    if ((v >> 5) == d1) atomicAdd(&hist[v & 31u], 1u);
+                }
+                __syncthreads();
+                if (warp == 0) { // the 5-bit digit (from the top) that holds the need-th key
+                    const int bin = 31 - lane;
+                    const int cnt = static_cast<int>(hist[bin]);
+                    int incl = cnt;
 #pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const int v = __shfl_up_sync(FULL, incl, o);
-                    if (lane >= o) incl += v;
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const int v = __shfl_up_sync(FULL, incl, o);
+                        if (lane >= o) incl += v;
+                    }
+                    if (incl - cnt < need && need <= incl) {
+                        sh[0] = bin;
+                        sh[1] = incl - cnt;
+                        sh[2] = cnt;
+                    }
                 }
-                if (incl - cnt < need && need <= incl) {
-                    sh[0] = bin;
-                    sh[1] = incl - cnt;
-                    sh[2] = cnt;
-                }
+                __syncthreads();
+                t16 = (d1 << 5) | static_cast<uint32_t>(sh[0]);
+                pfx = t16 << 16;
+                msk = 0xFFFF0000u;
+                needg = need - sh[1];
+                ng = d.y + sh[1] + sh[2];
+                __syncthreads();
             }
-            __syncthreads();
-            const uint32_t P = (d1 << 5) | static_cast<uint32_t>(sh[0]);
-            const int nc = sh[2]; // blocks whose key has the prefix P
-            if (nc <= CAND_CAP) {
-                int needc = need - sh[1];
-                uint32_t* const ck = keys + P16_CAP / 2;
-                // the candidates' full keys, in index order (one score read each)
-                int ca = 0, cs = 0;
-                for (int base = 0; base < nb; base += PIECE)
-                    scan_piece(min(PIECE, nb - base), [&](int j) { return static_cast<uint32_t>(p16[base + j]); },
-                               [&](uint32_t) { return false; },
-                               [&](uint32_t v, bool, int) { return v == P; },
-                               [&](int j, int rank) { ck[rank] = order_key(__ldg(srow + base + j)); }, ca, cs,
-                               wsum);
+            if (ng <= CAND_CAP) {
+                uint32_t* const gl = keys + P16_CAP / 2;
+                // (the bitmap in the kept-list area, free until the compaction)
+                const int n = gather_ge16(p16, nb, t16, reinterpret_cast<uint32_t*>(kept), gl, CAND_CAP, wsum);
                 __syncthreads();
-                uint32_t pfx = P << 16, msk = 0xFFFF0000u;
-                select_in_smem(ck, nc, pfx, msk, needc);
-                const uint32_t thr = pfx;
-                // mark the kept candidates (ties: the first needc in index order)
-                ca = cs = 0;
-                for (int base = 0; base < nc; base += PIECE)
-                    scan_piece(min(PIECE, nc - base), [&](int j) { return ck[base + j]; },
-                               [&](uint32_t k) { return k == thr; },
-                               [&](uint32_t k, bool eq, int rank) { return k > thr || (eq && rank < needc); },
-                               [&](int j, int) { ck[base + j] = KEPT; }, ca, cs, wsum);
+                // their full keys, one score read each, over the prefixes (no longer read)
+                for (int g = tid; g < n; g += THREADS) keys[g] = order_key(__ldg(srow + gl[g]));
                 __syncthreads();
-                // the compaction over the prefixes: above P kept, at P by the flag
-                ca = cs = 0;
-                for (int base = 0; base < nb; base += PIECE)
-                    scan_piece(min(PIECE, nb - base), [&](int j) { return static_cast<uint32_t>(p16[base + j]); },
-                               [&](uint32_t v) { return v == P; },
-                               [&](uint32_t v, bool isc, int rank) { return v > P || (isc && ck[rank] == KEPT); },
-                               [&](int j, int rank) { put_block(base + j, rank); }, ca, cs, wsum);
+                select_in_smem(keys, n, pfx, msk, needg);
+                compact_keys(keys, n, pfx, needg,
+                             [&](int g, int rank) { put_block(static_cast<int>(gl[g]), rank); }, wsum);
                 done = true;
             }
-            __syncthreads();
         }
         if (done) {
-            // selected from the prefixes and candidates
+            // selected from the prefixes and the gathered keys
         } else if (cand <= KEYS_CAP) {
             // gather that bin's keys, in index order, into shared memory
             int ca = 0, cs = 0;

@@ -112,6 +112,28 @@ def test_error_flags_clamp_and_do_not_fault(cuda_device):
     assert np.array_equal(got[~bad_pos], want_sel[~bad_pos])
 
 
+def test_sorted_rows_bound_the_first_pass(cuda_device):
+    """The first pass stops counting keys below the bin of the first 4096 blocks'
+    k-th key once it knows it. Rows sorted descending (the first piece holds the
+    row's top keys: the bound is the row's own digit), ascending (the lowest
+    bound) and with the top keys only at the end, at 256K contexts through the
+    short path (ratio 8), the prefix path (ratio 4) and the no-prefix path (ratio 1)."""
+    cap = I.TOPK_CAPACITY
+    for ratio, topk in ((8, 2048), (4, 2048), (1, 2048)):
+        nbk = cap // ratio
+        base = I.block_scores(1, nbk, 40 + ratio, cuda_device, specials=False)[0]
+        srt = torch.sort(base, descending=True).values
+        late = base.clone()
+        late[-3000:] = 5.0 + torch.arange(3000, device=cuda_device, dtype=torch.float32) * 1e-3
+        scores = torch.stack([srt, srt.flip(0), late, base])
+        # the last: a length whose block count leaves the last bitmap word partly
+        # past the row at ratios 4 and 8
+        lens = torch.tensor([cap, cap - 3, cap, cap - 8 * 101 - 5], dtype=torch.int32, device=cuda_device)
+        sel, cu = _run(scores, lens, topk, ratio, cap)
+        torch.cuda.synchronize()
+        _check(sel, cu, scores, lens, topk, ratio, cap)
+
+
 def test_changing_replay_index_equality_in_a_graph(cuda_device):
     """One captured graph: regenerate context lengths and scores on the device from
     the replay counter, then top-k + expansion; 60 replays, every fifth checked
@@ -205,12 +227,13 @@ def test_topk_feeds_the_decode_in_one_graph(cuda_device):
 def test_long_rows_through_every_path(cuda_device):
     """256K contexts (65,536 blocks at ratio 4, 262,144 at ratio 1), longer than the
     kernel keeps as keys in shared memory. At ratio 4 the first pass also keeps the
-    keys' top 16 bits: N(0,1) scores, and scores in [1, 1.25) with ties, leave few
-    enough blocks on the k-th key's 16-bit prefix to select from those; 20,000
-    scores within 2^-12 of 2 (one 16-bit prefix, the top of the row) take the
-    gathered-bin path; scores all within 2^-12 of 1 (every block in one 11-bit bin)
-    stream every pass. At ratio 1 (no prefixes) N(0,1) scores take the gathered
-    bin."""
+    keys' top 16 bits: N(0,1) scores leave few enough blocks at or above the k-th
+    key's top 11-bit digit to gather those from the prefixes; scores in [1, 1.25)
+    with ties (one 11-bit digit) gather from the k-th key's 16-bit prefix instead;
+    20,000 scores within 2^-12 of 2 (one 16-bit prefix, the top of the row) take
+    the gathered-bin path; scores all within 2^-12 of 1 (every block in one 11-bit
+    bin) stream every pass. At ratio 1 (no prefixes) N(0,1) scores take the
+    gathered bin."""
     cap = I.TOPK_CAPACITY
     g = torch.Generator(device=cuda_device).manual_seed(3)
     for ratio, topk, kind in ((4, 2048, "normal"), (4, 2048, "crowded"), (4, 2048, "top_cluster"),
