@@ -496,6 +496,8 @@ __global__ void __launch_bounds__(THREADS, 1) topk_expand_kernel(const Params p)
     __shared__ __align__(8) uint64_t bars[2];
     __shared__ int wsum[WARPS];
     __shared__ int sh[4];
+    __shared__ uint32_t few[32]; // the last radix pass's keys, when at most 32
+    __shared__ int nfew;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int b = blockIdx.x;
     const uint32_t bar0 = smem_u32(bars);
@@ -568,10 +570,15 @@ __global__ void __launch_bounds__(THREADS, 1) topk_expand_kernel(const Params p)
         }
     };
     // radix passes 1 and 2 (digits of 11 and 10 bits) over keys in shared memory
+    // radix passes 1 and 2 (digits of 11 and 10 bits) over keys in shared memory.
+    // When at most 32 keys are left for pass 2 (usually one or two), they are
+    // collected instead and one warp ranks them: the need-th largest is the key
+    // with fewer than need keys above it and at least need at or above it.
     auto select_in_smem = [&](const uint32_t* kk, int n, uint32_t& prefix, uint32_t& mask, int& need) {
         for (int pass = 1; pass < 3; ++pass) {
             const int shift = pass == 1 ? 10 : 0, bins = pass == 1 ? 2048 : 1024;
             clear_hist();
+            if (tid == 0) nfew = 0;
             for (int i = tid; i < n; i += THREADS) {
                 const uint32_t k = kk[i];
                 if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & (bins - 1)], 1u);
@@ -581,6 +588,38 @@ __global__ void __launch_bounds__(THREADS, 1) topk_expand_kernel(const Params p)
             prefix |= static_cast<uint32_t>(d.x) << shift;
             mask |= static_cast<uint32_t>(bins - 1) << shift;
             need -= d.y;
+            const int left = static_cast<int>(hist[d.x & (bins - 1)]); // keys matching the prefix now
+            __syncthreads();                                               // read before pass 2 clears it
+            if (pass == 1 && left <= 32) { // uniform
+                for (int i = tid; i < n; i += THREADS) {
+                    const uint32_t k = kk[i];
+                    if ((k & mask) == prefix) few[atomicAdd(&nfew, 1)] = k;
+                }
+                __syncthreads();
+                if (warp == 0) {
+                    const uint32_t k = lane < left ? few[lane] : 0u;
+                    int above = 0, at = 0;
+                    for (int j = 0; j < left; ++j) {
+                        const uint32_t o = few[j];
+                        above += o > k ? 1 : 0;
+                        at += o >= k ? 1 : 0;
+                    }
+                    const uint32_t hit = __ballot_sync(FULL, lane < left && above < need && need <= at);
+                    const int src = __ffs(hit) - 1;
+                    const uint32_t key = __shfl_sync(FULL, k, src);
+                    const int ab = __shfl_sync(FULL, above, src);
+                    if (lane == 0) {
+                        sh[2] = static_cast<int>(key);
+                        sh[3] = ab;
+                    }
+                }
+                __syncthreads();
+                prefix = static_cast<uint32_t>(sh[2]);
+                mask = 0xFFFFFFFFu;
+                need -= sh[3];
+                __syncthreads();
+                break;
+            }
         }
     };
 
