@@ -587,9 +587,12 @@ def measure_topk(args, dev, peak):
     n = max(min(args.steps, 200), 1)
     stream = torch.cuda.current_stream()
     rows = []
+    only = getattr(args, "topk_point", None)
     for cap in (8192, I.TOPK_CAPACITY):
         for bs in (1, BS):
             for ratio in (4, 8, 16):
+                if only is not None and (cap, bs, ratio) != only:
+                    continue
                 topk = I.topk_budget(ratio)
                 sets = [I.block_scores(bs, cap // ratio, 100 + k, dev, specials=False)
                         for k in range(2)]
@@ -627,19 +630,25 @@ def run_topk(args):
     pts = measure_topk(args, dev, peak)
     clocks = clk.summary(t0, time.perf_counter())
     clk.__exit__()
-    head = next(p for p in pts if p["context"] == I.TOPK_CAPACITY and p["bs"] == BS
-                and p["compress_ratio"] == 4)
+    if not pts:
+        raise SystemExit("--topk-point names no measured point (capacities 8192 / 262144, "
+                         "bs 1 / 128, ratios 4 / 8 / 16)")
+    head = next((p for p in pts if p["context"] == I.TOPK_CAPACITY and p["bs"] == BS
+                 and p["compress_ratio"] == 4), pts[0])
     print(json.dumps({
         "metric": "qsa_topk_expand calls/s (exact top-k 2048 tokens + index expansion, 256K contexts)",
         "op": "topk", "value": head["calls_per_s"], "unit": "calls/s", "n_gpus": 1,
         "steps": max(min(args.steps, 200), 1), "warmup": args.warmup,
         "ms_per_step": head["us_per_call"] * 1e-3, "higher_is_better": True, "dtype": "int32",
         "data": "synthetic",
-        "config": {"workload": "bs=128, 262144-token contexts, compress ratio 4, token_topk 2048, "
+        "config": {"workload": f"bs={head['bs']}, {head['context']}-token contexts, compress ratio "
+                               f"{head['compress_ratio']}, token_topk {head['token_topk']}, "
                                "64-token page table"},
         "roofline": {"bound": "hbm", "achieved": head["gb_s"], "peak": peak, "unit": "GB/s",
                      "frac": head["gb_s"] / peak, "peak_source": f"{kind} hbm_gbs",
-                     "bytes_per_launch": head["bytes_per_call"]},
+                     "bytes_per_launch": head["bytes_per_call"],
+                     "traffic": measured_traffic(
+                         f"topk_{head['context']}_bs{head['bs']}_r{head['compress_ratio']}", "qsa_topk.cu")},
         "points": pts, "clocks": clocks}), flush=True)
 
 
@@ -915,7 +924,15 @@ def parse_args(argv=None):
                     help="skip the quantised-pool and small-batch objects of the default line")
     ap.add_argument("--ref-rows", type=int, default=8,
                     help="sequences per step of the --impl reference sample")
+    ap.add_argument("--topk-point", default=None, metavar="CAPACITY,BS,RATIO",
+                    help="--op topk: measure this point only (e.g. 262144,128,4)")
     args = ap.parse_args(argv)
+    if args.topk_point is not None:
+        try:
+            cap, bs, ratio = (int(x) for x in args.topk_point.split(","))
+        except ValueError:
+            ap.error("--topk-point takes CAPACITY,BS,RATIO")
+        args.topk_point = (cap, bs, ratio)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     return args
