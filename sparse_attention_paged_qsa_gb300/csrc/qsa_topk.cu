@@ -41,6 +41,14 @@
 //    ballots give every block its rank among the ties (or the gathered bin) and
 //    among the kept blocks, warp totals a block-wide prefix. The kept blocks'
 //    r token slots are written after the selection, all blocks at once.
+//  * Small batches of long rows (at least 32,768 blocks; as many CTAs as fit the
+//    SMs, up to 8 per row) take a thread-block cluster per row: each CTA streams
+//    and counts its own part, the parts' histograms are reduced over distributed
+//    shared memory (each CTA sums one slice of the bins, then every CTA reads the
+//    slice that holds the k-th key), each part's candidates go to the leader CTA
+//    at their offset in index order, and the leader selects and writes the row.
+//    Every CTA reaches every cluster barrier; when the candidates do not fit the
+//    leader, it takes the whole row alone.
 //  * Each CTA computes its row's offset from the context lengths of the rows
 //    before it, so the whole step is one launch with no host readback, and a
 //    captured graph stays valid when the lengths and scores change.
@@ -70,6 +78,8 @@ constexpr unsigned FULL = 0xFFFFFFFFu;
 constexpr int NBINS = 2048;                    // bins of an 11-bit digit
 constexpr int P16_CAP = 65536;                 // blocks whose 16-bit key prefixes fit the key area
 constexpr int CAND_CAP = KEYS_CAP - P16_CAP / 2; // gathered block indices kept next to those prefixes
+constexpr int CCAP = CAND_CAP / 2;             // cluster rows: candidates the leader holds (indices, keys)
+constexpr int MAX_CLUSTER = 8;                 // CTAs per row for small batches (portable cluster size)
 constexpr long long WAIT_NS = 2000000000LL;    // bounded-wait limit (2 s)
 constexpr uint32_t KEPT = 0xFFFFFFFFu;         // not a key: order_key maps every NaN to 0
 // dynamic shared memory: the two ring slots, the keys, the histogram
@@ -80,6 +90,7 @@ constexpr int OFF_KEPT = OFF_HIST + NBINS * 4;           // kept block index by 
 constexpr int SMEM_BYTES = OFF_KEPT + (MAX_ROW + 1) * 4;
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 static_assert(NBINS % THREADS == 0 && NBINS / THREADS <= 4, "digit scan");
+static_assert(CCAP % 4 == 0 && (P16_CAP / 2 + CCAP) % 4 == 0, "cluster candidate lists stay 16-byte aligned");
 static_assert(ROUNDS % 4 == 0 && PIECE % 4096 == 0, "16-byte first-pass accesses stay aligned");
 static_assert(CAND_CAP > 0 && P16_CAP % 2 == 0, "prefix and candidate areas");
 static_assert(P16_CAP / 32 <= MAX_ROW + 1 && P16_CAP <= 128 * THREADS, "prefix bitmap in the kept-list area");
@@ -147,6 +158,35 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
 }
 __device__ __forceinline__ void fence_proxy_async() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// Thread-block clusters: this CTA's rank and the cluster's size, another CTA's
+// shared-memory address (distributed shared memory), and a barrier of every
+// thread of every CTA of the cluster (release / acquire).
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ uint32_t ld_dsmem(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_dsmem(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void fence_mbarrier_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -429,6 +469,41 @@ __device__ __forceinline__ int emit_bitmap(const uint32_t* bm, int n, int lo, in
     return pw.y;
 }
 
+// The same walk as emit_bitmap in two steps, for a caller that places the set
+// bits at an offset known only after the total: bitmap_ranks gives this thread's
+// first rank and the block's total; bitmap_emit calls emit(i, rank) for this
+// thread's set positions, ranks counted from `start`.
+__device__ __forceinline__ int2 bitmap_ranks(const uint32_t* bm, int n, int* wsum) {
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int words = (n + 31) >> 5, per = (words + THREADS - 1) / THREADS;
+    const int w0 = min(words, tid * per), w1 = min(words, w0 + per);
+    int cnt = 0;
+    for (int w = w0; w < w1; ++w) cnt += __popc(bm[w]);
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int x = __shfl_up_sync(FULL, incl, o);
+        if (lane >= o) incl += x;
+    }
+    const int2 pw = block_prefix(__shfl_sync(FULL, incl, 31), wsum);
+    return make_int2(pw.x + incl - cnt, pw.y);
+}
+template <class Emit>
+__device__ __forceinline__ void bitmap_emit(const uint32_t* bm, int n, int start, Emit emit) {
+    const int tid = threadIdx.x;
+    const int words = (n + 31) >> 5, per = (words + THREADS - 1) / THREADS;
+    const int w0 = min(words, tid * per), w1 = min(words, w0 + per);
+    int rank = start;
+    for (int w = w0; w < w1; ++w) {
+        uint32_t m = bm[w];
+        while (m != 0u) {
+            const int bit = __ffs(m) - 1;
+            m &= m - 1u;
+            emit(w * 32 + bit, rank++);
+        }
+    }
+}
+
 // Index-ordered gather of the prefixes >= t (see bitmap_ge16 and emit_bitmap).
 __device__ __forceinline__ int gather_ge16(const uint16_t* p16, int n, uint32_t t, uint32_t* bm, uint32_t* out,
                                            int cap, int* wsum) {
@@ -487,7 +562,14 @@ __device__ bool stream_row(const float* srow, int nb, float* ring, uint32_t bar0
     return ok;
 }
 
-__global__ void __launch_bounds__(THREADS, 1) topk_expand_kernel(const Params p) {
+// One row's top-k and expansion. CL: the row belongs to a thread-block cluster of
+// C CTAs (small batches): each streams and counts its own part of the row, the
+// parts' histograms are summed over distributed shared memory, each part's
+// candidates go to the leader (rank 0) in index order, and the leader finishes
+// the row; without CL, or when the candidates do not fit the leader, one CTA
+// takes the whole row.
+template <bool CL>
+__device__ __forceinline__ void topk_row(const Params& p) {
     extern __shared__ __align__(128) uint8_t smem[];
     float* const ring = reinterpret_cast<float*>(smem + OFF_RING);
     uint32_t* const keys = reinterpret_cast<uint32_t*>(smem + OFF_KEYS);
@@ -498,8 +580,13 @@ __global__ void __launch_bounds__(THREADS, 1) topk_expand_kernel(const Params p)
     __shared__ int sh[4];
     __shared__ uint32_t few[32]; // the last radix pass's keys, when at most 32
     __shared__ int nfew;
+    __shared__ int ccount[MAX_CLUSTER]; // cluster rows, in the leader: each part's candidate count
+    __shared__ int stot[MAX_CLUSTER];   // cluster rows: each CTA's histogram-slice total
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int b = blockIdx.x;
+    const int crank = CL ? static_cast<int>(cluster_ctarank()) : 0;
+    const int csize = CL ? static_cast<int>(cluster_nctarank()) : 1;
+    const bool leader = crank == 0;
+    const int b = CL ? static_cast<int>(blockIdx.x) / csize : static_cast<int>(blockIdx.x);
     const uint32_t bar0 = smem_u32(bars);
     if (tid == 0) {
         mbar_init(bar0, 1);
@@ -522,7 +609,7 @@ __global__ void __launch_bounds__(THREADS, 1) topk_expand_kernel(const Params p)
         atomicOr(p.err, QSA_DEVERR_CTX_LEN);
     const int T = clamp_len(Traw, p.capacity);
     const int nb = T / r, tail = T - nb * r;
-    if (tid == 0) {
+    if (tid == 0 && leader) {
         p.cu[b + 1] = off + row_len(T, r, kb);
         if (b == 0) p.cu[0] = 0;
     }
@@ -531,6 +618,7 @@ __global__ void __launch_bounds__(THREADS, 1) topk_expand_kernel(const Params p)
     bool bad = false;
 
     if (nb <= kb) { // every block kept: the row is positions 0 .. T - 1
+        if (!leader) return;
         for (int j = tid; j < T; j += THREADS) out[j] = slot_of(p, ptrow, j, bad);
         if (bad && p.err != nullptr) atomicOr(p.err, QSA_DEVERR_SLOT_RANGE);
         return;
@@ -625,6 +713,182 @@ __global__ void __launch_bounds__(THREADS, 1) topk_expand_kernel(const Params p)
 
     uint32_t prefix = 0u, mask = 0u;
     int need = kb; // rank of the wanted key among the keys that match the prefix
+    if constexpr (CL) {
+        // ------------------------------------------------ a cluster row
+        // Part k: blocks [lo, lo + nown), parts of a multiple of 32 blocks (the host
+        // launches clusters only when every part fits P16_CAP prefixes). Every CTA
+        // reaches every cluster barrier below, whatever happened before it.
+        const int C = csize;
+        const int part = (((nb + C - 1) / C) + 31) & ~31;
+        const int lo = min(nb, crank * part), nown = min(nb, lo + part) - lo;
+        uint16_t* const p16 = reinterpret_cast<uint16_t*>(keys);
+        clear_hist();
+        if (nown > 0) { // (a part of no blocks streams nothing)
+            const bool okc = stream_row(srow + lo, nown, ring, bar0, seq, [&](const float* piece, int base, int n) {
+                if (n == PIECE) { // 16-byte loads, 8-byte prefix stores: a thread takes 4 adjacent blocks
+                    float4 x[ROUNDS / 4];
+#pragma unroll
+                    for (int e = 0; e < ROUNDS / 4; ++e)
+                        x[e] = reinterpret_cast<const float4*>(piece)[tid + e * THREADS];
+#pragma unroll
+                    for (int e = 0; e < ROUNDS / 4; ++e) {
+                        const uint32_t k0 = order_key(x[e].x), k1 = order_key(x[e].y), k2 = order_key(x[e].z),
+                                       k3 = order_key(x[e].w);
+                        reinterpret_cast<uint2*>(p16 + base)[tid + e * THREADS] =
+                            make_uint2((k0 >> 16) | (k1 & 0xFFFF0000u), (k2 >> 16) | (k3 & 0xFFFF0000u));
+                        atomicAdd(&hist[k0 >> 21], 1u);
+                        atomicAdd(&hist[k1 >> 21], 1u);
+                        atomicAdd(&hist[k2 >> 21], 1u);
+                        atomicAdd(&hist[k3 >> 21], 1u);
+                    }
+                } else {
+                    for (int j = tid; j < n; j += THREADS) {
+                        const uint32_t k = order_key(piece[j]);
+                        p16[base + j] = static_cast<uint16_t>(k >> 16);
+                        atomicAdd(&hist[k >> 21], 1u);
+                    }
+                }
+            });
+            if (!okc) timed_out(); // (the row's result is then unspecified)
+        }
+        __syncthreads();
+        cluster_sync(); // every part counted
+        // The row's histogram, reduced and scattered: CTA k sums bins [k S, (k + 1) S)
+        // over every part (S = NBINS / C) into `slice` (over the candidate lists,
+        // written only after the next two barriers) and sends its slice's total to
+        // every CTA. Then each CTA finds, from the totals, the slice that holds the
+        // k-th key and reads only that slice, from its owner. Every remote load of a
+        // thread is issued before any is used.
+        const int S = NBINS / C;
+        uint32_t* const slice = keys + P16_CAP / 2;
+        {
+            constexpr int PER = NBINS / THREADS; // slice bins per thread, at most
+            uint32_t v[PER][MAX_CLUSTER];
+#pragma unroll
+            for (int q = 0; q < PER; ++q)
+#pragma unroll
+                for (int k = 0; k < MAX_CLUSTER; ++k) {
+                    const int i = tid + q * THREADS;
+                    v[q][k] = (i < S && k < C)
+                                  ? ld_dsmem(mapa(smem_u32(hist + crank * S + i), static_cast<uint32_t>(k)))
+                                  : 0u;
+                }
+            int mine = 0;
+#pragma unroll
+            for (int q = 0; q < PER; ++q) {
+                uint32_t c = 0u;
+#pragma unroll
+                for (int k = 0; k < MAX_CLUSTER; ++k) c += v[q][k];
+                if (tid + q * THREADS < S) slice[tid + q * THREADS] = c;
+                mine += static_cast<int>(c);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(FULL, mine, o);
+            const int total = block_prefix(mine, wsum).y;
+            if (tid < C) st_dsmem(mapa(smem_u32(&stot[crank]), static_cast<uint32_t>(tid)), static_cast<uint32_t>(total));
+        }
+        cluster_sync(); // slices summed, totals everywhere
+        int js = C - 1, above = 0; // the slice (from the top) that holds the need-th key
+        while (js > 0 && above + stot[js] < need) above += stot[js--];
+        uint32_t* const htot = reinterpret_cast<uint32_t*>(kept); // that slice in place, zeros elsewhere
+        {
+            constexpr int PER = NBINS / THREADS;
+            uint32_t v[PER];
+#pragma unroll
+            for (int q = 0; q < PER; ++q) {
+                const int i = tid + q * THREADS;
+                const bool in = i >= js * S && i < (js + 1) * S;
+                v[q] = in ? ld_dsmem(mapa(smem_u32(slice + (i - js * S)), static_cast<uint32_t>(js))) : 0u;
+            }
+#pragma unroll
+            for (int q = 0; q < PER; ++q) htot[tid + q * THREADS] = v[q];
+        }
+        __syncthreads();
+        const int2 dl = find_digit(htot, NBINS, need - above, wsum, sh);
+        const int2 d = make_int2(dl.x, dl.y + above);
+        const uint32_t d1 = static_cast<uint32_t>(d.x) & (NBINS - 1);
+        const int cand = static_cast<int>(htot[d1]);
+        int needc = need - d.y;
+        uint32_t t16 = d1 << 5, pfx = d1 << 21, msk = 0x7FFu << 21;
+        int ng = d.y + cand;
+        // (hist is read remotely only before the barrier above: the 5-bit step may reuse it)
+        if (ng > CCAP) { // (uniform over the cluster: the same histogram)
+            // the 5-bit digit below d1 that holds the k-th key, from every part's prefixes
+            if (tid < 32) hist[tid] = 0u;
+            __syncthreads();
+            for (int j = tid; j < nown; j += THREADS) {
+                const uint32_t v = p16[j];
+                if ((v >> 5) == d1) atomicAdd(&hist[v & 31u], 1u);
+            }
+            __syncthreads();
+            cluster_sync();
+            if (warp == 0) {
+                const int bin = 31 - lane;
+                const uint32_t a = smem_u32(hist + bin);
+                uint32_t v[MAX_CLUSTER];
+#pragma unroll
+                for (int k = 0; k < MAX_CLUSTER; ++k) v[k] = k < C ? ld_dsmem(mapa(a, static_cast<uint32_t>(k))) : 0u;
+                int cnt = 0;
+#pragma unroll
+                for (int k = 0; k < MAX_CLUSTER; ++k) cnt += static_cast<int>(v[k]);
+                int incl = cnt;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int v = __shfl_up_sync(FULL, incl, o);
+                    if (lane >= o) incl += v;
+                }
+                if (incl - cnt < needc && needc <= incl) {
+                    sh[0] = bin;
+                    sh[1] = incl - cnt;
+                    sh[2] = cnt;
+                }
+            }
+            __syncthreads();
+            t16 = (d1 << 5) | static_cast<uint32_t>(sh[0]);
+            pfx = t16 << 16;
+            msk = 0xFFFF0000u;
+            needc -= sh[1];
+            ng = d.y + sh[1] + sh[2];
+            cluster_sync(); // every part's 5-bit counts read, sh read
+        }
+        if (ng <= CCAP) {
+            // this part's blocks at or above t16, in index order, to the leader's lists
+            // at this part's offset: block index and full key (one score read each)
+            uint32_t* const bm = reinterpret_cast<uint32_t*>(kept);
+            if (nown > 0) bitmap_ge16(p16, nown, t16, bm);
+            const int2 rk = bitmap_ranks(bm, nown, wsum);
+            if (tid == 0) st_dsmem(mapa(smem_u32(&ccount[crank]), 0u), static_cast<uint32_t>(rk.y));
+            cluster_sync();
+            uint32_t cv[MAX_CLUSTER];
+#pragma unroll
+            for (int k = 0; k < MAX_CLUSTER; ++k) cv[k] = k < crank ? ld_dsmem(mapa(smem_u32(&ccount[k]), 0u)) : 0u;
+            int base = 0;
+#pragma unroll
+            for (int k = 0; k < MAX_CLUSTER; ++k) base += static_cast<int>(cv[k]);
+            const uint32_t glr = mapa(smem_u32(keys + P16_CAP / 2), 0u);
+            const uint32_t ckr = mapa(smem_u32(keys + P16_CAP / 2 + CCAP), 0u);
+            bitmap_emit(bm, nown, base + rk.x, [&](int j, int g) {
+                if (g < CCAP) { // exactly ng are emitted; the bound guards the lists
+                    const int i = lo + j;
+                    st_dsmem(glr + 4u * static_cast<uint32_t>(g), static_cast<uint32_t>(i));
+                    st_dsmem(ckr + 4u * static_cast<uint32_t>(g), order_key(__ldg(srow + i)));
+                }
+            });
+            cluster_sync(); // every candidate is in the leader
+            if (!leader) return;
+            uint32_t* const gl = keys + P16_CAP / 2;
+            uint32_t* const ck = gl + CCAP;
+            select_in_smem(ck, ng, pfx, msk, needc);
+            compact_keys(ck, ng, pfx, needc, [&](int g, int rank) { put_block(static_cast<int>(gl[g]), rank); },
+                         wsum);
+            write_kept(); // the kept blocks' slots, at their ranks
+            for (int t = tid; t < tail; t += THREADS) out[kb * r + t] = slot_of(p, ptrow, nb * r + t, bad);
+            if (bad && p.err != nullptr) atomicOr(p.err, QSA_DEVERR_SLOT_RANGE);
+            return;
+        }
+        // too many candidates for the leader: it takes the whole row alone
+        if (!leader) return;
+    }
     if (nb <= KEYS_CAP) {
         // ------------------------------------------------ the row fits: keys in shared memory
         clear_hist();
@@ -853,6 +1117,9 @@ __global__ void __launch_bounds__(THREADS, 1) topk_expand_kernel(const Params p)
     (void)warp;
 }
 
+__global__ void __launch_bounds__(THREADS, 1) topk_expand_kernel(const Params p) { topk_row<false>(p); }
+__global__ void __launch_bounds__(THREADS, 1) topk_cluster_kernel(const Params p) { topk_row<true>(p); }
+
 namespace {
 
 int fail(int code, const char* fmt, ...) {
@@ -953,29 +1220,65 @@ extern "C" int qsa_topk_expand(const qsa_tensor* scores, const qsa_tensor* ctx_l
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return fail(QSA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
     if (dev < 0 || dev >= 64) return fail(QSA_ERR_CUDA, "device ordinal %d out of range", dev);
+    static std::mutex mu;
+    static bool smem_set[64] = {};
+    static int sm_count[64] = {};
+    static signed char cluster_ok[64][MAX_CLUSTER + 1] = {}; // 0 unknown, 1 fits, -1 does not
     {
-        static std::mutex mu;
-        static bool smem_set[64] = {};
         std::lock_guard<std::mutex> lk(mu);
         if (!smem_set[dev]) {
-            e = cudaFuncSetAttribute(topk_expand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     SMEM_BYTES);
+            for (const void* k : {reinterpret_cast<const void*>(&topk_expand_kernel),
+                                  reinterpret_cast<const void*>(&topk_cluster_kernel)}) {
+                e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+                if (e != cudaSuccess)
+                    return fail(QSA_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+            }
+            e = cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
             if (e != cudaSuccess)
-                return fail(QSA_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+                return fail(QSA_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
             smem_set[dev] = true;
         }
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(bs));
     cfg.blockDim = dim3(THREADS);
     cfg.dynamicSmemBytes = SMEM_BYTES;
     cfg.stream = static_cast<cudaStream_t>(stream);
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, topk_expand_kernel, p);
+    // Small batches: a cluster of C CTAs per row, the largest C whose clusters fill
+    // no more than the SMs, when the longest row spans at least 8 pieces (below
+    // that the cluster's barriers cost more than its parts save; 4 CTAs at most
+    // below 16 pieces), each part's prefixes fit, and such a cluster can be resident.
+    int C = 1;
+    const long long nbmax_row = cap / r;
+    const int cmax = nbmax_row >= 16LL * PIECE ? MAX_CLUSTER : (nbmax_row >= 8LL * PIECE ? 4 : 1);
+    for (int c = cmax; c >= 2; c /= 2) {
+        const long long part = (((nbmax_row + c - 1) / c) + 31) & ~31LL;
+        if (bs * c > sm_count[dev] || part > P16_CAP) continue;
+        std::lock_guard<std::mutex> lk(mu);
+        if (cluster_ok[dev][c] == 0) {
+            cfg.gridDim = dim3(static_cast<unsigned>(c));
+            attr[1].val.clusterDim.x = static_cast<unsigned>(c);
+            attr[1].val.clusterDim.y = attr[1].val.clusterDim.z = 1;
+            cfg.numAttrs = 2;
+            int clusters = 0;
+            const cudaError_t q = cudaOccupancyMaxActiveClusters(&clusters, topk_cluster_kernel, &cfg);
+            cluster_ok[dev][c] = (q == cudaSuccess && clusters >= 1) ? 1 : -1;
+            if (q != cudaSuccess) (void)cudaGetLastError(); // a query that failed: no cluster launch
+        }
+        if (cluster_ok[dev][c] > 0) {
+            C = c;
+            break;
+        }
+    }
+    cfg.gridDim = dim3(static_cast<unsigned>(bs * C));
+    attr[1].val.clusterDim.x = static_cast<unsigned>(C);
+    attr[1].val.clusterDim.y = attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = C > 1 ? 2 : 1;
+    e = C > 1 ? cudaLaunchKernelEx(&cfg, topk_cluster_kernel, p) : cudaLaunchKernelEx(&cfg, topk_expand_kernel, p);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return fail(QSA_ERR_CUDA, "top-k launch: %s", cudaGetErrorString(e));
     qsa_detail_set_error("");

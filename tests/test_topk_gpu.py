@@ -134,6 +134,27 @@ def test_sorted_rows_bound_the_first_pass(cuda_device):
         _check(sel, cu, scores, lens, topk, ratio, cap)
 
 
+def test_every_cluster_size(cuda_device):
+    """Small batches with rows of at least 65,536 blocks take a cluster of CTAs per
+    row (8, 4 or 2 by batch size, 1 from 77 rows on a 152-SM GB300): each counts
+    and gathers its own part of the row, the leader selects. Rows of full, ragged
+    and short lengths at 256K contexts, ratio 4, through a page table, at batch
+    sizes that give every cluster size."""
+    cap, ratio, topk = I.TOPK_CAPACITY, 4, 2048
+    for bs in (1, 20, 40, 77):
+        scores = I.block_scores(bs, cap // ratio, 60 + bs, cuda_device)
+        lens = torch.full((bs,), cap, dtype=torch.int32)
+        lens[1::3] = cap - 8 * 101 - 5        # a part boundary inside the row's last word
+        lens[2::3] = 3 * 4096 + 17            # 3,076 blocks: parts of a few words
+        lens = lens.to(cuda_device)
+        pt = I.page_table(bs, cap, PAGE, 60 + bs, cuda_device)
+        err = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+        sel, cu = _run(scores, lens, topk, ratio, cap, pt, err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        _check(sel, cu, scores, lens, topk, ratio, cap, pt)
+
+
 def test_changing_replay_index_equality_in_a_graph(cuda_device):
     """One captured graph: regenerate context lengths and scores on the device from
     the replay counter, then top-k + expansion; 60 replays, every fifth checked
