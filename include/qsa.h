@@ -355,9 +355,12 @@ typedef struct {
  *  device_error optional int32 device word the QSA_DEVERR_* bits are OR-ed into.
  *  stream       cudaStream_t.
  *
- * Validates on the host, enqueues one kernel (one CTA per sequence), allocates
- * nothing and needs no scratch; a captured graph stays valid when ctx_lens and
- * scores change between replays. Returns QSA_OK or a negative QSA_ERR_*.
+ * Validates on the host, enqueues one kernel (one CTA per sequence, or for small
+ * batches of rows of at least 32,768 blocks a cluster of up to 8 CTAs per
+ * sequence, the cluster size chosen from bs, capacity / compress_ratio and the
+ * device's SM count, the same on every call with those), allocates nothing and
+ * needs no scratch; a captured graph stays valid when ctx_lens and scores change
+ * between replays. Returns QSA_OK or a negative QSA_ERR_*.
  */
 int qsa_topk_expand(const qsa_tensor* scores, const qsa_tensor* ctx_lens,
                     const qsa_tensor* page_table, const qsa_topk_params* params,

@@ -16,7 +16,8 @@
 //     tokens; a page table maps position p to slot pt[p / page] * page + p % page;
 //   * rows are packed in sequence order; cu_seqlens[b] is where row b starts.
 //
-// GB300 design: one CTA of 512 threads per sequence, no global scratch.
+// GB300 design: one CTA of 512 threads per sequence (a cluster of them for small
+// batches of long rows, below), no global scratch.
 //  * Scores become order-preserving 32-bit keys (sign-flipped IEEE bits, NaN ->
 //    0, -0.0 -> +0.0), so ranking is unsigned integer comparison.
 //  * The score row streams into shared memory in 16 KB pieces by bulk copies
