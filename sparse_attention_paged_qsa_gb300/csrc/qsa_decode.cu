@@ -94,6 +94,7 @@ constexpr int MAX_BS = 128;
 constexpr int MAX_CAPACITY = 2055;
 constexpr int MIN_TOKENS_PER_CTA = 64;
 constexpr unsigned FEW_SEGMENTS = 4;        // up to this many (sequence, KV head) segments ...
+constexpr unsigned UNIFORM_SEGMENTS = 64;   // ... or this many of nearly equal length ...
 constexpr unsigned MAX_FANIN = 16;          // ... each gets a whole number (<= this) of CTAs
 constexpr int PART_BYTES = 12416;           // fp32 O[12][256] + m[12] + l[12], 128-byte multiple
 constexpr int MERGE_BATCH = 6;             // partials per bulk-copy batch of the split merge (at most)
@@ -907,13 +908,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
     unsigned G = (N + MIN_TOKENS_PER_CTA - 1) / MIN_TOKENS_PER_CTA;
     G = G < gridDim.x ? G : gridDim.x;
     if (whole) G = S_all < gridDim.x ? S_all : gridDim.x;
-    // Few segments (bs * Hkv <= FEW_SEGMENTS): a whole number of CTAs per segment,
-    // at most MAX_FANIN. With equal lengths no CTA then holds pieces of two
-    // segments, so their merges run on different CTAs, and each merge reads at
-    // most MAX_FANIN partials.
+    // Few segments (bs * Hkv <= FEW_SEGMENTS), or up to UNIFORM_SEGMENTS of nearly
+    // equal length (mean at least 7/8 of the longest): a whole number of CTAs per
+    // segment, at most MAX_FANIN. With equal lengths no CTA then holds pieces of
+    // two segments, so their merges run on different CTAs, and each merge reads
+    // at most MAX_FANIN partials; with unequal lengths the equal-token split
+    // balances the CTAs better.
     {
         const unsigned S = static_cast<unsigned>(p.bs * Hkv);
-        if (!whole && S <= FEW_SEGMENTS && 2 * S <= G) {
+        const bool uniform = 8ull * N >= 7ull * S * static_cast<unsigned long long>(misc[20]);
+        if (!whole && (S <= FEW_SEGMENTS || (S <= UNIFORM_SEGMENTS && uniform)) && 2 * S <= G) {
             const unsigned per = G / S < MAX_FANIN ? G / S : MAX_FANIN;
             G = per * S;
         }
