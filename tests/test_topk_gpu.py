@@ -196,6 +196,42 @@ def test_changing_replay_index_equality_in_a_graph(cuda_device):
     assert int(err.item()) == 0 and len(seen) == 12   # the lengths did change every time
 
 
+def test_cluster_rows_in_a_replayed_graph(cuda_device):
+    """The cluster kernel (two 65,536-block rows, 8 CTAs each) captured in a graph:
+    lengths and scores regenerated on the device before every replay, every
+    replay bit-identical to the oracle."""
+    cap, ratio, topk, bs = I.TOPK_CAPACITY, 4, 2048, 2
+    dev = cuda_device
+    scores = torch.empty(bs, cap // ratio, device=dev)
+    lens = torch.empty(bs, dtype=torch.int32, device=dev)
+    pt = I.page_table(bs, cap, PAGE, 13, dev)
+    replay = torch.zeros((), dtype=torch.int64, device=dev)
+    sel = torch.empty(bs * (topk + ratio - 1), dtype=torch.int32, device=dev)
+    cu = torch.empty(bs + 1, dtype=torch.int32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    s = torch.cuda.Stream(device=dev)
+    s.wait_stream(torch.cuda.current_stream())
+
+    def body():
+        I.replay_context_lengths(17, replay, cap, lens)
+        lens.copy_(cap - torch.remainder(lens, 4096))  # long rows (the cluster path), varying
+        I.replay_block_scores(17, replay, scores)
+        qsa.qsa_topk_expand(scores, lens, sel, cu, topk, ratio, cap, page_table=pt,
+                            page_size=PAGE, error_word=err, stream=s)
+        replay.add_(1)
+
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        body()
+    seen = set()
+    for rep in range(8):
+        g.replay()
+        torch.cuda.synchronize()
+        _check(sel, cu, scores, lens, topk, ratio, cap, pt, fresh=False)
+        seen.add(tuple(lens.cpu().tolist()))
+    assert int(err.item()) == 0 and len(seen) == 8
+
+
 def test_topk_feeds_the_decode_in_one_graph(cuda_device):
     """Scores -> top-k + expansion (through a page table) -> qsa_decode, one captured
     graph; replays with new scores and lengths; the decode output matches the oracle
