@@ -25,6 +25,22 @@ def _parity(w, dev):
     return out
 
 
+def _within_one_ulp(a, b):
+    """The tiered kernel widens its cold int4 rows into int8 tiles and runs the
+    int8 fragment path over them, the int4-g32 kernel unpacks nibbles straight
+    into its fragments: the same products, summed in another order inside the
+    MMAs. An output may then differ by one bf16 ulp at its (sequence, head)
+    row's scale (an output near zero is a cancelling sum), and rarely."""
+    a, b = a.float(), b.float()
+    d = (a - b).abs()
+    row = torch.maximum(a.abs(), b.abs()).amax(dim=-1, keepdim=True)
+    _, e = torch.frexp(row)
+    ulp = torch.ldexp(torch.ones_like(row), e - 8)  # bf16: 8 significant bits
+    assert bool((d <= ulp).all()), float((d / ulp).max())
+    ndiff = int((d > 0).sum())
+    assert ndiff <= max(4, a.numel() // 1000), ndiff
+
+
 @pytest.mark.parametrize("hot_share", [0.0, 0.5, 1.0])
 @pytest.mark.parametrize("ring", [1024, 4096])
 def test_tiered_parity(cuda_device, hot_share, ring):
@@ -39,7 +55,7 @@ def test_tiered_tp2(cuda_device):
     _parity(w, cuda_device)
 
 
-def test_all_cold_equals_the_int4_g32_kernel_and_all_hot_the_oracle_int8_g64(cuda_device):
+def test_all_cold_matches_the_int4_g32_kernel_and_all_hot_the_oracle_int8_g64(cuda_device):
     w = I.tiered(seed=52, bs=6, num_slots=8192, ring_slots=8192, lengths=[64, 2055, 9, 512, 1, 300])
     cold = I.Workload(w.q, w.k_pool, w.v_pool, w.sel, w.cu, w.fmt, w.k_scale, w.v_scale,
                       capacity=w.capacity, extra=dict(w.extra))
@@ -49,7 +65,7 @@ def test_all_cold_equals_the_int4_g32_kernel_and_all_hot_the_oracle_int8_g64(cud
                      capacity=w.capacity)
     out_4, _ = run_cuda(g32.to(cuda_device))
     torch.cuda.synchronize()
-    assert torch.equal(out_t, out_4)
+    _within_one_ulp(out_t, out_4)
     # all hot: the ring has one row per slot (R = num_slots) and owner[p] = p
     hot = I.Workload(w.q, w.k_pool, w.v_pool, w.sel, w.cu, w.fmt, w.k_scale, w.v_scale,
                      capacity=w.capacity, extra=dict(w.extra))
@@ -66,6 +82,30 @@ def test_all_cold_equals_the_int4_g32_kernel_and_all_hot_the_oracle_int8_g64(cud
                         w.softmax_scale, hot.extra["k_ring_scale"], hot.extra["v_ring_scale"])
     compare(out_h, ref, w.lengths().numpy())
     assert ring_ids.numel() == t["owner"].numel()
+
+
+@pytest.mark.parametrize("seed,lengths", [
+    (60, [2055]),                      # two segments of 16 CTAs each
+    (61, [2055, 2055]),
+    (62, [2055] * 4),
+    (63, [2055, 1500, 700]),           # unequal: the equal-token split
+    (64, [2055] * 16),
+    (65, [1, 2055, 33, 2055, 64]),
+])
+def test_all_cold_matches_the_int4_g32_kernel_at_any_split(cuda_device, seed, lengths):
+    """Segments cut into many pieces: an all-cold tiered call meets the oracle's
+    gate and stays within one bf16 ulp of the int4-g32 call."""
+    w = I.tiered(seed=seed, bs=len(lengths), num_slots=8192, ring_slots=2048, lengths=lengths)
+    cold = I.Workload(w.q, w.k_pool, w.v_pool, w.sel, w.cu, w.fmt, w.k_scale, w.v_scale,
+                      capacity=w.capacity, extra=dict(w.extra))
+    cold.extra["owner"] = torch.full_like(w.extra["owner"], -1)
+    g32 = I.Workload(w.q, w.k_pool, w.v_pool, w.sel, w.cu, "int4_g32", w.k_scale, w.v_scale,
+                     capacity=w.capacity)
+    out_t, _ = run_cuda(cold.to(cuda_device))
+    out_4, _ = run_cuda(g32.to(cuda_device))
+    torch.cuda.synchronize()
+    _within_one_ulp(out_t, out_4)
+    compare(out_t, run_oracle(g32), w.lengths().numpy())
 
 
 def test_tiered_headline_sampled(cuda_device):
