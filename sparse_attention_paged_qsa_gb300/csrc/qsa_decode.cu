@@ -336,6 +336,22 @@ __device__ __noinline__ bool mbar_wait_copies(uint32_t bar, uint32_t parity, int
     }
 }
 
+// Wait until a split counter reaches `target` (acquire: the partials stored
+// before the increments are visible), for at most WAIT_NS.
+__device__ __noinline__ bool wait_count(const int* cnt, int target, int* err) {
+    const unsigned long long t0 = globaltimer();
+    for (uint32_t it = 0;; ++it) {
+        int v;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
+        if (v >= target) return true;
+        if ((it & 63) == 63 && globaltimer() - t0 > (unsigned long long)WAIT_NS) {
+            atomicOr(err, QSA_DEVERR_TIMEOUT);
+            return false;
+        }
+        __nanosleep(32);
+    }
+}
+
 // Programmatic dependent launch: wait until the grids this launch depends on
 // have completed and their memory is visible (a no-op for an ordinary launch);
 // let the next dependent launch be scheduled.
@@ -914,13 +930,19 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
     // two segments, so their merges run on different CTAs, and each merge reads
     // at most MAX_FANIN partials; with unequal lengths the equal-token split
     // balances the CTAs better.
+    // With every length equal as well, CTA c's range is [c L / per, (c + 1) L / per)
+    // of segment c / per: each CTA holds one piece, and the split segments are
+    // merged by all their contributors at once (misc[22], after the main loop).
     {
         const unsigned S = static_cast<unsigned>(p.bs * Hkv);
         const bool uniform = 8ull * N >= 7ull * S * static_cast<unsigned long long>(misc[20]);
+        bool wide = false;
         if (!whole && (S <= FEW_SEGMENTS || (S <= UNIFORM_SEGMENTS && uniform)) && 2 * S <= G) {
             const unsigned per = G / S < MAX_FANIN ? G / S : MAX_FANIN;
             G = per * S;
+            wide = N == S * static_cast<unsigned>(misc[20]);
         }
+        misc[22] = wide ? 1 : 0; // every thread writes the same value
     }
     if (blockIdx.x >= G) return;
     long long t_begin, t_end;
@@ -1916,6 +1938,62 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
     // its counter; the merger resets the counter to zero. The partial stores of
     // all consumer threads precede thread 0's acq_rel ticket through the
     // barrier (release), and the merger's reads follow its ticket (acquire).
+    // Equal lengths (misc[22]): this CTA's one piece is contributor r of the n
+    // CTAs of segment pend0, all of which stored their partial and took a ticket.
+    // Once the n tickets are in, each contributor merges float4 columns r, r + n,
+    // ... of the segment's 12 x 256 outputs from the n partials in CTA order; a
+    // second round of arrivals on the counter ends at 2n, and the contributor
+    // that brings it there resets it.
+    if (pend0 >= 0 && misc[22] != 0) {
+        unsigned Fs, cf, cl;
+        seg_range(pend0, Fs, cf, cl);
+        const unsigned n = cl - cf + 1, r = blockIdx.x - cf;
+        if (tid == 0) {
+            bool ok = true;
+            if (mstate[4] == static_cast<int>(n) - 1)
+                fence_acq_rel_gpu(); // the last ticket: every other partial precedes it
+            else
+                ok = wait_count(p.cnt + pend0, static_cast<int>(n), p.err);
+            misc[2] = ok ? 1 : 0;
+        }
+        if (consumer_sync_or(*abort_flag != 0) || misc[2] == 0) return;
+        const int b = pend0 / Hkv, g = pend0 - b * Hkv;
+        __nv_bfloat16* const outb = p.out + b * p.o_sb + (long long)(g * GROUP) * p.o_sh;
+        const float ninf = -INFINITY;
+        for (unsigned f = r + n * static_cast<unsigned>(tid); f < GROUP * D / 4; f += n * NCT) {
+            const int h = static_cast<int>(f) / (D / 4), d0 = (static_cast<int>(f) % (D / 4)) * 4;
+            const float* const p0 = reinterpret_cast<const float*>(p.part + static_cast<size_t>(cf * 2u) * PART_BYTES);
+            constexpr size_t PSTEP = 2 * PART_BYTES / 4; // floats from one CTA's slot 0 to the next's
+            float M = ninf;
+#pragma unroll 4
+            for (unsigned i = 0; i < n; ++i) M = fmaxf(M, __ldcg(p0 + i * PSTEP + GROUP * D + h));
+            float den = 0.f;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+            for (unsigned i = 0; i < n; ++i) {
+                const float* const pk = p0 + i * PSTEP;
+                const float m = __ldcg(pk + GROUP * D + h);
+                const float w = m == ninf ? 0.f : ex2(m - M);
+                const float l = __ldcg(pk + GROUP * D + GROUP + h);
+                const float4 o = __ldcg(reinterpret_cast<const float4*>(pk + h * D + d0));
+                den = fmaf(w, l, den);
+                acc.x = fmaf(w, o.x, acc.x);
+                acc.y = fmaf(w, o.y, acc.y);
+                acc.z = fmaf(w, o.z, acc.z);
+                acc.w = fmaf(w, o.w, acc.w);
+            }
+            const float fo = __fdividef(out_scale, den);
+            *reinterpret_cast<uint2*>(outb + h * p.o_sh + d0) =
+                make_uint2(pack_bf16x2(acc.x * fo, acc.y * fo), pack_bf16x2(acc.z * fo, acc.w * fo));
+        }
+        consumer_sync(); // every consumer thread's reads precede the release
+        if (tid == 0) {
+            __threadfence();
+            if (atomicAdd(p.cnt + pend0, 1) == static_cast<int>(2 * n) - 1) atomicExch(p.cnt + pend0, 0);
+        }
+        return;
+    }
+
     if (pend0 >= 0 || pend1 >= 0) {
         consumer_sync(); // every consumer thread's partial stores precede the release below
         if (tid == 0) {

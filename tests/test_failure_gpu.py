@@ -69,3 +69,36 @@ def test_stalled_stage_times_out_and_context_recovers(cuda_device):
     assert qsa.qsa_scratch_error(scratch) == 0
     assert (counters(scratch, w.bs, w.num_q_heads, w.capacity) == 0).all()
     compare(out, run_oracle(w), w.lengths().numpy())
+
+
+def test_stalled_contributor_of_an_equal_length_split_times_out(cuda_device):
+    """bs = 1, L = 2055 (equal lengths, 16 CTAs per KV head, each merging a slice of
+    its segment once all 16 partials are stored): CTA 0 never completes its second
+    stage and leaves without a partial; the other contributors' bounded wait for
+    the sixteenth ticket runs out, and the launch ends with the timeout status."""
+    lib = B.open_library(os.path.join(os.path.dirname(B.LIB_PATH), "libqsa_testhooks.so"))
+    lib.qsa_test_set_stall_stage.argtypes = [ctypes.c_int]
+    w = I.tp1_mixed(seed=24, bs=1, num_slots=65536, lengths=[2055])
+    wd = w.to(cuda_device)
+    meta = qsa.KVQuantMeta("bf16", w.capacity, None, None, w.softmax_scale)
+    out = torch.zeros_like(wd.q)
+    scratch = qsa.alloc_scratch(w.bs, w.num_q_heads, w.capacity, cuda_device)
+
+    lib.qsa_test_set_stall_stage(1)
+    t0 = time.monotonic()
+    try:
+        _decode(lib, wd, meta, out, scratch)
+        torch.cuda.synchronize()
+    finally:
+        lib.qsa_test_set_stall_stage(-1)
+    waited = time.monotonic() - t0
+    assert qsa.qsa_scratch_error(scratch, clear=True) & DEVERR_TIMEOUT
+    assert 1.0 < waited < 60.0, waited
+
+    qsa.qsa_scratch_init(scratch)
+    out.zero_()
+    _decode(lib, wd, meta, out, scratch)
+    torch.cuda.synchronize()
+    assert qsa.qsa_scratch_error(scratch) == 0
+    assert (counters(scratch, w.bs, w.num_q_heads, w.capacity) == 0).all()
+    compare(out, run_oracle(w), w.lengths().numpy())

@@ -237,3 +237,31 @@ def test_int8_wide_v_scales(cuda_device, max_ctas):
     vs[w.sel[lo:hi].long()] = w.v_scale.double()[w.sel[lo:hi].long()] * ramp[:, None]
     w.v_scale = vs.float()
     _parity(w, cuda_device, max_ctas)
+
+
+def _equal_lengths(seed, hq, bs, length, num_slots=65536):
+    hkv = hq // 12
+    kc, vc, ks, vs = I.make_pools(num_slots, hkv, "bf16", seed)
+    g = torch.Generator().manual_seed(seed)
+    sel = I.uniform_indices(bs * length, num_slots, g)
+    return I.Workload(I.make_query(bs, hq, seed), kc, vc, sel, I.cu_from_lengths([length] * bs),
+                      "bf16", ks, vs, capacity=length, name=f"equal_{hq}q_bs{bs}_L{length}")
+
+
+@pytest.mark.parametrize("hq,bs,length", [
+    (24, 1, 2055), (24, 3, 777), (24, 5, 2055), (24, 8, 2055), (24, 12, 700), (24, 20, 600),
+    (24, 32, 500), (12, 7, 1000), (12, 13, 333),
+])
+def test_equal_length_splits_every_fan_in(cuda_device, hq, bs, length):
+    """Equal lengths, a whole number of CTAs per (sequence, KV head) segment (fan-ins
+    16, 12, 15, 9, 6, 3, 2, 15 and 5 here): every contributor merges a slice of its
+    segment from all partials; the output, the error word and the counters."""
+    w = _equal_lengths(80 + bs, hq, bs, length)
+    out, scratch = run_cuda(w.to(cuda_device))
+    torch.cuda.synchronize()
+    compare(out, run_oracle(w), w.lengths().numpy())
+    assert qsa.qsa_scratch_error(scratch) == 0
+    assert (counters(scratch, w.bs, w.num_q_heads, w.capacity) == 0).all()
+    again, _ = run_cuda(w.to(cuda_device), scratch=scratch)
+    torch.cuda.synchronize()
+    assert torch.equal(again, out)
