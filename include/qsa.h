@@ -88,8 +88,14 @@ enum {
     QSA_DEVERR_SLOT_RANGE = 1, /* a selected slot id outside [0, num_slots); slot 0 read instead */
     QSA_DEVERR_CU_SEQLENS = 2, /* cu_seqlens decreasing, negative, past the index buffer,
                                   or a length above capacity; the length is clamped */
-    QSA_DEVERR_TIMEOUT = 4,    /* an internal pipeline wait exceeded its limit (a library
-                                  fault, not a data fault); the launch gave up early */
+    QSA_DEVERR_TIMEOUT = 4,    /* an internal wait exceeded its limit (2 s) and the launch
+                                  gave up early: a library fault, not a data fault, or --
+                                  when every selection has the same length and the batch
+                                  is small enough that each (sequence, KV head) gets a
+                                  whole number of CTAs, whose contributors wait for each
+                                  other to merge -- this call's CTAs could not all be
+                                  resident that long (kernels on other streams holding
+                                  the SMs) */
     QSA_DEVERR_CTX_LEN = 8     /* qsa_topk_expand: a context length outside [0, capacity];
                                   it is clamped into that range */
 };
