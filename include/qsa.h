@@ -90,10 +90,9 @@ enum {
                                   or a length above capacity; the length is clamped */
     QSA_DEVERR_TIMEOUT = 4,    /* an internal wait exceeded its limit (2 s) and the launch
                                   gave up early: a library fault, not a data fault, or --
-                                  when every selection has the same length and the batch
-                                  is small enough that each (sequence, KV head) gets a
-                                  whole number of CTAs, whose contributors wait for each
-                                  other to merge -- this call's CTAs could not all be
+                                  when the batch is small enough that each (sequence, KV
+                                  head) gets its own CTAs, whose contributors wait for
+                                  each other to merge -- this call's CTAs could not all be
                                   resident that long (kernels on other streams holding
                                   the SMs) */
     QSA_DEVERR_CTX_LEN = 8     /* qsa_topk_expand: a context length outside [0, capacity];

@@ -888,12 +888,20 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
         }
         const int total = __shfl_sync(0xFFFFFFFFu, incl, 31);
         int lmax = max(max(Ls[0], Ls[1]), max(Ls[2], Ls[3]));
+        int lmin = 0x7fffffff;
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) lmax = max(lmax, __shfl_xor_sync(0xFFFFFFFFu, lmax, off));
+        for (int k = 0; k < 4; ++k)
+            if (lane * 4 + k < p.bs) lmin = min(lmin, Ls[k]);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            lmax = max(lmax, __shfl_xor_sync(0xFFFFFFFFu, lmax, off));
+            lmin = min(lmin, __shfl_xor_sync(0xFFFFFFFFu, lmin, off));
+        }
         if (lane == 0) {
             segP[p.bs] = total;
             segL[p.bs] = 1; // sentinel for the segment walk
             misc[20] = lmax; // the longest selection
+            misc[23] = lmin; // the shortest
         }
         bad = __any_sync(0xFFFFFFFFu, bad);
         if (bad && lane == 0 && blockIdx.x == 0) atomicOr(p.err, QSA_DEVERR_CU_SEQLENS);
@@ -925,24 +933,23 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
     G = G < gridDim.x ? G : gridDim.x;
     if (whole) G = S_all < gridDim.x ? S_all : gridDim.x;
     // Few segments (bs * Hkv <= FEW_SEGMENTS), or up to UNIFORM_SEGMENTS of nearly
-    // equal length (mean at least 7/8 of the longest): a whole number of CTAs per
-    // segment, at most MAX_FANIN. With equal lengths no CTA then holds pieces of
-    // two segments, so their merges run on different CTAs, and each merge reads
-    // at most MAX_FANIN partials; with unequal lengths the equal-token split
-    // balances the CTAs better.
-    // With every length equal as well, CTA c's range is [c L / per, (c + 1) L / per)
-    // of segment c / per: each CTA holds one piece, and the split segments are
-    // merged by all their contributors at once (misc[22], after the main loop).
+    // equal length (mean at least 7/8 of the longest): a whole number per of CTAs
+    // per segment, at most MAX_FANIN. When the shortest selection has at least
+    // per tokens, the CTAs split each segment on their own (misc[22] = per): CTA
+    // c takes [r L_k / per, (r + 1) L_k / per) of segment k = c / per, r = c mod per
+    // (for equal lengths the ranges of the equal-token split), so each CTA holds
+    // one piece and every segment's contributors merge it together after the main
+    // loop. Otherwise the equal-token split over the per * S CTAs.
     {
         const unsigned S = static_cast<unsigned>(p.bs * Hkv);
         const bool uniform = 8ull * N >= 7ull * S * static_cast<unsigned long long>(misc[20]);
-        bool wide = false;
+        unsigned local = 0;
         if (!whole && (S <= FEW_SEGMENTS || (S <= UNIFORM_SEGMENTS && uniform)) && 2 * S <= G) {
             const unsigned per = G / S < MAX_FANIN ? G / S : MAX_FANIN;
             G = per * S;
-            wide = N == S * static_cast<unsigned>(misc[20]);
+            if (static_cast<unsigned>(misc[23]) >= per) local = per;
         }
-        misc[22] = wide ? 1 : 0; // every thread writes the same value
+        misc[22] = static_cast<int>(local); // every thread writes the same value
     }
     if (blockIdx.x >= G) return;
     long long t_begin, t_end;
@@ -954,6 +961,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
     } else {
         t_begin = cta_begin(blockIdx.x, N, G);
         t_end = cta_begin(blockIdx.x + 1, N, G);
+    }
+    if (const unsigned per = static_cast<unsigned>(misc[22]); per != 0) {
+        const unsigned k = blockIdx.x / per, r = blockIdx.x - k * per, b = k % static_cast<unsigned>(p.bs),
+                       g = k / static_cast<unsigned>(p.bs);
+        const unsigned Fs = g * static_cast<unsigned>(segP[p.bs]) + static_cast<unsigned>(segP[b]),
+                       L = static_cast<unsigned>(segL[b]);
+        t_begin = Fs + r * L / per;
+        t_end = Fs + (r + 1) * L / per;
     }
 
     uint8_t* const stage0 = smem + Ly::off_stage;
@@ -1938,16 +1953,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) qsa_decode_kernel(const Params p)
     // its counter; the merger resets the counter to zero. The partial stores of
     // all consumer threads precede thread 0's acq_rel ticket through the
     // barrier (release), and the merger's reads follow its ticket (acquire).
-    // Equal lengths (misc[22]): this CTA's one piece is contributor r of the n
-    // CTAs of segment pend0, all of which stored their partial and took a ticket.
+    // Segments split on their own (misc[22] = n): this CTA's one piece is
+    // contributor r of the n CTAs of segment pend0, all of which stored their
+    // partial and took a ticket.
     // Once the n tickets are in, each contributor merges float4 columns r, r + n,
     // ... of the segment's 12 x 256 outputs from the n partials in CTA order; a
     // second round of arrivals on the counter ends at 2n, and the contributor
     // that brings it there resets it.
     if (pend0 >= 0 && misc[22] != 0) {
-        unsigned Fs, cf, cl;
-        seg_range(pend0, Fs, cf, cl);
-        const unsigned n = cl - cf + 1, r = blockIdx.x - cf;
+        const unsigned n = static_cast<unsigned>(misc[22]), r = blockIdx.x % n, cf = blockIdx.x - r;
         if (tid == 0) {
             bool ok = true;
             if (mstate[4] == static_cast<int>(n) - 1)

@@ -265,3 +265,30 @@ def test_equal_length_splits_every_fan_in(cuda_device, hq, bs, length):
     again, _ = run_cuda(w.to(cuda_device), scratch=scratch)
     torch.cuda.synchronize()
     assert torch.equal(again, out)
+
+
+def _given_lengths(seed, hq, lengths, num_slots=65536):
+    hkv = hq // 12
+    kc, vc, ks, vs = I.make_pools(num_slots, hkv, "bf16", seed)
+    g = torch.Generator().manual_seed(seed)
+    sel = I.uniform_indices(int(sum(lengths)), num_slots, g)
+    return I.Workload(I.make_query(len(lengths), hq, seed), kc, vc, sel, I.cu_from_lengths(lengths),
+                      "bf16", ks, vs, capacity=max(lengths), name=f"given_{hq}q_bs{len(lengths)}")
+
+
+@pytest.mark.parametrize("hq,lengths", [
+    (24, [2055, 100]),                       # few segments, each split into its own CTAs
+    (12, [700, 65, 2055, 300]),
+    (12, [2055, 5, 700]),                    # a selection shorter than the CTAs per segment
+    (24, [1500, 1400, 1300, 1450, 1350]),    # ten nearly equal segments
+])
+def test_small_batches_of_unequal_lengths(cuda_device, hq, lengths):
+    w = _given_lengths(90 + len(lengths), hq, lengths)
+    out, scratch = run_cuda(w.to(cuda_device))
+    torch.cuda.synchronize()
+    compare(out, run_oracle(w), w.lengths().numpy())
+    assert qsa.qsa_scratch_error(scratch) == 0
+    assert (counters(scratch, w.bs, w.num_q_heads, w.capacity) == 0).all()
+    again, _ = run_cuda(w.to(cuda_device), scratch=scratch)
+    torch.cuda.synchronize()
+    assert torch.equal(again, out)
