@@ -2566,7 +2566,7 @@ struct StaticScratch {
 StaticScratch g_static[64];
 
 // Id of the calling thread's current CUDA context, unique for the life of the
-// process (the driver's cuCtxGetId, reached through the runtime's entry-point
+// process (the CUDA driver API's cuCtxGetId, reached through the runtime's entry-point
 // query); 0 when there is no current context or the query is unavailable.
 unsigned long long current_context_id() {
     using GetCurrent = CUresult (*)(CUcontext*);
