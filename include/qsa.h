@@ -35,6 +35,16 @@
  * launch, the kernel resets them in the same launch -- and the split-KV
  * partial results. Launches that share a scratch buffer must be ordered
  * (same stream or explicit dependencies).
+ *
+ * Residency. A small batch (at most 64 (sequence, KV head) segments, each cut
+ * into its own whole number of CTAs) is merged by all CTAs of a segment
+ * together: each waits, for at most 2 s, until the others have stored their
+ * partials, so all CTAs of that launch must become resident together (its grid
+ * never exceeds one CTA per SM). Kernels on other streams only delay this. Two
+ * such decodes in flight at once on different streams of one device whose grids
+ * together exceed the SMs can hold SMs the other waits for; both then end with
+ * QSA_DEVERR_TIMEOUT. Order such calls, or cap their grids with max_ctas so that
+ * they fit the SMs together.
  */
 #ifndef QSA_H_
 #define QSA_H_
