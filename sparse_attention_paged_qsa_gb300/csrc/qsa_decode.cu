@@ -14,15 +14,19 @@
 // GB300 design:
 //  * Persistent, balanced grid: the (sequence, KV head, token) space of the
 //    live lengths is cut into gridDim.x equal token ranges on the device, so
-//    a fixed (graph-captured) grid balances any length mix (with at most four
-//    segments, a whole number of CTAs per segment). A CTA whose range covers a
-//    whole (sequence, KV head) segment writes the output directly. A segment
-//    cut between CTAs is merged in the same launch: the CTA that holds its head
-//    at the end of its range merges directly when the other contributors have
-//    already arrived (they take their tickets as soon as their piece is done);
-//    otherwise the last CTA to arrive merges partials it bulk-copies into
-//    shared memory. Launches are programmatic dependent launches that wait for
-//    the previous grid before touching global memory.
+//    a fixed (graph-captured) grid balances any length mix. Small batches
+//    (at most four segments, or up to 64 of nearly equal length) get a whole
+//    number of CTAs per segment, each CTA splitting its own segment when every
+//    selection is long enough. A CTA whose range covers a whole (sequence, KV
+//    head) segment writes the output directly. A segment cut between CTAs is
+//    merged in the same launch: the CTA that holds its head at the end of its
+//    range merges directly when the other contributors have already arrived
+//    (they take their tickets as soon as their piece is done); otherwise the
+//    last CTA to arrive merges partials it bulk-copies into shared memory; and
+//    when each CTA holds one piece of one segment, all of that segment's CTAs
+//    merge a slice each once the last has arrived. Launches are programmatic
+//    dependent launches that wait for the previous grid before touching global
+//    memory.
 //  * Warp-specialised CTA (one per SM): four producer warps, one per SM
 //    sub-partition, gather whole K/V rows with 16-byte cp.async into a
 //    multi-stage shared-memory ring of 64-token stages, completing each stage
