@@ -36,15 +36,11 @@
  * partial results. Launches that share a scratch buffer must be ordered
  * (same stream or explicit dependencies).
  *
- * Residency. A small batch (at most 64 (sequence, KV head) segments, each cut
- * into its own whole number of CTAs) is merged by all CTAs of a segment
- * together: each waits, for at most 2 s, until the others have stored their
- * partials, so all CTAs of that launch must become resident together (its grid
- * never exceeds one CTA per SM). Kernels on other streams only delay this. Two
- * such decodes in flight at once on different streams of one device whose grids
- * together exceed the SMs can hold SMs the other waits for; both then end with
- * QSA_DEVERR_TIMEOUT. Order such calls, or cap their grids with max_ctas so that
- * they fit the SMs together.
+ * Residency. A small batch (at most 64 (sequence, KV head) segments) is
+ * launched cooperatively: all its CTAs (never more than one per SM) become
+ * resident together, waiting for SMs that kernels on other streams hold, so
+ * the merge in which the CTAs of one segment wait, for at most 2 s, for each
+ * other's partials always has all of them running.
  */
 #ifndef QSA_H_
 #define QSA_H_
@@ -99,12 +95,7 @@ enum {
     QSA_DEVERR_CU_SEQLENS = 2, /* cu_seqlens decreasing, negative, past the index buffer,
                                   or a length above capacity; the length is clamped */
     QSA_DEVERR_TIMEOUT = 4,    /* an internal wait exceeded its limit (2 s) and the launch
-                                  gave up early: a library fault, not a data fault, or --
-                                  when the batch is small enough that each (sequence, KV
-                                  head) gets its own CTAs, whose contributors wait for
-                                  each other to merge -- this call's CTAs could not all be
-                                  resident that long (kernels on other streams holding
-                                  the SMs) */
+                                  gave up early (a library fault, not a data fault) */
     QSA_DEVERR_CTX_LEN = 8     /* qsa_topk_expand: a context length outside [0, capacity];
                                   it is clamped into that range */
 };

@@ -2302,17 +2302,22 @@ int launch(const Params& prm, int grid, int dev, cudaStream_t stream) {
         }
     }
     // programmatic dependent launch: the kernel waits for the previous grid
-    // itself (griddepcontrol.wait) before it touches global memory
+    // itself (griddepcontrol.wait) before it touches global memory. Small
+    // batches (at most 64 segments, whose CTAs may wait for each other in the
+    // merge) launch cooperatively, so all their CTAs are resident together
+    // whatever else runs on the device (the grid is at most one CTA per SM).
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(NTHREADS);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeCooperative;
+    attr[1].val.cooperative = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = prm.bs * prm.Hkv <= static_cast<int>(UNIFORM_SEGMENTS) ? 2 : 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg, qsa_decode_kernel<FMT>, prm);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return fail(QSA_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
